@@ -1,0 +1,488 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test fixes a piece of the oracle to an independent source: a hand-worked
+value (tests/golden/format_values.txt), a closed form, an exhaustive
+comparison against independent encoder implementations (ml_dtypes, torch),
+brute-force nearest-value search, a high-precision (mpmath) evaluation of the
+activation in the pages' tanh form, or an invariant of the method.  A plausible
+mistake in the oracle (a dropped term, a wrong sign, a swapped operand, a
+transposed layout, a wrong tie rule) fails at least one of them.
+"""
+import math
+import os
+
+import ml_dtypes
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "format_values.txt")
+
+
+def _parse_float(s):
+    return float.fromhex(s) if "0x" in s and "p" in s else float(s)
+
+
+def _golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            kind, v, exp = line.split()
+            rows.append((kind, _parse_float(v), int(exp, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("kind,value,expected", _golden_rows())
+def test_hand_worked_values(kind, value, expected):
+    fn = {"e8m0": O.e8m0_rceil, "e4m3": O.e4m3_encode,
+          "nvfp4s": O.nvfp4_scale, "e2m1": O.e2m1_encode}[kind]
+    assert int(fn([value])[0]) == expected
+
+
+# ---------------------------------------------------------------- encoders --
+
+def _sweep_against(kind, first, n, ref_dtype, chunk=1 << 25):
+    """Compare oracle codes for all fp32 bit patterns first..first+n-1
+    against a cast through ref_dtype."""
+    done = 0
+    while done < n:
+        m = min(chunk, n - done)
+        start = first + done
+        ours = O.encode_bits(kind, start, m)
+        vals = np.arange(start, start + m, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        ref = vals.astype(ref_dtype).view(np.uint8)
+        if kind == 1:
+            ref = ref & 0xF
+        bad = np.nonzero(ours != ref)[0]
+        assert bad.size == 0, (hex(int(vals.view(np.uint32)[bad[0]])), ours[bad[0]], ref[bad[0]])
+        done += m
+
+
+@pytest.mark.slow
+def test_e4m3_exhaustive_nonnegative_vs_ml_dtypes():
+    # every non-negative fp32 up to and including 448
+    _sweep_against(0, 0, 0x43E00000 + 1, ml_dtypes.float8_e4m3fn)
+
+
+@pytest.mark.slow
+def test_e2m1_exhaustive_nonnegative_vs_ml_dtypes():
+    # every non-negative fp32 up to and including 6
+    _sweep_against(1, 0, 0x40C00000 + 1, ml_dtypes.float4_e2m1fn)
+
+
+def test_negative_values_mirror_positive():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 0x43E00001, 2_000_000, dtype=np.uint64).astype(np.uint32)
+    v = bits.view(np.float32)
+    assert np.array_equal(O.e4m3_encode(-v), O.e4m3_encode(v) | 0x80)
+    b2 = rng.integers(0, 0x40C00001, 2_000_000, dtype=np.uint64).astype(np.uint32)
+    v2 = b2.view(np.float32)
+    assert np.array_equal(O.e2m1_encode(-v2), O.e2m1_encode(v2) | 0x8)
+    # and against ml_dtypes on the negative side too
+    ref = (-v).astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+    assert np.array_equal(O.e4m3_encode(-v), ref)
+
+
+def test_e4m3_vs_torch_float8():
+    g = torch.Generator().manual_seed(7)
+    x = (torch.rand(4_000_000, generator=g) * 2 - 1) * 448
+    x = torch.cat([x, x * 1e-3, x * 1e-5, torch.tensor([0.0, -0.0, 448.0, -448.0])])
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x.numpy()), ref)
+
+
+def _e4m3_values_from_spec():
+    """All finite non-negative E4M3 magnitudes with their codes, built from
+    the format description (not from the oracle)."""
+    out = []
+    for ex in range(16):
+        for m in range(8):
+            if ex == 15 and m == 7:
+                continue
+            val = m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7)
+            out.append((val, (ex << 3) | m))
+    return out
+
+
+def _nearest_even(values_codes, a):
+    best = None
+    for val, code in values_codes:
+        d = abs(val - a)
+        if best is None or d < best[0] or (d == best[0] and (code & 1) == 0):
+            best = (d, code)
+    return best[1]
+
+
+def test_e4m3_brute_force_nearest():
+    vc = _e4m3_values_from_spec()
+    rng = np.random.default_rng(3)
+    # random magnitudes over the whole range, plus every exact midpoint
+    sample = list(np.exp2(rng.uniform(-12, 8.8, 3000)).astype(np.float32))
+    vals = sorted(v for v, _ in vc)
+    sample += [np.float32((a + b) / 2) for a, b in zip(vals, vals[1:])]
+    sample = [s for s in sample if s <= 448]
+    ours = O.e4m3_encode(np.array(sample, np.float32))
+    for s, c in zip(sample, ours):
+        assert c == _nearest_even(vc, float(s)), (s, c)
+
+
+def test_e2m1_brute_force_nearest_and_roundtrip():
+    vc = [(0.0, 0), (0.5, 1), (1.0, 2), (1.5, 3), (2.0, 4), (3.0, 5), (4.0, 6), (6.0, 7)]
+    grid = np.linspace(0, 6, 6001).astype(np.float32)
+    mids = np.array([(a[0] + b[0]) / 2 for a, b in zip(vc, vc[1:])], np.float32)
+    sample = np.concatenate([grid, mids])
+    ours = O.e2m1_encode(sample)
+    for s, c in zip(sample, ours):
+        assert c == _nearest_even(vc, float(s))
+    codes = np.arange(16, dtype=np.uint8)
+    assert np.array_equal(O.e2m1_encode(O.e2m1_decode(codes)), codes)
+
+
+def test_e4m3_decode_encode_roundtrip():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)
+    ref = codes.view(ml_dtypes.float8_e4m3fn).astype(np.float32)
+    assert np.array_equal(O.e4m3_decode(codes), ref)
+
+
+def test_e8m0_closed_form():
+    rng = np.random.default_rng(5)
+    ex = rng.integers(-149, 128, 200_000)
+    mant = rng.uniform(1, 2, 200_000)
+    amax = (mant * np.exp2(ex.astype(np.float64))).astype(np.float32)
+    amax = amax[np.isfinite(amax) & (amax > 0)]
+    edges = np.array([448.0 * 2.0 ** k for k in range(-140, 121)], np.float64)
+    edges = edges[(edges < 3.4e38) & (edges > 1e-45)].astype(np.float32)
+    amax = np.concatenate([amax, edges, np.nextafter(edges, np.float32(np.inf)),
+                           np.nextafter(edges, np.float32(0))])
+    s = O.e8m0_rceil(amax).astype(np.int64)
+    for a, b in zip(amax.astype(np.float64), s):
+        e = int(b) - 127
+        assert a <= 448.0 * 2.0 ** e, (a, e)
+        if e > -127:
+            assert a > 448.0 * 2.0 ** (e - 1), (a, e)
+    # the same bytes from the fp32 bit fields: biased exponent - 8, plus one
+    # when the significand exceeds 1.75 (448 = 1.75 * 2^8); floor at 0
+    nz = amax[amax >= np.float32(2.0 ** -126)]
+    u = nz.view(np.uint32).astype(np.int64)
+    byte = np.maximum((u >> 23) - 8 + ((u & 0x7FFFFF) > 0x600000), 0)
+    assert np.array_equal(O.e8m0_rceil(nz).astype(np.int64), byte)
+    assert O.e8m0_rceil([0.0])[0] == 0
+    assert O.e8m0_rceil([np.inf])[0] == 0xFF and O.e8m0_rceil([np.nan])[0] == 0xFF
+
+
+def test_nvfp4_scale_is_nearest_e4m3_of_quotient():
+    vc = _e4m3_values_from_spec()
+    rng = np.random.default_rng(9)
+    amax = np.exp2(rng.uniform(-14, 12, 2000)).astype(np.float32)
+    ours = O.nvfp4_scale(amax)
+    for a, c in zip(amax, ours):
+        q = float(np.float32(a) / np.float32(6.0))
+        exp = 0x7E if q >= 448 else _nearest_even(vc, q)
+        assert c == exp, (a, c, exp)
+
+
+def test_bf16_rne():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(1_000_000).astype(np.float32) * np.exp2(rng.integers(-60, 60, 1_000_000)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.bf16_rne(x), ref)
+
+
+# -------------------------------------------------------------- activation --
+
+def _all_bf16_in(lo, hi):
+    b = np.arange(0, 1 << 16, dtype=np.uint32)
+    v = (b << 16).view(np.float32)
+    v = v[np.isfinite(v) & (v >= lo) & (v <= hi)]
+    return np.unique(v.astype(np.float64))
+
+
+def test_activation_special_values():
+    for kind in (O.SILU, O.GELU_TANH):
+        assert O.act(kind, [0.0])[0] == 0.0
+        assert O.act_grad(kind, [0.0])[0] == 0.5
+        assert np.float32(O.act(kind, [60.0])[0]) == np.float32(60.0)
+        assert np.float32(O.act_grad(kind, [60.0])[0]) == np.float32(1.0)
+        # sign of tiny outputs in the negative tail
+        assert math.copysign(1, O.act(kind, [-500.0])[0]) == -1
+
+
+def test_activation_vs_mpmath_tanh_form():
+    mpmath = pytest.importorskip("mpmath")
+    # 1 + tanh(y) cancels down to e^(2y); at x = -14 that is e^-437, so the
+    # reference needs a few hundred digits to keep its own relative precision
+    mpmath.mp.dps = 420
+    c = mpmath.sqrt(2 / mpmath.pi)
+    a = mpmath.mpf("0.044715")
+
+    def gelu(x):
+        return x / 2 * (1 + mpmath.tanh(c * (x + a * x ** 3)))
+
+    def silu(x):
+        return x / (1 + mpmath.exp(-x))
+
+    for kind, f, lo, hi in ((O.SILU, silu, -120.0, 120.0), (O.GELU_TANH, gelu, -14.0, 14.0)):
+        xs = _all_bf16_in(lo, hi)[::7]
+        ours, ours_d = O.act(kind, xs), O.act_grad(kind, xs)
+        for x, y, dy in zip(xs, ours, ours_d):
+            X = mpmath.mpf(float(x))
+            ref = f(X)
+            dref = mpmath.diff(f, X)
+            # exp(t) has condition number |t|: the double evaluation's relative
+            # error grows with the argument (|t| ~ 0.07 |x|^3 for GELU); any
+            # formula mistake is O(1), far above this bound
+            cond = 1.0 + abs(float(x)) + (0.1 * abs(float(x)) ** 3 if kind == O.GELU_TANH else 0.0)
+            assert abs(y - float(ref)) <= 1e-15 * cond * abs(float(ref)) + 1e-300, (kind, x)
+            # act' has zeros; bound the error by its term magnitudes
+            scale = abs(float(dref)) + 1e-13 * (1 + abs(float(x)))
+            assert abs(dy - float(dref)) <= 1e-13 * cond * scale, (kind, x, dy, float(dref))
+
+
+def test_activation_vs_torch_float64():
+    # torch evaluates the tanh form, whose 1 + tanh(y) cancels for x << 0;
+    # stay where that library form is itself accurate (the tail is pinned
+    # against mpmath above)
+    x = torch.linspace(-3, 20, 20001, dtype=torch.float64)
+    assert np.allclose(O.act(O.SILU, x.numpy()), torch.nn.functional.silu(x).numpy(), rtol=1e-14, atol=0)
+    ref = torch.nn.functional.gelu(x, approximate="tanh").numpy()
+    assert np.allclose(O.act(O.GELU_TANH, x.numpy()), ref, rtol=1e-12, atol=1e-300)
+    # derivatives through autograd of the library forms
+    for kind, fn in ((O.SILU, torch.nn.functional.silu),
+                     (O.GELU_TANH, lambda t: torch.nn.functional.gelu(t, approximate="tanh"))):
+        t = x.clone().requires_grad_(True)
+        fn(t).sum().backward()
+        assert np.allclose(O.act_grad(kind, x.numpy()), t.grad.numpy(), rtol=1e-11, atol=1e-14)
+
+
+def test_activation_gradient_finite_differences():
+    xs = np.linspace(-9, 9, 1801)
+    h = 1e-5
+    for kind in (O.SILU, O.GELU_TANH):
+        fd = (O.act(kind, xs + h) - O.act(kind, xs - h)) / (2 * h)
+        assert np.allclose(O.act_grad(kind, xs), fd, rtol=0, atol=1e-8)
+
+
+# ---------------------------------------------------------- the full path --
+
+def _bf16_bits(x):
+    return np.asarray(x, np.float32).astype(ml_dtypes.bfloat16).view(np.uint16)
+
+
+def test_exact_activation_blocks_mxfp8_row():
+    # gate = 32: sigmoid(32) rounds to 1 in fp32 and h = 32 * up exactly, so
+    # every block below has a hand-computable scale and codes.
+    N = 32 * 6
+    up = np.zeros((2, N), np.float32)
+    up[0, 0] = 14.0                 # block 0: amax 448 -> scale 127, code 0x7E
+    up[0, 32] = 28.0                # block 1: amax 896 -> 128, 896/2 = 448 -> 0x7E
+    up[0, 64] = 2.0 ** -5           # block 2: amax 1 -> 119, v = 256 -> 0x78
+    up[0, 96] = 14.0                # block 3: e = 0 ...
+    up[0, 97] = 2.0 ** -14          # ... h = 2^-9 -> subnormal code 0x01
+    up[0, 98] = 3 * 2.0 ** -15      # ... h = 3*2^-10 -> tie -> 0x02
+    up[0, 99] = 17 * 2.0 ** -9      # ... h = 1.0625 -> tie -> 0x38
+    up[0, 100] = -(2.0 ** -16)      # ... h = -2^-11 -> 0x80
+    up[0, 128:160] = 0.0            # block 4: all zero -> scale 0, codes 0
+    up[0, 160:192] = -0.0           # block 5: all -0 -> scale 0, codes 0x80
+    up[0, 160] = 0.0
+    up[1] = up[0] * -1
+    gate = np.full((2, N), 32.0, np.float32)
+    for kind in (O.SILU, O.GELU_TANH):
+        r = O.glu_fwd(_bf16_bits(gate), _bf16_bits(up), act=kind, fmt=O.MXFP8, mode=O.ROW, want_h=True)
+        assert np.array_equal(r["h"][0], (32 * up[0]).astype(np.float32))
+        q, s = r["q_row"], r["s_row"]
+        assert list(s[0]) == [127, 128, 119, 127, 0, 0]
+        assert q[0, 0] == 0x7E and q[0, 32] == 0x7E and q[0, 64] == 0x78
+        assert list(q[0, 96:101]) == [0x7E, 0x01, 0x02, 0x38, 0x80]
+        assert np.all(q[0, 101:128] == 0) and np.all(q[0, 1:32] == 0)
+        assert np.all(q[0, 128:160] == 0)
+        assert q[0, 160] == 0 and np.all(q[0, 161:192] == 0x80)
+        # negated up: same scales, sign bits flipped (zeros flip too)
+        assert np.array_equal(s[1], s[0])
+        assert np.array_equal(q[1], q[0] ^ 0x80)
+
+
+def test_sign_of_zero_product():
+    gate = _bf16_bits(np.full((1, 32), -1.0))
+    up = _bf16_bits(np.zeros((1, 32)))
+    r = O.glu_fwd(gate, up, act=O.SILU, fmt=O.MXFP8, mode=O.ROW)
+    assert np.all(r["q_row"] == 0x80)  # silu(-1) < 0, times +0 = -0
+
+
+def test_exact_activation_nvfp4_interleaved():
+    H = 64
+    x = np.zeros((1, 2 * H), np.float32)
+    x[0, 0::2] = 32.0               # gate columns
+    ups = np.zeros(H, np.float32)
+    ups[0:4] = [6 / 32, -0.5 / 32, 0.25 / 32, 0.75 / 32]   # block 0: amax 6 -> s 1.0
+    ups[16] = 12 / 32                                      # block 1: amax 12 -> s 2.0
+    ups[17] = 3 / 32                                       # h = 3 -> v = 1.5 -> 0x3
+    ups[32] = 2.0 ** -20                                   # block 2: s -> 0, codes 0
+    ups[33] = -(2.0 ** -20)                                # -> sign-kept zero 0x8
+    ups[48:64] = 0.0                                       # block 3: zeros
+    x[0, 1::2] = ups
+    r = O.glu_fwd(_bf16_bits(x), act=O.GELU_TANH, fmt=O.NVFP4, layout=O.INTERLEAVED)
+    q, s = r["out"], r["s_nvfp4"]
+    # element 2i in the low nibble, 2i+1 in the high nibble
+    assert q[0, 0] == (0x7 | (0x9 << 4))      # 6 -> 7, -0.5 -> 0x9
+    assert q[0, 1] == (0x0 | (0x2 << 4))      # 0.25 tie -> 0, 0.75 tie -> 1.0
+    assert q[0, 8] == (0x7 | (0x3 << 4))      # 12/2 = 6 -> 7, 3/2 = 1.5 -> 3
+    assert q[0, 16] == (0x0 | (0x8 << 4))
+    # scales at the 128x4 offsets of row 0, columns 0..3
+    assert [s[O.swizzle_offset(0, c, 4)] for c in range(4)] == [0x38, 0x40, 0x00, 0x00]
+    # padding rows 1..127 are zero
+    assert s.sum() == 0x38 + 0x40
+
+
+def test_swizzle_is_bijection_on_padded_domain():
+    for M, N in ((128, 64), (784, 16384 // 64 * 64), (200, 80), (1, 16)):
+        C = N // 16
+        rp, cp = -(-M // 128) * 128, -(-C // 4) * 4
+        offs = np.array([O.swizzle_offset(r, c, cp) for r in range(rp) for c in range(cp)]) \
+            if rp * cp < 300_000 else None
+        if offs is None:
+            continue
+        assert np.array_equal(np.sort(offs), np.arange(rp * cp))
+    assert O.swizzle_offset(0, 0, 8) == 0
+    assert O.swizzle_offset(1, 0, 8) == 16
+    assert O.swizzle_offset(32, 0, 8) == 4
+    assert O.swizzle_offset(0, 1, 8) == 1
+    assert O.swizzle_offset(0, 4, 8) == 512
+    assert O.swizzle_offset(128, 0, 8) == 1024
+
+
+def _rand_inputs(M, N, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    g = _bf16_bits(rng.standard_normal((M, N)) * scale)
+    u = _bf16_bits(rng.standard_normal((M, N)) * scale)
+    return g, u
+
+
+@pytest.mark.parametrize("kind", [O.SILU, O.GELU_TANH])
+def test_both_equals_row_and_col(kind):
+    g, u = _rand_inputs(96, 160, 1)
+    b = O.glu_fwd(g, u, act=kind, fmt=O.MXFP8, mode=O.BOTH)
+    r = O.glu_fwd(g, u, act=kind, fmt=O.MXFP8, mode=O.ROW)
+    c = O.glu_fwd(g, u, act=kind, fmt=O.MXFP8, mode=O.COL)
+    for k in ("q_row", "s_row"):
+        assert np.array_equal(b[k], r[k])
+    for k in ("q_col", "s_col"):
+        assert np.array_equal(b[k], c[k])
+
+
+@pytest.mark.parametrize("kind", [O.SILU, O.GELU_TANH])
+def test_col_is_row_of_transpose(kind):
+    g, u = _rand_inputs(64, 96, 2)
+    c = O.glu_fwd(g, u, act=kind, fmt=O.MXFP8, mode=O.COL)
+    rt = O.glu_fwd(np.ascontiguousarray(g.T), np.ascontiguousarray(u.T), act=kind,
+                   fmt=O.MXFP8, mode=O.ROW)
+    # colwise codes are stored [N, M]: exactly the rowwise codes of the transpose
+    assert np.array_equal(c["q_col"], rt["q_row"])
+    assert np.array_equal(c["s_col"], rt["s_row"])
+
+
+def test_layout_invariance():
+    g, u = _rand_inputs(64, 128, 3)
+    M, N = g.shape
+    packed = np.concatenate([g, u], axis=1)               # [gate | up], ld = 2N
+    inter = np.empty((M, 2 * N), np.uint16)
+    inter[:, 0::2], inter[:, 1::2] = g, u
+    for fmt, mode in ((O.MXFP8, O.BOTH), (O.NVFP4, O.ROW), (O.FP32, O.ROW)):
+        a = O.glu_fwd(g, u, act=O.GELU_TANH, fmt=fmt, mode=mode)
+        b = O.glu_fwd(packed[:, :N], packed[:, N:], act=O.GELU_TANH, fmt=fmt, mode=mode)
+        c = O.glu_fwd(inter, act=O.GELU_TANH, fmt=fmt, mode=mode, layout=O.INTERLEAVED)
+        for k in a:
+            if a[k] is not None:
+                assert np.array_equal(a[k], b[k]) and np.array_equal(a[k], c[k]), (fmt, k)
+
+
+def test_row_chunk_invariance_and_determinism():
+    g, u = _rand_inputs(256, 64, 4)
+    full = O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.BOTH, nthreads=3)
+    again = O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.BOTH, nthreads=1)
+    top = O.glu_fwd(g[:128], u[:128], act=O.SILU, fmt=O.MXFP8, mode=O.BOTH)
+    bot = O.glu_fwd(g[128:], u[128:], act=O.SILU, fmt=O.MXFP8, mode=O.BOTH)
+    for k in full:
+        assert np.array_equal(full[k], again[k])
+    assert np.array_equal(full["q_row"], np.concatenate([top["q_row"], bot["q_row"]]))
+    assert np.array_equal(full["q_col"], np.concatenate([top["q_col"], bot["q_col"]], axis=1))
+    assert np.array_equal(full["s_col"], np.concatenate([top["s_col"], bot["s_col"]], axis=1))
+
+
+def test_dequantisation_error_bound():
+    g, u = _rand_inputs(64, 256, 5)
+    r = O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.ROW, want_h=True)
+    h = r["h"].astype(np.float64)
+    scale = np.repeat(O.e8m0_decode(r["s_row"]).astype(np.float64), 32, axis=1)
+    deq = O.e4m3_decode(r["q_row"]).astype(np.float64) * scale
+    v = np.abs(h / scale)
+    normal = v >= 2.0 ** -6
+    assert np.all(np.abs(deq - h)[normal] <= 2.0 ** -4 * np.abs(h)[normal])
+    assert np.all(np.abs(deq - h)[~normal] <= 2.0 ** -10 * scale[~normal])
+
+
+def test_backward_exact_activation():
+    # gate = 32: act'(32) rounds to 1 and act(32) = 32 in fp32, so
+    # dGate = dY*up and dUp = 32*dY exactly; they land in [dGate | dUp].
+    rng = np.random.default_rng(6)
+    M, N = 32, 64
+    gate = np.full((M, N), 32.0, np.float32)
+    up = rng.standard_normal((M, N)).astype(ml_dtypes.bfloat16).astype(np.float32)
+    dy = rng.standard_normal((M, N)).astype(ml_dtypes.bfloat16).astype(np.float32)
+    for kind in (O.SILU, O.GELU_TANH):
+        r = O.glu_bwd(_bf16_bits(gate), _bf16_bits(up), _bf16_bits(dy), act=kind, fmt=O.FP32)
+        out = r["out"]
+        assert np.array_equal(out[:, :N], (dy * up).astype(np.float32))
+        assert np.array_equal(out[:, N:], (32 * dy).astype(np.float32))
+
+
+def test_backward_formula_against_autograd():
+    g, u = _rand_inputs(32, 64, 8)
+    d, _ = _rand_inputs(32, 64, 9)
+    gf = torch.from_numpy(g.astype(np.uint32) << 16).view(torch.float32).double()
+    uf = torch.from_numpy(u.astype(np.uint32) << 16).view(torch.float32).double()
+    df = torch.from_numpy(d.astype(np.uint32) << 16).view(torch.float32).double()
+    for kind, fn in ((O.SILU, torch.nn.functional.silu),
+                     (O.GELU_TANH, lambda t: torch.nn.functional.gelu(t, approximate="tanh"))):
+        gg = gf.clone().requires_grad_(True)
+        uu = uf.clone().requires_grad_(True)
+        (fn(gg) * uu * df).sum().backward()
+        r = O.glu_bwd(g, u, d, act=kind, fmt=O.FP32)
+        ref = torch.cat([gg.grad, uu.grad], dim=1).float().numpy()
+        assert np.allclose(r["out"], ref, rtol=2e-7, atol=1e-30)
+
+
+def test_fp32_mode_is_rounded_exact_value():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    g, u = _rand_inputs(4, 64, 10)
+    r = O.glu_fwd(g, u, act=O.SILU, fmt=O.FP32)
+    gv = (g.astype(np.uint32) << 16).view(np.float32)
+    uv = (u.astype(np.uint32) << 16).view(np.float32)
+    for x, y, o in zip(gv.ravel(), uv.ravel(), r["out"].ravel()):
+        X = mpmath.mpf(float(x))
+        exact = X / (1 + mpmath.exp(-X)) * mpmath.mpf(float(y))
+        assert o == np.float32(float(exact))
+
+
+def test_boundary_distance():
+    # 1.0625 is the midpoint between E4M3 1.0 and 1.125: distance 0; one
+    # float above is 1 ulp away.
+    v = np.array([1.0625, np.nextafter(np.float32(1.0625), np.float32(2)), 1.0], np.float32)
+    assert list(O.boundary_ulps(O.MXFP8, v)) == [0, 1, 1 << 19]
+    assert O.boundary_ulps(O.NVFP4, np.array([0.25], np.float32))[0] == 0
+    assert O.boundary_ulps(O.BF16, np.array([1.0 + 2.0 ** -8], np.float32))[0] == 0
+
+
+def test_oracle_rejects_unsupported_arguments():
+    g, u = _rand_inputs(40, 48, 11)
+    with pytest.raises(ValueError):
+        O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.ROW)     # N % 32
+    g, u = _rand_inputs(40, 64, 11)
+    with pytest.raises(ValueError):
+        O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.COL)     # M % 32
+    with pytest.raises(ValueError):
+        O.glu_fwd(g, u, act=O.SILU, fmt=O.NVFP4, mode=O.BOTH)
