@@ -1,0 +1,531 @@
+"""Benchmark of the fused gated-GLU + MXFP8 quantisation path on GB300.
+
+Workload (one "step"): SwiGLU at M=131072, N=8192 (gate, up, dY bf16
+N(0,1) with 0.1% of elements set to +-60), MXFP8 E4M3/E8M0 outputs, the six
+calls forward {row, col, both} and backward {row, col, both}, each its own
+kernel launch.  The metric is effective bandwidth: algorithmic bytes read +
+written (4 B/elem read forward, 6 B/elem backward; 1 + 1/32 B written per
+element and direction) divided by device time, reported against the measured
+HBM copy bandwidth.  Inputs (6 GB) are far larger than L2, so nothing is
+flushed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--no-e2e] [--no-cpu] [--sweep FILE]
+
+One JSON line on stdout (rank 0).  ``--impl reference`` times the CPU oracle
+(the only reference implementation that exists for this path) on a bounded
+sample of the same workload.  ``--sweep FILE`` additionally writes one JSONL
+record per workload/mode/direction (CUDA-graph timing, 20 calls per replay).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GLU+quant effective GB/s and % of GB300 HBM peak; µs/call"
+M_FULL, N_FULL = 131072, 8192
+CALLS = [("fwd", 1), ("fwd", 2), ("fwd", 3), ("bwd", 1), ("bwd", 2), ("bwd", 3)]
+MODE_NAME = {1: "row", 2: "col", 3: "both"}
+# the pages' GB200 per-call times for these six calls at 131072x8192 (context)
+PAGE_GB200_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
+                 ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
+L2_BYTES = 129 * 2 ** 20
+
+
+def algo_bytes(direction: str, mode: int, M: int, N: int, fmt: str = "mxfp8") -> int:
+    """Algorithmic bytes of one call (read + written, unpadded)."""
+    MN = M * N
+    dirs = 2 if mode == 3 else 1
+    if direction == "fwd":
+        read = 4 * MN
+        if fmt == "mxfp8":
+            write = dirs * (MN + MN // 32)
+        elif fmt == "nvfp4":
+            write = MN // 2 + MN // 16
+        elif fmt == "bf16":
+            write = 2 * MN
+        else:
+            write = 4 * MN
+    else:
+        read = 6 * MN
+        if fmt == "mxfp8":
+            write = dirs * 2 * (MN + MN // 32)
+        elif fmt == "bf16":
+            write = 4 * MN
+        else:
+            write = 8 * MN
+    return read + write
+
+
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(world: int, bytes_per_rank_step: int, steps: int, max_ms: float) -> float:
+    """Weak scaling: every rank processes its own batch; the job's bandwidth
+    is all ranks' bytes over the slowest rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "of measured (MEASURED_PEAKS.json hbm_gbs)"}
+    return {"hbm_gbs": 6800.0, "source": "of fallback (6.8 TB/s)"}
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = csrc_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel_key and parts[2] == cur:
+            return float(parts[1])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append((float(p[1]), float(p[2]), float(p[3]), p[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r[2] > 200.0] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in load),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+def gpu_arm(args, rank, world, dist):
+    import torch
+
+    import fp4_quant_gb300 as G
+    import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sp = synth.spec("swiglu_131072")
+    M, N = sp.M, sp.N
+    x = synth.make(sp, dev, with_dy=True, seed_offset=rank * 10)
+    g, u, d = x["gate"], x["up"], x["dy"]
+
+    # preallocated outputs for each of the six calls
+    def outs(direction, mode):
+        W = N if direction == "fwd" else 2 * N
+        o = {"q_row": None, "s_row": None, "q_col": None, "s_col": None, "out": None}
+        if mode & 1:
+            o["q_row"] = torch.empty((M, W), dtype=torch.uint8, device=dev)
+            o["s_row"] = torch.empty((M, W // 32), dtype=torch.uint8, device=dev)
+        if mode & 2:
+            o["q_col"] = torch.empty((W, M), dtype=torch.uint8, device=dev)
+            o["s_col"] = torch.empty((W, M // 32), dtype=torch.uint8, device=dev)
+        return o
+
+    bufs = {c: outs(*c) for c in CALLS}
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def call(c):
+        direction, mode = c
+        if direction == "fwd":
+            G.fwd(g, u, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+        else:
+            G.bwd(g, u, d, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        for c in CALLS:
+            call(c)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in CALLS] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with Clocks(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for k in range(K):
+            for i, c in enumerate(CALLS):
+                ev[k][i][0].record(stream)
+                call(c)
+                ev[k][i][1].record(stream)
+                launches += 1
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_call_ms = {c: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)]
+                   for i, c in enumerate(CALLS)}
+    total_ms = reduce_max(total_ms, dist, dev)
+
+    step_bytes = sum(algo_bytes(dr, m, M, N) for dr, m in CALLS)
+    value = whole_job_gbps(world, step_bytes, K, total_ms)
+    peaks = measured_peaks()
+    modes = {}
+    for c in CALLS:
+        avg = statistics.mean(per_call_ms[c])
+        gbps = algo_bytes(c[0], c[1], M, N) / (avg * 1e-3) / 1e9
+        modes[f"{c[0]}_{MODE_NAME[c[1]]}"] = {
+            "us": round(avg * 1e3, 2), "us_min": round(min(per_call_ms[c]) * 1e3, 2),
+            "gbps": round(gbps, 1), "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
+            "page_gb200_us": PAGE_GB200_US[c]}
+    dom = max(CALLS, key=lambda c: statistics.mean(per_call_ms[c]))
+    dom_name = f"{dom[0]}_{MODE_NAME[dom[1]]}"
+    dom_gbps = modes[dom_name]["gbps"]
+    traffic = profiled_traffic(f"{dom[0]}_mx_{MODE_NAME[dom[1]]}_131072x8192")
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "swiglu_131072x8192_mxfp8_fwd+bwd_row+col+both",
+                   "M": M, "N": N, "act": "silu", "fmt": "mxfp8_e4m3_e8m0_rceil",
+                   "calls_per_step": len(CALLS), "global_batch_rows": world * M,
+                   "parallelism": f"dp{world}" if world > 1 else "single",
+                   "l2": "inputs 6 GB >> 129 MB L2; no flush"},
+        "modes": modes,
+        "roofline": {"bound": "hbm", "achieved": dom_gbps, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(dom_gbps / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "kernel": dom_name,
+                     "algo_bytes_per_launch": algo_bytes(dom[0], dom[1], M, N),
+                     "peak_source": peaks["source"]},
+        "page_context": {"gb200_same_calls_gbps": round(
+            step_bytes / (sum(PAGE_GB200_US.values()) * 1e-6) / 1e9, 1),
+            "note": "the pages' GB200 per-call times for the same six calls (context, not a target)"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        res["e2e"] = e2e_leg(args, G, g, u, d, bufs, dev, stream, dist, world, step_bytes)
+    return res
+
+
+def e2e_leg(args, G, g, u, d, bufs, dev, stream, dist, world, step_bytes):
+    """The same six calls through the public API with host buffers: every
+    step copies the inputs host->device from pinned memory and reads every
+    call's outputs back, inside the timed region."""
+    import torch
+    hg = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+    hu = torch.empty(u.shape, dtype=u.dtype, pin_memory=True)
+    hd = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+    hg.copy_(g)
+    hu.copy_(u)
+    hd.copy_(d)
+    biggest = max(CALLS, key=lambda c: sum(t.numel() for t in bufs[c].values() if t is not None))
+    hout = {k: (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) if t is not None else None)
+            for k, t in bufs[biggest].items()}
+    h2d = sum(t.numel() * t.element_size() for t in (hg, hu, hd))
+    d2h = sum(sum(t.numel() * t.element_size() for t in bufs[c].values() if t is not None)
+              for c in CALLS)
+    sh = stream.cuda_stream
+
+    def step():
+        g.copy_(hg, non_blocking=True)
+        u.copy_(hu, non_blocking=True)
+        d.copy_(hd, non_blocking=True)
+        for c in CALLS:
+            direction, mode = c
+            if direction == "fwd":
+                G.fwd(g, u, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+            else:
+                G.bwd(g, u, d, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+            for k, t in bufs[c].items():
+                if t is not None:
+                    hout[k].view(-1)[: t.numel()].copy_(t.view(-1), non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    K = max(1, min(args.steps, 3))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max(t0.elapsed_time(t1), dist, dev)
+    return {"value": round(whole_job_gbps(world, step_bytes, K, ms), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": round(ms / K, 3)}
+
+
+# ------------------------------------------------------------- CPU (oracle) --
+
+_SAMPLE_CACHE = {}
+
+
+def oracle_sample(rows: int, seed_offset: int = 0, nthreads: int | None = None):
+    """Time the oracle on `rows` rows of the same workload (host inputs drawn
+    once with the same generator recipe, on the CPU; drawing is not timed)."""
+    import oracle as O
+    import synth
+    key = (rows, seed_offset)
+    if key not in _SAMPLE_CACHE:
+        sp = synth.spec("swiglu_131072", M=rows)
+        x = synth.make(sp, "cpu", with_dy=True, seed_offset=seed_offset)
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = (sp, [synth.to_host_bits(x[k]) for k in ("gate", "up", "dy")])
+    sp, (gb, ub, db) = _SAMPLE_CACHE[key]
+    nthreads = nthreads or os.cpu_count() or 1
+    O.lib()
+    t0 = time.perf_counter()
+    for direction, mode in CALLS:
+        if direction == "fwd":
+            O.glu_fwd(gb, ub, act=O.SILU, fmt=O.MXFP8, mode=mode, nthreads=nthreads)
+        else:
+            O.glu_bwd(gb, ub, db, act=O.SILU, fmt=O.MXFP8, mode=mode, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    nbytes = sum(algo_bytes(dr, m, rows, sp.N) for dr, m in CALLS)
+    return nbytes / dt / 1e9, dt, nthreads
+
+
+def cpu_baseline(rows: int):
+    v, dt, n = oracle_sample(rows)
+    return {"value": round(v, 3), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{rows} of 131072 rows, all six calls, {dt:.1f} s wall"}
+
+
+def reference_arm(args, rank, world):
+    rows = args.ref_rows
+    for _ in range(max(args.warmup, 1)):
+        oracle_sample(rows)  # warm-up (page in, thread start)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, dt, n = oracle_sample(rows)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(statistics.median(times) * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "swiglu_131072x8192_mxfp8_fwd+bwd_row+col+both",
+                       "M": M_FULL, "N": N_FULL, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": n,
+                             "kind": "oracle",
+                             "sample": f"{rows} of 131072 rows per step, all six calls"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- sweep --
+
+def sweep(path: str):
+    """Per-workload, per-mode records (CUDA graph of 20 calls per replay, 25
+    warm-up replays, 30 samples; median and min us per call)."""
+    import torch
+
+    import fp4_quant_gb300 as G
+    import synth
+    dev = torch.device("cuda", 0)
+    peaks = measured_peaks()
+    recs = []
+
+    def time_graph(fn, reps=20, warm=25, samples=30):
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            fn(s.cuda_stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                for _ in range(reps):
+                    fn(s.cuda_stream)
+        torch.cuda.synchronize(dev)
+        for _ in range(warm):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        out = []
+        for _ in range(samples):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3 / reps)
+        return statistics.median(out), min(out)
+
+    def record(workload, direction, mode, fmt, act, M, N, fn):
+        med, mn = time_graph(fn)
+        nbytes = algo_bytes(direction, mode, M, N, fmt)
+        gbps = nbytes / (med * 1e-6) / 1e9
+        r = {"workload": workload, "direction": direction, "mode": MODE_NAME.get(mode, "row"),
+             "fmt": fmt, "act": act, "M": M, "N": N, "us_median": round(med, 3),
+             "us_min": round(mn, 3), "bytes": nbytes, "gbps": round(gbps, 1),
+             "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
+             "l2_resident": nbytes < L2_BYTES}
+        recs.append(r)
+        print(json.dumps(r), file=sys.stderr, flush=True)
+
+    fmts = {"mxfp8": G.FMT_MXFP8, "nvfp4": G.FMT_NVFP4, "bf16": G.FMT_BF16}
+    # workloads
+    x = synth.make(synth.spec("swiglu_128"), dev)
+    record("swiglu_128", "fwd", 1, "mxfp8", "silu", 128, 128,
+           lambda s: G.fwd(x["gate"], x["up"], mode=1, stream=s))
+    x = synth.make(synth.spec("swiglu_4096"), dev, with_dy=True)
+    for m in (1, 2, 3):
+        o = G.fwd(x["gate"], x["up"], mode=m)
+        record("swiglu_4096", "fwd", m, "mxfp8", "silu", 4096, 7168,
+               lambda s, m=m, o=o: G.fwd(x["gate"], x["up"], mode=m, out=o, stream=s))
+        o = G.bwd(x["gate"], x["up"], x["dy"], mode=m)
+        record("swiglu_4096", "bwd", m, "mxfp8", "silu", 4096, 7168,
+               lambda s, m=m, o=o: G.bwd(x["gate"], x["up"], x["dy"], mode=m, out=o, stream=s))
+    for N in (11008, 14336, 18944, 29568):
+        x = synth.make(synth.spec("geglu_8192", N=N), dev, with_dy=True)
+        for fname in ("mxfp8", "bf16"):
+            f = fmts[fname]
+            o = G.fwd(x["gate"], x["up"], act=1, fmt=f)
+            record("geglu_8192", "fwd", 1, fname, "gelu_tanh", 8192, N,
+                   lambda s, o=o, f=f: G.fwd(x["gate"], x["up"], act=1, fmt=f, out=o, stream=s))
+            o = G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=f)
+            record("geglu_8192", "bwd", 1, fname, "gelu_tanh", 8192, N,
+                   lambda s, o=o, f=f: G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=f, out=o,
+                                             stream=s))
+        del x
+    for M in (784, 968):
+        X = synth.make(synth.spec("geglu_nvfp4", M=M), dev)["x"]
+        o = G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1)
+        record("geglu_nvfp4", "fwd", 1, "nvfp4", "gelu_tanh", M, 16384,
+               lambda s, o=o: G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1, out=o, stream=s))
+    with open(path, "w") as f:
+        for r in recs:
+            f.write(json.dumps(r) + "\n")
+
+
+# ----------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=16384)
+    ap.add_argument("--ref-rows", type=int, default=2048)
+    ap.add_argument("--sweep", default=None)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle runs on host cores; under torchrun only rank 0 works
+        if rank == 0:
+            print(json.dumps(reference_arm(args, rank, world)), flush=True)
+        return
+
+    # CPU baseline first (no GPU context yet), rank 0 at N=1 only
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        cpu = cpu_baseline(args.cpu_rows)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = gpu_arm(args, rank, world, dist)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if args.sweep and rank == 0:
+        sweep(args.sweep)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+"""fp4_quant_gb300 — fused gated-GLU + block-scaled quantisation on GB300.
+
+A thin ctypes binding of the C ABI in ``include/glu_quant.h``
+(``libglu_quant.so``, built in-tree by ``fp4_quant_gb300.build``).  The
+functions with the C names take the C argument structs and a stream handle
+and do nothing but marshal; every step of the computation runs in the CUDA
+kernels.  ``fwd``/``bwd`` are conveniences that allocate the outputs with
+torch on the inputs' device and fill the argument struct from tensors.
+
+There is no CPU or eager fallback: if the library is missing, the first call
+raises ImportError (importing the package alone does not, so that
+``python -m fp4_quant_gb300.build`` can create it).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "glu_quant_fwd", "glu_quant_bwd", "glu_quant_fwd_sizes", "glu_quant_bwd_sizes",
+    "glu_quant_status_str", "glu_quant_abi_version", "GluQuantFwdArgs", "GluQuantBwdArgs",
+    "GluQuantError", "fwd", "bwd", "library_path",
+    "ACT_SILU", "ACT_GELU_TANH", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32",
+    "MODE_ROW", "MODE_COL", "MODE_BOTH", "LAYOUT_SPLIT", "LAYOUT_INTERLEAVED",
+]
+
+ACT_SILU, ACT_GELU_TANH = 0, 1
+FMT_MXFP8, FMT_NVFP4, FMT_BF16, FMT_FP32 = 0, 1, 2, 3
+MODE_ROW, MODE_COL, MODE_BOTH = 1, 2, 3
+LAYOUT_SPLIT, LAYOUT_INTERLEAVED = 0, 1
+
+GLU_OK, GLU_EINVAL, GLU_ESHAPE, GLU_EALIGN, GLU_EDEVICE, GLU_ELAUNCH = 0, -1, -2, -3, -4, -5
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libglu_quant.so")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class GluQuantFwdArgs(ctypes.Structure):
+    """Mirror of ``glu_quant_fwd_args``."""
+    _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("ld_in", ctypes.c_int64),
+                ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
+                ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
+
+
+class GluQuantBwdArgs(ctypes.Structure):
+    """Mirror of ``glu_quant_bwd_args``."""
+    _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("ld_in", ctypes.c_int64),
+                ("ld_dy", ctypes.c_int64),
+                ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("dy", ctypes.c_void_p),
+                ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
+
+
+class GluQuantError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({glu_quant_status_str(status)})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with `python -m fp4_quant_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    lib.glu_quant_fwd.argtypes = [ctypes.POINTER(GluQuantFwdArgs), ctypes.c_void_p]
+    lib.glu_quant_fwd.restype = ctypes.c_int
+    lib.glu_quant_bwd.argtypes = [ctypes.POINTER(GluQuantBwdArgs), ctypes.c_void_p]
+    lib.glu_quant_bwd.restype = ctypes.c_int
+    lib.glu_quant_fwd_sizes.argtypes = [ctypes.POINTER(GluQuantFwdArgs), ctypes.POINTER(ctypes.c_size_t)]
+    lib.glu_quant_fwd_sizes.restype = ctypes.c_int
+    lib.glu_quant_bwd_sizes.argtypes = [ctypes.POINTER(GluQuantBwdArgs), ctypes.POINTER(ctypes.c_size_t)]
+    lib.glu_quant_bwd_sizes.restype = ctypes.c_int
+    lib.glu_quant_status_str.argtypes = [ctypes.c_int]
+    lib.glu_quant_status_str.restype = ctypes.c_char_p
+    lib.glu_quant_abi_version.argtypes = []
+    lib.glu_quant_abi_version.restype = ctypes.c_int
+    return lib
+
+
+_handle = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _handle
+    if _handle is None:
+        _handle = _load()
+    return _handle
+
+
+# ---- the C entry points, same names -----------------------------------------
+
+def glu_quant_fwd(args: GluQuantFwdArgs, stream: int | None) -> int:
+    return _lib().glu_quant_fwd(ctypes.byref(args), stream)
+
+
+def glu_quant_bwd(args: GluQuantBwdArgs, stream: int | None) -> int:
+    return _lib().glu_quant_bwd(ctypes.byref(args), stream)
+
+
+def glu_quant_fwd_sizes(args: GluQuantFwdArgs) -> tuple[int, tuple[int, int, int, int]]:
+    s = (ctypes.c_size_t * 4)()
+    st = _lib().glu_quant_fwd_sizes(ctypes.byref(args), s)
+    return st, tuple(s)
+
+
+def glu_quant_bwd_sizes(args: GluQuantBwdArgs) -> tuple[int, tuple[int, int, int, int]]:
+    s = (ctypes.c_size_t * 4)()
+    st = _lib().glu_quant_bwd_sizes(ctypes.byref(args), s)
+    return st, tuple(s)
+
+
+def glu_quant_status_str(status: int) -> str:
+    return _lib().glu_quant_status_str(status).decode()
+
+
+def glu_quant_abi_version() -> int:
+    return _lib().glu_quant_abi_version()
+
+
+# ---- tensor conveniences ------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(device):
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _out_tensors(fmt, mode, M, W, device):
+    import torch
+    u8 = torch.uint8
+    e = torch.empty
+    if fmt == FMT_MXFP8:
+        return {"q_row": e((M, W), dtype=u8, device=device) if mode & MODE_ROW else None,
+                "s_row": e((M, W // 32), dtype=u8, device=device) if mode & MODE_ROW else None,
+                "q_col": e((W, M), dtype=u8, device=device) if mode & MODE_COL else None,
+                "s_col": e((W, M // 32), dtype=u8, device=device) if mode & MODE_COL else None,
+                "out": None}
+    if fmt == FMT_NVFP4:
+        rp, cp = -(-M // 128) * 128, -(-W // 64) * 4
+        return {"q_row": e((M, W // 2), dtype=u8, device=device),
+                "s_row": e((rp * cp,), dtype=u8, device=device),
+                "q_col": None, "s_col": None, "out": None}
+    dt = torch.bfloat16 if fmt == FMT_BF16 else torch.float32
+    return {"q_row": None, "s_row": None, "q_col": None, "s_col": None,
+            "out": e((M, W), dtype=dt, device=device)}
+
+
+def _check_input(t, name):
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def fwd(gate, up=None, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
+        layout=LAYOUT_SPLIT, N=None, out=None, stream=None) -> dict:
+    """Forward.  ``gate``/``up``: bf16 [M, N] (split) or ``gate`` = X [M, 2N]
+    (interleaved, ``up`` None).  Returns the output dict (q_row, s_row,
+    q_col, s_col, out); disabled outputs are None.  Raises GluQuantError on a
+    nonzero status (nothing was launched then)."""
+    _check_input(gate, "gate")
+    if up is not None:
+        _check_input(up, "up")
+        if up.stride(0) != gate.stride(0):
+            raise ValueError("gate and up must share the row stride")
+    M = gate.shape[0]
+    if N is None:
+        N = gate.shape[1] if layout == LAYOUT_SPLIT else gate.shape[1] // 2
+    o = out if out is not None else _out_tensors(fmt, mode, M, N, gate.device)
+    a = GluQuantFwdArgs(act, fmt, mode, layout, M, N, gate.stride(0), _ptr(gate), _ptr(up),
+                        _ptr(o["q_row"]), _ptr(o["s_row"]), _ptr(o["q_col"]), _ptr(o["s_col"]),
+                        _ptr(o["out"]))
+    st = glu_quant_fwd(a, stream if stream is not None else _stream_handle(gate.device))
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_fwd")
+    return o
+
+
+def bwd(gate, up, dy, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
+        layout=LAYOUT_SPLIT, N=None, out=None, stream=None) -> dict:
+    """Backward: outputs of the logical [M, 2N] matrix [dGate | dUp]."""
+    _check_input(gate, "gate")
+    _check_input(dy, "dy")
+    if up is not None:
+        _check_input(up, "up")
+        if up.stride(0) != gate.stride(0):
+            raise ValueError("gate and up must share the row stride")
+    M = gate.shape[0]
+    if N is None:
+        N = gate.shape[1] if layout == LAYOUT_SPLIT else gate.shape[1] // 2
+    o = out if out is not None else _out_tensors(fmt, mode, M, 2 * N, gate.device)
+    a = GluQuantBwdArgs(act, fmt, mode, layout, M, N, gate.stride(0), dy.stride(0), _ptr(gate),
+                        _ptr(up), _ptr(dy), _ptr(o["q_row"]), _ptr(o["s_row"]),
+                        _ptr(o["q_col"]), _ptr(o["s_col"]), _ptr(o["out"]))
+    st = glu_quant_bwd(a, stream if stream is not None else _stream_handle(gate.device))
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_bwd")
+    return o

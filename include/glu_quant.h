@@ -1,0 +1,174 @@
+/*
+ * glu_quant — fused gated-GLU activation + block-scaled quantisation for
+ * NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * The operation (forward):
+ *   h[i][j] = act(gate[i][j]) * up[i][j], computed in fp32 and never stored
+ *   in bf16, then emitted as
+ *     - MXFP8: E4M3 codes with E8M0 "RCEIL" scales, rowwise (1x32 blocks
+ *       along a row), colwise (32x1 blocks down a column) or both from a
+ *       single read of gate/up ("Add swiglu + MXFP8 fused CuTe DSL kernel",
+ *       Summary and API);
+ *     - NVFP4: packed E2M1 codes with one E4M3 scale per 16 elements, global
+ *       scale 1, scales in the 128x4 layout ("feat(phyai-kernel): add Thor
+ *       NVFP4 GeGLU kernel for pi0.5", Supported contract);
+ *     - BF16 or FP32: the unquantised activation ("perf: tile wide GeGLU rows
+ *       on SM103", Summary; FP32 is the checking mode).
+ *   act is SiLU (x * sigmoid(x)) or GELU with the tanh approximation
+ *   (0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))).
+ * The operation (backward), "Add swiglu + MXFP8 fused CuTe DSL kernel", API:
+ *   dGate = dY * up * act'(gate),  dUp = dY * act(gate), emitted as one
+ *   logical [M, 2N] matrix [dGate | dUp] in the same formats.
+ *
+ * Numerics: h (and dGate/dUp) equal act evaluated exactly and rounded once
+ * to fp32; E8M0 scale e = ceil(log2(amax/448)) clamped to [-127, 127]
+ * (byte e + 127, amax = 0 -> 0); codes are round-to-nearest-even,
+ * saturating, sign of zero kept.  NVFP4 scale = E4M3(amax/6), codes =
+ * E2M1(h / scale); a scale that rounds to 0 gives sign-kept zero codes.  A
+ * block holding a NaN or an Inf gets scale 0xFF and codes 0x7F (MXFP8) or
+ * scale 0x7F and codes 0 (NVFP4).
+ *
+ * Memory: every pointer is a DEVICE pointer owned by the caller.  The
+ * library never allocates, frees or synchronises, and never changes the
+ * current device; it launches on `stream` only (a cudaStream_t; NULL is the
+ * legacy default stream), so calls can be captured in a CUDA graph.  The
+ * inputs are read and the outputs fully overwritten; outputs must not alias
+ * inputs.
+ *
+ * Errors: every argument is checked before anything is launched.  A nonzero
+ * return means nothing was launched and nothing was written (fail closed; no
+ * fallback path exists).  GLU_ELAUNCH reports a CUDA error returned by the
+ * launch itself.
+ */
+#ifndef GLU_QUANT_H
+#define GLU_QUANT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GLU_QUANT_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define GLU_API __attribute__((visibility("default")))
+#else
+#define GLU_API
+#endif
+
+/* ---- status codes --------------------------------------------------- */
+#define GLU_OK 0
+#define GLU_EINVAL (-1)  /* NULL required pointer, bad enum, M or N <= 0,
+                            unsupported fmt x mode x direction, non-NULL
+                            pointer for a disabled output               */
+#define GLU_ESHAPE (-2)  /* N % 32 != 0 (MXFP8), M % 32 != 0 (COL),
+                            N % 16 != 0 (NVFP4), ld smaller than the row,
+                            size overflow                                 */
+#define GLU_EALIGN (-3)  /* a pointer not 16-byte aligned, or an ld not a
+                            multiple of 8 elements                        */
+#define GLU_EDEVICE (-4) /* no CUDA device, or the current device is not
+                            compute capability 10.3 (GB300)               */
+#define GLU_ELAUNCH (-5) /* the CUDA launch returned an error            */
+
+/* ---- enums ---------------------------------------------------------- */
+enum glu_act { GLU_ACT_SILU = 0, GLU_ACT_GELU_TANH = 1 };
+enum glu_fmt {
+  GLU_FMT_MXFP8_E4M3 = 0, /* E4M3 codes + E8M0 scales (row/col/both)      */
+  GLU_FMT_NVFP4_E2M1 = 1, /* packed E2M1 + E4M3 scales, 128x4 (row only)  */
+  GLU_FMT_BF16 = 2,       /* unquantised bf16 output (row only)          */
+  GLU_FMT_FP32 = 3        /* unquantised fp32 output (row only)          */
+};
+enum glu_mode { GLU_MODE_ROW = 1, GLU_MODE_COL = 2, GLU_MODE_BOTH = 3 };
+enum glu_layout {
+  GLU_LAYOUT_SPLIT = 0,      /* gate and up are two [M, N] matrices with row
+                                stride ld_in (a packed [gate | up] matrix is
+                                up = gate + N, ld_in = 2N)                 */
+  GLU_LAYOUT_INTERLEAVED = 1 /* one [M, 2N] matrix X, gate_j = X[:, 2j],
+                                up_j = X[:, 2j+1]; `up` must be NULL       */
+};
+
+/* ---- forward ---------------------------------------------------------
+ * Inputs (bf16, row-major, row stride ld_in elements):
+ *   SPLIT:       gate [M, N], up [M, N], ld_in >= N
+ *   INTERLEAVED: gate = X [M, 2N], up = NULL, ld_in >= 2N
+ * Outputs (uint8 unless stated), NULL exactly when not produced:
+ *   MXFP8, mode & ROW:  q_row [M, N] codes, s_row [M, N/32] scales
+ *   MXFP8, mode & COL:  q_col [N, M] codes (column j's rows are contiguous),
+ *                       s_col [N, M/32] scales
+ *   NVFP4 (ROW):        q_row [M, N/2] packed codes (element 2i in the low
+ *                       nibble), s_row the 128x4-layout E4M3 scales,
+ *                       ceil(M/128)*128 * ceil(N/64)*4 bytes; padding = 0
+ *   BF16 / FP32 (ROW):  out [M, N] bf16 / fp32
+ * Alignment: every pointer 16-byte aligned; ld_in a multiple of 8.
+ */
+typedef struct glu_quant_fwd_args {
+  int32_t act;    /* enum glu_act    */
+  int32_t fmt;    /* enum glu_fmt    */
+  int32_t mode;   /* enum glu_mode   */
+  int32_t layout; /* enum glu_layout */
+  int64_t M, N;   /* rows; output columns per operand */
+  int64_t ld_in;  /* input row stride, elements */
+  const void* gate;
+  const void* up;
+  void* q_row;
+  void* s_row;
+  void* q_col;
+  void* s_col;
+  void* out;
+} glu_quant_fwd_args;
+
+/* ---- backward --------------------------------------------------------
+ * As forward, plus dy [M, N] bf16 with row stride ld_dy (>= N, multiple of
+ * 8).  The output is the logical matrix [dGate | dUp] of shape [M, 2N]:
+ *   MXFP8 ROW: q_row [M, 2N], s_row [M, 2N/32]
+ *   MXFP8 COL: q_col [2N, M], s_col [2N, M/32]
+ *   BF16/FP32: out [M, 2N]
+ * NVFP4 backward is not provided (GLU_EINVAL).
+ */
+typedef struct glu_quant_bwd_args {
+  int32_t act, fmt, mode, layout;
+  int64_t M, N;
+  int64_t ld_in;
+  int64_t ld_dy;
+  const void* gate;
+  const void* up;
+  const void* dy;
+  void* q_row;
+  void* s_row;
+  void* q_col;
+  void* s_col;
+  void* out;
+} glu_quant_bwd_args;
+
+/* Forward: validate, then launch the fused kernel on `stream`.
+ * "Add swiglu + MXFP8 fused CuTe DSL kernel", Summary/API (MXFP8, SiLU);
+ * "feat(phyai-kernel): add Thor NVFP4 GeGLU kernel", Supported contract
+ * (NVFP4, GeGLU, interleaved); "perf: tile wide GeGLU rows on SM103",
+ * Summary (bf16 GeGLU).  Returns GLU_OK or a negative status. */
+GLU_API int glu_quant_fwd(const glu_quant_fwd_args* args, void* stream);
+
+/* Backward: dGate = dY*up*act'(gate), dUp = dY*act(gate), quantised like
+ * the forward ("Add swiglu + MXFP8 fused CuTe DSL kernel", API: backward
+ * returns concatenated [dGate | dUp]).  Returns GLU_OK or a negative
+ * status. */
+GLU_API int glu_quant_bwd(const glu_quant_bwd_args* args, void* stream);
+
+/* Byte sizes of the four outputs the arguments describe, in the order
+ * q_row, s_row, q_col, s_col (for BF16/FP32, sizes[0] is the `out` size and
+ * the rest are 0; disabled outputs are 0).  Checks the arguments like the
+ * launch does (pointers are not looked at).  Touches no device. */
+GLU_API int glu_quant_fwd_sizes(const glu_quant_fwd_args* args, size_t sizes[4]);
+GLU_API int glu_quant_bwd_sizes(const glu_quant_bwd_args* args, size_t sizes[4]);
+
+/* Static text for a status code. */
+GLU_API const char* glu_quant_status_str(int status);
+
+/* GLU_QUANT_ABI_VERSION of the built library. */
+GLU_API int glu_quant_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GLU_QUANT_H */

@@ -1,0 +1,152 @@
+"""Comparison of the CUDA path with the CPU oracle under the stated rules.
+
+Rules (the target's correctness statement):
+  * scales are bit-exact;
+  * codes are bit-exact, except where the oracle's fp32 pre-quant value lies
+    within 2 fp32 ulps of a code rounding boundary; there one code step (same
+    sign, adjacent magnitude) is allowed, and such elements are counted;
+  * unquantised fp32 output: max relative error 1e-5 against the oracle;
+    bf16 output: equal, except within 2 fp32 ulps of a bf16 midpoint (one
+    bf16 step allowed, counted).
+Expected values always come from ``oracle`` on host copies of the very same
+input bytes.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+
+WINDOW_ULPS = 2
+
+
+class Stats(dict):
+    def add(self, k, v):
+        self[k] = self.get(k, 0) + int(v)
+
+
+def _adjacent_e4m3(a, b):
+    return ((a & 0x80) == (b & 0x80)) & (np.abs((a & 0x7F).astype(np.int32) - (b & 0x7F).astype(np.int32)) == 1)
+
+
+def _adjacent_e2m1(a, b):
+    return ((a & 0x8) == (b & 0x8)) & (np.abs((a & 0x7).astype(np.int32) - (b & 0x7).astype(np.int32)) == 1)
+
+
+def check_codes(q_gpu, q_ref, v_ref, fmt, stats: Stats, what: str):
+    """Compare code arrays (unpacked, one code per element)."""
+    bad = q_gpu != q_ref
+    n = int(bad.sum())
+    stats.add(f"{what}.elements", q_ref.size)
+    if n == 0:
+        return
+    idx = np.nonzero(bad.ravel())[0]
+    g, r, v = q_gpu.ravel()[idx], q_ref.ravel()[idx], v_ref.ravel()[idx]
+    near = O.boundary_ulps(fmt, v) <= WINDOW_ULPS
+    adj = _adjacent_e4m3(g, r) if fmt == O.MXFP8 else _adjacent_e2m1(g, r)
+    ok = near & adj
+    stats.add(f"{what}.window_mismatch", ok.sum())
+    if not ok.all():
+        j = np.nonzero(~ok)[0][0]
+        raise AssertionError(
+            f"{what}: {int((~ok).sum())} code mismatches outside the 2-ulp window "
+            f"(first: gpu {g[j]:#04x} ref {r[j]:#04x} v {v[j]!r}); total mismatches {n}")
+
+
+def check_scales(s_gpu, s_ref, stats: Stats, what: str):
+    stats.add(f"{what}.scales", s_ref.size)
+    bad = s_gpu != s_ref
+    if bad.any():
+        i = np.nonzero(bad.ravel())[0][0]
+        raise AssertionError(f"{what}: {int(bad.sum())} scale mismatches "
+                             f"(first at flat {i}: gpu {s_gpu.ravel()[i]} ref {s_ref.ravel()[i]})")
+
+
+def mx_prequant_row(h, s_row):
+    """v = h * 2^-e for rowwise blocks (exact in fp32)."""
+    e = np.repeat(s_row.astype(np.int32), 32, axis=1) - 127
+    return (h.astype(np.float64) * np.exp2(-e.astype(np.float64))).astype(np.float32)
+
+
+def mx_prequant_col(h, s_col):
+    """v in the [W, M] colwise layout."""
+    e = np.repeat(s_col.astype(np.int32), 32, axis=1) - 127
+    return (h.T.astype(np.float64) * np.exp2(-e.astype(np.float64))).astype(np.float32)
+
+
+def check_mx(gpu: dict, ref: dict, mode: int, stats: Stats, what: str):
+    h = ref["h"]
+    if mode & O.ROW:
+        check_scales(gpu["s_row"], ref["s_row"], stats, what + ".row")
+        check_codes(gpu["q_row"], ref["q_row"], mx_prequant_row(h, ref["s_row"]), O.MXFP8, stats,
+                    what + ".row")
+    if mode & O.COL:
+        check_scales(gpu["s_col"], ref["s_col"], stats, what + ".col")
+        check_codes(gpu["q_col"], ref["q_col"], mx_prequant_col(h, ref["s_col"]), O.MXFP8, stats,
+                    what + ".col")
+
+
+def unswizzle(s_flat, M, N):
+    """128x4 layout -> plain [M, N/16] scale matrix (padding dropped)."""
+    C = N // 16
+    cp = -(-C // 4) * 4
+    r = np.arange(M)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * (cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    return s_flat[off]
+
+
+def check_nvfp4(gpu: dict, ref: dict, M: int, N: int, stats: Stats, what: str):
+    # the whole padded scale buffer (padding must be zero on both sides)
+    check_scales(gpu["s_row"], ref["s_nvfp4"], stats, what + ".scale_buffer")
+    q_g, q_r = gpu["q_row"], ref["out"]
+    unpack = lambda q: np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[0], -1)
+    s = O.e4m3_decode(unswizzle(ref["s_nvfp4"], M, N)).astype(np.float32)
+    sv = np.repeat(s, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(sv == 0, 0, ref["h"] / np.where(sv == 0, 1, sv)).astype(np.float32)
+    check_codes(unpack(q_g), unpack(q_r), v, O.NVFP4, stats, what + ".codes")
+
+
+def check_plain(gpu_out, ref: dict, fmt: int, stats: Stats, what: str):
+    h = ref["h"]
+    if fmt == O.FP32:
+        g = gpu_out.astype(np.float64)
+        r = h.astype(np.float64)
+        fin = np.isfinite(r)
+        assert np.array_equal(np.isnan(gpu_out), np.isnan(h)), what + ": NaN pattern differs"
+        assert np.array_equal(g[~fin & ~np.isnan(r)], r[~fin & ~np.isnan(r)]), what + ": Inf differs"
+        rel = np.abs(g[fin] - r[fin]) / np.maximum(np.abs(r[fin]), np.finfo(np.float32).tiny)
+        mx = float(rel.max()) if rel.size else 0.0
+        stats["%s.max_rel" % what] = max(stats.get("%s.max_rel" % what, 0.0), mx)
+        stats.add(what + ".ulp_diff", (gpu_out != h).sum())
+        assert mx <= 1e-5, f"{what}: max relative error {mx}"
+    else:
+        ref_b = ref["out"]
+        isnan = lambda b: ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+        assert np.array_equal(isnan(gpu_out), isnan(ref_b)), what + ": bf16 NaN pattern differs"
+        # NaN payloads are not part of the contract: any NaN equals any NaN
+        bad = (gpu_out != ref_b) & ~isnan(ref_b)
+        stats.add(what + ".elements", ref_b.size)
+        if bad.any():
+            hv = h[bad]
+            near = O.boundary_ulps(O.BF16, hv) <= WINDOW_ULPS
+            step = np.abs(gpu_out[bad].astype(np.int32) - ref_b[bad].astype(np.int32)) == 1
+            ok = near & step
+            stats.add(what + ".window_mismatch", ok.sum())
+            assert ok.all(), f"{what}: {int((~ok).sum())} bf16 mismatches outside the window"
+
+
+def host_bits(t):
+    """bf16 tensor -> host uint16 numpy array."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host(t):
+    import torch
+    if t is None:
+        return None
+    if t.dtype == torch.bfloat16:
+        return host_bits(t)
+    return t.detach().cpu().numpy()

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function ``include/glu_quant.h``
+declares, and reject every bad argument with the documented status before
+touching a device (argument checks run first, so on a machine without a GPU
+a well-formed call reports GLU_EDEVICE and a malformed one its own error).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp4_quant_gb300 as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "glu_quant.h")
+P = 1 << 12  # a 16-byte aligned placeholder address (never dereferenced)
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"GLU_API\s+[\w\s\*]+?\b(glu_quant_\w+)\s*\(", txt)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) == 6, names
+    lib = ctypes.CDLL(G.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings():
+    assert G.glu_quant_abi_version() == 1
+    for st in (0, -1, -2, -3, -4, -5):
+        assert G.glu_quant_status_str(st) != "unknown status"
+    assert G.glu_quant_status_str(7) == "unknown status"
+
+
+def fwd_args(**kw):
+    a = dict(act=0, fmt=0, mode=1, layout=0, M=64, N=256, ld_in=256, gate=P, up=P,
+             q_row=P, s_row=P, q_col=None, s_col=None, out=None)
+    a.update(kw)
+    return G.GluQuantFwdArgs(**a)
+
+
+def bwd_args(**kw):
+    a = dict(act=0, fmt=0, mode=1, layout=0, M=64, N=256, ld_in=256, ld_dy=256, gate=P, up=P,
+             dy=P, q_row=P, s_row=P, q_col=None, s_col=None, out=None)
+    a.update(kw)
+    return G.GluQuantBwdArgs(**a)
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(act=2), G.GLU_EINVAL),
+    (dict(fmt=4), G.GLU_EINVAL),
+    (dict(mode=0), G.GLU_EINVAL),
+    (dict(mode=4), G.GLU_EINVAL),
+    (dict(layout=2), G.GLU_EINVAL),
+    (dict(M=0), G.GLU_EINVAL),
+    (dict(N=-32), G.GLU_EINVAL),
+    (dict(gate=None), G.GLU_EINVAL),
+    (dict(up=None), G.GLU_EINVAL),                         # split needs up
+    (dict(layout=1, ld_in=512), G.GLU_EINVAL),              # interleaved must not pass up
+    (dict(q_row=None), G.GLU_EINVAL),                      # enabled output missing
+    (dict(q_col=P), G.GLU_EINVAL),                         # disabled output given
+    (dict(out=P), G.GLU_EINVAL),
+    (dict(fmt=1, mode=3), G.GLU_EINVAL),                   # NVFP4 is row only
+    (dict(fmt=2, q_row=None, s_row=None, out=P, mode=2), G.GLU_EINVAL),
+    (dict(N=240, ld_in=240), G.GLU_ESHAPE),                # N % 32 for MXFP8
+    (dict(mode=2, q_row=None, s_row=None, q_col=P, s_col=P, M=40), G.GLU_ESHAPE),
+    (dict(fmt=1, N=264, ld_in=264), G.GLU_ESHAPE),         # N % 16 for NVFP4
+    (dict(ld_in=128), G.GLU_ESHAPE),                       # ld < N
+    (dict(layout=1, up=None, ld_in=256), G.GLU_ESHAPE),    # interleaved ld < 2N
+    (dict(M=1 << 62), G.GLU_ESHAPE),                       # size overflow
+    (dict(ld_in=260), G.GLU_EALIGN),                       # ld % 8
+    (dict(gate=P + 2), G.GLU_EALIGN),
+    (dict(s_row=P + 8), G.GLU_EALIGN),
+])
+def test_fwd_rejections(kw, status):
+    assert G.glu_quant_fwd(fwd_args(**kw), None) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dy=None), G.GLU_EINVAL),
+    (dict(fmt=1), G.GLU_EINVAL),                           # no NVFP4 backward
+    (dict(ld_dy=128), G.GLU_ESHAPE),
+    (dict(ld_dy=260), G.GLU_EALIGN),
+    (dict(dy=P + 4), G.GLU_EALIGN),
+    (dict(N=240, ld_in=240, ld_dy=240), G.GLU_ESHAPE),     # N % 32 (not 2N)
+])
+def test_bwd_rejections(kw, status):
+    assert G.glu_quant_bwd(bwd_args(**kw), None) == status
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="checks the no-device status")
+def test_valid_call_without_device_reports_edevice():
+    assert G.glu_quant_fwd(fwd_args(), None) == G.GLU_EDEVICE
+    assert G.glu_quant_bwd(bwd_args(), None) == G.GLU_EDEVICE
+
+
+def test_sizes():
+    st, s = G.glu_quant_fwd_sizes(fwd_args(mode=3, q_col=P, s_col=P, M=4096, N=7168, ld_in=7168))
+    assert st == 0 and s == (4096 * 7168, 4096 * 224, 7168 * 4096, 7168 * 128)
+    st, s = G.glu_quant_bwd_sizes(bwd_args(mode=2, M=4096, N=7168, ld_in=7168, ld_dy=7168))
+    assert st == 0 and s == (0, 0, 14336 * 4096, 14336 * 128)
+    st, s = G.glu_quant_fwd_sizes(fwd_args(fmt=1, layout=1, M=784, N=16384, ld_in=32768))
+    assert st == 0 and s == (784 * 8192, 896 * 1024, 0, 0)
+    st, s = G.glu_quant_fwd_sizes(fwd_args(fmt=2, M=8, N=1001, ld_in=1008))
+    assert st == 0 and s == (8 * 1001 * 2, 0, 0, 0)
+    st, _ = G.glu_quant_fwd_sizes(fwd_args(N=250, ld_in=256))
+    assert st == G.GLU_ESHAPE

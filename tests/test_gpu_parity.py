@@ -1,0 +1,407 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every case draws seeded synthetic inputs on the GPU, runs the kernels through
+``glu_quant_fwd`` / ``glu_quant_bwd``, copies inputs and outputs to the host
+and checks them against ``oracle`` run on the very same input bytes, under
+the rules in ``parity_util``.  Small cases span several tiles with ragged
+row and column tails; the workload cases run at full size (the largest one
+on sampled 32-row groups, in the launch configuration the bench times).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from parity_util import Stats, check_mx, check_nvfp4, check_plain, host, host_bits
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import fp4_quant_gb300 as G  # noqa: E402  (raises if the library is missing)
+
+DEV = torch.device("cuda:0")
+ACTS = [(G.ACT_SILU, O.SILU), (G.ACT_GELU_TANH, O.GELU_TANH)]
+MODES = [G.MODE_ROW, G.MODE_COL, G.MODE_BOTH]
+
+
+def _randn(M, N, seed, scale=1.0):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    return (torch.randn(M, N, generator=g, device=DEV) * scale).to(torch.bfloat16)
+
+
+def _interleave(g, u):
+    M, N = g.shape
+    return torch.stack([g, u], dim=-1).reshape(M, 2 * N).contiguous()
+
+
+def run_fwd(g, u, act, fmt, mode, layout):
+    """GPU and oracle forward on the same bytes; returns (gpu, ref) dicts."""
+    if layout == G.LAYOUT_SPLIT:
+        out = G.fwd(g, u, act=act, fmt=fmt, mode=mode, layout=layout)
+        torch.cuda.synchronize()
+        ref = O.glu_fwd(host_bits(g), host_bits(u), act=act, fmt=fmt, mode=mode,
+                        layout=O.SPLIT, want_h=True)
+    else:
+        x = _interleave(g, u)
+        out = G.fwd(x, None, act=act, fmt=fmt, mode=mode, layout=layout)
+        torch.cuda.synchronize()
+        ref = O.glu_fwd(host_bits(x), act=act, fmt=fmt, mode=mode, layout=O.INTERLEAVED,
+                        want_h=True)
+    return {k: host(v) for k, v in out.items()}, ref
+
+
+def run_bwd(g, u, d, act, fmt, mode, layout):
+    if layout == G.LAYOUT_SPLIT:
+        out = G.bwd(g, u, d, act=act, fmt=fmt, mode=mode, layout=layout)
+        torch.cuda.synchronize()
+        ref = O.glu_bwd(host_bits(g), host_bits(u), host_bits(d), act=act, fmt=fmt, mode=mode,
+                        layout=O.SPLIT, want_h=True)
+    else:
+        x = _interleave(g, u)
+        out = G.bwd(x, None, d, act=act, fmt=fmt, mode=mode, layout=layout)
+        torch.cuda.synchronize()
+        ref = O.glu_bwd(host_bits(x), None, host_bits(d), act=act, fmt=fmt, mode=mode,
+                        layout=O.INTERLEAVED, want_h=True)
+    return {k: host(v) for k, v in out.items()}, ref
+
+
+def check(gpu, ref, fmt, mode, M, W, what):
+    st = Stats()
+    if fmt == G.FMT_MXFP8:
+        check_mx(gpu, ref, mode, st, what)
+    elif fmt == G.FMT_NVFP4:
+        check_nvfp4(gpu, ref, M, W, st, what)
+    else:
+        check_plain(gpu["out"], ref, fmt, st, what)
+    return st
+
+
+# ------------------------------------------------------------ small, ragged --
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+def test_mx_fwd_small(act, mode, layout):
+    M = 200 if mode == G.MODE_ROW else 160   # ragged row tile for ROW
+    N = 800                                   # 3 full 256-column tiles + 32
+    g, u = _randn(M, N, 11, 2.0), _randn(M, N, 12)
+    gpu, ref = run_fwd(g, u, act[0], G.FMT_MXFP8, mode, layout)
+    check(gpu, ref, G.FMT_MXFP8, mode, M, N, "fwd")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+def test_mx_bwd_small(act, mode, layout):
+    M = 104 if mode == G.MODE_ROW else 96
+    N = 416                                   # 3 full 128-column tiles + 32
+    g, u, d = _randn(M, N, 21, 2.0), _randn(M, N, 22), _randn(M, N, 23)
+    gpu, ref = run_bwd(g, u, d, act[0], G.FMT_MXFP8, mode, layout)
+    check(gpu, ref, G.FMT_MXFP8, mode, M, 2 * N, "bwd")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+@pytest.mark.parametrize("shape", [(200, 1296), (128, 64), (1, 16)], ids=["ragged", "one_tile", "tiny"])
+def test_nvfp4_small(act, layout, shape):
+    M, N = shape
+    g, u = _randn(M, N, 31, 2.0), _randn(M, N, 32, 2.0)
+    gpu, ref = run_fwd(g, u, act[0], G.FMT_NVFP4, G.MODE_ROW, layout)
+    check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, N, "nvfp4")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("fmt", [G.FMT_BF16, G.FMT_FP32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+@pytest.mark.parametrize("N", [1024, 1001], ids=["vec", "ragged"])
+@pytest.mark.parametrize("bwd", [False, True], ids=["fwd", "bwd"])
+def test_plain_small(act, fmt, layout, N, bwd):
+    M = 67
+    if layout == G.LAYOUT_INTERLEAVED and N % 8:
+        pytest.skip("interleaved rows of 2N elements need ld % 8 == 0")
+    # pad the row stride to a multiple of 8 for the ragged split case
+    ld = -(-N // 8) * 8
+    base_g, base_u, base_d = _randn(M, ld, 41, 2.0), _randn(M, ld, 42), _randn(M, ld, 43)
+    g, u, d = base_g[:, :N], base_u[:, :N], base_d[:, :N]
+    if bwd:
+        if layout == G.LAYOUT_SPLIT:
+            out = G.bwd(g, u, d, act=act[0], fmt=fmt, N=N)
+            torch.cuda.synchronize()
+            ref = O.glu_bwd(host_bits(base_g), host_bits(base_u), host_bits(base_d), act=act[0],
+                            fmt=fmt, N=N, want_h=True)
+        else:
+            x = _interleave(g.contiguous(), u.contiguous())
+            out = G.bwd(x, None, d.contiguous(), act=act[0], fmt=fmt, layout=layout)
+            torch.cuda.synchronize()
+            ref = O.glu_bwd(host_bits(x), None, host_bits(d), act=act[0], fmt=fmt,
+                            layout=O.INTERLEAVED, want_h=True)
+    else:
+        if layout == G.LAYOUT_SPLIT:
+            out = G.fwd(g, u, act=act[0], fmt=fmt, N=N)
+            torch.cuda.synchronize()
+            ref = O.glu_fwd(host_bits(base_g), host_bits(base_u), act=act[0], fmt=fmt, N=N,
+                            want_h=True)
+        else:
+            x = _interleave(g.contiguous(), u.contiguous())
+            out = G.fwd(x, None, act=act[0], fmt=fmt, layout=layout)
+            torch.cuda.synchronize()
+            ref = O.glu_fwd(host_bits(x), act=act[0], fmt=fmt, layout=O.INTERLEAVED, want_h=True)
+    st = Stats()
+    check_plain(host(out["out"]), ref, fmt, st, "plain")
+
+
+# ------------------------------------------------------------- special values --
+
+def _special_inputs(M, N, seed):
+    g, u = _randn(M, N, seed, 2.0), _randn(M, N, seed + 1)
+    gv = torch.tensor([0.0, -0.0, 2.0 ** -30, -(2.0 ** -30), 2.0 ** -130, 64.0, 100.0, -64.0,
+                       -100.0, -200.0, -9.0, -10.0, -11.0, -12.5, -20.0, 1e30, -1e30,
+                       float("inf"), float("-inf"), float("nan"), 60.0, -60.0],
+                      device=DEV).to(torch.bfloat16)
+    uv = torch.tensor([0.0, -0.0, 2.0 ** -120, 1e30, -1e-30, 3.0, float("inf"), 60.0],
+                      device=DEV).to(torch.bfloat16)
+    gen = torch.Generator(device=DEV).manual_seed(seed + 2)
+    mg = torch.randint(0, 8, (M, N), generator=gen, device=DEV) == 0
+    mu = torch.randint(0, 16, (M, N), generator=gen, device=DEV) == 0
+    ig = torch.randint(0, gv.numel(), (M, N), generator=gen, device=DEV)
+    iu = torch.randint(0, uv.numel(), (M, N), generator=gen, device=DEV)
+    g = torch.where(mg, gv[ig], g)
+    u = torch.where(mu, uv[iu], u)
+    # a few clean blocks so the NaN/Inf convention is not the only thing seen
+    g[: M // 2, :64] = _randn(M // 2, 64, seed + 3)
+    u[: M // 2, :64] = _randn(M // 2, 64, seed + 4)
+    return g.contiguous(), u.contiguous()
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
+                         ids=["fp32", "bf16", "mxfp8", "nvfp4"])
+def test_special_values_fwd(act, fmt):
+    M, N = 64, 256
+    g, u = _special_inputs(M, N, 51)
+    mode = G.MODE_BOTH if fmt == G.FMT_MXFP8 else G.MODE_ROW
+    gpu, ref = run_fwd(g, u, act[0], fmt, mode, G.LAYOUT_SPLIT)
+    check(gpu, ref, fmt, mode, M, N, "special")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_MXFP8], ids=["fp32", "mxfp8"])
+def test_special_values_bwd(act, fmt):
+    M, N = 64, 256
+    g, u = _special_inputs(M, N, 61)
+    d = _randn(M, N, 63)
+    d[::7, ::5] = torch.tensor(1e30, device=DEV).to(torch.bfloat16)
+    d[::11, ::3] = 0.0
+    mode = G.MODE_BOTH if fmt == G.FMT_MXFP8 else G.MODE_ROW
+    gpu, ref = run_bwd(g, u, d, act[0], fmt, mode, G.LAYOUT_SPLIT)
+    check(gpu, ref, fmt, mode, M, 2 * N, "special_bwd")
+
+
+def test_exact_activation_blocks_on_gpu():
+    # gate = 32: h = 32 * up exactly; amax at 448 * 2^k, ties, subnormal codes
+    M, N = 32, 64
+    up = torch.zeros(M, N)
+    up[:, 0] = 14.0
+    up[:, 1] = 2.0 ** -14
+    up[:, 2] = 3 * 2.0 ** -15
+    up[:, 3] = 17 * 2.0 ** -9
+    up[:, 4] = -(2.0 ** -16)
+    up[:, 32] = 28.0
+    g = torch.full((M, N), 32.0, device=DEV).to(torch.bfloat16)
+    u = up.to(DEV).to(torch.bfloat16)
+    for act in (G.ACT_SILU, G.ACT_GELU_TANH):
+        gpu, ref = run_fwd(g, u, act, G.FMT_MXFP8, G.MODE_BOTH, G.LAYOUT_SPLIT)
+        assert list(gpu["s_row"][0]) == [127, 128]
+        assert list(gpu["q_row"][0, :5]) == [0x7E, 0x01, 0x02, 0x38, 0x80]
+        check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, N, "exact")
+
+
+def test_nvfp4_codes_near_midpoints():
+    # gate = 32 makes h = 32 * up exactly; with amax = 6 the scale is 1.0 and
+    # v = h, so up values on and next to the E2M1 midpoints probe rounding
+    M, N = 128, 64
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    vals = []
+    for m in mids:
+        for k in (-2, -1, 0, 1, 2):
+            vals.append(m * (1 + k * 2.0 ** -7))  # neighbours on the bf16 grid
+    row = torch.zeros(N)
+    row[0] = 6.0
+    row[1: 1 + len(vals)] = torch.tensor(vals)
+    h = row.repeat(M, 1)
+    h[1::2] = -h[1::2]
+    g = torch.full((M, N), 32.0, device=DEV).to(torch.bfloat16)
+    u = (h / 32).to(DEV).to(torch.bfloat16)
+    for layout in (G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED):
+        gpu, ref = run_fwd(g, u, G.ACT_SILU, G.FMT_NVFP4, G.MODE_ROW, layout)
+        st = check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, N, "mid")
+        assert np.array_equal(gpu["q_row"], ref["out"])
+        assert st.get("mid.codes.window_mismatch", 0) == 0
+
+
+# ---------------------------------------------------------------- workloads --
+
+def test_workload_swiglu_128():
+    sp = synth.spec("swiglu_128")
+    x = synth.make(sp, DEV)
+    gpu, ref = run_fwd(x["gate"], x["up"], G.ACT_SILU, G.FMT_MXFP8, G.MODE_ROW, G.LAYOUT_SPLIT)
+    assert gpu["q_row"].shape == (128, 128) and gpu["s_row"].shape == (128, 4)
+    check(gpu, ref, G.FMT_MXFP8, G.MODE_ROW, 128, 128, "swiglu_128")
+
+
+@pytest.fixture(scope="module")
+def swiglu_4096():
+    return synth.make(synth.spec("swiglu_4096"), DEV, with_dy=True)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_workload_swiglu_4096(swiglu_4096, mode, direction):
+    x = swiglu_4096
+    if direction == "fwd":
+        gpu, ref = run_fwd(x["gate"], x["up"], G.ACT_SILU, G.FMT_MXFP8, mode, G.LAYOUT_SPLIT)
+        check(gpu, ref, G.FMT_MXFP8, mode, 4096, 7168, "swiglu_4096")
+    else:
+        gpu, ref = run_bwd(x["gate"], x["up"], x["dy"], G.ACT_SILU, G.FMT_MXFP8, mode,
+                           G.LAYOUT_SPLIT)
+        check(gpu, ref, G.FMT_MXFP8, mode, 4096, 2 * 7168, "swiglu_4096_bwd")
+
+
+@pytest.mark.parametrize("N", [11008, 14336, 18944, 29568])
+@pytest.mark.parametrize("fmt", [G.FMT_MXFP8, G.FMT_BF16], ids=["mxfp8", "bf16"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_workload_geglu_8192(N, fmt, direction):
+    x = synth.make(synth.spec("geglu_8192", N=N), DEV, with_dy=True)
+    if direction == "fwd":
+        gpu, ref = run_fwd(x["gate"], x["up"], G.ACT_GELU_TANH, fmt, G.MODE_ROW, G.LAYOUT_SPLIT)
+        check(gpu, ref, fmt, G.MODE_ROW, 8192, N, "geglu_8192")
+    else:
+        gpu, ref = run_bwd(x["gate"], x["up"], x["dy"], G.ACT_GELU_TANH, fmt, G.MODE_ROW,
+                           G.LAYOUT_SPLIT)
+        check(gpu, ref, fmt, G.MODE_ROW, 8192, 2 * N, "geglu_8192_bwd")
+
+
+@pytest.mark.parametrize("M", [784, 968])
+def test_workload_geglu_nvfp4(M):
+    sp = synth.spec("geglu_nvfp4", M=M)
+    x = synth.make(sp, DEV)["x"]
+    out = G.fwd(x, None, act=G.ACT_GELU_TANH, fmt=G.FMT_NVFP4, layout=G.LAYOUT_INTERLEAVED)
+    torch.cuda.synchronize()
+    gpu = {k: host(v) for k, v in out.items()}
+    assert gpu["q_row"].shape == (M, 8192)
+    assert gpu["s_row"].size == (-(-M // 128) * 128) * 1024
+    ref = O.glu_fwd(host_bits(x), act=O.GELU_TANH, fmt=O.NVFP4, layout=O.INTERLEAVED,
+                    want_h=True)
+    check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, 16384, "geglu_nvfp4")
+
+
+@pytest.fixture(scope="module")
+def swiglu_131072():
+    return synth.make(synth.spec("swiglu_131072"), DEV, with_dy=True)
+
+
+def _sample_groups(M, n=24):
+    groups = sorted(set([0, M // 32 - 1] + list(np.linspace(1, M // 32 - 2, n).astype(int))))
+    return [int(g) * 32 for g in groups]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_workload_swiglu_131072_sampled(swiglu_131072, mode, direction):
+    """Full-size launch; the oracle checks sampled 32-row groups (every
+    output block of those rows, rowwise and colwise)."""
+    x = swiglu_131072
+    M, N = x["gate"].shape
+    W = N if direction == "fwd" else 2 * N
+    if direction == "fwd":
+        out = G.fwd(x["gate"], x["up"], act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode)
+    else:
+        out = G.bwd(x["gate"], x["up"], x["dy"], act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode)
+    torch.cuda.synchronize()
+    st = Stats()
+    for r0 in _sample_groups(M):
+        sl = slice(r0, r0 + 32)
+        if direction == "fwd":
+            ref = O.glu_fwd(host_bits(x["gate"][sl]), host_bits(x["up"][sl]), act=O.SILU,
+                            fmt=O.MXFP8, mode=mode, want_h=True)
+        else:
+            ref = O.glu_bwd(host_bits(x["gate"][sl]), host_bits(x["up"][sl]),
+                            host_bits(x["dy"][sl]), act=O.SILU, fmt=O.MXFP8, mode=mode,
+                            want_h=True)
+        gpu = {}
+        if mode & G.MODE_ROW:
+            gpu["q_row"] = host(out["q_row"][sl])
+            gpu["s_row"] = host(out["s_row"][sl])
+        if mode & G.MODE_COL:
+            gpu["q_col"] = host(out["q_col"][:, sl])
+            gpu["s_col"] = host(out["s_col"][:, r0 // 32: r0 // 32 + 1])
+        check_mx(gpu, ref, mode, st, "swiglu_131072")
+    assert st["swiglu_131072." + ("row" if mode & G.MODE_ROW else "col") + ".elements"] > 0
+
+
+# -------------------------------------------------- host-visible behaviour --
+
+def test_rejected_call_writes_nothing():
+    g, u = _randn(64, 256, 71), _randn(64, 256, 72)
+    q = torch.full((64, 256), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((64, 8), 0xAB, dtype=torch.uint8, device=DEV)
+    a = G.GluQuantFwdArgs(G.ACT_SILU, G.FMT_MXFP8, G.MODE_ROW, G.LAYOUT_SPLIT, 64, 256, 256,
+                          g.data_ptr() + 2, u.data_ptr(), q.data_ptr(), s.data_ptr(), None, None,
+                          None)
+    assert G.glu_quant_fwd(a, torch.cuda.current_stream().cuda_stream) == G.GLU_EALIGN
+    a.gate = g.data_ptr()
+    a.N = 240
+    assert G.glu_quant_fwd(a, torch.cuda.current_stream().cuda_stream) == G.GLU_ESHAPE
+    torch.cuda.synchronize()
+    assert bool((q == 0xAB).all()) and bool((s == 0xAB).all())
+
+
+def test_repeat_calls_and_graph_replay_are_identical():
+    g, u, d = _randn(512, 2048, 81), _randn(512, 2048, 82), _randn(512, 2048, 83)
+    a = G.fwd(g, u, mode=G.MODE_BOTH)
+    b = G.bwd(g, u, d, mode=G.MODE_BOTH)
+    a2 = G.fwd(g, u, mode=G.MODE_BOTH)
+    outs = {k: torch.empty_like(v) for k, v in a.items() if v is not None}
+    outs.update({k: None for k, v in a.items() if v is None})
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        G.fwd(g, u, mode=G.MODE_BOTH, out=outs, stream=s.cuda_stream)  # warm-up on side stream
+        with torch.cuda.graph(graph, stream=s):
+            G.fwd(g, u, mode=G.MODE_BOTH, out=outs, stream=s.cuda_stream)
+    for v in outs.values():
+        if v is not None:
+            v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for k in ("q_row", "s_row", "q_col", "s_col"):
+        assert torch.equal(a[k], a2[k]) and torch.equal(a[k], outs[k]), k
+    b2 = G.bwd(g, u, d, mode=G.MODE_BOTH)
+    for k in ("q_row", "s_row", "q_col", "s_col"):
+        assert torch.equal(b[k], b2[k])
+
+
+def test_row_chunks_equal_full_batch():
+    # batch invariance: each 32-row group depends on its own rows only
+    g, u, d = _randn(256, 1024, 91), _randn(256, 1024, 92), _randn(256, 1024, 93)
+    full = G.bwd(g, u, d, mode=G.MODE_BOTH)
+    top = G.bwd(g[:96], u[:96], d[:96], mode=G.MODE_BOTH)
+    bot = G.bwd(g[96:], u[96:], d[96:], mode=G.MODE_BOTH)
+    assert torch.equal(full["q_row"], torch.cat([top["q_row"], bot["q_row"]]))
+    assert torch.equal(full["q_col"], torch.cat([top["q_col"], bot["q_col"]], dim=1))
+    assert torch.equal(full["s_col"], torch.cat([top["s_col"], bot["s_col"]], dim=1))
+
+
+def test_packed_gate_up_layout():
+    # [gate | up] packed in one [M, 2N] tensor: up = gate + N, ld = 2N
+    M, N = 128, 512
+    gu = _randn(M, 2 * N, 101)
+    g, u = gu[:, :N], gu[:, N:]
+    a = G.fwd(g, u, mode=G.MODE_BOTH)
+    b = G.fwd(g.contiguous(), u.contiguous(), mode=G.MODE_BOTH)
+    for k in ("q_row", "s_row", "q_col", "s_col"):
+        assert torch.equal(a[k], b[k])
