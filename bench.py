@@ -117,12 +117,15 @@ def profiled_traffic(kernel_key: str):
 class Clocks:
     """nvidia-smi sampling during the timed region."""
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, enabled: bool = True):
         self.proc = None
+        self.enabled = enabled
         self.index = index
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -183,8 +186,10 @@ def gpu_arm(args, rank, world, dist):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    sp = synth.spec("swiglu_131072")
+    sp = synth.spec("swiglu_131072", M=args.rows)
     M, N = sp.M, sp.N
+    calls = [c for c in CALLS if f"{c[0]}_{MODE_NAME[c[1]]}" in args.calls.split(",")] \
+        if args.calls else CALLS
     x = synth.make(sp, dev, with_dy=True, seed_offset=rank * 10)
     g, u, d = x["gate"], x["up"], x["dy"]
 
@@ -200,7 +205,7 @@ def gpu_arm(args, rank, world, dist):
             o["s_col"] = torch.empty((W, M // 32), dtype=torch.uint8, device=dev)
         return o
 
-    bufs = {c: outs(*c) for c in CALLS}
+    bufs = {c: outs(*c) for c in calls}
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
@@ -216,21 +221,21 @@ def gpu_arm(args, rank, world, dist):
             dist.barrier()
 
     for _ in range(args.warmup):
-        for c in CALLS:
+        for c in calls:
             call(c)
     torch.cuda.synchronize(dev)
 
     K = args.steps
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in CALLS] for _ in range(K)]
+           for _ in calls] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
-    with Clocks(dev.index) as clk:
+    with Clocks(dev.index, enabled=not args.no_clocks) as clk:
         barrier()
         torch.cuda.synchronize(dev)
         t0.record(stream)
         for k in range(K):
-            for i, c in enumerate(CALLS):
+            for i, c in enumerate(calls):
                 ev[k][i][0].record(stream)
                 call(c)
                 ev[k][i][1].record(stream)
@@ -240,33 +245,34 @@ def gpu_arm(args, rank, world, dist):
         barrier()
     total_ms = t0.elapsed_time(t1)
     per_call_ms = {c: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)]
-                   for i, c in enumerate(CALLS)}
+                   for i, c in enumerate(calls)}
     total_ms = reduce_max(total_ms, dist, dev)
 
-    step_bytes = sum(algo_bytes(dr, m, M, N) for dr, m in CALLS)
+    step_bytes = sum(algo_bytes(dr, m, M, N) for dr, m in calls)
     value = whole_job_gbps(world, step_bytes, K, total_ms)
     peaks = measured_peaks()
     modes = {}
-    for c in CALLS:
+    for c in calls:
         avg = statistics.mean(per_call_ms[c])
         gbps = algo_bytes(c[0], c[1], M, N) / (avg * 1e-3) / 1e9
         modes[f"{c[0]}_{MODE_NAME[c[1]]}"] = {
             "us": round(avg * 1e3, 2), "us_min": round(min(per_call_ms[c]) * 1e3, 2),
             "gbps": round(gbps, 1), "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
             "page_gb200_us": PAGE_GB200_US[c]}
-    dom = max(CALLS, key=lambda c: statistics.mean(per_call_ms[c]))
+    dom = max(calls, key=lambda c: statistics.mean(per_call_ms[c]))
     dom_name = f"{dom[0]}_{MODE_NAME[dom[1]]}"
     dom_gbps = modes[dom_name]["gbps"]
-    traffic = profiled_traffic(f"{dom[0]}_mx_{MODE_NAME[dom[1]]}_131072x8192")
+    traffic = profiled_traffic(f"{dom[0]}_mx_{MODE_NAME[dom[1]]}_{M}x{N}")
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "swiglu_131072x8192_mxfp8_fwd+bwd_row+col+both",
+        "config": {"workload": f"swiglu_{M}x{N}_mxfp8_" + "+".join(
+                       f"{c[0]}_{MODE_NAME[c[1]]}" for c in calls),
                    "M": M, "N": N, "act": "silu", "fmt": "mxfp8_e4m3_e8m0_rceil",
-                   "calls_per_step": len(CALLS), "global_batch_rows": world * M,
+                   "calls_per_step": len(calls), "global_batch_rows": world * M,
                    "parallelism": f"dp{world}" if world > 1 else "single",
                    "l2": "inputs 6 GB >> 129 MB L2; no flush"},
         "modes": modes,
@@ -276,18 +282,19 @@ def gpu_arm(args, rank, world, dist):
                      "algo_bytes_per_launch": algo_bytes(dom[0], dom[1], M, N),
                      "peak_source": peaks["source"]},
         "page_context": {"gb200_same_calls_gbps": round(
-            step_bytes / (sum(PAGE_GB200_US.values()) * 1e-6) / 1e9, 1),
+            sum(algo_bytes(dr, m, M_FULL, N_FULL) for dr, m in CALLS)
+            / (sum(PAGE_GB200_US.values()) * 1e-6) / 1e9, 1),
             "note": "the pages' GB200 per-call times for the same six calls (context, not a target)"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
 
     if not args.no_e2e:
-        res["e2e"] = e2e_leg(args, G, g, u, d, bufs, dev, stream, dist, world, step_bytes)
+        res["e2e"] = e2e_leg(args, G, g, u, d, bufs, calls, dev, stream, dist, world, step_bytes)
     return res
 
 
-def e2e_leg(args, G, g, u, d, bufs, dev, stream, dist, world, step_bytes):
+def e2e_leg(args, G, g, u, d, bufs, calls, dev, stream, dist, world, step_bytes):
     """The same six calls through the public API with host buffers: every
     step copies the inputs host->device from pinned memory and reads every
     call's outputs back, inside the timed region."""
@@ -298,19 +305,19 @@ def e2e_leg(args, G, g, u, d, bufs, dev, stream, dist, world, step_bytes):
     hg.copy_(g)
     hu.copy_(u)
     hd.copy_(d)
-    biggest = max(CALLS, key=lambda c: sum(t.numel() for t in bufs[c].values() if t is not None))
+    biggest = max(calls, key=lambda c: sum(t.numel() for t in bufs[c].values() if t is not None))
     hout = {k: (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) if t is not None else None)
             for k, t in bufs[biggest].items()}
     h2d = sum(t.numel() * t.element_size() for t in (hg, hu, hd))
     d2h = sum(sum(t.numel() * t.element_size() for t in bufs[c].values() if t is not None)
-              for c in CALLS)
+              for c in calls)
     sh = stream.cuda_stream
 
     def step():
         g.copy_(hg, non_blocking=True)
         u.copy_(hu, non_blocking=True)
         d.copy_(hd, non_blocking=True)
-        for c in CALLS:
+        for c in calls:
             direction, mode = c
             if direction == "fwd":
                 G.fwd(g, u, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
@@ -491,9 +498,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--sweep", default=None)
+    ap.add_argument("--rows", type=int, default=M_FULL,
+                    help="rows of the SwiGLU workload (smaller cases for profiling)")
+    ap.add_argument("--calls", default="",
+                    help="comma-separated subset of fwd_row,fwd_col,fwd_both,bwd_row,bwd_col,bwd_both")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -4,34 +4,80 @@
 // once, the bf16 activation tensor is never materialized, and rowwise (1x32),
 // colwise (32x1), or both scales come out of a single pass") and API.
 //
-// Work decomposition (GB300: 152 SMs, 227 KB shared memory per block):
-//   * one persistent CTA per SM of G groups x 256 threads; the CTA holds one
-//     copy of the activation table in shared memory (53 KB);
-//   * a group processes 32-row x 256-column tiles; warp w of the group owns
-//     rows w, w+8, w+16, w+24 and lane l owns columns 8l..8l+7, so every
-//     load is a coalesced 16-byte vector (a warp reads one 512-byte row
-//     segment per instruction) and a thread keeps 8 independent loads in
-//     flight;
-//   * rowwise: a 32-column block spans 4 lanes: amax by two xor-shuffles,
-//     each lane stores 8 codes (a warp writes 256 contiguous bytes);
-//   * colwise: the group stages the fp32 tile in shared memory (32 KB),
-//     then thread t walks column t down the 32 rows: amax, scale, 32 codes,
-//     stored as one full 32-byte sector of the [N, M] code matrix.
+// Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
+//   * one persistent CTA per SM: a producer warp and 24 consumer warps in three
+//     groups.  Tiles are 32 rows x 256 columns; the producer streams them
+//     into a shared-memory ring with 2-D TMA loads (cp.async.bulk.tensor,
+//     completion counted in transaction bytes on an mbarrier) of 32-row
+//     boxes with 128-byte rows (64 bf16 columns, or 32 gate/up pairs) and the
+//     hardware 128-byte swizzle, so that a lane can read its whole row of a
+//     box without shared-memory bank conflicts;
+//   * tiles go round-robin to the CTAs (column strips first for colwise, so
+//     the CTAs working at once cover neighbouring 32-row groups of the same
+//     columns) and rotate over the groups;
+//   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31 and
+//     lane l its row l: a rowwise 1x32 block is one lane's 32 values (amax,
+//     scale and codes in registers, 32 code bytes stored as one sector);
+//     for colwise the warp transposes its sub-tile through a private padded
+//     shared-memory buffer and lane l quantises column l (32 code bytes, one
+//     sector of the [N, M] code matrix).  No barrier spans more than a warp;
+//   * the activation is the fast fp32 form; codes the rounding test cannot
+//     decide are recomputed one element at a time from the exact value, and a
+//     whole block only when its scale is undecided (exact values come from the
+//     hot slice of the activation table kept in shared memory).
+#include <cstring>
+
 #include "glu_common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int kTR = 32;    // tile rows
-constexpr int kTC = 256;   // tile columns (outputs)
-constexpr int kGroupThreads = 256;
-constexpr int kTabBytes = kTabEntries * 8;
+constexpr int kTR = 32;                       // tile rows
+constexpr int kWC = 32;                       // columns per warp sub-tile
+constexpr int kGroupWarps = 8;
+constexpr int kTC = kWC * kGroupWarps;        // tile columns
+// rowwise: 3 groups (more warps to hide latency); colwise/both: 2 (room for
+// the transpose buffers and fewer registers per thread to spill)
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_ROW ? 3 : 2; }
+__host__ __device__ constexpr int threads_for(int mode) { return (groups_for(mode) * kGroupWarps + 1) * 32; }
+constexpr int kStageBytes = kTR * kTC * 4;    // 32 KB: gate + up, or the pairs
+constexpr int kTStride = 33;                  // floats per transpose-buffer row
+constexpr int kTBytes = kTR * kTStride * 4;
+constexpr int kHotBytes = kHotEntries * 8;
+// Each consumer group has a private ring of kSlots stages: a stage is always
+// consumed, in order, by the one group that waits on it, so an mbarrier
+// parity wait can never be satisfied by an older phase of the same parity.
+// Warps copy their box to registers and release the stage at once, so one
+// slot per group keeps the next tile loading while the group computes.
+constexpr int kSlots = 1;
+// Codes leave through per-warp shared-memory boxes (32 x 32 bytes, 32-byte
+// swizzle) written to global memory by TMA stores.
+constexpr int kQBytes = 1024;
 
-struct FwdP {
-  const uint8_t* gate;
-  const uint8_t* up;
-  int64_t M, N, ld;  // ld in elements
+__host__ __device__ constexpr int smem_for(int mode) {
+  return 1024 + groups_for(mode) * kSlots * kStageBytes + kHotBytes +
+         groups_for(mode) * kGroupWarps *
+             (((mode & GLU_MODE_COL) ? kTBytes : 0) + (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes) +
+         2 * 4 * 8;
+}
+
+// Byte offset of (row r, 16-byte chunk k) in a 32 x 32-byte code box with
+// the 32-byte swizzle (chunk ^= (r >> 2) & 1).
+__device__ __forceinline__ int qswz(int r, int k) { return r * 32 + 16 * (k ^ ((r >> 2) & 1)); }
+
+__device__ uint32_t g_err_fwd_mx;
+
+struct alignas(64) FwdP {
+  CUtensorMap tm_a;   // gate [M, N] bf16 (boxes 64 x 32) or X as (gate, up) pairs (32 x 32)
+  CUtensorMap tm_b;   // up [M, N] bf16 (split layout)
+  CUtensorMap tm_qr;  // q_row [M, N] bytes, boxes 32 x 32
+  CUtensorMap tm_qc;  // q_col [N, M] bytes, boxes 32 x 32
+  const uint16_t* gate;  // the same operands in global memory, for the exact path
+  const uint16_t* up;
+  int64_t ld;
+  int64_t M, N;
   uint8_t* q_row;
   uint8_t* s_row;
   uint8_t* q_col;
@@ -39,32 +85,227 @@ struct FwdP {
   int64_t n_rt, n_ct, ntiles;
 };
 
-__device__ __forceinline__ bool is_cold(float h) {
-  uint32_t b = absbits(h);
-  return b >= kInfBits || (b != 0u && b < kTinyBits);
+// Boxes have 32 rows of 128 bytes; the 128-byte swizzle stores the 16-byte
+// chunk k of row r at chunk k ^ (r & 7).  Split layout: a box holds 64 bf16
+// columns (two warps' sub-tiles, 4 KB per operand per box pair); interleaved:
+// a box holds one warp's 32 (gate, up) pairs.
+constexpr int kBoxBytes = 4096;
+__device__ __forceinline__ int swz(int r, int chunk) { return r * 128 + 16 * (chunk ^ (r & 7)); }
+
+// Exact act(g) * u of element (row, col) of the input, read from global
+// memory (the rare path runs after the warp has released its stage).
+template <int ACT, int LAYOUT>
+__device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t row, int64_t col) {
+  uint32_t gb, ub;
+  if (LAYOUT == GLU_LAYOUT_SPLIT) {
+    gb = __ldg(p.gate + row * p.ld + col);
+    ub = __ldg(p.up + row * p.ld + col);
+  } else {
+    gb = __ldg(p.gate + row * p.ld + 2 * col);
+    ub = __ldg(p.gate + row * p.ld + 2 * col + 1);
+  }
+  return exact_act_mul_hot<ACT>(hot, __uint_as_float(gb << 16), __uint_as_float(ub << 16));
 }
 
-template <int ACT, int MODE, int LAYOUT, int G>
-__global__ void __launch_bounds__(kGroupThreads* G, 1) fwd_mx_kernel(const FwdP p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
-    uint4* dst = reinterpret_cast<uint4*>(smem);
-    for (int i = threadIdx.x; i < kTabBytes / 16; i += blockDim.x) dst[i] = src[i];
+// v[e] = x for a runtime e, keeping v in registers.
+__device__ __forceinline__ void set_elem(float (&v)[32], int e, float x) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    if (k == e) v[k] = x;
+}
+
+__device__ __forceinline__ float amax32(const float (&v)[32]) {
+  float m8[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m8[j] = amax8(*reinterpret_cast<const float(*)[8]>(&v[8 * j]));
+  return amax2(amax2(m8[0], m8[1]), amax2(m8[2], m8[3]));
+}
+
+__device__ __forceinline__ void codes32(const float (&v)[32], float mul, uint32_t (&q)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    q[j] = e4m3x4(v[4 * j] * mul, v[4 * j + 1] * mul, v[4 * j + 2] * mul, v[4 * j + 3] * mul);
+}
+
+// 4-bit mask of the nonzero bytes of x.
+__device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
+  return uint32_t((x & 0xFFu) != 0u) | (uint32_t((x & 0xFF00u) != 0u) << 1) |
+         (uint32_t((x & 0xFF0000u) != 0u) << 2) | (uint32_t((x & 0xFF000000u) != 0u) << 3);
+}
+
+// Quantise one 32-value MXFP8 block held by this thread.  Element e sits at
+// input (row0 + e, c0 + lane) for a column block and at (row0 + lane, c0 + e)
+// for a row block.  Codes are decided from the fast values where the
+// rounding test allows and from exact values elsewhere; the whole block is
+// recomputed from exact values when its scale is undecided.  Writes 8 code
+// words, returns the scale byte.
+template <int ACT, int LAYOUT, bool COLUMN>
+__device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
+                                                const float2* hot, int64_t row0, int64_t c0,
+                                                int lane) {
+  constexpr float d = kBracket;
+  uint32_t sc = e8m0_checked(amax32(v), d);
+  if (sc != 0x100u) {
+    const float mul = e8m0_inv_scale(sc);
+    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+    uint32_t wbad = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      bool bad = false;
+      q[j] = e4m3x4_bracket2(make_float2(v[4 * j], v[4 * j + 1]), make_float2(v[4 * j + 2], v[4 * j + 3]),
+                             splat2(mlo), splat2(mhi), bad);
+      wbad |= uint32_t(bad) << j;
+    }
+    if (wbad != 0u) {
+      // rare: find the straddling elements, take their exact values
+      uint32_t emask = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
+                                   v[4 * j + 3] * mlo);
+        const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
+                                   v[4 * j + 3] * mhi);
+        emask |= byte_mask(ql ^ qh) << (4 * j);
+      }
+      while (emask != 0u) {
+        const int e = __ffs(emask) - 1;
+        emask &= emask - 1u;
+        const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + e, c0 + lane)
+                               : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
+        set_elem(v, e, x);
+      }
+      codes32(v, mul, q);
+    }
+    return sc;
+  }
+  // undecided scale (or a NaN/Inf/tiny block): the block from exact values
+#pragma unroll 1
+  for (int e = 0; e < 32; ++e) {
+    const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + e, c0 + lane)
+                           : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
+    set_elem(v, e, x);
+  }
+  sc = e8m0_of(amax32(v));
+  if (sc == 0xFFu) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
+  } else {
+    codes32(v, e8m0_inv_scale(sc), q);
+  }
+  return sc;
+}
+
+template <int ACT, int MODE, int LAYOUT>
+__global__ void __launch_bounds__(threads_for(MODE), 1)
+    fwd_mx_kernel(const __grid_constant__ FwdP p) {
+  constexpr int kGroups = groups_for(MODE);
+  constexpr int kConsumers = kGroups * kGroupWarps;
+  constexpr int kStages = kGroups * kSlots;
+  constexpr int kQPerWarp = (MODE == GLU_MODE_BOTH ? 2 : 1) * kQBytes;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = smem;
+  uint8_t* hot_raw = smem + kStages * kStageBytes;
+  const float2* hot = reinterpret_cast<const float2*>(hot_raw);
+  uint8_t* Qbase = hot_raw + kHotBytes;  // 1024-aligned (stages and hot table are)
+  float* Tbase = reinterpret_cast<float*>(Qbase + kConsumers * kQPerWarp);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Tbase) +
+                                               ((MODE & GLU_MODE_COL) ? kConsumers * kTBytes : 0));
+  uint64_t* empty = full + kStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  load_hot_table<8>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kGroupWarps);
+    }
+    fence_barrier_init();
   }
   __syncthreads();
-  const float2* tab = reinterpret_cast<const float2*>(smem);
 
-  const int grp = threadIdx.x / kGroupThreads;
-  const int tid = threadIdx.x % kGroupThreads;
-  const int warp = tid >> 5, lane = tid & 31;
-  float* H = reinterpret_cast<float*>(smem + kTabBytes) + grp * (kTR * kTC);
+  const int64_t G = gridDim.x;
+  const int64_t my_tiles = (p.ntiles - blockIdx.x + G - 1) / G;
 
-  // Fill for masked-out elements: gate = 1.0 (in the table), up = 0.
-  constexpr uint32_t kFillG = (LAYOUT == GLU_LAYOUT_SPLIT) ? 0x3F803F80u : 0x00003F80u;
-  constexpr uint32_t kFillU = (LAYOUT == GLU_LAYOUT_SPLIT) ? 0u : 0x00003F80u;
+  // ------------------------------------------------------------ producer --
+  // Stage layout: split: gate boxes 0..3 then up boxes 0..3 (box b holds the
+  // columns of warps 2b and 2b+1); interleaved: pair boxes 0..7.
+  // Tile i goes to group i % kGroups, slot (i / kGroups) % kSlots of that
+  // group's ring.
+  if (warp == kConsumers) {
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_a);
+      if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
+      if (MODE & GLU_MODE_ROW) prefetch_tensormap(&p.tm_qr);
+      if (MODE & GLU_MODE_COL) prefetch_tensormap(&p.tm_qc);
+    }
+    int64_t last_k[kStages];
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) last_k[st] = -1;
+    for (int64_t i = 0; i < my_tiles; ++i) {
+      const int grp = int(i % kGroups);
+      const int64_t k = i / kGroups;
+      const int st = grp * kSlots + int(k % kSlots);
+      bool ok = true;
+      if (lane == 0 && k >= kSlots) ok = mbar_wait(&empty[st], uint32_t((k / kSlots) & 1) ^ 1u);
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+        if (lane == 0) atomicOr(&g_err_fwd_mx, kErrWaitEmpty);
+        break;
+      }
+      const int64_t t = blockIdx.x + i * G;
+      int64_t rt, ct;
+      if (MODE == GLU_MODE_ROW) {
+        rt = t / p.n_ct;
+        ct = t - rt * p.n_ct;
+      } else {
+        ct = t / p.n_rt;
+        rt = t - ct * p.n_rt;
+      }
+      uint8_t* dst = stages + st * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageBytes);
+      __syncwarp();
+      // eight boxes per tile, issued by lanes 0..7
+      if (lane < 8) {
+        const int32_t y = int32_t(rt * kTR);
+        if (LAYOUT == GLU_LAYOUT_SPLIT) {
+          const int b = lane & 3;
+          tma_load_2d(dst + lane * kBoxBytes, lane < 4 ? &p.tm_a : &p.tm_b,
+                      int32_t(ct * kTC + b * 64), y, &full[st]);
+        } else {
+          tma_load_2d(dst + lane * kBoxBytes, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &full[st]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kStages; ++q)
+        if (q == st) last_k[q] = k;
+    }
+    // never leave with copies in flight: wait (bounded) for the last load of
+    // every slot (already complete unless a consumer gave up)
+    if (lane == 0) {
+#pragma unroll
+      for (int st = 0; st < kStages; ++st)
+        if (last_k[st] >= 0 && !mbar_wait(&full[st], uint32_t((last_k[st] / kSlots) & 1)))
+          atomicOr(&g_err_fwd_mx, kErrDrain);
+    }
+    return;
+  }
 
-  for (int64_t t = int64_t(blockIdx.x) * G + grp; t < p.ntiles; t += int64_t(gridDim.x) * G) {
+  // ----------------------------------------------------------- consumers --
+  const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
+  float* T = Tbase + warp * (kTR * kTStride);
+  uint8_t* Qr = Qbase + warp * kQPerWarp;                                 // row codes
+  uint8_t* Qc = Qr + ((MODE == GLU_MODE_BOTH) ? kQBytes : 0);             // column codes
+
+  for (int64_t k = 0;; ++k) {
+    const int64_t i = kGroups * k + grp;
+    if (i >= my_tiles) break;
+    const int s = grp * kSlots + int(k % kSlots);
+    if (!mbar_wait(&full[s], uint32_t((k / kSlots) & 1))) {
+      if (lane == 0) atomicOr(&g_err_fwd_mx, kErrWaitFull);
+      break;
+    }
+    const int64_t t = blockIdx.x + i * G;
     int64_t rt, ct;
     if (MODE == GLU_MODE_ROW) {
       rt = t / p.n_ct;
@@ -73,169 +314,155 @@ __global__ void __launch_bounds__(kGroupThreads* G, 1) fwd_mx_kernel(const FwdP 
       ct = t / p.n_rt;
       rt = t - ct * p.n_rt;
     }
-    const int64_t row0 = rt * kTR, col0 = ct * kTC;
-    const int64_t col = col0 + lane * 8;
-    const bool col_ok = col < p.N;
-
-    // ---- loads: 8 x 16 B per thread, all issued before any use
-    uint4 wa[4], wb[4];
+    const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;  // this warp's sub-tile
+    const bool active = c0 < p.N;
+    // ---- row `lane` of the warp's box, two halves of 16 elements, then
+    // free the stage; fast activation in pairs
+    float h[32];
+    uint32_t gmax = 0;  // running max of the raw gate patterns (range check)
+    if (active) {
+      const uint8_t* st_base = stages + s * kStageBytes;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = row0 + warp + 8 * i;
-      wa[i] = make_uint4(kFillG, kFillG, kFillG, kFillG);
-      wb[i] = make_uint4(kFillU, kFillU, kFillU, kFillU);
-      if (col_ok && r < p.M) {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t xw[16];  // split: 8 gate words then 8 up words; pairs: 16 words
         if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          wa[i] = ld_stream(p.gate + (r * p.ld + col) * 2);
-          wb[i] = ld_stream(p.up + (r * p.ld + col) * 2);
-        } else {
-          const uint8_t* x = p.gate + (r * p.ld + 2 * col) * 2;
-          wa[i] = ld_stream(x);
-          wb[i] = ld_stream(x + 16);
-        }
-      }
-    }
-
-    // ---- activation: h = act(g) * u, one rounding
-    float h[4][8];
-    bool cold = false;
+          const uint8_t* A = st_base + (w >> 1) * kBoxBytes;
+          const uint8_t* B = A + 4 * kBoxBytes;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t a[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
-      const uint32_t b[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t g16;
-        float u;
-        if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          const uint32_t gw = a[k >> 1], uw = b[k >> 1];
-          g16 = (k & 1) ? (gw >> 16) : (gw & 0xFFFFu);
-          u = (k & 1) ? bf16_hi(uw) : bf16_lo(uw);
-        } else {
-          const uint32_t w = (k < 4) ? a[k] : b[k - 4];
-          g16 = w & 0xFFFFu;
-          u = bf16_hi(w);
-        }
-        h[i][k] = tab_mul(tab[tab_index(g16)], u);
-        cold |= is_cold(h[i][k]);
-      }
-    }
-    if (cold) {
-      // rare: table miss, NaN/Inf, or a result too small for the lo part;
-      // the inputs are read again rather than kept live in registers
-#pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int64_t r = row0 + warp + 8 * i;
-        if (!(col_ok && r < p.M)) continue;
-        uint4 x0, x1;
-        if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          x0 = ld_stream(p.gate + (r * p.ld + col) * 2);
-          x1 = ld_stream(p.up + (r * p.ld + col) * 2);
-        } else {
-          const uint8_t* x = p.gate + (r * p.ld + 2 * col) * 2;
-          x0 = ld_stream(x);
-          x1 = ld_stream(x + 16);
-        }
-        const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w};
-        const uint32_t b[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float g, u;
-          if (LAYOUT == GLU_LAYOUT_SPLIT) {
-            g = (k & 1) ? bf16_hi(a[k >> 1]) : bf16_lo(a[k >> 1]);
-            u = (k & 1) ? bf16_hi(b[k >> 1]) : bf16_lo(b[k >> 1]);
-          } else {
-            const uint32_t w = (k < 4) ? a[k] : b[k - 4];
-            g = bf16_lo(w);
-            u = bf16_hi(w);
+          for (int k = 0; k < 2; ++k) {
+            const int o = swz(lane, 4 * (w & 1) + 2 * half + k);
+            const uint4 x = *reinterpret_cast<const uint4*>(A + o);
+            const uint4 y = *reinterpret_cast<const uint4*>(B + o);
+            xw[4 * k] = x.x; xw[4 * k + 1] = x.y; xw[4 * k + 2] = x.z; xw[4 * k + 3] = x.w;
+            xw[8 + 4 * k] = y.x; xw[9 + 4 * k] = y.y; xw[10 + 4 * k] = y.z; xw[11 + 4 * k] = y.w;
           }
-          // select by row index so the array stays in registers
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii)
-            if (ii == i && is_cold(h[ii][k])) h[ii][k] = slow_act_mul(ACT, g, u);
-        }
-      }
-    }
-
-    // ---- rowwise 1x32
-    if (MODE & GLU_MODE_ROW) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m = max(m, absbits(h[i][k]));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        const uint32_t s = e8m0_from_amax_bits(m);
-        uint2 q;
-        if (s == 0xFFu) {
-          q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
-          const float mul = e8m0_inv_scale(s);
-          q.x = e4m3x4(h[i][0] * mul, h[i][1] * mul, h[i][2] * mul, h[i][3] * mul);
-          q.y = e4m3x4(h[i][4] * mul, h[i][5] * mul, h[i][6] * mul, h[i][7] * mul);
+          const uint8_t* A = st_base + w * kBoxBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 x = *reinterpret_cast<const uint4*>(A + swz(lane, 4 * half + k));
+            xw[4 * k] = x.x; xw[4 * k + 1] = x.y; xw[4 * k + 2] = x.z; xw[4 * k + 3] = x.w;
+          }
         }
-        const int64_t r = row0 + warp + 8 * i;
-        if (col_ok && r < p.M) {
-          st_stream(p.q_row + r * p.N + col, q);
-          if ((lane & 3) == 0) st_byte(p.s_row + r * (p.N / 32) + col / 32, s);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float2 g2, u2;
+          if (LAYOUT == GLU_LAYOUT_SPLIT) {
+            g2 = bf16x2_f2(xw[j]);
+            u2 = bf16x2_f2(xw[8 + j]);
+            gmax = vmax_u16x2(gmax, xw[j]);
+          } else {
+            const uint32_t p0 = xw[2 * j], p1 = xw[2 * j + 1];
+            g2 = make_float2(bf16_lo(p0), bf16_lo(p1));
+            u2 = make_float2(bf16_hi(p0), bf16_hi(p1));
+            gmax = vmax_u16x2(gmax, (p0 & 0xFFFFu) | (p1 << 16));
+          }
+          const float2 h2 = fast_h2<ACT>(g2, u2);
+          h[16 * half + 2 * j] = h2.x;
+          h[16 * half + 2 * j + 1] = h2.y;
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (!active) continue;
 
-    // ---- colwise 32x1 through the shared-memory tile
+    if (!fast_range_ok<ACT>(gmax)) {
+      // gates outside the fast range (rare): exact values for those
+      uint32_t emask = 0;
+#pragma unroll 1
+      for (int e = 0; e < 32; ++e) {
+        const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + lane) * p.ld + c0 + e)
+                                                        : __ldg(p.gate + (row0 + lane) * p.ld + 2 * (c0 + e));
+        emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << e;
+      }
+      while (emask != 0u) {
+        const int e = __ffs(emask) - 1;
+        emask &= emask - 1u;
+        set_elem(h, e, exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e));
+      }
+    }
+
+    const bool row_ok = row0 + lane < p.M;
     if (MODE & GLU_MODE_COL) {
-      group_sync(1 + grp, kGroupThreads);  // previous tile fully consumed
+      // stage the values for the column pass before the row pass may
+      // replace some of them (either is exact enough for the other pass)
+      // (row stride 33 floats: the row writes and the column reads below
+      // both touch 32 distinct banks)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float4* dst = reinterpret_cast<float4*>(H + (warp + 8 * i) * kTC + lane * 8);
-        dst[0] = make_float4(h[i][0], h[i][1], h[i][2], h[i][3]);
-        dst[1] = make_float4(h[i][4], h[i][5], h[i][6], h[i][7]);
+      for (int e = 0; e < 32; ++e) T[lane * kTStride + e] = h[e];
+    }
+
+    // ---- rowwise 1x32: this lane's 32 values
+    if (MODE & GLU_MODE_ROW) {
+      uint32_t q[8];
+      const uint32_t sc = quant_block<ACT, LAYOUT, false>(h, q, p, hot, row0, c0, lane);
+      // previous tile's code box must have been read out by its TMA store
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      *reinterpret_cast<uint4*>(Qr + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(Qr + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tm_qr, int32_t(c0), int32_t(row0), Qr);  // rows >= M are clipped
+        bulk_commit();
       }
-      group_sync(1 + grp, kGroupThreads);
-      const int64_t c = col0 + tid;
-      if (c < p.N) {
-        float v[kTR];
-        uint32_t m = 0;
+      if (row_ok) st_byte(p.s_row + (row0 + lane) * (p.N / 32) + c0 / 32, sc);
+    }
+
+    // ---- colwise 32x1: lane l takes column l of the transposed sub-tile
+    if (MODE & GLU_MODE_COL) {
+      __syncwarp();
+      float v[32];
 #pragma unroll
-        for (int r = 0; r < kTR; ++r) {
-          v[r] = H[r * kTC + tid];
-          m = max(m, absbits(v[r]));
-        }
-        const uint32_t s = e8m0_from_amax_bits(m);
-        uint32_t q[8];
-        if (s == 0xFFu) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
-        } else {
-          const float mul = e8m0_inv_scale(s);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            q[j] = e4m3x4(v[4 * j] * mul, v[4 * j + 1] * mul, v[4 * j + 2] * mul,
-                          v[4 * j + 3] * mul);
-        }
-        uint8_t* dst = p.q_col + c * p.M + row0;
-        st_stream(dst, make_uint4(q[0], q[1], q[2], q[3]));
-        st_stream(dst + 16, make_uint4(q[4], q[5], q[6], q[7]));
-        st_byte(p.s_col + c * (p.M / 32) + row0 / 32, s);
+      for (int r = 0; r < kTR; ++r) v[r] = T[r * kTStride + lane];
+      __syncwarp();  // the buffer may be rewritten by the next tile
+      uint32_t q[8];
+      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
+      if (MODE == GLU_MODE_COL) {
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+      }  // (both: the wait above already covered this tile's previous stores)
+      *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(c0), Qc);
+        bulk_commit();
       }
+      st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
     }
   }
+  if (lane == 0) bulk_wait0();  // no code box may still be in flight at exit
 }
 
 template <int ACT, int MODE, int LAYOUT>
 cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
-  constexpr int G = 3;
-  auto kern = fwd_mx_kernel<ACT, MODE, LAYOUT, G>;
-  const int smem = kTabBytes + ((MODE & GLU_MODE_COL) ? G * kTR * kTC * 4 : 0);
+  auto kern = fwd_mx_kernel<ACT, MODE, LAYOUT>;
+  const int smem = smem_for(MODE);
+  constexpr int kGroups = groups_for(MODE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   FwdP p;
-  p.gate = static_cast<const uint8_t*>(a.gate);
-  p.up = static_cast<const uint8_t*>(a.up);
+  memset(&p, 0, sizeof p);
+  p.gate = static_cast<const uint16_t*>(a.gate);
+  p.up = static_cast<const uint16_t*>(a.up);
+  p.ld = a.ld_in;
+  if (LAYOUT == GLU_LAYOUT_SPLIT) {
+    e = make_tile_map(&p.tm_a, a.gate, 2, a.N, a.M, a.ld_in * 2, 64, kTR, 128);
+    if (e == cudaSuccess) e = make_tile_map(&p.tm_b, a.up, 2, a.N, a.M, a.ld_in * 2, 64, kTR, 128);
+  } else {
+    e = make_tile_map(&p.tm_a, a.gate, 4, a.N, a.M, a.ld_in * 2, kWC, kTR, 128);
+  }
+  if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
+    e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N, a.M, a.N, kWC, kTR, 32);
+  if (e == cudaSuccess && (MODE & GLU_MODE_COL))
+    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, a.N, a.M, kTR, kWC, 32);
+  if (e != cudaSuccess) return e;
   p.M = a.M;
   p.N = a.N;
-  p.ld = a.ld_in;
   p.q_row = static_cast<uint8_t*>(a.q_row);
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.q_col = static_cast<uint8_t*>(a.q_col);
@@ -243,11 +470,10 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
   p.ntiles = p.n_rt * p.n_ct;
-  const int64_t ctas = (p.ntiles + G - 1) / G;
-  const int grid = int(ctas < d.sms ? ctas : d.sms);
+  const int grid = int(p.ntiles < d.sms ? p.ntiles : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGroupThreads * G);
+  cfg.blockDim = dim3(threads_for(MODE));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   return cudaLaunchKernelEx(&cfg, kern, p);
@@ -272,6 +498,15 @@ cudaError_t by_mode(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& 
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   return a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+}
+
+cudaError_t read_err_fwd_mx(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_err_fwd_mx, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_err_fwd_mx, &z, sizeof(uint32_t));
+  }
+  return e;
 }
 
 }  // namespace gq

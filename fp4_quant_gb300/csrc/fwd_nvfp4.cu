@@ -49,10 +49,12 @@ __device__ __forceinline__ bool is_cold(float h) {
 // then rb is exact and q0 already is.  Quotients or residuals in the
 // subnormal range only arise for |a/b| < 2^-90, which encodes to a zero
 // code either way.
+// b > 0 here, so the quotient carries a's sign; copysign restores it for a
+// zero a, where the residual step would give (+0) + (-0) = +0.
 __device__ __forceinline__ float div_rn(float a, float b, float rb) {
   const float q0 = __fmul_rn(a, rb);
   const float r = __fmaf_rn(-b, q0, a);
-  return __fmaf_rn(r, rb, q0);
+  return copysignf(__fmaf_rn(r, rb, q0), a);
 }
 
 template <int ACT, int LAYOUT, int G>

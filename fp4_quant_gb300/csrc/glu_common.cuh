@@ -1,18 +1,30 @@
 // Device building blocks shared by the fused GLU + quantisation kernels.
 //
-// Numerics (see gen_act_tables.c for why tables):
-//   h = act(g) * u is formed as fma(hi, u, lo * u) from an (hi, lo) table
-//   entry indexed by the bf16 bit pattern of g; elements outside the table,
-//   NaN/Inf results and results too small for the lo part to be exact take
-//   an fp64 slow path that evaluates the same formula in double and rounds
-//   once.
+// Numerics.  Every code and scale must equal the one obtained from the
+// exactly rounded h = RN(act(g) * u) (E8M0 scales flip at amax = 448 * 2^k,
+// E4M3/E2M1 codes at their rounding midpoints).  Two evaluations of h exist:
+//   * fast: h = (g*u) * S(g) in fp32 with the hardware ex2/rcp
+//     approximations (S = sigmoid(x) for SiLU, sigmoid(2y) for GELU; g*u is
+//     exact for bf16 operands).  Its relative error is bounded by kBound*
+//     (measured over every bf16 gate, see the GPU tests), and it costs no
+//     memory traffic;
+//   * exact: an (hi, lo) table entry indexed by the bf16 pattern of g (built
+//     by gen_act_tables.c, read through the read-only cache) combined as
+//     fma(hi, u, lo * u), and an fp64 evaluation of the same formula for the
+//     gates the table does not cover.
+//   A quantised value is taken from the fast h only when rounding cannot
+//   tell the two apart: v*(1 - d) and v*(1 + d) (d above the fast path's
+//   relative error) must give the same code, and amax*(1 -/+ d) the same
+//   scale (a Ziv-style rounding test).  Otherwise the block is recomputed
+//   from the exact h.  This happens for roughly 1 element in 10^5.
 //   MXFP8: E8M0 "RCEIL" scale e = ceil(log2(amax/448)) read off the fp32
 //   exponent field of amax (448 = 1.75 * 2^8: e = E - 8, plus one when the
 //   significand exceeds 1.75), clamped at -127; codes = E4M3(h * 2^-e) with
 //   the packed round-to-nearest-even saturating cvt ("Add swiglu + MXFP8
 //   fused CuTe DSL kernel", Summary: RCEIL MXFP8 cast, rowwise/colwise/both).
-//   NVFP4: s = E4M3(amax / 6) (IEEE fp32 division), codes = E2M1(h / s)
-//   ("feat(phyai-kernel): add Thor NVFP4 GeGLU kernel", Supported contract).
+//   NVFP4: s = E4M3(amax / 6), codes = E2M1(h / s), both divisions correctly
+//   rounded ("feat(phyai-kernel): add Thor NVFP4 GeGLU kernel", Supported
+//   contract).
 #pragma once
 
 #include <cstdint>
@@ -77,7 +89,11 @@ __device__ __forceinline__ uint32_t tab_index(uint32_t g16) {
   return t + (g16 >> 15) * (kTabHalf + 1);
 }
 
+// ------------------------------------------------------------ exact path --
+
 // act(g) * u from a forward entry (hi, lo): one rounding of hi*u + lo*u.
+// hi is act(g) rounded toward zero, so lo has hi's sign and a zero or
+// infinite u gives the correctly signed result.
 __device__ __forceinline__ float tab_mul(float2 e, float u) {
   return __fmaf_rn(e.x, u, __fmul_rn(e.y, u));
 }
@@ -112,6 +128,229 @@ static __device__ __noinline__ float slow_grad_mul(int act, float g, float dy, f
   return (float)(((double)dy * (double)u) * act_grad_f64(act, (double)g));
 }
 
+// Result of the table combination that the table cannot vouch for: NaN
+// (out-of-range sentinel or NaN/Inf operand), infinite, or subnormal (the lo
+// part may have lost bits).
+__device__ __forceinline__ bool tab_cold(float h) {
+  const uint32_t b = __float_as_uint(h) & 0x7FFFFFFFu;
+  return b >= kInfBits || (b != 0u && b < kTinyBits);
+}
+
+// Exactly rounded act(g) * u, from the forward table of ACT in global
+// memory (read-only cache).
+template <int ACT>
+__device__ __forceinline__ float exact_act_mul(float g, float u) {
+  const float2* tab = reinterpret_cast<const float2*>(ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  const float2 e = __ldg(tab + tab_index(__float_as_uint(g) >> 16));
+  const float h = tab_mul(e, u);
+  return tab_cold(h) ? slow_act_mul(ACT, g, u) : h;
+}
+
+// Exactly rounded (dy * u) * act'(g), from the backward table (act, act').
+template <int ACT>
+__device__ __forceinline__ float exact_grad_mul(float g, float dy, float u) {
+  const float4* tab = reinterpret_cast<const float4*>(ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+  const float4 e = __ldg(tab + tab_index(__float_as_uint(g) >> 16));
+  const float h = tab_mul(make_float2(e.z, e.w), __fmul_rn(dy, u));
+  return tab_cold(h) ? slow_grad_mul(ACT, g, dy, u) : h;
+}
+
+// Hot slice of a table kept in shared memory: bf16 exponent fields
+// kHotExpLo .. kHotExpLo + kHotBinades - 1 (2^-10 <= |g| < 16), positive
+// gates then negative gates.  It serves the exact path of the kernels, whose
+// undecided blocks are rare but otherwise wait on L2 latency.
+constexpr uint32_t kHotExpLo = 117;
+constexpr uint32_t kHotBinades = 14;
+constexpr uint32_t kHotHalf = kHotBinades * 128;
+constexpr uint32_t kHotEntries = 2 * kHotHalf;
+constexpr uint32_t kHotSkip = (kHotExpLo - GQ_TAB_EXP_LO) * 128;  // first hot slot per sign
+
+// Copy the hot slice of a global table (entries of EB bytes) to shared
+// memory; all threads of the block take part.
+// (8-byte words: the negative half of a table starts at an odd entry.)
+template <int EB>
+__device__ __forceinline__ void load_hot_table(uint8_t* dst, const void* table) {
+  constexpr int kWords = int(kHotHalf) * EB / 8;
+  const uint2* src = reinterpret_cast<const uint2*>(table);
+  uint2* d = reinterpret_cast<uint2*>(dst);
+  for (int i = threadIdx.x; i < 2 * kWords; i += blockDim.x) {
+    const int sign = i / kWords, j = i - sign * kWords;
+    const int base = int(sign * (kTabHalf + 1) + kHotSkip) * EB / 8;
+    d[i] = src[base + j];
+  }
+}
+
+// Hot-slice slot of a bf16 pattern, or -1.
+__device__ __forceinline__ int hot_index(uint32_t g16) {
+  const uint32_t t = (g16 & 0x7FFFu) - (kHotExpLo << 7);
+  return t < kHotHalf ? int(t + (g16 >> 15) * kHotHalf) : -1;
+}
+
+// Exact act(g) * u with the hot slice in shared memory (fwd entries).
+template <int ACT>
+__device__ __forceinline__ float exact_act_mul_hot(const float2* hot, float g, float u) {
+  const int k = hot_index(__float_as_uint(g) >> 16);
+  if (k < 0) return exact_act_mul<ACT>(g, u);
+  const float h = tab_mul(hot[k], u);
+  return tab_cold(h) ? slow_act_mul(ACT, g, u) : h;
+}
+
+// ---------------------------------------------------- packed fp32 pairs --
+// sm_100+ issues two fp32 multiplies/adds per instruction on register pairs.
+
+__device__ __forceinline__ uint64_t pk2(float2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t r) {
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+  return upk2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+  return upk2(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+  return upk2(r);
+}
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+
+// bf16x2 word -> (element 0, element 1) as fp32 (exact)
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ------------------------------------------------------------- fast path --
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Fast activation factor S(g) = 1 / (1 + E):
+//   SiLU: E = 2^(-g log2 e),                      S = sigmoid(g)
+//   GELU: E = 2^(-K (g + 0.044715 g^3)), K = 2 sqrt(2/pi) log2(e),
+//         S = sigmoid(2y), since 0.5 (1 + tanh y) = sigmoid(2y).
+// fast_s: the exponent is one rounded product (the forward kernels).
+//   Measured over every bf16 gate: |S - sigmoid| / sigmoid <= 54 * 2^-24
+//   (SiLU, |g| < 64) and <= 33 * 2^-24 (GELU, -7 < g < 64).
+// fast_s_acc: the exponent carries a second word (the backward kernels,
+//   which also need E for act'): <= 2.9 * 2^-24 (SiLU, |g| < 64) and
+//   <= 31 * 2^-24 (GELU, -6 < g < 64).  -log2(e) and K are split into a
+//   16-bit head, so the head product with an 8-bit bf16 g is exact.
+// Outside those ranges fast_ok() / fast_ok_acc() are false and the exact
+// path is used.
+template <int ACT>
+__device__ __forceinline__ float fast_s(float g) {
+  float t;
+  if (ACT == 0) {
+    t = __fmul_rn(g, -1.44269502162933349609375f);
+  } else {
+    const float w = __fmaf_rn(-0.10294324159622192f, __fmul_rn(g, g), -2.302208185195922851562f);
+    t = __fmul_rn(g, w);
+  }
+  return rcp_approx(__fadd_rn(1.0f, ex2_approx(t)));
+}
+
+template <int ACT>
+__device__ __forceinline__ bool fast_ok(float g) {
+  return ACT == 0 ? fabsf(g) < 64.0f : (g > -7.0f && g < 64.0f);
+}
+
+// act(g) * u for a pair, fast form (same arithmetic as fast_s, packed).
+template <int ACT>
+__device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
+  float2 t;
+  if (ACT == 0) {
+    t = mul2(g, splat2(-1.44269502162933349609375f));
+  } else {
+    const float2 w = fma2(splat2(-0.10294324159622192f), mul2(g, g), splat2(-2.302208185195922851562f));
+    t = mul2(g, w);
+  }
+  const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), splat2(1.0f));
+  return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// Largest raw bf16 pattern of the gates (two per word, unsigned per half):
+// negative gates have the sign bit set, so the running max of the raw
+// patterns reaches kFastNegLimit exactly when some gate is at or below the
+// fast path's lower limit (SiLU -87: beyond it 1/(1+E) leaves the normal
+// range; GELU -7).  Positive gates never reach it.
+template <int ACT>
+struct FastRange {
+  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC2AEu : 0xC0E0u;  // bf16 -87, -7
+};
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+template <int ACT>
+__device__ __forceinline__ bool fast_range_ok(uint32_t vmax) {
+  return (vmax & 0xFFFFu) < FastRange<ACT>::kNegLimit && (vmax >> 16) < FastRange<ACT>::kNegLimit;
+}
+
+template <int ACT>
+__device__ __forceinline__ void fast_s_acc(float g, float& S, float& E) {
+  if (ACT == 0) {
+    const float th = __fmul_rn(g, -0x1.7154p+0f);            // exact
+    const float tl = __fmul_rn(g, -4.888495368504664e-06f);  // tail * ln2
+    const float e0 = ex2_approx(th);
+    E = __fmaf_rn(e0, tl, e0);
+  } else {
+    const float q = __fmul_rn(g, g), g3 = __fmul_rn(q, g);  // exact
+    const float w = __fmaf_rn(-0.10294324159622192f, g3, __fmul_rn(g, -2.3139550575201895e-05f));
+    E = ex2_approx(__fadd_rn(__fmul_rn(g, -0x1.26aep+1f), w));
+  }
+  S = rcp_approx(__fadd_rn(1.0f, E));
+}
+
+template <int ACT>
+__device__ __forceinline__ bool fast_ok_acc(float g) {
+  return ACT == 0 ? fabsf(g) < 64.0f : (g > -6.0f && g < 64.0f);
+}
+
+// act'(g) from S and E:  1 - S = E*S, so
+//   silu'(g) = S (1 + g E S),  gelu'(g) = S (1 + 2 g E S y'(g)),
+//   y'(g) = sqrt(2/pi) (1 + 3 * 0.044715 g^2).
+// Near the zero of act' the sum 1 + x cancels and magnifies the errors of
+// E and S; grad_ok() is false there (|1 + x| < |x| / 6) and the exact path
+// is used.
+template <int ACT>
+__device__ __forceinline__ float fast_grad(float g, float S, float E, float& x) {
+  const float es = __fmul_rn(E, S);
+  if (ACT == 0) {
+    x = __fmul_rn(g, es);
+  } else {
+    const float y2 = __fmaf_rn(0.21406444881780073f, __fmul_rn(g, g), 1.5957691216057308f);
+    x = __fmul_rn(__fmul_rn(g, es), y2);  // 2 y' g E S
+  }
+  return __fmaf_rn(S, x, S);
+}
+
+__device__ __forceinline__ bool grad_ok(float x) {
+  return fabsf(__fadd_rn(1.0f, x)) * 6.0f >= fabsf(x);
+}
+
+// Relative half-width d of the rounding test, above the fast path's worst
+// error plus one ulp each for the product rounding, the exact path's own
+// rounding and the bracket products.  The GPU tests measure the fast path
+// over every bf16 gate against these widths.
+constexpr float kBracket = 0x1p-17f;      // forward values and dUp
+constexpr float kBracketGrad = 0x1p-15f;  // dGate (act' amplifies E, S errors)
+
 // ----------------------------------------------------------------- MXFP8 --
 
 __device__ __forceinline__ uint32_t absbits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
@@ -137,7 +376,14 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 
 // Four fp32 (already scaled) -> one word of E4M3 codes, element 0 lowest.
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+  uint32_t r;
+  asm("{.reg .b16 lo, hi;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 // ----------------------------------------------------------------- NVFP4 --
@@ -159,6 +405,63 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   uint32_t ex = (c >> 3) & 0xFu, m = c & 7u;
   float mag = ex == 0 ? float(m) * 0x1p-9f : __uint_as_float(((ex + 120u) << 23) | (m << 20));
   return (c & 0x80u) ? -mag : mag;
+}
+
+// ------------------------------------------------------- rounding tests --
+
+// NaN-propagating max of |x| (a NaN or Inf anywhere reaches the block scale).
+__device__ __forceinline__ float amax_acc(float m, float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+  return r;
+}
+__device__ __forceinline__ float amax2(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)));
+  return r;
+}
+// max |x| over 8 values as a tree (depth 3)
+__device__ __forceinline__ float amax8(const float (&v)[8]) {
+  return amax2(amax2(amax2(v[0], v[1]), amax2(v[2], v[3])),
+               amax2(amax2(v[4], v[5]), amax2(v[6], v[7])));
+}
+
+// E8M0 byte for amax, or 0x100 when the fast amax cannot decide it: the
+// bracket amax*(1 -/+ d) straddles a 448 * 2^k boundary, the block holds a
+// NaN/Inf (or an overflowed product), or the block is tiny (its elements'
+// subnormal precision would matter after scaling by up to 2^127).
+__device__ __forceinline__ uint32_t e8m0_checked(float amax, float d) {
+  const uint32_t ab = __float_as_uint(amax);
+  if (!(ab < kInfBits) || (ab != 0u && ab < kTinyBits)) return 0x100u;
+  const uint32_t lo = e8m0_from_amax_bits(__float_as_uint(__fmul_rn(amax, 1.0f - d)));
+  const uint32_t hi = e8m0_from_amax_bits(__float_as_uint(__fmul_rn(amax, 1.0f + d)));
+  return lo == hi ? lo : 0x100u;
+}
+
+// E4M3 codes of four values scaled by the block multiplier, decided from
+// the bracket: mlo = 2^-e (1 - d), mhi = 2^-e (1 + d) (exact products of a
+// power of two).  `bad` is set when any value straddles a code boundary.
+__device__ __forceinline__ uint32_t e4m3x4_bracket(float a, float b, float c, float e, float mlo,
+                                                   float mhi, bool& bad) {
+  const uint32_t ql = e4m3x4(__fmul_rn(a, mlo), __fmul_rn(b, mlo), __fmul_rn(c, mlo), __fmul_rn(e, mlo));
+  const uint32_t qh = e4m3x4(__fmul_rn(a, mhi), __fmul_rn(b, mhi), __fmul_rn(c, mhi), __fmul_rn(e, mhi));
+  bad |= ql != qh;
+  return ql;
+}
+
+// Same test on two pairs with packed multiplies.
+__device__ __forceinline__ uint32_t e4m3x4_bracket2(float2 a, float2 b, float2 mlo, float2 mhi,
+                                                    bool& bad) {
+  const float2 al = mul2(a, mlo), bl = mul2(b, mlo), ah = mul2(a, mhi), bh = mul2(b, mhi);
+  const uint32_t ql = e4m3x4(al.x, al.y, bl.x, bl.y);
+  const uint32_t qh = e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  bad |= ql != qh;
+  return ql;
+}
+
+// E8M0 byte from a float amax (NaN/Inf -> 0xFF).
+__device__ __forceinline__ uint32_t e8m0_of(float amax) {
+  return e8m0_from_amax_bits(__float_as_uint(amax) & 0x7FFFFFFFu);
 }
 
 }  // namespace gq

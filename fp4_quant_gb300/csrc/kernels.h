@@ -3,9 +3,10 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/glu_quant.h"
+#include "glu_quant.h"
 
 namespace gq {
 
@@ -18,5 +19,13 @@ cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
 cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_fwd_plain(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_plain(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
+
+// 2-D TMA descriptor of a row-major matrix (tmap.cu).
+cudaError_t make_tile_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t cols,
+                          int64_t rows, int64_t row_stride_bytes, int box_cols, int box_rows,
+                          int swizzle_bytes = 0);
+
+// Error bits recorded by a kernel family (bounded waits that gave up).
+cudaError_t read_err_fwd_mx(uint32_t* v, bool clear);
 
 }  // namespace gq
