@@ -38,9 +38,9 @@ constexpr int kTR = 32;                       // tile rows
 constexpr int kWC = 32;                       // columns per warp sub-tile
 constexpr int kGroupWarps = 8;
 constexpr int kTC = kWC * kGroupWarps;        // tile columns
-// rowwise: 3 groups (more warps to hide latency); colwise/both: 2 (room for
-// the transpose buffers and fewer registers per thread to spill)
-__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_ROW ? 3 : 2; }
+// rowwise and colwise: 3 groups (more warps to hide latency); both: 2 (room
+// for the transpose buffers, fewer registers per thread to spill)
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 2 : 3; }
 __host__ __device__ constexpr int threads_for(int mode) { return (groups_for(mode) * kGroupWarps + 1) * 32; }
 constexpr int kStageBytes = kTR * kTC * 4;    // 32 KB: gate + up, or the pairs
 constexpr int kTStride = 33;                  // floats per transpose-buffer row
@@ -59,7 +59,7 @@ constexpr int kQBytes = 1024;
 __host__ __device__ constexpr int smem_for(int mode) {
   return 1024 + groups_for(mode) * kSlots * kStageBytes + kHotBytes +
          groups_for(mode) * kGroupWarps *
-             (((mode & GLU_MODE_COL) ? kTBytes : 0) + (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes) +
+             ((mode == GLU_MODE_BOTH ? kTBytes : 0) + (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes) +
          2 * 4 * 8;
 }
 
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   uint8_t* Qbase = hot_raw + kHotBytes;  // 1024-aligned (stages and hot table are)
   float* Tbase = reinterpret_cast<float*>(Qbase + kConsumers * kQPerWarp);
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Tbase) +
-                                               ((MODE & GLU_MODE_COL) ? kConsumers * kTBytes : 0));
+                                               (MODE == GLU_MODE_BOTH ? kConsumers * kTBytes : 0));
   uint64_t* empty = full + kStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -316,6 +316,76 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
     const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;  // this warp's sub-tile
     const bool active = c0 < p.N;
+    if (MODE == GLU_MODE_COL) {
+      // ---- column `lane` of the warp's box: 32 rows, read straight from the
+      // swizzled stage (for a fixed row the warp reads one 128-byte line)
+      float v[32];
+      uint32_t gmax = 0;
+      if (active) {
+        const uint8_t* st_base = stages + s * kStageBytes;
+#pragma unroll
+        for (int r = 0; r < kTR; r += 2) {
+          float2 g2, u2;
+          uint32_t g16a, g16b;
+          if (LAYOUT == GLU_LAYOUT_SPLIT) {
+            const uint8_t* A = st_base + (w >> 1) * kBoxBytes;
+            const uint8_t* B = A + 4 * kBoxBytes;
+            const int ck = 4 * (w & 1) + (lane >> 3), cb = 2 * (lane & 7);
+            g16a = *reinterpret_cast<const uint16_t*>(A + swz(r, ck) + cb);
+            g16b = *reinterpret_cast<const uint16_t*>(A + swz(r + 1, ck) + cb);
+            const uint32_t u16a = *reinterpret_cast<const uint16_t*>(B + swz(r, ck) + cb);
+            const uint32_t u16b = *reinterpret_cast<const uint16_t*>(B + swz(r + 1, ck) + cb);
+            g2 = make_float2(__uint_as_float(g16a << 16), __uint_as_float(g16b << 16));
+            u2 = make_float2(__uint_as_float(u16a << 16), __uint_as_float(u16b << 16));
+          } else {
+            const uint8_t* A = st_base + w * kBoxBytes;
+            const int ck = lane >> 2, cb = 4 * (lane & 3);
+            const uint32_t pa = *reinterpret_cast<const uint32_t*>(A + swz(r, ck) + cb);
+            const uint32_t pb = *reinterpret_cast<const uint32_t*>(A + swz(r + 1, ck) + cb);
+            g16a = pa & 0xFFFFu;
+            g16b = pb & 0xFFFFu;
+            g2 = make_float2(bf16_lo(pa), bf16_lo(pb));
+            u2 = make_float2(bf16_hi(pa), bf16_hi(pb));
+          }
+          gmax = vmax_u16x2(gmax, g16a | (g16b << 16));
+          const float2 h2 = fast_h2<ACT>(g2, u2);
+          v[r] = h2.x;
+          v[r + 1] = h2.y;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (!active) continue;
+      if (!fast_range_ok<ACT>(gmax)) {
+        uint32_t emask = 0;
+#pragma unroll 1
+        for (int r = 0; r < kTR; ++r) {
+          const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + r) * p.ld + c0 + lane)
+                                                          : __ldg(p.gate + (row0 + r) * p.ld + 2 * (c0 + lane));
+          emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << r;
+        }
+        while (emask != 0u) {
+          const int r = __ffs(emask) - 1;
+          emask &= emask - 1u;
+          set_elem(v, r, exact_at<ACT, LAYOUT>(p, hot, row0 + r, c0 + lane));
+        }
+      }
+      uint32_t q[8];
+      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(c0), Qc);
+        bulk_commit();
+      }
+      st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+      continue;
+    }
+
     // ---- row `lane` of the warp's box, two halves of 16 elements, then
     // free the stage; fast activation in pairs
     float h[32];
@@ -384,7 +454,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
 
     const bool row_ok = row0 + lane < p.M;
-    if (MODE & GLU_MODE_COL) {
+    if (MODE == GLU_MODE_BOTH) {
       // stage the values for the column pass before the row pass may
       // replace some of them (either is exact enough for the other pass)
       // (row stride 33 floats: the row writes and the column reads below
@@ -411,8 +481,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       if (row_ok) st_byte(p.s_row + (row0 + lane) * (p.N / 32) + c0 / 32, sc);
     }
 
-    // ---- colwise 32x1: lane l takes column l of the transposed sub-tile
-    if (MODE & GLU_MODE_COL) {
+    // ---- colwise 32x1 (both): lane l takes column l of the transposed sub-tile
+    if (MODE == GLU_MODE_BOTH) {
       __syncwarp();
       float v[32];
 #pragma unroll
@@ -420,10 +490,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       __syncwarp();  // the buffer may be rewritten by the next tile
       uint32_t q[8];
       const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
-      if (MODE == GLU_MODE_COL) {
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-      }  // (both: the wait above already covered this tile's previous stores)
+      // (the wait before the row box above covered this tile's previous stores)
       *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
       *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
       fence_proxy_async();
