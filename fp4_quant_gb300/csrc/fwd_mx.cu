@@ -5,26 +5,27 @@
 // colwise (32x1), or both scales come out of a single pass") and API.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
-//   * one persistent CTA per SM: a producer warp and 24 consumer warps in three
-//     groups.  Tiles are 32 rows x 256 columns; the producer streams them
-//     into a shared-memory ring with 2-D TMA loads (cp.async.bulk.tensor,
-//     completion counted in transaction bytes on an mbarrier) of 32-row
-//     boxes with 128-byte rows (64 bf16 columns, or 32 gate/up pairs) and the
-//     hardware 128-byte swizzle, so that a lane can read its whole row of a
-//     box without shared-memory bank conflicts;
-//   * tiles go round-robin to the CTAs (column strips first for colwise, so
-//     the CTAs working at once cover neighbouring 32-row groups of the same
-//     columns) and rotate over the groups;
-//   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31 and
-//     lane l its row l: a rowwise 1x32 block is one lane's 32 values (amax,
-//     scale and codes in registers, 32 code bytes stored as one sector);
-//     for colwise the warp transposes its sub-tile through a private padded
-//     shared-memory buffer and lane l quantises column l (32 code bytes, one
-//     sector of the [N, M] code matrix).  No barrier spans more than a warp;
+//   * one persistent CTA per SM with two groups of eight warps.  Tiles are
+//     32 rows x 256 columns; each group has a private two-slot ring of
+//     stages, filled by 2-D TMA loads (cp.async.bulk.tensor, completion
+//     counted in transaction bytes on an mbarrier) of 32-row boxes with
+//     128-byte rows (64 bf16 columns, or 32 gate/up pairs) and the hardware
+//     128-byte swizzle, so that a lane can read its row, or a warp a column,
+//     of a box without shared-memory bank conflicts.  No warp is set aside to
+//     produce: the warp that frees a stage last issues the next load into it;
+//   * tiles go round-robin to the CTAs (column strips first for colwise and
+//     both, so that the CTAs working at once cover neighbouring 32-row groups
+//     of the same columns, rows first for rowwise) and rotate over the groups;
+//   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31.
+//     Rowwise: lane l takes row l, a 1x32 block (amax, scale and codes in
+//     registers).  Colwise: lane l reads column l straight from the stage.
+//     Both: the row values also go through a private swizzled transpose
+//     buffer from which lane l reads column l.  Code boxes (32 x 32 bytes)
+//     leave through TMA stores; no barrier spans more than a warp;
 //   * the activation is the fast fp32 form; codes the rounding test cannot
 //     decide are recomputed one element at a time from the exact value, and a
-//     whole block only when its scale is undecided (exact values come from the
-//     hot slice of the activation table kept in shared memory).
+//     whole block only when its scale is undecided (exact values come from
+//     the activation table).
 #include <cstring>
 
 #include "glu_common.cuh"
@@ -38,30 +39,67 @@ constexpr int kTR = 32;                       // tile rows
 constexpr int kWC = 32;                       // columns per warp sub-tile
 constexpr int kGroupWarps = 8;
 constexpr int kTC = kWC * kGroupWarps;        // tile columns
-// rowwise and colwise: 3 groups (more warps to hide latency); both: 2 (room
-// for the transpose buffers, fewer registers per thread to spill)
-__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 2 : 3; }
-__host__ __device__ constexpr int threads_for(int mode) { return (groups_for(mode) * kGroupWarps + 1) * 32; }
+// Two groups of eight consumer warps: with two ring slots per group and the
+// hot table this fills about 190 KB of shared memory, and 544 threads leave
+// up to 120 registers per thread (three groups spilled and measured slower).
+__host__ __device__ constexpr int groups_for(int) { return 2; }
+__host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
 constexpr int kStageBytes = kTR * kTC * 4;    // 32 KB: gate + up, or the pairs
-constexpr int kTStride = 33;                  // floats per transpose-buffer row
-constexpr int kTBytes = kTR * kTStride * 4;
-constexpr int kHotBytes = kHotEntries * 8;
+// The exact path reads the hot slice of the activation table from shared
+// memory (kHotSmem; else everything from global memory through the
+// read-only cache, which measured 5-8% slower).
+constexpr bool kHotSmem = true;
+constexpr int kHotBytes = kHotSmem ? kHotEntries * 8 : 0;
 // Each consumer group has a private ring of kSlots stages: a stage is always
 // consumed, in order, by the one group that waits on it, so an mbarrier
 // parity wait can never be satisfied by an older phase of the same parity.
-// Warps copy their box to registers and release the stage at once, so one
-// slot per group keeps the next tile loading while the group computes.
-constexpr int kSlots = 1;
+// Two slots per group keep the group's next two tiles loading while it
+// computes (one slot leaves the load latency exposed at each tile).
+constexpr int kSlots = 2;
 // Codes leave through per-warp shared-memory boxes (32 x 32 bytes, 32-byte
 // swizzle) written to global memory by TMA stores.
 constexpr int kQBytes = 1024;
 
+// Ring control block in shared memory.  There is no producer warp: the
+// consumer warp that frees a stage last (an atomic count per stage) issues
+// the TMA loads of its group's next tile into it.  That keeps every warp a
+// consumer (16 warps: four per SM sub-partition, so up to 128 registers per
+// thread) and starts each load the moment its stage is free.
+struct alignas(16) RingCtl {
+  uint64_t full[8];     // per stage: one arrival (with the tile's byte count) + TMA bytes
+  uint32_t freed[8];    // per stage: warps that have freed it (wraps at kGroupWarps)
+  int64_t rt[8], ct[8];  // per stage: tile coordinates of the load in flight
+  int64_t major[4], minor[4];  // per group: walk position of its next tile to load
+  int64_t n_minor, dmaj, dmin;  // walk step (shared by the groups)
+};
+constexpr int kCtlBytes = int(sizeof(RingCtl));
+
 __host__ __device__ constexpr int smem_for(int mode) {
   return 1024 + groups_for(mode) * kSlots * kStageBytes + kHotBytes +
-         groups_for(mode) * kGroupWarps *
-             ((mode == GLU_MODE_BOTH ? kTBytes : 0) + (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes) +
-         2 * 4 * 8;
+         groups_for(mode) * kGroupWarps * (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes + kCtlBytes;
 }
+static_assert(2 * kSlots <= 8 && groups_for(0) <= 4, "ring control block too small");
+static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
+                  smem_for(GLU_MODE_BOTH) <= 232448,
+              "shared memory per CTA exceeds 227 KB");
+
+
+// Tile t of the grid-stride sequence as (major, minor) = (t / n_minor, t %
+// n_minor), advanced by a fixed step without dividing in the loop.
+struct TileWalk {
+  int64_t major, minor, n_minor, dmaj, dmin;
+  __device__ TileWalk(int64_t t0, int64_t step, int64_t n_min)
+      : major(t0 / n_min), minor(t0 % n_min), n_minor(n_min), dmaj(step / n_min),
+        dmin(step % n_min) {}
+  __device__ void next() {
+    major += dmaj;
+    minor += dmin;
+    if (minor >= n_minor) {
+      minor -= n_minor;
+      ++major;
+    }
+  }
+};
 
 // Byte offset of (row r, 16-byte chunk k) in a 32 x 32-byte code box with
 // the 32-byte swizzle (chunk ^= (r >> 2) & 1).
@@ -104,7 +142,8 @@ __device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t
     gb = __ldg(p.gate + row * p.ld + 2 * col);
     ub = __ldg(p.gate + row * p.ld + 2 * col + 1);
   }
-  return exact_act_mul_hot<ACT>(hot, __uint_as_float(gb << 16), __uint_as_float(ub << 16));
+  const float g = __uint_as_float(gb << 16), u = __uint_as_float(ub << 16);
+  return kHotSmem ? exact_act_mul_hot<ACT>(hot, g, u) : exact_act_mul<ACT>(g, u);
 }
 
 // v[e] = x for a runtime e, keeping v in registers.
@@ -134,15 +173,15 @@ __device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
 }
 
 // Quantise one 32-value MXFP8 block held by this thread.  Element e sits at
-// input (row0 + e, c0 + lane) for a column block and at (row0 + lane, c0 + e)
-// for a row block.  Codes are decided from the fast values where the
+// input (row0 + (e ^ rx), c0 + lane) for a column block and at (row0 + lane,
+// c0 + e) for a row block.  Codes are decided from the fast values where the
 // rounding test allows and from exact values elsewhere; the whole block is
 // recomputed from exact values when its scale is undecided.  Writes 8 code
 // words, returns the scale byte.
 template <int ACT, int LAYOUT, bool COLUMN>
 __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
                                                 const float2* hot, int64_t row0, int64_t c0,
-                                                int lane) {
+                                                int lane, int rx = 0) {
   constexpr float d = kBracket;
   uint32_t sc = e8m0_checked(amax32(v), d);
   if (sc != 0x100u) {
@@ -170,7 +209,7 @@ __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8]
       while (emask != 0u) {
         const int e = __ffs(emask) - 1;
         emask &= emask - 1u;
-        const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + e, c0 + lane)
+        const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
                                : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
         set_elem(v, e, x);
       }
@@ -181,7 +220,7 @@ __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8]
   // undecided scale (or a NaN/Inf/tiny block): the block from exact values
 #pragma unroll 1
   for (int e = 0; e < 32; ++e) {
-    const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + e, c0 + lane)
+    const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
                            : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
     set_elem(v, e, x);
   }
@@ -209,111 +248,110 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   uint8_t* hot_raw = smem + kStages * kStageBytes;
   const float2* hot = reinterpret_cast<const float2*>(hot_raw);
   uint8_t* Qbase = hot_raw + kHotBytes;  // 1024-aligned (stages and hot table are)
-  float* Tbase = reinterpret_cast<float*>(Qbase + kConsumers * kQPerWarp);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Tbase) +
-                                               (MODE == GLU_MODE_BOTH ? kConsumers * kTBytes : 0));
-  uint64_t* empty = full + kStages;
+  RingCtl* ctl = reinterpret_cast<RingCtl*>(Qbase + kConsumers * kQPerWarp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t my_tiles = (p.ntiles - blockIdx.x + G - 1) / G;
 
-  load_hot_table<8>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  if (kHotSmem) load_hot_table<8>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGroupWarps);
+    prefetch_tensormap(&p.tm_a);
+    if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
+    if (MODE & GLU_MODE_ROW) prefetch_tensormap(&p.tm_qr);
+    if (MODE & GLU_MODE_COL) prefetch_tensormap(&p.tm_qc);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&ctl->full[st], 1);
+      ctl->freed[st] = 0;
+    }
+    // group g loads the CTA's tiles g, g + kGroups, ... of the grid-stride
+    // sequence blockIdx.x + i * gridDim.x
+    const int64_t n_minor = MODE == GLU_MODE_ROW ? p.n_ct : p.n_rt;
+    for (int g = 0; g < kGroups; ++g) {
+      const TileWalk tw(blockIdx.x + g * G, kGroups * G, n_minor);
+      ctl->major[g] = tw.major;
+      ctl->minor[g] = tw.minor;
+      if (g == 0) {
+        ctl->n_minor = tw.n_minor;
+        ctl->dmaj = tw.dmaj;
+        ctl->dmin = tw.dmin;
+      }
     }
     fence_barrier_init();
   }
   __syncthreads();
 
-  const int64_t G = gridDim.x;
-  const int64_t my_tiles = (p.ntiles - blockIdx.x + G - 1) / G;
-
-  // ------------------------------------------------------------ producer --
   // Stage layout: split: gate boxes 0..3 then up boxes 0..3 (box b holds the
-  // columns of warps 2b and 2b+1); interleaved: pair boxes 0..7.
-  // Tile i goes to group i % kGroups, slot (i / kGroups) % kSlots of that
-  // group's ring.
-  if (warp == kConsumers) {
+  // columns of warps 2b and 2b+1); interleaved: pair boxes 0..7.  The k-th
+  // tile of group g uses stage g * kSlots + k % kSlots.
+  auto issue = [&](int st, int g) {  // whole warp; lanes 0..7 issue one box each
+    int64_t rt = 0, ct = 0;
     if (lane == 0) {
-      prefetch_tensormap(&p.tm_a);
-      if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
-      if (MODE & GLU_MODE_ROW) prefetch_tensormap(&p.tm_qr);
-      if (MODE & GLU_MODE_COL) prefetch_tensormap(&p.tm_qc);
-    }
-    int64_t last_k[kStages];
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) last_k[st] = -1;
-    for (int64_t i = 0; i < my_tiles; ++i) {
-      const int grp = int(i % kGroups);
-      const int64_t k = i / kGroups;
-      const int st = grp * kSlots + int(k % kSlots);
-      bool ok = true;
-      if (lane == 0 && k >= kSlots) ok = mbar_wait(&empty[st], uint32_t((k / kSlots) & 1) ^ 1u);
-      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-        if (lane == 0) atomicOr(&g_err_fwd_mx, kErrWaitEmpty);
-        break;
+      const int64_t major = ctl->major[g], minor = ctl->minor[g];
+      rt = MODE == GLU_MODE_ROW ? major : minor;
+      ct = MODE == GLU_MODE_ROW ? minor : major;
+      ctl->rt[st] = rt;
+      ctl->ct[st] = ct;
+      int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
+      if (mn >= ctl->n_minor) {
+        mn -= ctl->n_minor;
+        ++mj;
       }
-      const int64_t t = blockIdx.x + i * G;
-      int64_t rt, ct;
-      if (MODE == GLU_MODE_ROW) {
-        rt = t / p.n_ct;
-        ct = t - rt * p.n_ct;
-      } else {
-        ct = t / p.n_rt;
-        rt = t - ct * p.n_rt;
-      }
-      uint8_t* dst = stages + st * kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageBytes);
-      __syncwarp();
-      // eight boxes per tile, issued by lanes 0..7
-      if (lane < 8) {
-        const int32_t y = int32_t(rt * kTR);
-        if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          const int b = lane & 3;
-          tma_load_2d(dst + lane * kBoxBytes, lane < 4 ? &p.tm_a : &p.tm_b,
-                      int32_t(ct * kTC + b * 64), y, &full[st]);
-        } else {
-          tma_load_2d(dst + lane * kBoxBytes, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &full[st]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kStages; ++q)
-        if (q == st) last_k[q] = k;
+      ctl->major[g] = mj;
+      ctl->minor[g] = mn;
+      mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
     }
-    // never leave with copies in flight: wait (bounded) for the last load of
-    // every slot (already complete unless a consumer gave up)
-    if (lane == 0) {
-#pragma unroll
-      for (int st = 0; st < kStages; ++st)
-        if (last_k[st] >= 0 && !mbar_wait(&full[st], uint32_t((last_k[st] / kSlots) & 1)))
-          atomicOr(&g_err_fwd_mx, kErrDrain);
+    rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
+    ct = __shfl_sync(0xFFFFFFFFu, ct, 0);
+    if (lane < 8) {
+      uint8_t* dst = stages + st * kStageBytes + lane * kBoxBytes;
+      const int32_t y = int32_t(rt * kTR);
+      if (LAYOUT == GLU_LAYOUT_SPLIT)
+        tma_load_2d(dst, lane < 4 ? &p.tm_a : &p.tm_b, int32_t(ct * kTC + (lane & 3) * 64), y,
+                    &ctl->full[st]);
+      else
+        tma_load_2d(dst, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &ctl->full[st]);
     }
-    return;
-  }
-
+  };
   // ----------------------------------------------------------- consumers --
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
-  float* T = Tbase + warp * (kTR * kTStride);
   uint8_t* Qr = Qbase + warp * kQPerWarp;                                 // row codes
   uint8_t* Qc = Qr + ((MODE == GLU_MODE_BOTH) ? kQBytes : 0);             // column codes
 
-  for (int64_t k = 0;; ++k) {
+  // Free stage s after this warp's last read of it; the last of the group's
+  // warps to do so loads the group's tile k + kSlots into it.
+  auto release = [&](int s, int64_t k) {
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicInc(&ctl->freed[s], kGroupWarps - 1) == kGroupWarps - 1;
+      if (last) __threadfence_block();
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0) && grp + kGroups * (k + kSlots) < my_tiles) {
+      if (MODE == GLU_MODE_BOTH) fence_proxy_async();  // the stage was written (transpose)
+      issue(s, grp);
+    }
+  };
+
+  // the group's first warp loads its first kSlots tiles (a warp of the same
+  // group, so that these issues precede every later one of the group)
+  if (w == 0) {
+    for (int j = 0; j < kSlots; ++j)
+      if (grp + int64_t(kGroups) * j < my_tiles) issue(grp * kSlots + j, grp);
+  }
+
+  int64_t k = 0;
+  bool failed = false;
+  for (;; ++k) {
     const int64_t i = kGroups * k + grp;
     if (i >= my_tiles) break;
     const int s = grp * kSlots + int(k % kSlots);
-    if (!mbar_wait(&full[s], uint32_t((k / kSlots) & 1))) {
+    if (!mbar_wait(&ctl->full[s], uint32_t((k / kSlots) & 1))) {
       if (lane == 0) atomicOr(&g_err_fwd_mx, kErrWaitFull);
+      failed = true;
       break;
     }
-    const int64_t t = blockIdx.x + i * G;
-    int64_t rt, ct;
-    if (MODE == GLU_MODE_ROW) {
-      rt = t / p.n_ct;
-      ct = t - rt * p.n_ct;
-    } else {
-      ct = t / p.n_rt;
-      rt = t - ct * p.n_rt;
-    }
+    const int64_t rt = ctl->rt[s], ct = ctl->ct[s];
     const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;  // this warp's sub-tile
     const bool active = c0 < p.N;
     if (MODE == GLU_MODE_COL) {
@@ -353,8 +391,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           v[r + 1] = h2.y;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      release(s, k);
       if (!active) continue;
       if (!fast_range_ok<ACT>(gmax)) {
         uint32_t emask = 0;
@@ -433,8 +470,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    // (both: the stage is kept for the transpose below)
+    if (MODE != GLU_MODE_BOTH || !active) release(s, k);
     if (!active) continue;
 
     if (!fast_range_ok<ACT>(gmax)) {
@@ -454,13 +491,32 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
 
     const bool row_ok = row0 + lane < p.M;
+    // Both: transpose through the warp's own part of the stage.  Lane l has
+    // read exactly the bytes of row l that belong to this warp (split: 64
+    // bytes of the gate box and 64 of the up box; pairs: the 128-byte row of
+    // the warp's box), so it may overwrite them with its 32 fp32 values (chunk
+    // j of 16 bytes at the j-th of those chunk slots) without waiting for the
+    // other lanes.  The values are staged before the row pass may replace some
+    // of them with exact ones (either is exact enough for the other pass).
+    // Column reads: lane c reads chunk c / 4; in the split layout lanes 16..31
+    // (the up box, same banks as the gate box) read row r ^ 4 at step r, which
+    // moves them to the other four chunk slots of the swizzle, so no two
+    // lanes share a bank; their v[] is in row order r ^ 4.  The column reads
+    // wait until the row pass is done, so that h[] and v[] are never live
+    // together (the stage stays held meanwhile; the group's other slot is
+    // loading).
+    const int rx = (LAYOUT == GLU_LAYOUT_SPLIT && lane >= 16) ? 4 : 0;
+    uint8_t* const A = LAYOUT == GLU_LAYOUT_SPLIT ? stages + s * kStageBytes + (w >> 1) * kBoxBytes
+                                                  : stages + s * kStageBytes + w * kBoxBytes;
+    const int cbase = LAYOUT == GLU_LAYOUT_SPLIT ? 4 * (w & 1) : 0;
     if (MODE == GLU_MODE_BOTH) {
-      // stage the values for the column pass before the row pass may
-      // replace some of them (either is exact enough for the other pass)
-      // (row stride 33 floats: the row writes and the column reads below
-      // both touch 32 distinct banks)
 #pragma unroll
-      for (int e = 0; e < 32; ++e) T[lane * kTStride + e] = h[e];
+      for (int j = 0; j < 8; ++j) {
+        uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && j >= 4) ? A + 4 * kBoxBytes : A;
+        const int chunk = LAYOUT == GLU_LAYOUT_SPLIT ? cbase + (j & 3) : j;
+        *reinterpret_cast<float4*>(box + swz(lane, chunk)) =
+            make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+      }
     }
 
     // ---- rowwise 1x32: this lane's 32 values
@@ -481,15 +537,31 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       if (row_ok) st_byte(p.s_row + (row0 + lane) * (p.N / 32) + c0 / 32, sc);
     }
 
-    // ---- colwise 32x1 (both): lane l takes column l of the transposed sub-tile
+    // ---- colwise 32x1 (both): lane l takes column l of the staged values
     if (MODE == GLU_MODE_BOTH) {
-      __syncwarp();
       float v[32];
+      __syncwarp();
+      {
+        const uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && lane >= 16) ? A + 4 * kBoxBytes : A;
+        const int chunk = LAYOUT == GLU_LAYOUT_SPLIT ? cbase + ((lane >> 2) & 3) : (lane >> 2);
+        const int wb = 4 * (lane & 3);
 #pragma unroll
-      for (int r = 0; r < kTR; ++r) v[r] = T[r * kTStride + lane];
-      __syncwarp();  // the buffer may be rewritten by the next tile
+        for (int r = 0; r < kTR; ++r)
+          v[r] = *reinterpret_cast<const float*>(box + swz(r ^ rx, chunk) + wb);
+      }
+      // generic-proxy writes to the stage precede the next TMA load into it
+      fence_proxy_async();
+      release(s, k);
       uint32_t q[8];
-      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
+      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane, rx);
+      if (rx != 0) {  // back to row order: words 2i and 2i + 1 trade places
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t t0 = q[2 * i];
+          q[2 * i] = q[2 * i + 1];
+          q[2 * i + 1] = t0;
+        }
+      }
       // (the wait before the row box above covered this tile's previous stores)
       *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
       *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
@@ -500,6 +572,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         bulk_commit();
       }
       st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+    }
+  }
+  if (failed && lane == 0) {
+    // a wait gave up: never leave with loads in flight; wait (bounded) for
+    // the group's loads that may have been issued
+    for (int64_t kk = k; kk < k + kSlots; ++kk) {
+      if (grp + kGroups * kk >= my_tiles) break;
+      if (!mbar_wait(&ctl->full[grp * kSlots + int(kk % kSlots)], uint32_t((kk / kSlots) & 1)))
+        atomicOr(&g_err_fwd_mx, kErrDrain);
     }
   }
   if (lane == 0) bulk_wait0();  // no code box may still be in flight at exit
