@@ -46,19 +46,31 @@ __host__ __device__ constexpr int groups_for(int) { return 2; }
 __host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
 constexpr int kStageBytes = kTR * kTC * 4;    // 32 KB: gate + up, or the pairs
 // The exact path reads the hot slice of the activation table from shared
-// memory (kHotSmem; else everything from global memory through the
-// read-only cache, which measured 5-8% slower).
-constexpr bool kHotSmem = true;
-constexpr int kHotBytes = kHotSmem ? kHotEntries * 8 : 0;
+// memory (reading it from global memory through the read-only cache
+// measured 5-8% slower): 2^-10 <= |g| < 16, or 2^-6 <= |g| < 4 where both
+// code boxes need the room.
+__host__ __device__ constexpr uint32_t hot_lo_for(int mode) { return mode == GLU_MODE_BOTH ? 121u : kHotExpLo; }
+__host__ __device__ constexpr uint32_t hot_bin_for(int mode) { return mode == GLU_MODE_BOTH ? 8u : kHotBinades; }
+__host__ __device__ constexpr int hot_bytes_for(int mode) { return int(hot_bin_for(mode)) * 256 * 8; }
 // Each consumer group has a private ring of kSlots stages: a stage is always
 // consumed, in order, by the one group that waits on it, so an mbarrier
 // parity wait can never be satisfied by an older phase of the same parity.
 // Two slots per group keep the group's next two tiles loading while it
 // computes (one slot leaves the load latency exposed at each tile).
 constexpr int kSlots = 2;
-// Codes leave through per-warp shared-memory boxes (32 x 32 bytes, 32-byte
-// swizzle) written to global memory by TMA stores.
+// Codes leave through per-warp shared-memory boxes written to global memory
+// by TMA stores.  Rowwise: 32 rows x 32 bytes (32-byte swizzle), one box per
+// tile.  Colwise: the [N, M] code matrix takes 32 bytes per column from a
+// tile, and stores of such 32-byte pieces at a stride of M bytes measured
+// 20% slower than the rowwise pattern; so a group walks kSuper row tiles of
+// the same columns in a row and the warp fills a 32 x 128-byte box (128-byte
+// swizzle), stored once per kSuper tiles.
 constexpr int kQBytes = 1024;
+constexpr int kSuper = 4;
+constexpr int kQcBytes = 32 * 32 * kSuper;
+__host__ __device__ constexpr int qbytes_for(int mode) {
+  return (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
+}
 
 // Ring control block in shared memory.  There is no producer warp: the
 // consumer warp that frees a stage last (an atomic count per stage) issues
@@ -75,8 +87,8 @@ struct alignas(16) RingCtl {
 constexpr int kCtlBytes = int(sizeof(RingCtl));
 
 __host__ __device__ constexpr int smem_for(int mode) {
-  return 1024 + groups_for(mode) * kSlots * kStageBytes + kHotBytes +
-         groups_for(mode) * kGroupWarps * (mode == GLU_MODE_BOTH ? 2 : 1) * kQBytes + kCtlBytes;
+  return 1024 + groups_for(mode) * kSlots * kStageBytes + hot_bytes_for(mode) +
+         groups_for(mode) * kGroupWarps * qbytes_for(mode) + kCtlBytes;
 }
 static_assert(2 * kSlots <= 8 && groups_for(0) <= 4, "ring control block too small");
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
@@ -121,6 +133,7 @@ struct alignas(64) FwdP {
   uint8_t* q_col;
   uint8_t* s_col;
   int64_t n_rt, n_ct, ntiles;
+  int64_t n_rs;  // colwise: groups of kSuper row tiles
 };
 
 // Boxes have 32 rows of 128 bytes; the 128-byte swizzle stores the 16-byte
@@ -132,7 +145,7 @@ __device__ __forceinline__ int swz(int r, int chunk) { return r * 128 + 16 * (ch
 
 // Exact act(g) * u of element (row, col) of the input, read from global
 // memory (the rare path runs after the warp has released its stage).
-template <int ACT, int LAYOUT>
+template <int ACT, int MODE, int LAYOUT>
 __device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t row, int64_t col) {
   uint32_t gb, ub;
   if (LAYOUT == GLU_LAYOUT_SPLIT) {
@@ -143,7 +156,7 @@ __device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t
     ub = __ldg(p.gate + row * p.ld + 2 * col + 1);
   }
   const float g = __uint_as_float(gb << 16), u = __uint_as_float(ub << 16);
-  return kHotSmem ? exact_act_mul_hot<ACT>(hot, g, u) : exact_act_mul<ACT>(g, u);
+  return exact_act_mul_hot<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, g, u);
 }
 
 // v[e] = x for a runtime e, keeping v in registers.
@@ -178,7 +191,7 @@ __device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
 // rounding test allows and from exact values elsewhere; the whole block is
 // recomputed from exact values when its scale is undecided.  Writes 8 code
 // words, returns the scale byte.
-template <int ACT, int LAYOUT, bool COLUMN>
+template <int ACT, int MODE, int LAYOUT, bool COLUMN>
 __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
                                                 const float2* hot, int64_t row0, int64_t c0,
                                                 int lane, int rx = 0) {
@@ -209,8 +222,8 @@ __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8]
       while (emask != 0u) {
         const int e = __ffs(emask) - 1;
         emask &= emask - 1u;
-        const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
-                               : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
+        const float x = COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
+                               : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
         set_elem(v, e, x);
       }
       codes32(v, mul, q);
@@ -220,8 +233,8 @@ __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8]
   // undecided scale (or a NaN/Inf/tiny block): the block from exact values
 #pragma unroll 1
   for (int e = 0; e < 32; ++e) {
-    const float x = COLUMN ? exact_at<ACT, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
-                           : exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e);
+    const float x = COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
+                           : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
     set_elem(v, e, x);
   }
   sc = e8m0_of(amax32(v));
@@ -234,26 +247,51 @@ __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8]
   return sc;
 }
 
+// Colwise codes of row tile j of a unit into the warp's 32 x 128-byte box:
+// lane l (column l) owns box row l, bytes 32j..32j+31 (16-byte chunks 2j and
+// 2j + 1, at chunk c ^ (l & 7) under the 128-byte swizzle).
+__device__ __forceinline__ void put_qc(uint8_t* Qc, int lane, int j, const uint32_t (&q)[8]) {
+  *reinterpret_cast<uint4*>(Qc + swz(lane, 2 * j)) = make_uint4(q[0], q[1], q[2], q[3]);
+  *reinterpret_cast<uint4*>(Qc + swz(lane, 2 * j + 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+}
+
+// Store the warp's colwise box: columns c0..c0+31 of the [N, M] code matrix,
+// bytes row0..row0+127 of each (the part past M is clipped by the copy).
+__device__ __forceinline__ void store_qc(const CUtensorMap* map, const uint8_t* Qc, int64_t row0,
+                                         int64_t c0, int lane) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, int32_t(row0), int32_t(c0), Qc);
+    bulk_commit();
+  }
+}
+
 template <int ACT, int MODE, int LAYOUT>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     fwd_mx_kernel(const __grid_constant__ FwdP p) {
   constexpr int kGroups = groups_for(MODE);
   constexpr int kConsumers = kGroups * kGroupWarps;
   constexpr int kStages = kGroups * kSlots;
-  constexpr int kQPerWarp = (MODE == GLU_MODE_BOTH ? 2 : 1) * kQBytes;
+  constexpr int kQPerWarp = qbytes_for(MODE);
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
   uint8_t* hot_raw = smem + kStages * kStageBytes;
   const float2* hot = reinterpret_cast<const float2*>(hot_raw);
-  uint8_t* Qbase = hot_raw + kHotBytes;  // 1024-aligned (stages and hot table are)
+  uint8_t* Qbase = hot_raw + hot_bytes_for(MODE);  // 1024-aligned (stages and hot table are)
   RingCtl* ctl = reinterpret_cast<RingCtl*>(Qbase + kConsumers * kQPerWarp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
-  const int64_t my_tiles = (p.ntiles - blockIdx.x + G - 1) / G;
+  // Work units: rowwise a tile, else kSuper row tiles of the same columns.
+  // Unit u of the grid-stride sequence blockIdx.x + i * gridDim.x goes to
+  // group i % kGroups; n_g counts the tiles of this warp's group.
+  constexpr int kPer = MODE == GLU_MODE_ROW ? 1 : kSuper;
+  const int64_t units = MODE == GLU_MODE_ROW ? p.ntiles : p.n_rs * p.n_ct;
+  const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  if (kHotSmem) load_hot_table<8>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -263,9 +301,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
     }
-    // group g loads the CTA's tiles g, g + kGroups, ... of the grid-stride
-    // sequence blockIdx.x + i * gridDim.x
-    const int64_t n_minor = MODE == GLU_MODE_ROW ? p.n_ct : p.n_rt;
+    const int64_t n_minor = MODE == GLU_MODE_ROW ? p.n_ct : p.n_rs;
     for (int g = 0; g < kGroups; ++g) {
       const TileWalk tw(blockIdx.x + g * G, kGroups * G, n_minor);
       ctl->major[g] = tw.major;
@@ -282,27 +318,35 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
 
   // Stage layout: split: gate boxes 0..3 then up boxes 0..3 (box b holds the
   // columns of warps 2b and 2b+1); interleaved: pair boxes 0..7.  The k-th
-  // tile of group g uses stage g * kSlots + k % kSlots.
-  auto issue = [&](int st, int g) {  // whole warp; lanes 0..7 issue one box each
+  // tile of group g uses stage g * kSlots + k % kSlots.  Colwise row tiles
+  // past the last one (the ragged end of a unit) load nothing: the stage's
+  // phase completes on the plain arrival and the consumers skip the tile.
+  auto issue = [&](int st, int g, int64_t kk) {  // whole warp; lanes 0..7 issue one box each
     int64_t rt = 0, ct = 0;
     if (lane == 0) {
       const int64_t major = ctl->major[g], minor = ctl->minor[g];
-      rt = MODE == GLU_MODE_ROW ? major : minor;
+      const int j = int(kk % kPer);
+      rt = MODE == GLU_MODE_ROW ? major : kSuper * minor + j;
       ct = MODE == GLU_MODE_ROW ? minor : major;
       ctl->rt[st] = rt;
       ctl->ct[st] = ct;
-      int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
-      if (mn >= ctl->n_minor) {
-        mn -= ctl->n_minor;
-        ++mj;
+      if (j == kPer - 1) {
+        int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
+        if (mn >= ctl->n_minor) {
+          mn -= ctl->n_minor;
+          ++mj;
+        }
+        ctl->major[g] = mj;
+        ctl->minor[g] = mn;
       }
-      ctl->major[g] = mj;
-      ctl->minor[g] = mn;
-      mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
+      if (rt < p.n_rt)
+        mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
+      else
+        mbar_arrive(&ctl->full[st]);
     }
     rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
     ct = __shfl_sync(0xFFFFFFFFu, ct, 0);
-    if (lane < 8) {
+    if (lane < 8 && rt < p.n_rt) {
       uint8_t* dst = stages + st * kStageBytes + lane * kBoxBytes;
       const int32_t y = int32_t(rt * kTR);
       if (LAYOUT == GLU_LAYOUT_SPLIT)
@@ -316,6 +360,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
   uint8_t* Qr = Qbase + warp * kQPerWarp;                                 // row codes
   uint8_t* Qc = Qr + ((MODE == GLU_MODE_BOTH) ? kQBytes : 0);             // column codes
+  const int64_t n_g = kPer * (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0);
 
   // Free stage s after this warp's last read of it; the last of the group's
   // warps to do so loads the group's tile k + kSlots into it.
@@ -327,9 +372,9 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       last = atomicInc(&ctl->freed[s], kGroupWarps - 1) == kGroupWarps - 1;
       if (last) __threadfence_block();
     }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0) && grp + kGroups * (k + kSlots) < my_tiles) {
+    if (__shfl_sync(0xFFFFFFFFu, last, 0) && k + kSlots < n_g) {
       if (MODE == GLU_MODE_BOTH) fence_proxy_async();  // the stage was written (transpose)
-      issue(s, grp);
+      issue(s, grp, k + kSlots);
     }
   };
 
@@ -337,14 +382,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   // group, so that these issues precede every later one of the group)
   if (w == 0) {
     for (int j = 0; j < kSlots; ++j)
-      if (grp + int64_t(kGroups) * j < my_tiles) issue(grp * kSlots + j, grp);
+      if (j < n_g) issue(grp * kSlots + j, grp, j);
   }
 
   int64_t k = 0;
   bool failed = false;
-  for (;; ++k) {
-    const int64_t i = kGroups * k + grp;
-    if (i >= my_tiles) break;
+  for (; k < n_g; ++k) {
     const int s = grp * kSlots + int(k % kSlots);
     if (!mbar_wait(&ctl->full[s], uint32_t((k / kSlots) & 1))) {
       if (lane == 0) atomicOr(&g_err_fwd_mx, kErrWaitFull);
@@ -353,13 +396,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
     const int64_t rt = ctl->rt[s], ct = ctl->ct[s];
     const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;  // this warp's sub-tile
-    const bool active = c0 < p.N;
+    const int j = int(k % kPer);        // colwise: position in the unit
+    const bool active = c0 < p.N;       // the warp has columns
+    const bool work = active && rt < p.n_rt;  // ... and the tile has rows
     if (MODE == GLU_MODE_COL) {
       // ---- column `lane` of the warp's box: 32 rows, read straight from the
       // swizzled stage (for a fixed row the warp reads one 128-byte line)
       float v[32];
       uint32_t gmax = 0;
-      if (active) {
+      if (work) {
         const uint8_t* st_base = stages + s * kStageBytes;
 #pragma unroll
         for (int r = 0; r < kTR; r += 2) {
@@ -393,33 +438,31 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
       release(s, k);
       if (!active) continue;
-      if (!fast_range_ok<ACT>(gmax)) {
-        uint32_t emask = 0;
+      if (j == 0) {  // the unit's box: the previous unit's store has read it out
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+      }
+      if (work) {
+        if (!fast_range_ok<ACT>(gmax)) {
+          uint32_t emask = 0;
 #pragma unroll 1
-        for (int r = 0; r < kTR; ++r) {
-          const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + r) * p.ld + c0 + lane)
-                                                          : __ldg(p.gate + (row0 + r) * p.ld + 2 * (c0 + lane));
-          emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << r;
+          for (int r = 0; r < kTR; ++r) {
+            const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + r) * p.ld + c0 + lane)
+                                                            : __ldg(p.gate + (row0 + r) * p.ld + 2 * (c0 + lane));
+            emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << r;
+          }
+          while (emask != 0u) {
+            const int r = __ffs(emask) - 1;
+            emask &= emask - 1u;
+            set_elem(v, r, exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + r, c0 + lane));
+          }
         }
-        while (emask != 0u) {
-          const int r = __ffs(emask) - 1;
-          emask &= emask - 1u;
-          set_elem(v, r, exact_at<ACT, LAYOUT>(p, hot, row0 + r, c0 + lane));
-        }
+        uint32_t q[8];
+        const uint32_t sc = quant_block<ACT, MODE, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
+        put_qc(Qc, lane, j, q);
+        st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
       }
-      uint32_t q[8];
-      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
-      if (lane == 0) bulk_wait_read0();
-      __syncwarp();
-      *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
-      *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(c0), Qc);
-        bulk_commit();
-      }
-      st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+      if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
       continue;
     }
 
@@ -427,7 +470,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // free the stage; fast activation in pairs
     float h[32];
     uint32_t gmax = 0;  // running max of the raw gate patterns (range check)
-    if (active) {
+    if (work) {
       const uint8_t* st_base = stages + s * kStageBytes;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -471,8 +514,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
     }
     // (both: the stage is kept for the transpose below)
-    if (MODE != GLU_MODE_BOTH || !active) release(s, k);
-    if (!active) continue;
+    if (MODE != GLU_MODE_BOTH || !work) release(s, k);
+    if (!work) {
+      if (MODE == GLU_MODE_BOTH && active && j == kSuper - 1)
+        store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+      continue;
+    }
 
     if (!fast_range_ok<ACT>(gmax)) {
       // gates outside the fast range (rare): exact values for those
@@ -486,7 +533,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       while (emask != 0u) {
         const int e = __ffs(emask) - 1;
         emask &= emask - 1u;
-        set_elem(h, e, exact_at<ACT, LAYOUT>(p, hot, row0 + lane, c0 + e));
+        set_elem(h, e, exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e));
       }
     }
 
@@ -522,7 +569,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // ---- rowwise 1x32: this lane's 32 values
     if (MODE & GLU_MODE_ROW) {
       uint32_t q[8];
-      const uint32_t sc = quant_block<ACT, LAYOUT, false>(h, q, p, hot, row0, c0, lane);
+      const uint32_t sc = quant_block<ACT, MODE, LAYOUT, false>(h, q, p, hot, row0, c0, lane);
       // previous tile's code box must have been read out by its TMA store
       if (lane == 0) bulk_wait_read0();
       __syncwarp();
@@ -553,7 +600,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       fence_proxy_async();
       release(s, k);
       uint32_t q[8];
-      const uint32_t sc = quant_block<ACT, LAYOUT, true>(v, q, p, hot, row0, c0, lane, rx);
+      const uint32_t sc = quant_block<ACT, MODE, LAYOUT, true>(v, q, p, hot, row0, c0, lane, rx);
       if (rx != 0) {  // back to row order: words 2i and 2i + 1 trade places
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -562,23 +609,17 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           q[2 * i + 1] = t0;
         }
       }
-      // (the wait before the row box above covered this tile's previous stores)
-      *reinterpret_cast<uint4*>(Qc + qswz(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
-      *reinterpret_cast<uint4*>(Qc + qswz(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(c0), Qc);
-        bulk_commit();
-      }
+      // (the wait before the row box above covered the previous unit's store)
+      put_qc(Qc, lane, j, q);
       st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+      if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
     }
   }
   if (failed && lane == 0) {
     // a wait gave up: never leave with loads in flight; wait (bounded) for
     // the group's loads that may have been issued
     for (int64_t kk = k; kk < k + kSlots; ++kk) {
-      if (grp + kGroups * kk >= my_tiles) break;
+      if (kk >= n_g) break;
       if (!mbar_wait(&ctl->full[grp * kSlots + int(kk % kSlots)], uint32_t((kk / kSlots) & 1)))
         atomicOr(&g_err_fwd_mx, kErrDrain);
     }
@@ -607,7 +648,7 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
     e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N, a.M, a.N, kWC, kTR, 32);
   if (e == cudaSuccess && (MODE & GLU_MODE_COL))
-    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, a.N, a.M, kTR, kWC, 32);
+    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, a.N, a.M, kTR * kSuper, kWC, 128);
   if (e != cudaSuccess) return e;
   p.M = a.M;
   p.N = a.N;
@@ -618,7 +659,9 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
   p.ntiles = p.n_rt * p.n_ct;
-  const int grid = int(p.ntiles < d.sms ? p.ntiles : d.sms);
+  p.n_rs = (p.n_rt + kSuper - 1) / kSuper;
+  const int64_t units = MODE == GLU_MODE_ROW ? p.ntiles : p.n_rs * p.n_ct;
+  const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(threads_for(MODE));

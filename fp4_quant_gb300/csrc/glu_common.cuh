@@ -156,40 +156,47 @@ __device__ __forceinline__ float exact_grad_mul(float g, float dy, float u) {
 }
 
 // Hot slice of a table kept in shared memory: bf16 exponent fields
-// kHotExpLo .. kHotExpLo + kHotBinades - 1 (2^-10 <= |g| < 16), positive
-// gates then negative gates.  It serves the exact path of the kernels, whose
-// undecided blocks are rare but otherwise wait on L2 latency.
+// LO .. LO + BIN - 1, positive gates then negative gates.  It serves the
+// exact path of the kernels, whose undecided blocks are rare but otherwise
+// wait on L2 latency.  Default slice: 2^-10 <= |g| < 16.
 constexpr uint32_t kHotExpLo = 117;
 constexpr uint32_t kHotBinades = 14;
-constexpr uint32_t kHotHalf = kHotBinades * 128;
-constexpr uint32_t kHotEntries = 2 * kHotHalf;
-constexpr uint32_t kHotSkip = (kHotExpLo - GQ_TAB_EXP_LO) * 128;  // first hot slot per sign
+template <uint32_t BIN = kHotBinades>
+struct HotSize {
+  static constexpr uint32_t kHalf = BIN * 128;
+  static constexpr uint32_t kEntries = 2 * kHalf;
+};
+constexpr uint32_t kHotEntries = HotSize<>::kEntries;
 
 // Copy the hot slice of a global table (entries of EB bytes) to shared
 // memory; all threads of the block take part.
 // (8-byte words: the negative half of a table starts at an odd entry.)
-template <int EB>
+template <int EB, uint32_t LO = kHotExpLo, uint32_t BIN = kHotBinades>
 __device__ __forceinline__ void load_hot_table(uint8_t* dst, const void* table) {
-  constexpr int kWords = int(kHotHalf) * EB / 8;
+  constexpr uint32_t kHalf = HotSize<BIN>::kHalf;
+  constexpr uint32_t kSkip = (LO - GQ_TAB_EXP_LO) * 128;  // first hot slot per sign
+  constexpr int kWords = int(kHalf) * EB / 8;
   const uint2* src = reinterpret_cast<const uint2*>(table);
   uint2* d = reinterpret_cast<uint2*>(dst);
   for (int i = threadIdx.x; i < 2 * kWords; i += blockDim.x) {
     const int sign = i / kWords, j = i - sign * kWords;
-    const int base = int(sign * (kTabHalf + 1) + kHotSkip) * EB / 8;
+    const int base = int(sign * (kTabHalf + 1) + kSkip) * EB / 8;
     d[i] = src[base + j];
   }
 }
 
 // Hot-slice slot of a bf16 pattern, or -1.
+template <uint32_t LO = kHotExpLo, uint32_t BIN = kHotBinades>
 __device__ __forceinline__ int hot_index(uint32_t g16) {
-  const uint32_t t = (g16 & 0x7FFFu) - (kHotExpLo << 7);
-  return t < kHotHalf ? int(t + (g16 >> 15) * kHotHalf) : -1;
+  constexpr uint32_t kHalf = HotSize<BIN>::kHalf;
+  const uint32_t t = (g16 & 0x7FFFu) - (LO << 7);
+  return t < kHalf ? int(t + (g16 >> 15) * kHalf) : -1;
 }
 
 // Exact act(g) * u with the hot slice in shared memory (fwd entries).
-template <int ACT>
+template <int ACT, uint32_t LO = kHotExpLo, uint32_t BIN = kHotBinades>
 __device__ __forceinline__ float exact_act_mul_hot(const float2* hot, float g, float u) {
-  const int k = hot_index(__float_as_uint(g) >> 16);
+  const int k = hot_index<LO, BIN>(__float_as_uint(g) >> 16);
   if (k < 0) return exact_act_mul<ACT>(g, u);
   const float h = tab_mul(hot[k], u);
   return tab_cold(h) ? slow_act_mul(ACT, g, u) : h;
