@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.replace(tmp, tables)
     # 2. translation units
     nvcc = _nvcc()
-    headers = [os.path.join(CSRC, h) for h in ("glu_common.cuh", "kernels.h", "tma.cuh")]
+    headers = [os.path.join(CSRC, h) for h in ("glu_common.cuh", "kernels.h", "tma.cuh", "mx_block.cuh", "ring.cuh")]
     headers += [tables, os.path.join(INCLUDE, "glu_quant.h")]
     objs, jobs = [], []
     for u in UNITS:

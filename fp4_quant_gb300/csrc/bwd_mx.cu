@@ -4,272 +4,466 @@
 // grad_h and gated_input and returns concatenated [dGate | dUp]; Numerics and
 // tests for the rowwise/colwise/both modes).
 //
-// Same structure as the forward kernel, with a 16-byte table entry
-// (act hi/lo, act' hi/lo) and 32-row x 128-column tiles: lanes 0-15 of a
-// warp read one row's 256-byte segment of each operand and lanes 16-31 the
-// next row, so a thread owns 2 rows x 8 columns and keeps 6 loads in flight.
-// dY*up is exact in fp32 (two 8-bit significands); when it is not (overflow
-// or underflow) the result lands in the slow path's range and is redone in
-// fp64.
+// Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
+//   * one persistent CTA per SM with three groups of four warps (twelve
+//     warps: three per SM sub-partition, up to 168 registers per thread).
+//     Tiles are 32 rows x 128 columns of N; each group has a private
+//     two-slot ring of 24 KB stages filled by 2-D TMA loads of 32-row boxes
+//     with 128-byte rows and the 128-byte swizzle (gate, up and dY: two
+//     boxes each, or four boxes of (gate, up) pairs and two of dY).  The
+//     warp that frees a stage last issues the group's next load into it;
+//   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31 of
+//     the tile and produces both outputs for it.  Rowwise pass: lane l reads
+//     row l and quantises its dGate and dUp 1x32 blocks.  Colwise pass: lane
+//     l reads column l straight from the stage and quantises the two 32x1
+//     blocks (both modes run both passes on the same stage, each computing
+//     its own values, so nothing is transposed through memory);
+//   * the stage stays held until both passes are done, so the rare exact
+//     path reads its operands from shared memory; the activation and its
+//     derivative come from the fast fp32 forms (exponent carried in two
+//     words), with the rounding test deciding codes and scales and the
+//     activation table settling the rest;
+//   * code boxes leave through TMA stores: rowwise 32 x 32 bytes at columns
+//     c and N + c of [M, 2N]; colwise, a group walks two row tiles of the
+//     same columns in a row and stores 32 x 64-byte boxes into [2N, M].
+#include <cstring>
+
 #include "glu_common.cuh"
 #include "kernels.h"
+#include "mx_block.cuh"
+#include "ring.cuh"
+#include "tma.cuh"
 
 namespace gq {
 namespace {
 
 constexpr int kTR = 32;
-constexpr int kTC = 128;
-constexpr int kGroupThreads = 256;
-constexpr int kTabBytes = kTabEntries * 16;
+constexpr int kWC = 32;
+constexpr int kGroupWarps = 4;
+constexpr int kTC = kWC * kGroupWarps;  // 128 columns
+constexpr int kGroups = 3;
+constexpr int kThreads = kGroups * kGroupWarps * 32;
+constexpr int kBoxBytes = 4096;         // 32 rows x 128 bytes
+constexpr int kStageBytes = 6 * kBoxBytes;
+constexpr int kSlots = 2;
+constexpr int kStages = kGroups * kSlots;
+constexpr int kSuper = 2;               // colwise: row tiles per unit
+constexpr int kQrBytes = 32 * 32;       // rowwise box, 32-byte swizzle
+constexpr int kQcBytes = 32 * 32 * kSuper;  // colwise box, 64-byte swizzle
+using Ctl = RingCtl<kStages, kGroups>;
+
+// Hot slice of the backward table (16-byte entries: act and act' as hi/lo
+// pairs) for the exact path: 2^-6 <= |g| < 4, where the shared memory has
+// room (rowwise, colwise); both modes read the table from global memory.
+constexpr uint32_t kHotLo = 121, kHotBin = 8;
+__host__ __device__ constexpr int hot_bytes_for(int mode) {
+  return mode == GLU_MODE_BOTH ? 0 : int(kHotBin) * 256 * 16;
+}
+__host__ __device__ constexpr int qbytes_for(int mode) {
+  return (mode & GLU_MODE_ROW ? 2 * kQrBytes : 0) + (mode & GLU_MODE_COL ? 2 * kQcBytes : 0);
+}
+__host__ __device__ constexpr int smem_for(int mode) {
+  return 1024 + kStages * kStageBytes + hot_bytes_for(mode) +
+         kGroups * kGroupWarps * qbytes_for(mode) + int(sizeof(Ctl));
+}
+static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
+                  smem_for(GLU_MODE_BOTH) <= 232448,
+              "shared memory per CTA exceeds 227 KB");
+
+__device__ uint32_t g_err_bwd_mx;
 
 struct BwdP {
-  const uint8_t* gate;
-  const uint8_t* up;
-  const uint8_t* dy;
-  int64_t M, N, ld, ld_dy;
-  uint8_t* q_row;
+  CUtensorMap tm_a;   // gate [M, N] bf16 (boxes 64 x 32) or X as (gate, up) pairs (32 x 32)
+  CUtensorMap tm_b;   // up [M, N] bf16 (split layout)
+  CUtensorMap tm_d;   // dY [M, N] bf16 (boxes 64 x 32)
+  CUtensorMap tm_qr;  // q_row [M, 2N] bytes, boxes 32 x 32
+  CUtensorMap tm_qc;  // q_col [2N, M] bytes, boxes 64 x 32
+  int64_t M, N;
   uint8_t* s_row;
-  uint8_t* q_col;
   uint8_t* s_col;
-  int64_t n_rt, n_ct, ntiles;
+  int64_t n_rt, n_ct, n_rs;
 };
 
-__device__ __forceinline__ bool is_cold(float h) {
-  uint32_t b = absbits(h);
-  return b >= kInfBits || (b != 0u && b < kTinyBits);
-}
+// Byte offset of (row r, 16-byte chunk k) under the 128-, 64- and 32-byte
+// swizzles (chunk index XORed with bits of the row).
+__device__ __forceinline__ int swz128(int r, int k) { return r * 128 + 16 * (k ^ (r & 7)); }
+__device__ __forceinline__ int swz64(int r, int k) { return r * 64 + 16 * (k ^ ((r >> 1) & 3)); }
+__device__ __forceinline__ int swz32(int r, int k) { return r * 32 + 16 * (k ^ ((r >> 2) & 1)); }
 
+// The warp's view of a stage: raw bf16 of gate, up and dY at (row r, column
+// c) of its 32 x 32 sub-tile.  Split layout: gate boxes 0-1, up 2-3, dY 4-5
+// (box b holds 64 columns, i.e. warps 2b' and 2b'+1); pairs: box w holds the
+// warp's 32 (gate, up) pairs, dY boxes 4-5.
 template <int LAYOUT>
-__device__ __forceinline__ void load_gu(const BwdP& p, int64_t r, int64_t col, uint4& a, uint4& b) {
-  if (LAYOUT == GLU_LAYOUT_SPLIT) {
-    a = ld_stream(p.gate + (r * p.ld + col) * 2);
-    b = ld_stream(p.up + (r * p.ld + col) * 2);
-  } else {
-    const uint8_t* x = p.gate + (r * p.ld + 2 * col) * 2;
-    a = ld_stream(x);
-    b = ld_stream(x + 16);
+struct StageView {
+  const uint8_t* st;
+  int w;
+  __device__ int dchunk(int c) const { return 4 * (w & 1) + (c >> 3); }
+  __device__ uint32_t g16(int r, int c) const {
+    if (LAYOUT == GLU_LAYOUT_SPLIT)
+      return *reinterpret_cast<const uint16_t*>(st + (w >> 1) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
+    return *reinterpret_cast<const uint16_t*>(st + w * kBoxBytes + swz128(r, c >> 2) + 4 * (c & 3));
   }
+  __device__ uint32_t u16(int r, int c) const {
+    if (LAYOUT == GLU_LAYOUT_SPLIT)
+      return *reinterpret_cast<const uint16_t*>(st + (2 + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
+    return *reinterpret_cast<const uint16_t*>(st + w * kBoxBytes + swz128(r, c >> 2) + 4 * (c & 3) + 2);
+  }
+  __device__ uint32_t d16(int r, int c) const {
+    return *reinterpret_cast<const uint16_t*>(st + (4 + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
+  }
+};
+
+__device__ __forceinline__ float bf(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Gates at or below the fast path's lower limit (raw bf16 patterns, the
+// sign bit set): SiLU -64, GELU -6.
+template <int ACT>
+struct FastRangeAcc {
+  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC280u : 0xC0C0u;
+};
+template <int ACT>
+__device__ __forceinline__ bool range_ok(uint32_t vmax) {
+  return (vmax & 0xFFFFu) < FastRangeAcc<ACT>::kNegLimit && (vmax >> 16) < FastRangeAcc<ACT>::kNegLimit;
 }
 
-template <int LAYOUT>
-__device__ __forceinline__ void unpack_gu(const uint4& wa, const uint4& wb, int k, uint32_t& g16,
-                                          float& u) {
-  const uint32_t a[4] = {wa.x, wa.y, wa.z, wa.w};
-  const uint32_t b[4] = {wb.x, wb.y, wb.z, wb.w};
-  if (LAYOUT == GLU_LAYOUT_SPLIT) {
-    g16 = (k & 1) ? (a[k >> 1] >> 16) : (a[k >> 1] & 0xFFFFu);
-    u = (k & 1) ? bf16_hi(b[k >> 1]) : bf16_lo(b[k >> 1]);
-  } else {
-    const uint32_t w = (k < 4) ? a[k] : b[k - 4];
-    g16 = w & 0xFFFFu;
-    u = bf16_hi(w);
+// Exact dGate (WHICH 0) or dUp (WHICH 1) of one element, from the hot slice
+// in shared memory when present, else from the global table.
+template <int ACT, bool HOT>
+__device__ __noinline__ float exact_bwd(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db,
+                                        int which) {
+  const float g = bf(gb), u = bf(ub), d = bf(db);
+  if (HOT) {
+    const int k = hot_index<kHotLo, kHotBin>(gb);
+    if (k >= 0) {
+      const float4 e = hot[k];
+      const float h = which == 0 ? tab_mul(make_float2(e.z, e.w), __fmul_rn(d, u))
+                                 : tab_mul(make_float2(e.x, e.y), d);
+      if (!tab_cold(h)) return h;
+      return which == 0 ? slow_grad_mul(ACT, g, d, u) : slow_act_mul(ACT, g, d);
+    }
   }
+  return which == 0 ? exact_grad_mul<ACT>(g, d, u) : exact_act_mul<ACT>(g, d);
 }
 
-__device__ __forceinline__ float unpack_dy(const uint4& w, int k) {
-  const uint32_t d[4] = {w.x, w.y, w.z, w.w};
-  return (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
+// Exact dGate of an element flagged by grad_ok() (or out of the fast
+// range): the cancellation table holds act' for the run of gates where the
+// fast form cancels; anything else goes to exact_bwd().
+template <int ACT, bool HOT>
+__device__ __forceinline__ float dgate_fix(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db) {
+  const uint32_t idx = gb - (ACT == 0 ? GQ_CANCEL_P0_0 : GQ_CANCEL_P0_1);
+  if (idx < (ACT == 0 ? GQ_CANCEL_SPAN_0 : GQ_CANCEL_SPAN_1)) {
+    const float2 e = __ldg(reinterpret_cast<const float2*>(ACT == 0 ? gq_tab_cancel_0 : gq_tab_cancel_1) + idx);
+    const float h = tab_mul(e, __fmul_rn(bf(db), bf(ub)));
+    if (!tab_cold(h)) return h;
+  }
+  return exact_bwd<ACT, HOT>(hot, gb, ub, db, 0);
 }
 
-// Rowwise quantisation of 8 values held by this lane (a 32-block = 4 lanes).
-__device__ __forceinline__ void row_quant(const float (&v)[8], uint2& q, uint32_t& s) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) m = max(m, absbits(v[k]));
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-  s = e8m0_from_amax_bits(m);
-  if (s == 0xFFu) {
-    q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-  } else {
-    const float mul = e8m0_inv_scale(s);
-    q.x = e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
-    q.y = e4m3x4(v[4] * mul, v[5] * mul, v[6] * mul, v[7] * mul);
-  }
+// Colwise codes of row tile j of a unit into a 32 x 64-byte box: lane l
+// (column l) owns box row l, bytes 32j..32j+31.
+__device__ __forceinline__ void put_qc(uint8_t* Q, int lane, int j, const uint32_t (&q)[8]) {
+  *reinterpret_cast<uint4*>(Q + swz64(lane, 2 * j)) = make_uint4(q[0], q[1], q[2], q[3]);
+  *reinterpret_cast<uint4*>(Q + swz64(lane, 2 * j + 1)) = make_uint4(q[4], q[5], q[6], q[7]);
 }
-
-template <int ACT, int MODE, int LAYOUT, int G>
-__global__ void __launch_bounds__(kGroupThreads* G, 1) bwd_mx_kernel(const BwdP p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
-    uint4* dst = reinterpret_cast<uint4*>(smem);
-    for (int i = threadIdx.x; i < kTabBytes / 16; i += blockDim.x) dst[i] = src[i];
-  }
-  __syncthreads();
-  const float4* tab = reinterpret_cast<const float4*>(smem);
-
-  const int grp = threadIdx.x / kGroupThreads;
-  const int tid = threadIdx.x % kGroupThreads;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int half = lane >> 4, l16 = lane & 15;
-  // [32 rows][128 cols] of dGate, then the same of dUp
-  float* H = reinterpret_cast<float*>(smem + kTabBytes) + grp * (2 * kTR * kTC);
-
-  constexpr uint32_t kFillG = (LAYOUT == GLU_LAYOUT_SPLIT) ? 0x3F803F80u : 0x00003F80u;
-  constexpr uint32_t kFillU = (LAYOUT == GLU_LAYOUT_SPLIT) ? 0u : 0x00003F80u;
-  const int64_t W = 2 * p.N;
-
-  for (int64_t t = int64_t(blockIdx.x) * G + grp; t < p.ntiles; t += int64_t(gridDim.x) * G) {
-    int64_t rt, ct;
-    if (MODE == GLU_MODE_ROW) {
-      rt = t / p.n_ct;
-      ct = t - rt * p.n_ct;
-    } else {
-      ct = t / p.n_rt;
-      rt = t - ct * p.n_rt;
-    }
-    const int64_t row0 = rt * kTR, col0 = ct * kTC;
-    const int64_t col = col0 + l16 * 8;
-    const bool col_ok = col < p.N;
-
-    uint4 wa[2], wb[2], wd[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int64_t r = row0 + 2 * warp + half + 16 * i;
-      wa[i] = make_uint4(kFillG, kFillG, kFillG, kFillG);
-      wb[i] = make_uint4(kFillU, kFillU, kFillU, kFillU);
-      wd[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok && r < p.M) {
-        load_gu<LAYOUT>(p, r, col, wa[i], wb[i]);
-        wd[i] = ld_stream(p.dy + (r * p.ld_dy + col) * 2);
-      }
-    }
-
-    float dg[2][8], du[2][8];
-    bool cold = false;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t g16;
-        float u;
-        unpack_gu<LAYOUT>(wa[i], wb[i], k, g16, u);
-        const float d = unpack_dy(wd[i], k);
-        const float4 e = tab[tab_index(g16)];
-        du[i][k] = tab_mul(make_float2(e.x, e.y), d);
-        dg[i][k] = tab_mul(make_float2(e.z, e.w), __fmul_rn(d, u));
-        cold |= is_cold(du[i][k]) | is_cold(dg[i][k]);
-      }
-    }
-    if (cold) {
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        const int64_t r = row0 + 2 * warp + half + 16 * i;
-        if (!(col_ok && r < p.M)) continue;
-        uint4 a, b;
-        load_gu<LAYOUT>(p, r, col, a, b);
-        const uint4 dd = ld_stream(p.dy + (r * p.ld_dy + col) * 2);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint32_t g16;
-          float u;
-          unpack_gu<LAYOUT>(a, b, k, g16, u);
-          const float g = __uint_as_float(g16 << 16);
-          const float d = unpack_dy(dd, k);
-#pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            if (ii != i) continue;
-            if (is_cold(du[ii][k])) du[ii][k] = slow_act_mul(ACT, g, d);
-            if (is_cold(dg[ii][k])) dg[ii][k] = slow_grad_mul(ACT, g, d, u);
-          }
-        }
-      }
-    }
-
-    if (MODE & GLU_MODE_ROW) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int64_t r = row0 + 2 * warp + half + 16 * i;
-        uint2 qg, qu;
-        uint32_t sg, su;
-        row_quant(dg[i], qg, sg);
-        row_quant(du[i], qu, su);
-        if (col_ok && r < p.M) {
-          st_stream(p.q_row + r * W + col, qg);
-          st_stream(p.q_row + r * W + p.N + col, qu);
-          if ((l16 & 3) == 0) {
-            st_byte(p.s_row + r * (W / 32) + col / 32, sg);
-            st_byte(p.s_row + r * (W / 32) + (p.N + col) / 32, su);
-          }
-        }
-      }
-    }
-
-    if (MODE & GLU_MODE_COL) {
-      group_sync(1 + grp, kGroupThreads);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int rl = 2 * warp + half + 16 * i;
-        float4* d0 = reinterpret_cast<float4*>(H + rl * kTC + l16 * 8);
-        float4* d1 = reinterpret_cast<float4*>(H + kTR * kTC + rl * kTC + l16 * 8);
-        d0[0] = make_float4(dg[i][0], dg[i][1], dg[i][2], dg[i][3]);
-        d0[1] = make_float4(dg[i][4], dg[i][5], dg[i][6], dg[i][7]);
-        d1[0] = make_float4(du[i][0], du[i][1], du[i][2], du[i][3]);
-        d1[1] = make_float4(du[i][4], du[i][5], du[i][6], du[i][7]);
-      }
-      group_sync(1 + grp, kGroupThreads);
-      // threads 0..127: dGate columns; 128..255: dUp columns
-      const int which = tid >> 7, cl = tid & 127;
-      const int64_t c = col0 + cl;
-      if (c < p.N) {
-        const float* src = H + which * (kTR * kTC) + cl;
-        float v[kTR];
-        uint32_t m = 0;
-#pragma unroll
-        for (int r = 0; r < kTR; ++r) {
-          v[r] = src[r * kTC];
-          m = max(m, absbits(v[r]));
-        }
-        const uint32_t s = e8m0_from_amax_bits(m);
-        uint32_t q[8];
-        if (s == 0xFFu) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
-        } else {
-          const float mul = e8m0_inv_scale(s);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            q[j] = e4m3x4(v[4 * j] * mul, v[4 * j + 1] * mul, v[4 * j + 2] * mul,
-                          v[4 * j + 3] * mul);
-        }
-        const int64_t oc = c + which * p.N;  // output column in [dGate | dUp]
-        uint8_t* dst = p.q_col + oc * p.M + row0;
-        st_stream(dst, make_uint4(q[0], q[1], q[2], q[3]));
-        st_stream(dst + 16, make_uint4(q[4], q[5], q[6], q[7]));
-        st_byte(p.s_col + oc * (p.M / 32) + row0 / 32, s);
-      }
-    }
+__device__ __forceinline__ void put_qr(uint8_t* Q, int lane, const uint32_t (&q)[8]) {
+  *reinterpret_cast<uint4*>(Q + swz32(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
+  *reinterpret_cast<uint4*>(Q + swz32(lane, 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+}
+// Store two boxes (dGate at y0, dUp at y1) with one bulk group.
+__device__ __forceinline__ void store2(const CUtensorMap* map, const uint8_t* Qg, const uint8_t* Qu,
+                                       int32_t x0, int32_t y0, int32_t x1, int32_t y1, int lane) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, x0, y0, Qg);
+    tma_store_2d(map, x1, y1, Qu);
+    bulk_commit();
   }
 }
 
 template <int ACT, int MODE, int LAYOUT>
+__global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_constant__ BwdP p) {
+  constexpr bool kHot = hot_bytes_for(MODE) > 0;
+  constexpr int kQPerWarp = qbytes_for(MODE);
+  constexpr int kPer = MODE == GLU_MODE_ROW ? 1 : kSuper;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = smem;
+  uint8_t* hot_raw = smem + kStages * kStageBytes;
+  const float4* hot = reinterpret_cast<const float4*>(hot_raw);
+  uint8_t* Qbase = hot_raw + hot_bytes_for(MODE);
+  Ctl* ctl = reinterpret_cast<Ctl*>(Qbase + kGroups * kGroupWarps * kQPerWarp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t units = MODE == GLU_MODE_ROW ? p.n_rt * p.n_ct : p.n_rs * p.n_ct;
+  const int64_t my_units = (units - blockIdx.x + G - 1) / G;
+
+  if (kHot) load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&p.tm_a);
+    if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
+    prefetch_tensormap(&p.tm_d);
+    if (MODE & GLU_MODE_ROW) prefetch_tensormap(&p.tm_qr);
+    if (MODE & GLU_MODE_COL) prefetch_tensormap(&p.tm_qc);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&ctl->full[st], 1);
+      ctl->freed[st] = 0;
+    }
+    const int64_t n_minor = MODE == GLU_MODE_ROW ? p.n_ct : p.n_rs;
+    for (int g = 0; g < kGroups; ++g) {
+      const TileWalk tw(blockIdx.x + g * G, kGroups * G, n_minor);
+      ctl->major[g] = tw.major;
+      ctl->minor[g] = tw.minor;
+      if (g == 0) {
+        ctl->n_minor = tw.n_minor;
+        ctl->dmaj = tw.dmaj;
+        ctl->dmin = tw.dmin;
+      }
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Load the group's tile kk into stage st (whole warp; lanes 0..5 issue one
+  // box each).  Colwise row tiles past the last one load nothing: the
+  // phase completes on the plain arrival and the consumers skip the tile.
+  auto issue = [&](int st, int g, int64_t kk) {
+    int64_t rt = 0, ct = 0;
+    if (lane == 0) {
+      const int64_t major = ctl->major[g], minor = ctl->minor[g];
+      const int j = int(kk % kPer);
+      rt = MODE == GLU_MODE_ROW ? major : kSuper * minor + j;
+      ct = MODE == GLU_MODE_ROW ? minor : major;
+      ctl->rt[st] = rt;
+      ctl->ct[st] = ct;
+      if (j == kPer - 1) {
+        int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
+        if (mn >= ctl->n_minor) {
+          mn -= ctl->n_minor;
+          ++mj;
+        }
+        ctl->major[g] = mj;
+        ctl->minor[g] = mn;
+      }
+      if (rt < p.n_rt)
+        mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
+      else
+        mbar_arrive(&ctl->full[st]);
+    }
+    rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
+    ct = __shfl_sync(0xFFFFFFFFu, ct, 0);
+    if (lane < 6 && rt < p.n_rt) {
+      uint8_t* dst = stages + st * kStageBytes + lane * kBoxBytes;
+      const int32_t y = int32_t(rt * kTR);
+      if (lane >= 4) {
+        tma_load_2d(dst, &p.tm_d, int32_t(ct * kTC + (lane - 4) * 64), y, &ctl->full[st]);
+      } else if (LAYOUT == GLU_LAYOUT_SPLIT) {
+        tma_load_2d(dst, lane < 2 ? &p.tm_a : &p.tm_b, int32_t(ct * kTC + (lane & 1) * 64), y,
+                    &ctl->full[st]);
+      } else {
+        tma_load_2d(dst, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &ctl->full[st]);
+      }
+    }
+  };
+
+  const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
+  uint8_t* Qrg = Qbase + warp * kQPerWarp;                                   // rowwise dGate
+  uint8_t* Qru = Qrg + kQrBytes;                                             // rowwise dUp
+  uint8_t* Qcg = Qrg + ((MODE & GLU_MODE_ROW) ? 2 * kQrBytes : 0);           // colwise dGate
+  uint8_t* Qcu = Qcg + kQcBytes;                                             // colwise dUp
+  const int64_t n_g = kPer * (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0);
+  const int64_t W = 2 * p.N;
+
+  if (w == 0) {
+    for (int j = 0; j < kSlots; ++j)
+      if (j < n_g) issue(grp * kSlots + j, grp, j);
+  }
+
+  int64_t k = 0;
+  bool failed = false;
+  for (; k < n_g; ++k) {
+    const int s = grp * kSlots + int(k % kSlots);
+    if (!mbar_wait(&ctl->full[s], uint32_t((k / kSlots) & 1))) {
+      if (lane == 0) atomicOr(&g_err_bwd_mx, kErrWaitFull);
+      failed = true;
+      break;
+    }
+    const int64_t rt = ctl->rt[s], ct = ctl->ct[s];
+    const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;
+    const int j = int(k % kPer);
+    const bool active = c0 < p.N;
+    const bool work = active && rt < p.n_rt;
+    const StageView<LAYOUT> sv{stages + s * kStageBytes, w};
+
+    // ------------------------------------------------- rowwise: row `lane`
+    if ((MODE & GLU_MODE_ROW) && work) {
+      float dg[32], du[32];
+      uint32_t gmax = 0, gbad = 0;
+      const uint8_t* st = stages + s * kStageBytes;
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {  // 8 columns per step
+        uint32_t gw[4], uw[4];
+        if (LAYOUT == GLU_LAYOUT_SPLIT) {
+          const int o = swz128(lane, 4 * (w & 1) + c8);
+          const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
+          const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+          gw[0] = a.x; gw[1] = a.y; gw[2] = a.z; gw[3] = a.w;
+          uw[0] = b.x; uw[1] = b.y; uw[2] = b.z; uw[3] = b.w;
+        } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
+          const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
+          const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
+          gw[0] = __byte_perm(a.x, a.y, 0x5410); uw[0] = __byte_perm(a.x, a.y, 0x7632);
+          gw[1] = __byte_perm(a.z, a.w, 0x5410); uw[1] = __byte_perm(a.z, a.w, 0x7632);
+          gw[2] = __byte_perm(b.x, b.y, 0x5410); uw[2] = __byte_perm(b.x, b.y, 0x7632);
+          gw[3] = __byte_perm(b.z, b.w, 0x5410); uw[3] = __byte_perm(b.z, b.w, 0x7632);
+        }
+        const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
+                                                         swz128(lane, 4 * (w & 1) + c8));
+        const uint32_t dw[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 dg2, du2, x2;
+          bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, x2);
+          gmax = vmax_u16x2(gmax, gw[i]);
+          const int e = 8 * c8 + 2 * i;
+          dg[e] = dg2.x; dg[e + 1] = dg2.y;
+          du[e] = du2.x; du[e + 1] = du2.y;
+          gbad |= (grad_ok(x2.x) ? 0u : 1u << e) | (grad_ok(x2.y) ? 0u : 2u << e);
+        }
+      }
+      if (!range_ok<ACT>(gmax)) {  // rare: gates below the fast range
+#pragma unroll 1
+        for (int e = 0; e < 32; ++e)
+          if (sv.g16(lane, e) >= FastRangeAcc<ACT>::kNegLimit) {
+            gbad |= 1u << e;
+            set_elem(du, e, exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 1));
+          }
+      }
+      while (gbad != 0u) {  // rare: dGate where the fast form cancels or is out of range
+        const int e = __ffs(gbad) - 1;
+        gbad &= gbad - 1u;
+        set_elem(dg, e, dgate_fix<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e)));
+      }
+      uint32_t qg[8], qu[8];
+      const uint32_t sg = mx_block(dg, qg, kBracketGrad, [&](int e) {
+        return exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 0);
+      });
+      const uint32_t su = mx_block(du, qu, kBracket, [&](int e) {
+        return exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 1);
+      });
+      if (lane == 0) bulk_wait_read0();  // the previous boxes have been read out
+      __syncwarp();
+      put_qr(Qrg, lane, qg);
+      put_qr(Qru, lane, qu);
+      store2(&p.tm_qr, Qrg, Qru, int32_t(c0), int32_t(row0), int32_t(p.N + c0), int32_t(row0), lane);
+      if (row0 + lane < p.M) {
+        st_byte(p.s_row + (row0 + lane) * (W / 32) + c0 / 32, sg);
+        st_byte(p.s_row + (row0 + lane) * (W / 32) + (p.N + c0) / 32, su);
+      }
+    }
+
+    // ---------------------------------------------- colwise: column `lane`
+    if ((MODE & GLU_MODE_COL) && active) {
+      if (MODE == GLU_MODE_COL && j == 0) {  // the unit's boxes are free again
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+      }
+      if (work) {
+        float dg[32], du[32];
+        uint32_t gmax = 0, gbad = 0;
+#pragma unroll
+        for (int r = 0; r < kTR; r += 2) {
+          const uint32_t gp = sv.g16(r, lane) | (sv.g16(r + 1, lane) << 16);
+          const uint32_t up = sv.u16(r, lane) | (sv.u16(r + 1, lane) << 16);
+          const uint32_t dp = sv.d16(r, lane) | (sv.d16(r + 1, lane) << 16);
+          float2 dg2, du2, x2;
+          bwd_fast2<ACT>(bf16x2_f2(gp), bf16x2_f2(up), bf16x2_f2(dp), dg2, du2, x2);
+          gmax = vmax_u16x2(gmax, gp);
+          dg[r] = dg2.x; dg[r + 1] = dg2.y;
+          du[r] = du2.x; du[r + 1] = du2.y;
+          gbad |= (grad_ok(x2.x) ? 0u : 1u << r) | (grad_ok(x2.y) ? 0u : 2u << r);
+        }
+        if (!range_ok<ACT>(gmax)) {
+#pragma unroll 1
+          for (int r = 0; r < kTR; ++r)
+            if (sv.g16(r, lane) >= FastRangeAcc<ACT>::kNegLimit) {
+              gbad |= 1u << r;
+              set_elem(du, r, exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 1));
+            }
+        }
+        while (gbad != 0u) {
+          const int r = __ffs(gbad) - 1;
+          gbad &= gbad - 1u;
+          set_elem(dg, r, dgate_fix<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane)));
+        }
+        uint32_t qg[8], qu[8];
+        const uint32_t sg = mx_block(dg, qg, kBracketGrad, [&](int r) {
+          return exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 0);
+        });
+        const uint32_t su = mx_block(du, qu, kBracket, [&](int r) {
+          return exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 1);
+        });
+        // (both: the rowwise pass above waited for the previous boxes)
+        put_qc(Qcg, lane, j, qg);
+        put_qc(Qcu, lane, j, qu);
+        st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sg);
+        st_byte(p.s_col + (p.N + c0 + lane) * (p.M / 32) + row0 / 32, su);
+      }
+    }
+
+    // both passes are done with the stage
+    if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
+
+    if ((MODE & GLU_MODE_COL) && active && j == kSuper - 1) {
+      const int64_t urow0 = row0 - j * kTR;
+      store2(&p.tm_qc, Qcg, Qcu, int32_t(urow0), int32_t(c0), int32_t(urow0), int32_t(p.N + c0), lane);
+    }
+  }
+  if (failed && lane == 0) {
+    // a wait gave up: never leave with loads in flight; wait (bounded) for
+    // the group's loads that may have been issued
+    for (int64_t kk = k; kk < k + kSlots; ++kk) {
+      if (kk >= n_g) break;
+      if (!mbar_wait(&ctl->full[grp * kSlots + int(kk % kSlots)], uint32_t((kk / kSlots) & 1)))
+        atomicOr(&g_err_bwd_mx, kErrDrain);
+    }
+  }
+  if (lane == 0) bulk_wait0();  // no code box may still be in flight at exit
+}
+
+template <int ACT, int MODE, int LAYOUT>
 cudaError_t launch_t(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
-  constexpr int G = 3;
-  auto kern = bwd_mx_kernel<ACT, MODE, LAYOUT, G>;
-  const int smem = kTabBytes + ((MODE & GLU_MODE_COL) ? G * 2 * kTR * kTC * 4 : 0);
+  auto kern = bwd_mx_kernel<ACT, MODE, LAYOUT>;
+  const int smem = smem_for(MODE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   BwdP p;
-  p.gate = static_cast<const uint8_t*>(a.gate);
-  p.up = static_cast<const uint8_t*>(a.up);
-  p.dy = static_cast<const uint8_t*>(a.dy);
+  memset(&p, 0, sizeof p);
+  if (LAYOUT == GLU_LAYOUT_SPLIT) {
+    e = make_tile_map(&p.tm_a, a.gate, 2, a.N, a.M, a.ld_in * 2, 64, kTR, 128);
+    if (e == cudaSuccess) e = make_tile_map(&p.tm_b, a.up, 2, a.N, a.M, a.ld_in * 2, 64, kTR, 128);
+  } else {
+    e = make_tile_map(&p.tm_a, a.gate, 4, a.N, a.M, a.ld_in * 2, kWC, kTR, 128);
+  }
+  if (e == cudaSuccess) e = make_tile_map(&p.tm_d, a.dy, 2, a.N, a.M, a.ld_dy * 2, 64, kTR, 128);
+  if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
+    e = make_tile_map(&p.tm_qr, a.q_row, 1, 2 * a.N, a.M, 2 * a.N, kWC, kTR, 32);
+  if (e == cudaSuccess && (MODE & GLU_MODE_COL))
+    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, 2 * a.N, a.M, kTR * kSuper, kWC, 64);
+  if (e != cudaSuccess) return e;
   p.M = a.M;
   p.N = a.N;
-  p.ld = a.ld_in;
-  p.ld_dy = a.ld_dy;
-  p.q_row = static_cast<uint8_t*>(a.q_row);
   p.s_row = static_cast<uint8_t*>(a.s_row);
-  p.q_col = static_cast<uint8_t*>(a.q_col);
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
-  p.ntiles = p.n_rt * p.n_ct;
-  const int64_t ctas = (p.ntiles + G - 1) / G;
-  const int grid = int(ctas < d.sms ? ctas : d.sms);
+  p.n_rs = (p.n_rt + kSuper - 1) / kSuper;
+  const int64_t units = MODE == GLU_MODE_ROW ? p.n_rt * p.n_ct : p.n_rs * p.n_ct;
+  const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGroupThreads * G);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   return cudaLaunchKernelEx(&cfg, kern, p);
@@ -294,6 +488,15 @@ cudaError_t by_mode(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& 
 
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
   return a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+}
+
+cudaError_t read_err_bwd_mx(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_err_bwd_mx, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_err_bwd_mx, &z, sizeof(uint32_t));
+  }
+  return e;
 }
 
 }  // namespace gq

@@ -30,6 +30,8 @@
 
 #include "glu_common.cuh"
 #include "kernels.h"
+#include "mx_block.cuh"
+#include "ring.cuh"
 #include "tma.cuh"
 
 namespace gq {
@@ -72,46 +74,18 @@ __host__ __device__ constexpr int qbytes_for(int mode) {
   return (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
 }
 
-// Ring control block in shared memory.  There is no producer warp: the
-// consumer warp that frees a stage last (an atomic count per stage) issues
-// the TMA loads of its group's next tile into it.  That keeps every warp a
-// consumer (16 warps: four per SM sub-partition, so up to 128 registers per
-// thread) and starts each load the moment its stage is free.
-struct alignas(16) RingCtl {
-  uint64_t full[8];     // per stage: one arrival (with the tile's byte count) + TMA bytes
-  uint32_t freed[8];    // per stage: warps that have freed it (wraps at kGroupWarps)
-  int64_t rt[8], ct[8];  // per stage: tile coordinates of the load in flight
-  int64_t major[4], minor[4];  // per group: walk position of its next tile to load
-  int64_t n_minor, dmaj, dmin;  // walk step (shared by the groups)
-};
-constexpr int kCtlBytes = int(sizeof(RingCtl));
+using Ctl = RingCtl<groups_for(0) * kSlots, groups_for(0)>;
+constexpr int kCtlBytes = int(sizeof(Ctl));
 
 __host__ __device__ constexpr int smem_for(int mode) {
   return 1024 + groups_for(mode) * kSlots * kStageBytes + hot_bytes_for(mode) +
          groups_for(mode) * kGroupWarps * qbytes_for(mode) + kCtlBytes;
 }
-static_assert(2 * kSlots <= 8 && groups_for(0) <= 4, "ring control block too small");
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
                   smem_for(GLU_MODE_BOTH) <= 232448,
               "shared memory per CTA exceeds 227 KB");
 
 
-// Tile t of the grid-stride sequence as (major, minor) = (t / n_minor, t %
-// n_minor), advanced by a fixed step without dividing in the loop.
-struct TileWalk {
-  int64_t major, minor, n_minor, dmaj, dmin;
-  __device__ TileWalk(int64_t t0, int64_t step, int64_t n_min)
-      : major(t0 / n_min), minor(t0 % n_min), n_minor(n_min), dmaj(step / n_min),
-        dmin(step % n_min) {}
-  __device__ void next() {
-    major += dmaj;
-    minor += dmin;
-    if (minor >= n_minor) {
-      minor -= n_minor;
-      ++major;
-    }
-  }
-};
 
 // Byte offset of (row r, 16-byte chunk k) in a 32 x 32-byte code box with
 // the 32-byte swizzle (chunk ^= (r >> 2) & 1).
@@ -119,7 +93,7 @@ __device__ __forceinline__ int qswz(int r, int k) { return r * 32 + 16 * (k ^ ((
 
 __device__ uint32_t g_err_fwd_mx;
 
-struct alignas(64) FwdP {
+struct FwdP {
   CUtensorMap tm_a;   // gate [M, N] bf16 (boxes 64 x 32) or X as (gate, up) pairs (32 x 32)
   CUtensorMap tm_b;   // up [M, N] bf16 (split layout)
   CUtensorMap tm_qr;  // q_row [M, N] bytes, boxes 32 x 32
@@ -159,92 +133,17 @@ __device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t
   return exact_act_mul_hot<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, g, u);
 }
 
-// v[e] = x for a runtime e, keeping v in registers.
-__device__ __forceinline__ void set_elem(float (&v)[32], int e, float x) {
-#pragma unroll
-  for (int k = 0; k < 32; ++k)
-    if (k == e) v[k] = x;
-}
-
-__device__ __forceinline__ float amax32(const float (&v)[32]) {
-  float m8[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) m8[j] = amax8(*reinterpret_cast<const float(*)[8]>(&v[8 * j]));
-  return amax2(amax2(m8[0], m8[1]), amax2(m8[2], m8[3]));
-}
-
-__device__ __forceinline__ void codes32(const float (&v)[32], float mul, uint32_t (&q)[8]) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    q[j] = e4m3x4(v[4 * j] * mul, v[4 * j + 1] * mul, v[4 * j + 2] * mul, v[4 * j + 3] * mul);
-}
-
-// 4-bit mask of the nonzero bytes of x.
-__device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
-  return uint32_t((x & 0xFFu) != 0u) | (uint32_t((x & 0xFF00u) != 0u) << 1) |
-         (uint32_t((x & 0xFF0000u) != 0u) << 2) | (uint32_t((x & 0xFF000000u) != 0u) << 3);
-}
-
 // Quantise one 32-value MXFP8 block held by this thread.  Element e sits at
 // input (row0 + (e ^ rx), c0 + lane) for a column block and at (row0 + lane,
-// c0 + e) for a row block.  Codes are decided from the fast values where the
-// rounding test allows and from exact values elsewhere; the whole block is
-// recomputed from exact values when its scale is undecided.  Writes 8 code
-// words, returns the scale byte.
+// c0 + e) for a row block.
 template <int ACT, int MODE, int LAYOUT, bool COLUMN>
 __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
                                                 const float2* hot, int64_t row0, int64_t c0,
                                                 int lane, int rx = 0) {
-  constexpr float d = kBracket;
-  uint32_t sc = e8m0_checked(amax32(v), d);
-  if (sc != 0x100u) {
-    const float mul = e8m0_inv_scale(sc);
-    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-    uint32_t wbad = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      bool bad = false;
-      q[j] = e4m3x4_bracket2(make_float2(v[4 * j], v[4 * j + 1]), make_float2(v[4 * j + 2], v[4 * j + 3]),
-                             splat2(mlo), splat2(mhi), bad);
-      wbad |= uint32_t(bad) << j;
-    }
-    if (wbad != 0u) {
-      // rare: find the straddling elements, take their exact values
-      uint32_t emask = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
-                                   v[4 * j + 3] * mlo);
-        const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
-                                   v[4 * j + 3] * mhi);
-        emask |= byte_mask(ql ^ qh) << (4 * j);
-      }
-      while (emask != 0u) {
-        const int e = __ffs(emask) - 1;
-        emask &= emask - 1u;
-        const float x = COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
-                               : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
-        set_elem(v, e, x);
-      }
-      codes32(v, mul, q);
-    }
-    return sc;
-  }
-  // undecided scale (or a NaN/Inf/tiny block): the block from exact values
-#pragma unroll 1
-  for (int e = 0; e < 32; ++e) {
-    const float x = COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
-                           : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
-    set_elem(v, e, x);
-  }
-  sc = e8m0_of(amax32(v));
-  if (sc == 0xFFu) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
-  } else {
-    codes32(v, e8m0_inv_scale(sc), q);
-  }
-  return sc;
+  return mx_block(v, q, kBracket, [&](int e) {
+    return COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
+                  : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
+  });
 }
 
 // Colwise codes of row tile j of a unit into the warp's 32 x 128-byte box:
@@ -281,7 +180,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   uint8_t* hot_raw = smem + kStages * kStageBytes;
   const float2* hot = reinterpret_cast<const float2*>(hot_raw);
   uint8_t* Qbase = hot_raw + hot_bytes_for(MODE);  // 1024-aligned (stages and hot table are)
-  RingCtl* ctl = reinterpret_cast<RingCtl*>(Qbase + kConsumers * kQPerWarp);
+  Ctl* ctl = reinterpret_cast<Ctl*>(Qbase + kConsumers * kQPerWarp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   // Work units: rowwise a tile, else kSuper row tiles of the same columns.
@@ -365,14 +264,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   // Free stage s after this warp's last read of it; the last of the group's
   // warps to do so loads the group's tile k + kSlots into it.
   auto release = [&](int s, int64_t k) {
-    __syncwarp();
-    uint32_t last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicInc(&ctl->freed[s], kGroupWarps - 1) == kGroupWarps - 1;
-      if (last) __threadfence_block();
-    }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0) && k + kSlots < n_g) {
+    if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) {
       if (MODE == GLU_MODE_BOTH) fence_proxy_async();  // the stage was written (transpose)
       issue(s, grp, k + kSlots);
     }

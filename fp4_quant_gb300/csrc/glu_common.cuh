@@ -333,8 +333,11 @@ __device__ __forceinline__ bool fast_ok_acc(float g) {
 //   silu'(g) = S (1 + g E S),  gelu'(g) = S (1 + 2 g E S y'(g)),
 //   y'(g) = sqrt(2/pi) (1 + 3 * 0.044715 g^2).
 // Near the zero of act' the sum 1 + x cancels and magnifies the errors of
-// E and S; grad_ok() is false there (|1 + x| < |x| / 6) and the exact path
-// is used.
+// E and S; grad_ok() is false there (|1 + x| < |x| / 64: four bf16 gates
+// per activation) and the value comes from the cancellation table.
+// Measured over every bf16 gate of the fast range with grad_ok() true, the
+// packed form below is within 81 (SiLU) and 56 (GELU) units of 2^-24 of
+// act'(g), against a rounding-test width of 2^-15 = 512 units.
 template <int ACT>
 __device__ __forceinline__ float fast_grad(float g, float S, float E, float& x) {
   const float es = __fmul_rn(E, S);
@@ -348,8 +351,43 @@ __device__ __forceinline__ float fast_grad(float g, float S, float E, float& x) 
 }
 
 __device__ __forceinline__ bool grad_ok(float x) {
-  return fabsf(__fadd_rn(1.0f, x)) * 6.0f >= fabsf(x);
+  return fabsf(__fadd_rn(1.0f, x)) * 64.0f >= fabsf(x);
 }
+
+// Fast dGate and dUp for a pair of elements; x2 receives the factor whose
+// cancellation (1 + x near 0) grad_ok() screens.  Same arithmetic as
+// fast_s_acc + fast_grad, on packed pairs (dUp = (dY g) S, dGate =
+// (dY up) act', both products dY g and dY up exact).
+template <int ACT>
+__device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du,
+                                          float2& x) {
+  float2 E, q;
+  if (ACT == 0) {
+    const float2 th = mul2(g, splat2(-0x1.7154p+0f));            // exact
+    const float2 tl = mul2(g, splat2(-4.888495368504664e-06f));  // tail * ln2
+    const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+    E = fma2(e0, tl, e0);
+  } else {
+    q = mul2(g, g);
+    const float2 g3 = mul2(q, g);  // exact
+    const float2 w = fma2(splat2(-0.10294324159622192f), g3, mul2(g, splat2(-2.3139550575201895e-05f)));
+    const float2 t = add2(mul2(g, splat2(-0x1.26aep+1f)), w);
+    E = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+  }
+  const float2 den = add2(E, splat2(1.0f));
+  const float2 S = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+  const float2 es = mul2(E, S);
+  if (ACT == 0) {
+    x = mul2(g, es);
+  } else {
+    const float2 y2 = fma2(splat2(0.21406444881780073f), q, splat2(1.5957691216057308f));
+    x = mul2(mul2(g, es), y2);
+  }
+  const float2 ap = fma2(S, x, S);
+  du = mul2(mul2(d, g), S);
+  dg = mul2(mul2(d, u), ap);
+}
+
 
 // Relative half-width d of the rounding test, above the fast path's worst
 // error plus one ulp each for the product rounding, the exact path's own

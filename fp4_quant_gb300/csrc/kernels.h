@@ -27,5 +27,6 @@ cudaError_t make_tile_map(CUtensorMap* map, const void* base, int elem_bytes, in
 
 // Error bits recorded by a kernel family (bounded waits that gave up).
 cudaError_t read_err_fwd_mx(uint32_t* v, bool clear);
+cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);
 
 }  // namespace gq

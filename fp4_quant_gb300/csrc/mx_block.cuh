@@ -1,0 +1,91 @@
+// One MXFP8 block (32 values held by one thread) quantised with the
+// rounding test: E8M0 scale (RCEIL) and E4M3 codes decided from fast fp32
+// values where a relative perturbation of +-d cannot change them, from exact
+// values elsewhere.  "Add swiglu + MXFP8 fused CuTe DSL kernel", Numerics
+// (E8M0 scales, E4M3 payload, 32-element blocks).
+#pragma once
+
+#include "glu_common.cuh"
+
+namespace gq {
+
+// v[e] = x for a runtime e, keeping v in registers.
+__device__ __forceinline__ void set_elem(float (&v)[32], int e, float x) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    if (k == e) v[k] = x;
+}
+
+__device__ __forceinline__ float amax32(const float (&v)[32]) {
+  float m8[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m8[j] = amax8(*reinterpret_cast<const float(*)[8]>(&v[8 * j]));
+  return amax2(amax2(m8[0], m8[1]), amax2(m8[2], m8[3]));
+}
+
+__device__ __forceinline__ void codes32(const float (&v)[32], float mul, uint32_t (&q)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    q[j] = e4m3x4(v[4 * j] * mul, v[4 * j + 1] * mul, v[4 * j + 2] * mul, v[4 * j + 3] * mul);
+}
+
+// 4-bit mask of the nonzero bytes of x.
+__device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
+  return uint32_t((x & 0xFFu) != 0u) | (uint32_t((x & 0xFF00u) != 0u) << 1) |
+         (uint32_t((x & 0xFF0000u) != 0u) << 2) | (uint32_t((x & 0xFF000000u) != 0u) << 3);
+}
+
+// Quantise the block v (element e of 32).  `exact(e)` returns the exact
+// value of element e; it is called only for elements whose code the test
+// cannot decide, and for the whole block when its scale is undecided (or
+// the block holds a NaN, an infinity or a tiny amax).  Writes the 8 code
+// words (element 4j + b in byte b of q[j]) and returns the scale byte.
+template <class Exact>
+__device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], const float d,
+                                             Exact&& exact) {
+  uint32_t sc = e8m0_checked(amax32(v), d);
+  if (sc != 0x100u) {
+    const float mul = e8m0_inv_scale(sc);
+    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+    uint32_t wbad = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      bool bad = false;
+      q[j] = e4m3x4_bracket2(make_float2(v[4 * j], v[4 * j + 1]), make_float2(v[4 * j + 2], v[4 * j + 3]),
+                             splat2(mlo), splat2(mhi), bad);
+      wbad |= uint32_t(bad) << j;
+    }
+    if (wbad != 0u) {
+      // rare: find the straddling elements, take their exact values
+      uint32_t emask = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
+                                   v[4 * j + 3] * mlo);
+        const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
+                                   v[4 * j + 3] * mhi);
+        emask |= byte_mask(ql ^ qh) << (4 * j);
+      }
+      while (emask != 0u) {
+        const int e = __ffs(emask) - 1;
+        emask &= emask - 1u;
+        set_elem(v, e, exact(e));
+      }
+      codes32(v, mul, q);
+    }
+    return sc;
+  }
+  // undecided scale (or a NaN/Inf/tiny block): the block from exact values
+#pragma unroll 1
+  for (int e = 0; e < 32; ++e) set_elem(v, e, exact(e));
+  sc = e8m0_of(amax32(v));
+  if (sc == 0xFFu) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
+  } else {
+    codes32(v, e8m0_inv_scale(sc), q);
+  }
+  return sc;
+}
+
+}  // namespace gq

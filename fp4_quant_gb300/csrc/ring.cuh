@@ -1,0 +1,54 @@
+// Shared-memory ring of TMA stages fed without a producer warp: the
+// consumer warp that frees a stage last (an atomic count per stage) issues
+// the TMA loads of its group's next tile into it.  Every warp stays a
+// consumer and each load starts the moment its stage is free.  Each group
+// of warps has a private ring, consumed in order by that group alone, so an
+// mbarrier parity wait can never be satisfied by an older phase of the same
+// parity.
+#pragma once
+
+#include <cstdint>
+
+namespace gq {
+
+template <int STAGES, int GROUPS>
+struct alignas(16) RingCtl {
+  uint64_t full[STAGES];    // per stage: one arrival (with the tile's byte count) + TMA bytes
+  uint32_t freed[STAGES];   // per stage: warps that have freed it (wraps at the group size)
+  int64_t rt[STAGES], ct[STAGES];  // per stage: tile coordinates of the load in flight
+  int64_t major[GROUPS], minor[GROUPS];  // per group: walk position of its next unit
+  int64_t n_minor, dmaj, dmin;           // walk step (shared by the groups)
+};
+
+// Tile t of the grid-stride sequence as (major, minor) = (t / n_minor, t %
+// n_minor), advanced by a fixed step without dividing in the loop.
+struct TileWalk {
+  int64_t major, minor, n_minor, dmaj, dmin;
+  __device__ TileWalk(int64_t t0, int64_t step, int64_t n_min)
+      : major(t0 / n_min), minor(t0 % n_min), n_minor(n_min), dmaj(step / n_min),
+        dmin(step % n_min) {}
+  __device__ void next() {
+    major += dmaj;
+    minor += dmin;
+    if (minor >= n_minor) {
+      minor -= n_minor;
+      ++major;
+    }
+  }
+};
+
+// Free a stage after this warp's last read of it (all lanes call).  Returns
+// true in every lane of the warp that freed it last.
+template <int GROUP_WARPS>
+__device__ __forceinline__ bool ring_free(uint32_t* freed, int lane) {
+  __syncwarp();
+  uint32_t last = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    last = atomicInc(freed, GROUP_WARPS - 1) == GROUP_WARPS - 1;
+    if (last) __threadfence_block();
+  }
+  return __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
+}
+
+}  // namespace gq

@@ -200,6 +200,27 @@ def test_special_values_bwd(act, fmt):
     check(gpu, ref, fmt, mode, M, 2 * N, "special_bwd")
 
 
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_every_bf16_gate(act, direction):
+    """All 65536 bf16 gate patterns (NaN, infinities, subnormals, the run
+    where act' cancels, both ends of the fast range) through MXFP8 both
+    modes; up and dY random, with a shuffle so that every block mixes
+    magnitudes."""
+    M, N = 256, 256
+    pats = torch.arange(65536, dtype=torch.int32)
+    perm = torch.randperm(65536, generator=torch.Generator().manual_seed(71))
+    g = pats[perm].to(torch.int16).view(torch.bfloat16).reshape(M, N).to(DEV)
+    u = _randn(M, N, 72)
+    if direction == "fwd":
+        gpu, ref = run_fwd(g, u, act[0], G.FMT_MXFP8, G.MODE_BOTH, G.LAYOUT_SPLIT)
+        check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, N, "all_gates_fwd")
+    else:
+        d = _randn(M, N, 73)
+        gpu, ref = run_bwd(g, u, d, act[0], G.FMT_MXFP8, G.MODE_BOTH, G.LAYOUT_SPLIT)
+        check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, 2 * N, "all_gates_bwd")
+
+
 def test_exact_activation_blocks_on_gpu():
     # gate = 32: h = 32 * up exactly; amax at 448 * 2^k, ties, subnormal codes
     M, N = 32, 64
