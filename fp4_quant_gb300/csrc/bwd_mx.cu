@@ -130,7 +130,7 @@ __device__ __forceinline__ bool range_ok(uint32_t vmax) {
 // Exact dGate (WHICH 0) or dUp (WHICH 1) of one element, from the hot slice
 // in shared memory when present, else from the global table.
 template <int ACT, bool HOT>
-__device__ __noinline__ float exact_bwd(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db,
+__device__ __forceinline__ float exact_bwd(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db,
                                         int which) {
   const float g = bf(gb), u = bf(ub), d = bf(db);
   if (HOT) {
@@ -296,115 +296,109 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
     const bool work = active && rt < p.n_rt;
     const StageView<LAYOUT> sv{stages + s * kStageBytes, w};
 
-    // ------------------------------------------------- rowwise: row `lane`
-    if ((MODE & GLU_MODE_ROW) && work) {
+    // One pass per direction on the held stage: rowwise (lane l takes row l
+    // of the sub-tile) and/or colwise (lane l takes column l).  The passes
+    // share one copy of the arithmetic (a runtime loop keeps the hot code
+    // small enough for the instruction cache).
+    if ((MODE & GLU_MODE_COL) && MODE != GLU_MODE_BOTH && active && j == 0) {
+      if (lane == 0) bulk_wait_read0();  // the unit's boxes are free again
+      __syncwarp();
+    }
+    constexpr int kP0 = (MODE & GLU_MODE_ROW) ? 0 : 1, kP1 = (MODE & GLU_MODE_COL) ? 1 : 0;
+#pragma unroll 1
+    for (int pass = kP0; pass <= kP1 && work; ++pass) {
+      const bool colp = pass == 1;
+      // bf16 pairs along the block: word i holds elements 2i and 2i + 1
+      uint32_t gw[16], uw[16], dw[16];
+      if (!colp) {
+        const uint8_t* st = sv.st;
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          if (LAYOUT == GLU_LAYOUT_SPLIT) {
+            const int o = swz128(lane, 4 * (w & 1) + c8);
+            const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
+            const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+            gw[4 * c8] = a.x; gw[4 * c8 + 1] = a.y; gw[4 * c8 + 2] = a.z; gw[4 * c8 + 3] = a.w;
+            uw[4 * c8] = b.x; uw[4 * c8 + 1] = b.y; uw[4 * c8 + 2] = b.z; uw[4 * c8 + 3] = b.w;
+          } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
+            const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
+            const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
+            gw[4 * c8] = __byte_perm(a.x, a.y, 0x5410); uw[4 * c8] = __byte_perm(a.x, a.y, 0x7632);
+            gw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x5410); uw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x7632);
+            gw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x7632);
+            gw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x7632);
+          }
+          const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
+                                                           swz128(lane, 4 * (w & 1) + c8));
+          dw[4 * c8] = dd.x; dw[4 * c8 + 1] = dd.y; dw[4 * c8 + 2] = dd.z; dw[4 * c8 + 3] = dd.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          gw[i] = sv.g16(2 * i, lane) | (sv.g16(2 * i + 1, lane) << 16);
+          uw[i] = sv.u16(2 * i, lane) | (sv.u16(2 * i + 1, lane) << 16);
+          dw[i] = sv.d16(2 * i, lane) | (sv.d16(2 * i + 1, lane) << 16);
+        }
+      }
       float dg[32], du[32];
       uint32_t gmax = 0, gbad = 0;
-      const uint8_t* st = stages + s * kStageBytes;
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {  // 8 columns per step
-        uint32_t gw[4], uw[4];
-        if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          const int o = swz128(lane, 4 * (w & 1) + c8);
-          const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-          const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
-          gw[0] = a.x; gw[1] = a.y; gw[2] = a.z; gw[3] = a.w;
-          uw[0] = b.x; uw[1] = b.y; uw[2] = b.z; uw[3] = b.w;
-        } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
-          const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
-          const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
-          gw[0] = __byte_perm(a.x, a.y, 0x5410); uw[0] = __byte_perm(a.x, a.y, 0x7632);
-          gw[1] = __byte_perm(a.z, a.w, 0x5410); uw[1] = __byte_perm(a.z, a.w, 0x7632);
-          gw[2] = __byte_perm(b.x, b.y, 0x5410); uw[2] = __byte_perm(b.x, b.y, 0x7632);
-          gw[3] = __byte_perm(b.z, b.w, 0x5410); uw[3] = __byte_perm(b.z, b.w, 0x7632);
-        }
-        const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
-                                                         swz128(lane, 4 * (w & 1) + c8));
-        const uint32_t dw[4] = {dd.x, dd.y, dd.z, dd.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float2 dg2, du2, x2;
-          bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, x2);
-          gmax = vmax_u16x2(gmax, gw[i]);
-          const int e = 8 * c8 + 2 * i;
-          dg[e] = dg2.x; dg[e + 1] = dg2.y;
-          du[e] = du2.x; du[e + 1] = du2.y;
-          gbad |= (grad_ok(x2.x) ? 0u : 1u << e) | (grad_ok(x2.y) ? 0u : 2u << e);
-        }
+      for (int i = 0; i < 16; ++i) {
+        float2 dg2, du2, x2;
+        bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, x2);
+        gmax = vmax_u16x2(gmax, gw[i]);
+        dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;
+        du[2 * i] = du2.x; du[2 * i + 1] = du2.y;
+        gbad |= (grad_ok(x2.x) ? 0u : 1u << (2 * i)) | (grad_ok(x2.y) ? 0u : 2u << (2 * i));
       }
+      // element e of the blocks sits at (row, column) (lane, e) or (e, lane)
+      auto raw = [&](int e, uint32_t& gb, uint32_t& ub, uint32_t& db) {
+        const int r = colp ? e : lane, c = colp ? lane : e;
+        gb = sv.g16(r, c);
+        ub = sv.u16(r, c);
+        db = sv.d16(r, c);
+      };
       if (!range_ok<ACT>(gmax)) {  // rare: gates below the fast range
 #pragma unroll 1
-        for (int e = 0; e < 32; ++e)
-          if (sv.g16(lane, e) >= FastRangeAcc<ACT>::kNegLimit) {
+        for (int e = 0; e < 32; ++e) {
+          uint32_t gb, ub, db;
+          raw(e, gb, ub, db);
+          if (gb >= FastRangeAcc<ACT>::kNegLimit) {
             gbad |= 1u << e;
-            set_elem(du, e, exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 1));
+            set_elem(du, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 1));
           }
+        }
       }
-      while (gbad != 0u) {  // rare: dGate where the fast form cancels or is out of range
+      while (gbad != 0u) {  // dGate where the fast form cancels or is out of range
         const int e = __ffs(gbad) - 1;
         gbad &= gbad - 1u;
-        set_elem(dg, e, dgate_fix<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e)));
+        uint32_t gb, ub, db;
+        raw(e, gb, ub, db);
+        set_elem(dg, e, dgate_fix<ACT, kHot>(hot, gb, ub, db));
       }
       uint32_t qg[8], qu[8];
-      const uint32_t sg = mx_block(dg, qg, kBracketGrad, [&](int e) {
-        return exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 0);
+      const uint32_t sg = mx_block(dg, qg, Bracket<ACT>::kDGate, [&](int e) {
+        uint32_t gb, ub, db;
+        raw(e, gb, ub, db);
+        return exact_bwd<ACT, kHot>(hot, gb, ub, db, 0);
       });
-      const uint32_t su = mx_block(du, qu, kBracket, [&](int e) {
-        return exact_bwd<ACT, kHot>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 1);
+      const uint32_t su = mx_block(du, qu, Bracket<ACT>::kDUp, [&](int e) {
+        uint32_t gb, ub, db;
+        raw(e, gb, ub, db);
+        return exact_bwd<ACT, kHot>(hot, gb, ub, db, 1);
       });
-      if (lane == 0) bulk_wait_read0();  // the previous boxes have been read out
-      __syncwarp();
-      put_qr(Qrg, lane, qg);
-      put_qr(Qru, lane, qu);
-      store2(&p.tm_qr, Qrg, Qru, int32_t(c0), int32_t(row0), int32_t(p.N + c0), int32_t(row0), lane);
-      if (row0 + lane < p.M) {
-        st_byte(p.s_row + (row0 + lane) * (W / 32) + c0 / 32, sg);
-        st_byte(p.s_row + (row0 + lane) * (W / 32) + (p.N + c0) / 32, su);
-      }
-    }
-
-    // ---------------------------------------------- colwise: column `lane`
-    if ((MODE & GLU_MODE_COL) && active) {
-      if (MODE == GLU_MODE_COL && j == 0) {  // the unit's boxes are free again
-        if (lane == 0) bulk_wait_read0();
+      if (!colp) {
+        if (lane == 0) bulk_wait_read0();  // the previous boxes have been read out
         __syncwarp();
-      }
-      if (work) {
-        float dg[32], du[32];
-        uint32_t gmax = 0, gbad = 0;
-#pragma unroll
-        for (int r = 0; r < kTR; r += 2) {
-          const uint32_t gp = sv.g16(r, lane) | (sv.g16(r + 1, lane) << 16);
-          const uint32_t up = sv.u16(r, lane) | (sv.u16(r + 1, lane) << 16);
-          const uint32_t dp = sv.d16(r, lane) | (sv.d16(r + 1, lane) << 16);
-          float2 dg2, du2, x2;
-          bwd_fast2<ACT>(bf16x2_f2(gp), bf16x2_f2(up), bf16x2_f2(dp), dg2, du2, x2);
-          gmax = vmax_u16x2(gmax, gp);
-          dg[r] = dg2.x; dg[r + 1] = dg2.y;
-          du[r] = du2.x; du[r + 1] = du2.y;
-          gbad |= (grad_ok(x2.x) ? 0u : 1u << r) | (grad_ok(x2.y) ? 0u : 2u << r);
+        put_qr(Qrg, lane, qg);
+        put_qr(Qru, lane, qu);
+        store2(&p.tm_qr, Qrg, Qru, int32_t(c0), int32_t(row0), int32_t(p.N + c0), int32_t(row0), lane);
+        if (row0 + lane < p.M) {
+          st_byte(p.s_row + (row0 + lane) * (W / 32) + c0 / 32, sg);
+          st_byte(p.s_row + (row0 + lane) * (W / 32) + (p.N + c0) / 32, su);
         }
-        if (!range_ok<ACT>(gmax)) {
-#pragma unroll 1
-          for (int r = 0; r < kTR; ++r)
-            if (sv.g16(r, lane) >= FastRangeAcc<ACT>::kNegLimit) {
-              gbad |= 1u << r;
-              set_elem(du, r, exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 1));
-            }
-        }
-        while (gbad != 0u) {
-          const int r = __ffs(gbad) - 1;
-          gbad &= gbad - 1u;
-          set_elem(dg, r, dgate_fix<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane)));
-        }
-        uint32_t qg[8], qu[8];
-        const uint32_t sg = mx_block(dg, qg, kBracketGrad, [&](int r) {
-          return exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 0);
-        });
-        const uint32_t su = mx_block(du, qu, kBracket, [&](int r) {
-          return exact_bwd<ACT, kHot>(hot, sv.g16(r, lane), sv.u16(r, lane), sv.d16(r, lane), 1);
-        });
-        // (both: the rowwise pass above waited for the previous boxes)
+      } else {
+        // (both: the rowwise pass waited for the previous boxes)
         put_qc(Qcg, lane, j, qg);
         put_qc(Qcu, lane, j, qu);
         st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sg);

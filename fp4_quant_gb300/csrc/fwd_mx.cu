@@ -120,7 +120,7 @@ __device__ __forceinline__ int swz(int r, int chunk) { return r * 128 + 16 * (ch
 // Exact act(g) * u of element (row, col) of the input, read from global
 // memory (the rare path runs after the warp has released its stage).
 template <int ACT, int MODE, int LAYOUT>
-__device__ __noinline__ float exact_at(const FwdP& p, const float2* hot, int64_t row, int64_t col) {
+__device__ __forceinline__ float exact_at(const FwdP& p, const float2* hot, int64_t row, int64_t col) {
   uint32_t gb, ub;
   if (LAYOUT == GLU_LAYOUT_SPLIT) {
     gb = __ldg(p.gate + row * p.ld + col);
@@ -140,7 +140,7 @@ template <int ACT, int MODE, int LAYOUT, bool COLUMN>
 __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
                                                 const float2* hot, int64_t row0, int64_t c0,
                                                 int lane, int rx = 0) {
-  return mx_block(v, q, kBracket, [&](int e) {
+  return mx_block(v, q, Bracket<ACT>::kAct, [&](int e) {
     return COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
                   : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
   });

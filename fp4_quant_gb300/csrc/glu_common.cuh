@@ -280,28 +280,33 @@ __device__ __forceinline__ bool fast_ok(float g) {
   return ACT == 0 ? fabsf(g) < 64.0f : (g > -7.0f && g < 64.0f);
 }
 
-// act(g) * u for a pair, fast form (same arithmetic as fast_s, packed).
+// act(g) * u for a pair, fast form, packed: SiLU with the two-word
+// exponent of fast_s_acc, GELU with the one-word exponent of fast_s.
 template <int ACT>
 __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
-  float2 t;
+  float2 E;
   if (ACT == 0) {
-    t = mul2(g, splat2(-1.44269502162933349609375f));
+    const float2 th = mul2(g, splat2(-0x1.7154p+0f));            // exact
+    const float2 tl = mul2(g, splat2(-4.888495368504664e-06f));  // tail * ln2
+    const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+    E = fma2(e0, tl, e0);
   } else {
     const float2 w = fma2(splat2(-0.10294324159622192f), mul2(g, g), splat2(-2.302208185195922851562f));
-    t = mul2(g, w);
+    const float2 t = mul2(g, w);
+    E = make_float2(ex2_approx(t.x), ex2_approx(t.y));
   }
-  const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), splat2(1.0f));
+  const float2 d = add2(E, splat2(1.0f));
   return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
 // Largest raw bf16 pattern of the gates (two per word, unsigned per half):
 // negative gates have the sign bit set, so the running max of the raw
-// patterns reaches kFastNegLimit exactly when some gate is at or below the
-// fast path's lower limit (SiLU -87: beyond it 1/(1+E) leaves the normal
-// range; GELU -7).  Positive gates never reach it.
+// patterns reaches kNegLimit exactly when some gate is at or below the fast
+// path's lower limit (SiLU -64, GELU -7: the ranges over which the fast
+// forms were measured).  Positive gates never reach it.
 template <int ACT>
 struct FastRange {
-  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC2AEu : 0xC0E0u;  // bf16 -87, -7
+  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
 };
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
 template <int ACT>
@@ -337,7 +342,7 @@ __device__ __forceinline__ bool fast_ok_acc(float g) {
 // per activation) and the value comes from the cancellation table.
 // Measured over every bf16 gate of the fast range with grad_ok() true, the
 // packed form below is within 81 (SiLU) and 56 (GELU) units of 2^-24 of
-// act'(g), against a rounding-test width of 2^-15 = 512 units.
+// act'(g), against a rounding-test width of 2^-16 = 256 units.
 template <int ACT>
 __device__ __forceinline__ float fast_grad(float g, float S, float E, float& x) {
   const float es = __fmul_rn(E, S);
@@ -389,12 +394,18 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 }
 
 
-// Relative half-width d of the rounding test, above the fast path's worst
-// error plus one ulp each for the product rounding, the exact path's own
-// rounding and the bracket products.  The GPU tests measure the fast path
-// over every bf16 gate against these widths.
-constexpr float kBracket = 0x1p-17f;      // forward values and dUp
-constexpr float kBracketGrad = 0x1p-15f;  // dGate (act' amplifies E, S errors)
+// Relative half-width d of the rounding test: above the fast path's worst
+// error (measured over every bf16 gate of the fast range, in units of
+// 2^-24) plus one unit each for the rounding of the final product, of the
+// exact value and of the bracket products.
+//   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-17
+//   dUp = dY act(g):   same forms                             -> 2^-20, 2^-18
+//   dGate = dY up act'(g), grad_ok(): SiLU 81, GELU 56        -> 2^-16, 2^-17
+template <int ACT> struct Bracket {
+  static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-17f;
+  static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
+  static constexpr float kDGate = ACT == 0 ? 0x1p-16f : 0x1p-17f;
+};
 
 // ----------------------------------------------------------------- MXFP8 --
 

@@ -35,11 +35,21 @@ __device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
          (uint32_t((x & 0xFF0000u) != 0u) << 2) | (uint32_t((x & 0xFF000000u) != 0u) << 3);
 }
 
+// Replace byte b of word q[j] (j = e >> 2, b = e & 3) by the low byte of c.
+__device__ __forceinline__ void patch_code(uint32_t (&q)[8], int e, uint32_t c) {
+  const int b = e & 3;
+  const uint32_t sel = 0x3210u ^ ((uint32_t(b) ^ 4u) << (4 * b));  // byte b from c
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j == (e >> 2)) q[j] = __byte_perm(q[j], c, sel);
+}
+
 // Quantise the block v (element e of 32).  `exact(e)` returns the exact
 // value of element e; it is called only for elements whose code the test
-// cannot decide, and for the whole block when its scale is undecided (or
-// the block holds a NaN, an infinity or a tiny amax).  Writes the 8 code
-// words (element 4j + b in byte b of q[j]) and returns the scale byte.
+// cannot decide (their code bytes are patched in place), and for the whole
+// block when its scale is undecided (or the block holds a NaN, an infinity
+// or a tiny amax).  Writes the 8 code words (element 4j + b in byte b of
+// q[j]) and returns the scale byte.
 template <class Exact>
 __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], const float d,
                                              Exact&& exact) {
@@ -56,10 +66,12 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
       wbad |= uint32_t(bad) << j;
     }
     if (wbad != 0u) {
-      // rare: find the straddling elements, take their exact values
+      // rare: the straddling elements of the undecided words get codes from
+      // their exact values
       uint32_t emask = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        if (!((wbad >> j) & 1u)) continue;
         const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
                                    v[4 * j + 3] * mlo);
         const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
@@ -69,9 +81,8 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
       while (emask != 0u) {
         const int e = __ffs(emask) - 1;
         emask &= emask - 1u;
-        set_elem(v, e, exact(e));
+        patch_code(q, e, e4m3(exact(e) * mul));
       }
-      codes32(v, mul, q);
     }
     return sc;
   }
