@@ -62,9 +62,13 @@ __host__ __device__ constexpr int hot_bytes_for(int mode) {
 __host__ __device__ constexpr int qbytes_for(int mode) {
   return (mode & GLU_MODE_ROW ? 2 * kQrBytes : 0) + (mode & GLU_MODE_COL ? 2 * kQcBytes : 0);
 }
+// act' of the cancellation run (see the table generator), copied to shared
+// memory: at most kCancelMax (hi, lo) pairs.
+constexpr int kCancelMax = 16;
+static_assert(GQ_CANCEL_SPAN_0 <= kCancelMax && GQ_CANCEL_SPAN_1 <= kCancelMax, "cancellation run");
 __host__ __device__ constexpr int smem_for(int mode) {
   return 1024 + kStages * kStageBytes + hot_bytes_for(mode) +
-         kGroups * kGroupWarps * qbytes_for(mode) + int(sizeof(Ctl));
+         kGroups * kGroupWarps * qbytes_for(mode) + int(sizeof(Ctl)) + kCancelMax * 8;
 }
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
                   smem_for(GLU_MODE_BOTH) <= 232448,
@@ -146,20 +150,6 @@ __device__ __forceinline__ float exact_bwd(const float4* hot, uint32_t gb, uint3
   return which == 0 ? exact_grad_mul<ACT>(g, d, u) : exact_act_mul<ACT>(g, d);
 }
 
-// Exact dGate of an element flagged by grad_ok() (or out of the fast
-// range): the cancellation table holds act' for the run of gates where the
-// fast form cancels; anything else goes to exact_bwd().
-template <int ACT, bool HOT>
-__device__ __forceinline__ float dgate_fix(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db) {
-  const uint32_t idx = gb - (ACT == 0 ? GQ_CANCEL_P0_0 : GQ_CANCEL_P0_1);
-  if (idx < (ACT == 0 ? GQ_CANCEL_SPAN_0 : GQ_CANCEL_SPAN_1)) {
-    const float2 e = __ldg(reinterpret_cast<const float2*>(ACT == 0 ? gq_tab_cancel_0 : gq_tab_cancel_1) + idx);
-    const float h = tab_mul(e, __fmul_rn(bf(db), bf(ub)));
-    if (!tab_cold(h)) return h;
-  }
-  return exact_bwd<ACT, HOT>(hot, gb, ub, db, 0);
-}
-
 // Colwise codes of row tile j of a unit into a 32 x 64-byte box: lane l
 // (column l) owns box row l, bytes 32j..32j+31.
 __device__ __forceinline__ void put_qc(uint8_t* Q, int lane, int j, const uint32_t (&q)[8]) {
@@ -194,12 +184,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
   const float4* hot = reinterpret_cast<const float4*>(hot_raw);
   uint8_t* Qbase = hot_raw + hot_bytes_for(MODE);
   Ctl* ctl = reinterpret_cast<Ctl*>(Qbase + kGroups * kGroupWarps * kQPerWarp);
+  float2* cancel = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(Ctl));
+  constexpr uint32_t kCP0 = ACT == 0 ? GQ_CANCEL_P0_0 : GQ_CANCEL_P0_1;
+  constexpr uint32_t kCSpan = ACT == 0 ? GQ_CANCEL_SPAN_0 : GQ_CANCEL_SPAN_1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   const int64_t units = MODE == GLU_MODE_ROW ? p.n_rt * p.n_ct : p.n_rs * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
   if (kHot) load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+  if (threadIdx.x < kCSpan)
+    cancel[threadIdx.x] = reinterpret_cast<const float2*>(ACT == 0 ? gq_tab_cancel_0 : gq_tab_cancel_1)[threadIdx.x];
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -341,15 +336,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
         }
       }
       float dg[32], du[32];
-      uint32_t gmax = 0, gbad = 0;
+      uint32_t gmax = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float2 dg2, du2, x2;
-        bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, x2);
+        const float2 g2 = bf16x2_f2(gw[i]), u2 = bf16x2_f2(uw[i]), d2 = bf16x2_f2(dw[i]);
+        float2 dg2, du2;
+        bwd_fast2<ACT>(g2, u2, d2, dg2, du2);
         gmax = vmax_u16x2(gmax, gw[i]);
+        // gates of the cancellation run (two bf16 halves at once): act' from
+        // the table, (dY up) act' correctly rounded
+        const uint32_t ci = __vsub2(gw[i], kCP0 * 0x10001u);
+        const uint32_t cm = __vcmpltu2(ci, kCSpan * 0x10001u);
+        if (cm != 0u) {
+          const float2 p2 = mul2(d2, u2);
+          if (cm & 0xFFFFu) dg2.x = tab_mul(cancel[ci & 0xFFFFu], p2.x);
+          if (cm >> 16) dg2.y = tab_mul(cancel[ci >> 16], p2.y);
+        }
         dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;
         du[2 * i] = du2.x; du[2 * i + 1] = du2.y;
-        gbad |= (grad_ok(x2.x) ? 0u : 1u << (2 * i)) | (grad_ok(x2.y) ? 0u : 2u << (2 * i));
       }
       // element e of the blocks sits at (row, column) (lane, e) or (e, lane)
       auto raw = [&](int e, uint32_t& gb, uint32_t& ub, uint32_t& db) {
@@ -364,17 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
           uint32_t gb, ub, db;
           raw(e, gb, ub, db);
           if (gb >= FastRangeAcc<ACT>::kNegLimit) {
-            gbad |= 1u << e;
+            set_elem(dg, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 0));
             set_elem(du, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 1));
           }
         }
-      }
-      while (gbad != 0u) {  // dGate where the fast form cancels or is out of range
-        const int e = __ffs(gbad) - 1;
-        gbad &= gbad - 1u;
-        uint32_t gb, ub, db;
-        raw(e, gb, ub, db);
-        set_elem(dg, e, dgate_fix<ACT, kHot>(hot, gb, ub, db));
       }
       uint32_t qg[8], qu[8];
       const uint32_t sg = mx_block(dg, qg, Bracket<ACT>::kDGate, [&](int e) {

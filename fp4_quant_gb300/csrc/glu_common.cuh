@@ -250,38 +250,22 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// Fast activation factor S(g) = 1 / (1 + E):
+// Fast activation factor S(g) = 1 / (1 + E), on packed pairs:
 //   SiLU: E = 2^(-g log2 e),                      S = sigmoid(g)
 //   GELU: E = 2^(-K (g + 0.044715 g^3)), K = 2 sqrt(2/pi) log2(e),
 //         S = sigmoid(2y), since 0.5 (1 + tanh y) = sigmoid(2y).
-// fast_s: the exponent is one rounded product (the forward kernels).
-//   Measured over every bf16 gate: |S - sigmoid| / sigmoid <= 54 * 2^-24
-//   (SiLU, |g| < 64) and <= 33 * 2^-24 (GELU, -7 < g < 64).
-// fast_s_acc: the exponent carries a second word (the backward kernels,
-//   which also need E for act'): <= 2.9 * 2^-24 (SiLU, |g| < 64) and
-//   <= 31 * 2^-24 (GELU, -6 < g < 64).  -log2(e) and K are split into a
-//   16-bit head, so the head product with an 8-bit bf16 g is exact.
-// Outside those ranges fast_ok() / fast_ok_acc() are false and the exact
-// path is used.
-template <int ACT>
-__device__ __forceinline__ float fast_s(float g) {
-  float t;
-  if (ACT == 0) {
-    t = __fmul_rn(g, -1.44269502162933349609375f);
-  } else {
-    const float w = __fmaf_rn(-0.10294324159622192f, __fmul_rn(g, g), -2.302208185195922851562f);
-    t = __fmul_rn(g, w);
-  }
-  return rcp_approx(__fadd_rn(1.0f, ex2_approx(t)));
-}
+// The SiLU exponent carries a second word (-log2 e split into a 16-bit head,
+// whose product with an 8-bit bf16 g is exact, and a tail folded in with one
+// fma); the backward GELU exponent is split the same way, the forward one is
+// a single rounded product.  E and S then take ex2.approx and rcp.approx.
+// Measured over every bf16 gate of the fast range (SiLU |g| < 64, GELU
+// -7 < g < 64 forward, -6 < g < 64 backward), in units of 2^-24:
+//   fast_h2:   |act(g) u - h| / |act(g) u| <= 3.5 (SiLU), 33 (GELU)
+//   bwd_fast2: dUp 3.5 (SiLU), 31 (GELU); dGate 81 (SiLU), 56 (GELU)
+//              outside the cancellation run (below).
+// Gates outside the range take the exact path.
 
-template <int ACT>
-__device__ __forceinline__ bool fast_ok(float g) {
-  return ACT == 0 ? fabsf(g) < 64.0f : (g > -7.0f && g < 64.0f);
-}
-
-// act(g) * u for a pair, fast form, packed: SiLU with the two-word
-// exponent of fast_s_acc, GELU with the one-word exponent of fast_s.
+// act(g) * u for a pair.
 template <int ACT>
 __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
   float2 E;
@@ -302,8 +286,7 @@ __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
 // Largest raw bf16 pattern of the gates (two per word, unsigned per half):
 // negative gates have the sign bit set, so the running max of the raw
 // patterns reaches kNegLimit exactly when some gate is at or below the fast
-// path's lower limit (SiLU -64, GELU -7: the ranges over which the fast
-// forms were measured).  Positive gates never reach it.
+// path's lower limit.  Positive gates never reach it.
 template <int ACT>
 struct FastRange {
   static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
@@ -314,58 +297,15 @@ __device__ __forceinline__ bool fast_range_ok(uint32_t vmax) {
   return (vmax & 0xFFFFu) < FastRange<ACT>::kNegLimit && (vmax >> 16) < FastRange<ACT>::kNegLimit;
 }
 
+// Fast dGate and dUp for a pair of elements:
+//   dUp = (dY g) S,  dGate = (dY up) act'(g),  act'(g) = S (1 + x),
+//   x = g E S (SiLU) or 2 y'(g) g E S (GELU), y'(g) = sqrt(2/pi) (1 + 3 *
+//   0.044715 g^2), using 1 - S = E S; the products dY g and dY up are exact.
+// Near the zero of act' the sum 1 + x cancels and magnifies the errors of E
+// and S: for the run of bf16 gates where |1 + x| * 48 < |x| the backward
+// kernel takes act' from the cancellation table instead.
 template <int ACT>
-__device__ __forceinline__ void fast_s_acc(float g, float& S, float& E) {
-  if (ACT == 0) {
-    const float th = __fmul_rn(g, -0x1.7154p+0f);            // exact
-    const float tl = __fmul_rn(g, -4.888495368504664e-06f);  // tail * ln2
-    const float e0 = ex2_approx(th);
-    E = __fmaf_rn(e0, tl, e0);
-  } else {
-    const float q = __fmul_rn(g, g), g3 = __fmul_rn(q, g);  // exact
-    const float w = __fmaf_rn(-0.10294324159622192f, g3, __fmul_rn(g, -2.3139550575201895e-05f));
-    E = ex2_approx(__fadd_rn(__fmul_rn(g, -0x1.26aep+1f), w));
-  }
-  S = rcp_approx(__fadd_rn(1.0f, E));
-}
-
-template <int ACT>
-__device__ __forceinline__ bool fast_ok_acc(float g) {
-  return ACT == 0 ? fabsf(g) < 64.0f : (g > -6.0f && g < 64.0f);
-}
-
-// act'(g) from S and E:  1 - S = E*S, so
-//   silu'(g) = S (1 + g E S),  gelu'(g) = S (1 + 2 g E S y'(g)),
-//   y'(g) = sqrt(2/pi) (1 + 3 * 0.044715 g^2).
-// Near the zero of act' the sum 1 + x cancels and magnifies the errors of
-// E and S; grad_ok() is false there (|1 + x| < |x| / 64: four bf16 gates
-// per activation) and the value comes from the cancellation table.
-// Measured over every bf16 gate of the fast range with grad_ok() true, the
-// packed form below is within 81 (SiLU) and 56 (GELU) units of 2^-24 of
-// act'(g), against a rounding-test width of 2^-16 = 256 units.
-template <int ACT>
-__device__ __forceinline__ float fast_grad(float g, float S, float E, float& x) {
-  const float es = __fmul_rn(E, S);
-  if (ACT == 0) {
-    x = __fmul_rn(g, es);
-  } else {
-    const float y2 = __fmaf_rn(0.21406444881780073f, __fmul_rn(g, g), 1.5957691216057308f);
-    x = __fmul_rn(__fmul_rn(g, es), y2);  // 2 y' g E S
-  }
-  return __fmaf_rn(S, x, S);
-}
-
-__device__ __forceinline__ bool grad_ok(float x) {
-  return fabsf(__fadd_rn(1.0f, x)) * 64.0f >= fabsf(x);
-}
-
-// Fast dGate and dUp for a pair of elements; x2 receives the factor whose
-// cancellation (1 + x near 0) grad_ok() screens.  Same arithmetic as
-// fast_s_acc + fast_grad, on packed pairs (dUp = (dY g) S, dGate =
-// (dY up) act', both products dY g and dY up exact).
-template <int ACT>
-__device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du,
-                                          float2& x) {
+__device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du) {
   float2 E, q;
   if (ACT == 0) {
     const float2 th = mul2(g, splat2(-0x1.7154p+0f));            // exact
@@ -382,6 +322,7 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
   const float2 den = add2(E, splat2(1.0f));
   const float2 S = make_float2(rcp_approx(den.x), rcp_approx(den.y));
   const float2 es = mul2(E, S);
+  float2 x;
   if (ACT == 0) {
     x = mul2(g, es);
   } else {
@@ -393,14 +334,14 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
   dg = mul2(mul2(d, u), ap);
 }
 
-
 // Relative half-width d of the rounding test: above the fast path's worst
 // error (measured over every bf16 gate of the fast range, in units of
 // 2^-24) plus one unit each for the rounding of the final product, of the
 // exact value and of the bracket products.
 //   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-17
 //   dUp = dY act(g):   same forms                             -> 2^-20, 2^-18
-//   dGate = dY up act'(g), grad_ok(): SiLU 81, GELU 56        -> 2^-16, 2^-17
+//   dGate = dY up act'(g) off the cancellation run: SiLU 81, GELU 56
+//                                                             -> 2^-16, 2^-17
 template <int ACT> struct Bracket {
   static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-17f;
   static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
