@@ -17,7 +17,7 @@
 //     row l and quantises its dGate and dUp 1x32 blocks.  Colwise pass: lane
 //     l reads column l straight from the stage and quantises the two 32x1
 //     blocks (both modes run both passes on the same stage, each computing
-//     its own values, so nothing is transposed through memory);
+//     its own values);
 //   * the stage stays held until both passes are done, so the rare exact
 //     path reads its operands from shared memory; the activation and its
 //     derivative come from the fast fp32 forms (exponent carried in two
@@ -41,34 +41,38 @@ constexpr int kTR = 32;
 constexpr int kWC = 32;
 constexpr int kGroupWarps = 4;
 constexpr int kTC = kWC * kGroupWarps;  // 128 columns
-constexpr int kGroups = 3;
-constexpr int kThreads = kGroups * kGroupWarps * 32;
+// Groups of four warps and ring slots per group (mode-dependent: both
+// directions need more registers per thread).
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 3 : 3; }
+__host__ __device__ constexpr int slots_for(int mode) { return mode == GLU_MODE_BOTH ? 2 : 2; }
+__host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
 constexpr int kBoxBytes = 4096;         // 32 rows x 128 bytes
 constexpr int kStageBytes = 6 * kBoxBytes;
-constexpr int kSlots = 2;
-constexpr int kStages = kGroups * kSlots;
-constexpr int kSuper = 2;               // colwise: row tiles per unit
+
+// Colwise: row tiles per unit (a group's consecutive tiles share their
+// columns, so each warp stores 32 x (32 super)-byte boxes into [2N, M]).
+__host__ __device__ constexpr int super_for(int mode) { return mode == GLU_MODE_BOTH ? 2 : 2; }
 constexpr int kQrBytes = 32 * 32;       // rowwise box, 32-byte swizzle
-constexpr int kQcBytes = 32 * 32 * kSuper;  // colwise box, 64-byte swizzle
-using Ctl = RingCtl<kStages, kGroups>;
+
+using Ctl = RingCtl<8, 4>;
 
 // Hot slice of the backward table (16-byte entries: act and act' as hi/lo
 // pairs) for the exact path: 2^-6 <= |g| < 4, where the shared memory has
 // room (rowwise, colwise); both modes read the table from global memory.
 constexpr uint32_t kHotLo = 121, kHotBin = 8;
 __host__ __device__ constexpr int hot_bytes_for(int mode) {
-  return mode == GLU_MODE_BOTH ? 0 : int(kHotBin) * 256 * 16;
+  return mode == GLU_MODE_BOTH && super_for(mode) == 2 ? 0 : int(kHotBin) * 256 * 16;
 }
 __host__ __device__ constexpr int qbytes_for(int mode) {
-  return (mode & GLU_MODE_ROW ? 2 * kQrBytes : 0) + (mode & GLU_MODE_COL ? 2 * kQcBytes : 0);
+  return (mode & GLU_MODE_ROW ? 2 * kQrBytes : 0) + (mode & GLU_MODE_COL ? 2 * 32 * 32 * super_for(mode) : 0);
 }
 // act' of the cancellation run (see the table generator), copied to shared
 // memory: at most kCancelMax (hi, lo) pairs.
 constexpr int kCancelMax = 16;
 static_assert(GQ_CANCEL_SPAN_0 <= kCancelMax && GQ_CANCEL_SPAN_1 <= kCancelMax, "cancellation run");
 __host__ __device__ constexpr int smem_for(int mode) {
-  return 1024 + kStages * kStageBytes + hot_bytes_for(mode) +
-         kGroups * kGroupWarps * qbytes_for(mode) + int(sizeof(Ctl)) + kCancelMax * 8;
+  return 1024 + groups_for(mode) * slots_for(mode) * kStageBytes + hot_bytes_for(mode) +
+         groups_for(mode) * kGroupWarps * qbytes_for(mode) + int(sizeof(Ctl)) + kCancelMax * 8;
 }
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
                   smem_for(GLU_MODE_BOTH) <= 232448,
@@ -150,11 +154,14 @@ __device__ __forceinline__ float exact_bwd(const float4* hot, uint32_t gb, uint3
   return which == 0 ? exact_grad_mul<ACT>(g, d, u) : exact_act_mul<ACT>(g, d);
 }
 
-// Colwise codes of row tile j of a unit into a 32 x 64-byte box: lane l
-// (column l) owns box row l, bytes 32j..32j+31.
+// Colwise codes of row tile j of a unit into a 32 x (32 SUP)-byte box: lane
+// l (column l) owns box row l, bytes 32j..32j+31 (64- or 32-byte swizzle).
+template <int SUP>
 __device__ __forceinline__ void put_qc(uint8_t* Q, int lane, int j, const uint32_t (&q)[8]) {
-  *reinterpret_cast<uint4*>(Q + swz64(lane, 2 * j)) = make_uint4(q[0], q[1], q[2], q[3]);
-  *reinterpret_cast<uint4*>(Q + swz64(lane, 2 * j + 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+  const int o0 = SUP == 2 ? swz64(lane, 2 * j) : swz32(lane, 0);
+  const int o1 = SUP == 2 ? swz64(lane, 2 * j + 1) : swz32(lane, 1);
+  *reinterpret_cast<uint4*>(Q + o0) = make_uint4(q[0], q[1], q[2], q[3]);
+  *reinterpret_cast<uint4*>(Q + o1) = make_uint4(q[4], q[5], q[6], q[7]);
 }
 __device__ __forceinline__ void put_qr(uint8_t* Q, int lane, const uint32_t (&q)[8]) {
   *reinterpret_cast<uint4*>(Q + swz32(lane, 0)) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -173,9 +180,13 @@ __device__ __forceinline__ void store2(const CUtensorMap* map, const uint8_t* Qg
 }
 
 template <int ACT, int MODE, int LAYOUT>
-__global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_constant__ BwdP p) {
+__global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __grid_constant__ BwdP p) {
+  constexpr int kGroups = groups_for(MODE), kSlots = slots_for(MODE), kStages = kGroups * kSlots;
+  static_assert(kStages <= 8 && kGroups <= 4, "ring control block");
   constexpr bool kHot = hot_bytes_for(MODE) > 0;
   constexpr int kQPerWarp = qbytes_for(MODE);
+  constexpr int kSuper = super_for(MODE);
+  constexpr int kQcBytes = 32 * 32 * kSuper;
   constexpr int kPer = MODE == GLU_MODE_ROW ? 1 : kSuper;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -291,88 +302,93 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
     const bool work = active && rt < p.n_rt;
     const StageView<LAYOUT> sv{stages + s * kStageBytes, w};
 
-    // One pass per direction on the held stage: rowwise (lane l takes row l
-    // of the sub-tile) and/or colwise (lane l takes column l).  The passes
-    // share one copy of the arithmetic (a runtime loop keeps the hot code
-    // small enough for the instruction cache).
-    if ((MODE & GLU_MODE_COL) && MODE != GLU_MODE_BOTH && active && j == 0) {
+    // One pass per direction on the held stage, sharing one copy of the
+    // arithmetic (a runtime loop keeps the code small).  Rowwise: lane l
+    // takes row l of the sub-tile; colwise: lane l takes column l, read
+    // straight from the stage.  Both modes run both passes, each computing
+    // its own values (measured faster than transposing the rowwise values
+    // through the stage: the kernel is bound by issue and latency, not by
+    // the extra activation work).
+    if (MODE == GLU_MODE_COL && active && j == 0) {
       if (lane == 0) bulk_wait_read0();  // the unit's boxes are free again
       __syncwarp();
     }
     constexpr int kP0 = (MODE & GLU_MODE_ROW) ? 0 : 1, kP1 = (MODE & GLU_MODE_COL) ? 1 : 0;
+    float dg[32], du[32];
 #pragma unroll 1
     for (int pass = kP0; pass <= kP1 && work; ++pass) {
       const bool colp = pass == 1;
-      // bf16 pairs along the block: word i holds elements 2i and 2i + 1
-      uint32_t gw[16], uw[16], dw[16];
-      if (!colp) {
-        const uint8_t* st = sv.st;
+      {
+        // bf16 pairs along the block: word i holds elements 2i and 2i + 1
+        uint32_t gw[16], uw[16], dw[16];
+        if (!colp) {
+          const uint8_t* st = sv.st;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          if (LAYOUT == GLU_LAYOUT_SPLIT) {
-            const int o = swz128(lane, 4 * (w & 1) + c8);
-            const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-            const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
-            gw[4 * c8] = a.x; gw[4 * c8 + 1] = a.y; gw[4 * c8 + 2] = a.z; gw[4 * c8 + 3] = a.w;
-            uw[4 * c8] = b.x; uw[4 * c8 + 1] = b.y; uw[4 * c8 + 2] = b.z; uw[4 * c8 + 3] = b.w;
-          } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
-            const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
-            const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
-            gw[4 * c8] = __byte_perm(a.x, a.y, 0x5410); uw[4 * c8] = __byte_perm(a.x, a.y, 0x7632);
-            gw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x5410); uw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x7632);
-            gw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x7632);
-            gw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x7632);
+          for (int c8 = 0; c8 < 4; ++c8) {
+            if (LAYOUT == GLU_LAYOUT_SPLIT) {
+              const int o = swz128(lane, 4 * (w & 1) + c8);
+              const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
+              const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+              gw[4 * c8] = a.x; gw[4 * c8 + 1] = a.y; gw[4 * c8 + 2] = a.z; gw[4 * c8 + 3] = a.w;
+              uw[4 * c8] = b.x; uw[4 * c8 + 1] = b.y; uw[4 * c8 + 2] = b.z; uw[4 * c8 + 3] = b.w;
+            } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
+              const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
+              const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
+              gw[4 * c8] = __byte_perm(a.x, a.y, 0x5410); uw[4 * c8] = __byte_perm(a.x, a.y, 0x7632);
+              gw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x5410); uw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x7632);
+              gw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x7632);
+              gw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x7632);
+            }
+            const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
+                                                             swz128(lane, 4 * (w & 1) + c8));
+            dw[4 * c8] = dd.x; dw[4 * c8 + 1] = dd.y; dw[4 * c8 + 2] = dd.z; dw[4 * c8 + 3] = dd.w;
           }
-          const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
-                                                           swz128(lane, 4 * (w & 1) + c8));
-          dw[4 * c8] = dd.x; dw[4 * c8 + 1] = dd.y; dw[4 * c8 + 2] = dd.z; dw[4 * c8 + 3] = dd.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            gw[i] = sv.g16(2 * i, lane) | (sv.g16(2 * i + 1, lane) << 16);
+            uw[i] = sv.u16(2 * i, lane) | (sv.u16(2 * i + 1, lane) << 16);
+            dw[i] = sv.d16(2 * i, lane) | (sv.d16(2 * i + 1, lane) << 16);
+          }
         }
-      } else {
+        uint32_t gmax = 0;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          gw[i] = sv.g16(2 * i, lane) | (sv.g16(2 * i + 1, lane) << 16);
-          uw[i] = sv.u16(2 * i, lane) | (sv.u16(2 * i + 1, lane) << 16);
-          dw[i] = sv.d16(2 * i, lane) | (sv.d16(2 * i + 1, lane) << 16);
+          const float2 g2 = bf16x2_f2(gw[i]), u2 = bf16x2_f2(uw[i]), d2 = bf16x2_f2(dw[i]);
+          float2 dg2, du2;
+          bwd_fast2<ACT>(g2, u2, d2, dg2, du2);
+          gmax = vmax_u16x2(gmax, gw[i]);
+          // gates of the cancellation run (two bf16 halves at once): act'
+          // from the table, (dY up) act' correctly rounded
+          const uint32_t ci = __vsub2(gw[i], kCP0 * 0x10001u);
+          const uint32_t cm = __vcmpltu2(ci, kCSpan * 0x10001u);
+          if (cm != 0u) {
+            const float2 p2 = mul2(d2, u2);
+            if (cm & 0xFFFFu) dg2.x = tab_mul(cancel[ci & 0xFFFFu], p2.x);
+            if (cm >> 16) dg2.y = tab_mul(cancel[ci >> 16], p2.y);
+          }
+          dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;
+          du[2 * i] = du2.x; du[2 * i + 1] = du2.y;
+        }
+        if (!range_ok<ACT>(gmax)) {  // rare: gates below the fast range
+#pragma unroll 1
+          for (int e = 0; e < 32; ++e) {
+            const int r = colp ? e : lane, c = colp ? lane : e;
+            const uint32_t gb = sv.g16(r, c), ub = sv.u16(r, c), db = sv.d16(r, c);
+            if (gb >= FastRangeAcc<ACT>::kNegLimit) {
+              set_elem(dg, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 0));
+              set_elem(du, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 1));
+            }
+          }
         }
       }
-      float dg[32], du[32];
-      uint32_t gmax = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 g2 = bf16x2_f2(gw[i]), u2 = bf16x2_f2(uw[i]), d2 = bf16x2_f2(dw[i]);
-        float2 dg2, du2;
-        bwd_fast2<ACT>(g2, u2, d2, dg2, du2);
-        gmax = vmax_u16x2(gmax, gw[i]);
-        // gates of the cancellation run (two bf16 halves at once): act' from
-        // the table, (dY up) act' correctly rounded
-        const uint32_t ci = __vsub2(gw[i], kCP0 * 0x10001u);
-        const uint32_t cm = __vcmpltu2(ci, kCSpan * 0x10001u);
-        if (cm != 0u) {
-          const float2 p2 = mul2(d2, u2);
-          if (cm & 0xFFFFu) dg2.x = tab_mul(cancel[ci & 0xFFFFu], p2.x);
-          if (cm >> 16) dg2.y = tab_mul(cancel[ci >> 16], p2.y);
-        }
-        dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;
-        du[2 * i] = du2.x; du[2 * i + 1] = du2.y;
-      }
-      // element e of the blocks sits at (row, column) (lane, e) or (e, lane)
+      // exact operands of element e: at (lane, e) or (e, lane) of the stage
       auto raw = [&](int e, uint32_t& gb, uint32_t& ub, uint32_t& db) {
         const int r = colp ? e : lane, c = colp ? lane : e;
         gb = sv.g16(r, c);
         ub = sv.u16(r, c);
         db = sv.d16(r, c);
       };
-      if (!range_ok<ACT>(gmax)) {  // rare: gates below the fast range
-#pragma unroll 1
-        for (int e = 0; e < 32; ++e) {
-          uint32_t gb, ub, db;
-          raw(e, gb, ub, db);
-          if (gb >= FastRangeAcc<ACT>::kNegLimit) {
-            set_elem(dg, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 0));
-            set_elem(du, e, exact_bwd<ACT, kHot>(hot, gb, ub, db, 1));
-          }
-        }
-      }
       uint32_t qg[8], qu[8];
       const uint32_t sg = mx_block(dg, qg, Bracket<ACT>::kDGate, [&](int e) {
         uint32_t gb, ub, db;
@@ -396,14 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_mx_kernel(const __grid_consta
         }
       } else {
         // (both: the rowwise pass waited for the previous boxes)
-        put_qc(Qcg, lane, j, qg);
-        put_qc(Qcu, lane, j, qu);
+        put_qc<kSuper>(Qcg, lane, j, qg);
+        put_qc<kSuper>(Qcu, lane, j, qu);
         st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sg);
         st_byte(p.s_col + (p.N + c0 + lane) * (p.M / 32) + row0 / 32, su);
       }
     }
 
-    // both passes are done with the stage
+    // the passes are done with the stage
     if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
 
     if ((MODE & GLU_MODE_COL) && active && j == kSuper - 1) {
@@ -441,7 +457,8 @@ cudaError_t launch_t(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo&
   if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
     e = make_tile_map(&p.tm_qr, a.q_row, 1, 2 * a.N, a.M, 2 * a.N, kWC, kTR, 32);
   if (e == cudaSuccess && (MODE & GLU_MODE_COL))
-    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, 2 * a.N, a.M, kTR * kSuper, kWC, 64);
+    e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, 2 * a.N, a.M, kTR * super_for(MODE), kWC,
+                      super_for(MODE) == 2 ? 64 : 32);
   if (e != cudaSuccess) return e;
   p.M = a.M;
   p.N = a.N;
@@ -449,12 +466,12 @@ cudaError_t launch_t(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo&
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
-  p.n_rs = (p.n_rt + kSuper - 1) / kSuper;
+  p.n_rs = (p.n_rt + super_for(MODE) - 1) / super_for(MODE);
   const int64_t units = MODE == GLU_MODE_ROW ? p.n_rt * p.n_ct : p.n_rs * p.n_ct;
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(MODE));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   return cudaLaunchKernelEx(&cfg, kern, p);
