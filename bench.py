@@ -26,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -121,7 +122,7 @@ class Clocks:
         self.proc = None
         self.enabled = enabled
         self.index = index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"glu_quant_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         if not self.enabled:
