@@ -417,6 +417,12 @@ __device__ __forceinline__ float amax2(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)));
   return r;
 }
+// NaN-propagating max of three magnitudes (three-input max, sm_100+).
+__device__ __forceinline__ float amax3(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
 // max |x| over 8 values as a tree (depth 3)
 __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return amax2(amax2(amax2(v[0], v[1]), amax2(v[2], v[3])),

@@ -17,10 +17,14 @@ __device__ __forceinline__ void set_elem(float (&v)[32], int e, float x) {
 }
 
 __device__ __forceinline__ float amax32(const float (&v)[32]) {
-  float m8[4];
+  // three-input maxima: 11 + 4 + 1 + 1 instead of 31 two-input ones
+  float m[11];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) m8[j] = amax8(*reinterpret_cast<const float(*)[8]>(&v[8 * j]));
-  return amax2(amax2(m8[0], m8[1]), amax2(m8[2], m8[3]));
+  for (int j = 0; j < 10; ++j) m[j] = amax3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+  m[10] = amax2(v[30], v[31]);
+  const float a = amax3(m[0], m[1], m[2]), b = amax3(m[3], m[4], m[5]);
+  const float c = amax3(m[6], m[7], m[8]), e = amax2(m[9], m[10]);
+  return amax2(amax3(a, b, c), e);
 }
 
 __device__ __forceinline__ void codes32(const float (&v)[32], float mul, uint32_t (&q)[8]) {
