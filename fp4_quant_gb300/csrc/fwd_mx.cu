@@ -5,8 +5,9 @@
 // colwise (32x1), or both scales come out of a single pass") and API.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
-//   * one persistent CTA per SM with two groups of eight warps.  Tiles are
-//     32 rows x 256 columns; each group has a private two-slot ring of
+//   * one persistent CTA per SM with two groups of eight warps (three groups
+//     of four for both directions).  Tiles are 32 rows x 256 columns (128
+//     for both); each group has a private two-slot ring of
 //     stages, filled by 2-D TMA loads (cp.async.bulk.tensor, completion
 //     counted in transaction bytes on an mbarrier) of 32-row boxes with
 //     128-byte rows (64 bf16 columns, or 32 gate/up pairs) and the hardware
@@ -39,20 +40,24 @@ namespace {
 
 constexpr int kTR = 32;                       // tile rows
 constexpr int kWC = 32;                       // columns per warp sub-tile
-constexpr int kGroupWarps = 8;
-constexpr int kTC = kWC * kGroupWarps;        // tile columns
+// Warps per group (one 32-column sub-tile each) and groups per CTA: two
+// groups of eight for rowwise and colwise (16 warps, up to 128 registers);
+// three groups of four for both (12 warps, up to 168 registers: the both
+// path spilled at 128).
+__host__ __device__ constexpr int group_warps_for(int mode) { return mode == GLU_MODE_BOTH ? 4 : 8; }
+__host__ __device__ constexpr int tc_for(int mode) { return kWC * group_warps_for(mode); }  // tile columns
 // Two groups of eight consumer warps: with two ring slots per group and the
 // hot table this fills about 190 KB of shared memory, and 544 threads leave
 // up to 120 registers per thread (three groups spilled and measured slower).
-__host__ __device__ constexpr int groups_for(int) { return 2; }
-__host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
-constexpr int kStageBytes = kTR * kTC * 4;    // 32 KB: gate + up, or the pairs
-// The exact path reads the hot slice of the activation table from shared
-// memory (reading it from global memory through the read-only cache
-// measured 5-8% slower): 2^-10 <= |g| < 16, or 2^-6 <= |g| < 4 where both
-// code boxes need the room.
-__host__ __device__ constexpr uint32_t hot_lo_for(int mode) { return mode == GLU_MODE_BOTH ? 121u : kHotExpLo; }
-__host__ __device__ constexpr uint32_t hot_bin_for(int mode) { return mode == GLU_MODE_BOTH ? 8u : kHotBinades; }
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 3 : 2; }
+__host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * group_warps_for(mode) * 32; }
+// gate + up, or the pairs: 32 KB (256 columns) or 16 KB (128 columns)
+__host__ __device__ constexpr int stage_bytes_for(int mode) { return kTR * tc_for(mode) * 4; }
+// The exact path reads the hot slice of the activation table (2^-10 <= |g|
+// < 16) from shared memory; reading it from global memory through the
+// read-only cache measured 5-8% slower.
+__host__ __device__ constexpr uint32_t hot_lo_for(int) { return kHotExpLo; }
+__host__ __device__ constexpr uint32_t hot_bin_for(int) { return kHotBinades; }
 __host__ __device__ constexpr int hot_bytes_for(int mode) { return int(hot_bin_for(mode)) * 256 * 8; }
 // Each consumer group has a private ring of kSlots stages: a stage is always
 // consumed, in order, by the one group that waits on it, so an mbarrier
@@ -74,12 +79,12 @@ __host__ __device__ constexpr int qbytes_for(int mode) {
   return (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
 }
 
-using Ctl = RingCtl<groups_for(0) * kSlots, groups_for(0)>;
+using Ctl = RingCtl<3 * kSlots, 3>;
 constexpr int kCtlBytes = int(sizeof(Ctl));
 
 __host__ __device__ constexpr int smem_for(int mode) {
-  return 1024 + groups_for(mode) * kSlots * kStageBytes + hot_bytes_for(mode) +
-         groups_for(mode) * kGroupWarps * qbytes_for(mode) + kCtlBytes;
+  return 1024 + groups_for(mode) * kSlots * stage_bytes_for(mode) + hot_bytes_for(mode) +
+         groups_for(mode) * group_warps_for(mode) * qbytes_for(mode) + kCtlBytes;
 }
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
                   smem_for(GLU_MODE_BOTH) <= 232448,
@@ -170,6 +175,11 @@ template <int ACT, int MODE, int LAYOUT>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
     fwd_mx_kernel(const __grid_constant__ FwdP p) {
   constexpr int kGroups = groups_for(MODE);
+  constexpr int kGroupWarps = group_warps_for(MODE);
+  constexpr int kTC = tc_for(MODE);
+  constexpr int kStageBytes = stage_bytes_for(MODE);
+  constexpr int kUpBox = kTC / 64;  // split layout: first up box (after the gate boxes)
+  constexpr int kBoxes = 2 * kUpBox;  // TMA boxes per tile
   constexpr int kConsumers = kGroups * kGroupWarps;
   constexpr int kStages = kGroups * kSlots;
   constexpr int kQPerWarp = qbytes_for(MODE);
@@ -245,11 +255,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     }
     rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
     ct = __shfl_sync(0xFFFFFFFFu, ct, 0);
-    if (lane < 8 && rt < p.n_rt) {
-      uint8_t* dst = stages + st * kStageBytes + lane * kBoxBytes;
+    if (lane < kBoxes && rt < p.n_rt) {
+      uint8_t* dst = stages + st * kStageBytes + lane * kBoxBytes;  // lane < kBoxes
       const int32_t y = int32_t(rt * kTR);
       if (LAYOUT == GLU_LAYOUT_SPLIT)
-        tma_load_2d(dst, lane < 4 ? &p.tm_a : &p.tm_b, int32_t(ct * kTC + (lane & 3) * 64), y,
+        tma_load_2d(dst, lane < kUpBox ? &p.tm_a : &p.tm_b, int32_t(ct * kTC + (lane % kUpBox) * 64), y,
                     &ctl->full[st]);
       else
         tma_load_2d(dst, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &ctl->full[st]);
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           uint32_t g16a, g16b;
           if (LAYOUT == GLU_LAYOUT_SPLIT) {
             const uint8_t* A = st_base + (w >> 1) * kBoxBytes;
-            const uint8_t* B = A + 4 * kBoxBytes;
+            const uint8_t* B = A + kUpBox * kBoxBytes;
             const int ck = 4 * (w & 1) + (lane >> 3), cb = 2 * (lane & 7);
             g16a = *reinterpret_cast<const uint16_t*>(A + swz(r, ck) + cb);
             g16b = *reinterpret_cast<const uint16_t*>(A + swz(r + 1, ck) + cb);
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         uint32_t xw[16];  // split: 8 gate words then 8 up words; pairs: 16 words
         if (LAYOUT == GLU_LAYOUT_SPLIT) {
           const uint8_t* A = st_base + (w >> 1) * kBoxBytes;
-          const uint8_t* B = A + 4 * kBoxBytes;
+          const uint8_t* B = A + kUpBox * kBoxBytes;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int o = swz(lane, 4 * (w & 1) + 2 * half + k);
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     if (MODE == GLU_MODE_BOTH) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && j >= 4) ? A + 4 * kBoxBytes : A;
+        uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && j >= 4) ? A + kUpBox * kBoxBytes : A;
         const int chunk = LAYOUT == GLU_LAYOUT_SPLIT ? cbase + (j & 3) : j;
         *reinterpret_cast<float4*>(box + swz(lane, chunk)) =
             make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       float v[32];
       __syncwarp();
       {
-        const uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && lane >= 16) ? A + 4 * kBoxBytes : A;
+        const uint8_t* box = (LAYOUT == GLU_LAYOUT_SPLIT && lane >= 16) ? A + kUpBox * kBoxBytes : A;
         const int chunk = LAYOUT == GLU_LAYOUT_SPLIT ? cbase + ((lane >> 2) & 3) : (lane >> 2);
         const int wb = 4 * (lane & 3);
 #pragma unroll
@@ -523,7 +533,6 @@ template <int ACT, int MODE, int LAYOUT>
 cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   auto kern = fwd_mx_kernel<ACT, MODE, LAYOUT>;
   const int smem = smem_for(MODE);
-  constexpr int kGroups = groups_for(MODE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   FwdP p;
@@ -549,7 +558,7 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   p.q_col = static_cast<uint8_t*>(a.q_col);
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.n_rt = (a.M + kTR - 1) / kTR;
-  p.n_ct = (a.N + kTC - 1) / kTC;
+  p.n_ct = (a.N + tc_for(MODE) - 1) / tc_for(MODE);
   p.ntiles = p.n_rt * p.n_ct;
   p.n_rs = (p.n_rt + kSuper - 1) / kSuper;
   const int64_t units = MODE == GLU_MODE_ROW ? p.ntiles : p.n_rs * p.n_ct;
