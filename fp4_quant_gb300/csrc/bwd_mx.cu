@@ -63,8 +63,12 @@ constexpr uint32_t kHotLo = 121, kHotBin = 8;
 __host__ __device__ constexpr int hot_bytes_for(int mode) {
   return mode == GLU_MODE_BOTH && super_for(mode) == 2 ? 0 : int(kHotBin) * 256 * 16;
 }
+// Rowwise boxes are double-buffered where the shared memory has room
+// (rowwise mode), so the wait before refilling one only covers the store
+// issued two tiles earlier.
+__host__ __device__ constexpr int qr_bufs_for(int mode) { return mode == GLU_MODE_ROW ? 2 : 1; }
 __host__ __device__ constexpr int qbytes_for(int mode) {
-  return (mode & GLU_MODE_ROW ? 2 * kQrBytes : 0) + (mode & GLU_MODE_COL ? 2 * 32 * 32 * super_for(mode) : 0);
+  return (mode & GLU_MODE_ROW ? 2 * kQrBytes * qr_bufs_for(mode) : 0) + (mode & GLU_MODE_COL ? 2 * 32 * 32 * super_for(mode) : 0);
 }
 // act' of the cancellation run (see the table generator), copied to shared
 // memory: at most kCancelMax (hi, lo) pairs.
@@ -274,9 +278,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
   };
 
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
-  uint8_t* Qrg = Qbase + warp * kQPerWarp;                                   // rowwise dGate
-  uint8_t* Qru = Qrg + kQrBytes;                                             // rowwise dUp
-  uint8_t* Qcg = Qrg + ((MODE & GLU_MODE_ROW) ? 2 * kQrBytes : 0);           // colwise dGate
+  uint8_t* Qr0 = Qbase + warp * kQPerWarp;                                   // rowwise boxes
+  uint8_t* Qcg = Qr0 + ((MODE & GLU_MODE_ROW) ? 2 * kQrBytes * qr_bufs_for(MODE) : 0);  // colwise dGate
   uint8_t* Qcu = Qcg + kQcBytes;                                             // colwise dUp
   const int64_t n_g = kPer * (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0);
   const int64_t W = 2 * p.N;
@@ -401,7 +404,14 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
         return exact_bwd<ACT, kHot>(hot, gb, ub, db, 1);
       });
       if (!colp) {
-        if (lane == 0) bulk_wait_read0();  // the previous boxes have been read out
+        uint8_t* Qrg = Qr0 + (qr_bufs_for(MODE) == 2 ? int(k & 1) * 2 * kQrBytes : 0);
+        uint8_t* Qru = Qrg + kQrBytes;
+        if (lane == 0) {  // this buffer's previous boxes have been read out
+          if (qr_bufs_for(MODE) == 2)
+            bulk_wait_read1();
+          else
+            bulk_wait_read0();
+        }
         __syncwarp();
         put_qr(Qrg, lane, qg);
         put_qr(Qru, lane, qu);
