@@ -221,6 +221,21 @@ def test_every_bf16_gate(act, direction):
         check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, 2 * N, "all_gates_bwd")
 
 
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+def test_every_bf16_gate_nvfp4(act, layout):
+    """All 65536 bf16 gate patterns through the NVFP4 forward (shuffled, up
+    random and scaled so that blocks reach every scale and the s = 0 case)."""
+    M, N = 256, 256
+    pats = torch.arange(65536, dtype=torch.int32)
+    perm = torch.randperm(65536, generator=torch.Generator().manual_seed(74))
+    g = pats[perm].to(torch.int16).view(torch.bfloat16).reshape(M, N).to(DEV)
+    u = _randn(M, N, 75)
+    u[::5] *= 1e-3
+    gpu, ref = run_fwd(g, u, act[0], G.FMT_NVFP4, G.MODE_ROW, layout)
+    check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, N, "all_gates_nvfp4")
+
+
 def test_exact_activation_blocks_on_gpu():
     # gate = 32: h = 32 * up exactly; amax at 448 * 2^k, ties, subnormal codes
     M, N = 32, 64
