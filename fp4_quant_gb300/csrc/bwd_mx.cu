@@ -278,9 +278,15 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
   };
 
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
-  uint8_t* Qr0 = Qbase + warp * kQPerWarp;                                   // rowwise boxes
-  uint8_t* Qcg = Qr0 + ((MODE & GLU_MODE_ROW) ? 2 * kQrBytes * qr_bufs_for(MODE) : 0);  // colwise dGate
-  uint8_t* Qcu = Qcg + kQcBytes;                                             // colwise dUp
+  // Code boxes of the warp.  Both: warps 0-1 of a group take the rowwise
+  // passes of the tile's four sub-tiles (two each, so two rowwise box
+  // pairs), warps 2-3 the colwise passes (two colwise box pairs); the
+  // group's share is the same 4 x kQPerWarp bytes.
+  uint8_t* Qw = Qbase + grp * kGroupWarps * kQPerWarp +
+                (MODE != GLU_MODE_BOTH ? w * kQPerWarp
+                                       : (w < 2 ? w * 4 * kQrBytes : 8 * kQrBytes + (w - 2) * 4 * kQcBytes));
+  static_assert(MODE != GLU_MODE_BOTH || 2 * 4 * kQrBytes + 2 * 4 * kQcBytes <= kGroupWarps * kQPerWarp,
+                "both-mode code boxes");
   const int64_t n_g = kPer * (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0);
   const int64_t W = 2 * p.N;
 
@@ -299,28 +305,31 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
       break;
     }
     const int64_t rt = ctl->rt[s], ct = ctl->ct[s];
-    const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;
     const int j = int(k % kPer);
-    const bool active = c0 < p.N;
-    const bool work = active && rt < p.n_rt;
-    const StageView<LAYOUT> sv{stages + s * kStageBytes, w};
+    // warp roles (both): rowwise or colwise passes on two sub-tiles
+    constexpr int kSubs = MODE == GLU_MODE_BOTH ? 2 : 1;
+    const bool colp = MODE == GLU_MODE_COL || (MODE == GLU_MODE_BOTH && w >= 2);
+    const int64_t row0 = rt * kTR;
 
-    // One pass per direction on the held stage, sharing one copy of the
-    // arithmetic (a runtime loop keeps the code small).  Rowwise: lane l
-    // takes row l of the sub-tile; colwise: lane l takes column l, read
-    // straight from the stage.  Both modes run both passes, each computing
-    // its own values (measured faster than transposing the rowwise values
-    // through the stage: the kernel is bound by issue and latency, not by
-    // the extra activation work).
-    if (MODE == GLU_MODE_COL && active && j == 0) {
+    // One pass per sub-tile on the held stage.  Rowwise: lane l takes row l
+    // of the sub-tile; colwise: lane l takes column l, read straight from
+    // the stage.  Both modes split the passes between the warps (each warp
+    // keeps one kind of pass, so its registers and code are those of the
+    // single-direction kernels), each pass computing its own values.
+    if (colp && j == 0) {
       if (lane == 0) bulk_wait_read0();  // the unit's boxes are free again
       __syncwarp();
     }
-    constexpr int kP0 = (MODE & GLU_MODE_ROW) ? 0 : 1, kP1 = (MODE & GLU_MODE_COL) ? 1 : 0;
-    float dg[32], du[32];
 #pragma unroll 1
-    for (int pass = kP0; pass <= kP1 && work; ++pass) {
-      const bool colp = pass == 1;
+    for (int sub = 0; sub < kSubs; ++sub) {
+      const int ws = MODE == GLU_MODE_BOTH ? 2 * (w & 1) + sub : w;  // sub-tile
+      const int64_t c0 = ct * kTC + ws * kWC;
+      const bool work = c0 < p.N && rt < p.n_rt;
+      const StageView<LAYOUT> sv{stages + s * kStageBytes, ws};
+      uint8_t* const Qcg = Qw + (MODE == GLU_MODE_BOTH ? sub * 2 * kQcBytes : 0);  // colwise dGate
+      uint8_t* const Qcu = Qcg + kQcBytes;                                          // colwise dUp
+    if (work) {
+      float dg[32], du[32];
       {
         // bf16 pairs along the block: word i holds elements 2i and 2i + 1
         uint32_t gw[16], uw[16], dw[16];
@@ -329,21 +338,21 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
             if (LAYOUT == GLU_LAYOUT_SPLIT) {
-              const int o = swz128(lane, 4 * (w & 1) + c8);
-              const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-              const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+              const int o = swz128(lane, 4 * (ws & 1) + c8);
+              const uint4 a = *reinterpret_cast<const uint4*>(st + (ws >> 1) * kBoxBytes + o);
+              const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (ws >> 1)) * kBoxBytes + o);
               gw[4 * c8] = a.x; gw[4 * c8 + 1] = a.y; gw[4 * c8 + 2] = a.z; gw[4 * c8 + 3] = a.w;
               uw[4 * c8] = b.x; uw[4 * c8 + 1] = b.y; uw[4 * c8 + 2] = b.z; uw[4 * c8 + 3] = b.w;
             } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
-              const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
-              const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
+              const uint4 a = *reinterpret_cast<const uint4*>(st + ws * kBoxBytes + swz128(lane, 2 * c8));
+              const uint4 b = *reinterpret_cast<const uint4*>(st + ws * kBoxBytes + swz128(lane, 2 * c8 + 1));
               gw[4 * c8] = __byte_perm(a.x, a.y, 0x5410); uw[4 * c8] = __byte_perm(a.x, a.y, 0x7632);
               gw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x5410); uw[4 * c8 + 1] = __byte_perm(a.z, a.w, 0x7632);
               gw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x7632);
               gw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x7632);
             }
-            const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
-                                                             swz128(lane, 4 * (w & 1) + c8));
+            const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (ws >> 1)) * kBoxBytes +
+                                                             swz128(lane, 4 * (ws & 1) + c8));
             dw[4 * c8] = dd.x; dw[4 * c8 + 1] = dd.y; dw[4 * c8 + 2] = dd.z; dw[4 * c8 + 3] = dd.w;
           }
         } else {
@@ -404,12 +413,14 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
         return exact_bwd<ACT, kHot>(hot, gb, ub, db, 1);
       });
       if (!colp) {
-        uint8_t* Qrg = Qr0 + (qr_bufs_for(MODE) == 2 ? int(k & 1) * 2 * kQrBytes : 0);
+        // rowwise boxes: double-buffered over tiles (rowwise mode) or one
+        // pair per sub-tile (both)
+        uint8_t* Qrg = Qw + (MODE == GLU_MODE_BOTH ? sub : int(k & 1)) * 2 * kQrBytes;
         uint8_t* Qru = Qrg + kQrBytes;
-        if (lane == 0) {  // this buffer's previous boxes have been read out
-          if (qr_bufs_for(MODE) == 2)
+        if (lane == 0) {  // this box pair's previous stores have read it out
+          if (MODE != GLU_MODE_BOTH)
             bulk_wait_read1();
-          else
+          else if (sub == 0)
             bulk_wait_read0();
         }
         __syncwarp();
@@ -421,20 +432,28 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_mx_kernel(const __gr
           st_byte(p.s_row + (row0 + lane) * (W / 32) + (p.N + c0) / 32, su);
         }
       } else {
-        // (both: the rowwise pass waited for the previous boxes)
         put_qc<kSuper>(Qcg, lane, j, qg);
         put_qc<kSuper>(Qcu, lane, j, qu);
         st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sg);
         st_byte(p.s_col + (p.N + c0 + lane) * (p.M / 32) + row0 / 32, su);
       }
     }
+    }
 
     // the passes are done with the stage
     if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
 
-    if ((MODE & GLU_MODE_COL) && active && j == kSuper - 1) {
+    if (colp && j == kSuper - 1) {  // the unit's colwise boxes are complete
       const int64_t urow0 = row0 - j * kTR;
-      store2(&p.tm_qc, Qcg, Qcu, int32_t(urow0), int32_t(c0), int32_t(urow0), int32_t(p.N + c0), lane);
+#pragma unroll 1
+      for (int sub = 0; sub < kSubs; ++sub) {
+        const int ws = MODE == GLU_MODE_BOTH ? 2 * (w & 1) + sub : w;
+        const int64_t c0 = ct * kTC + ws * kWC;
+        if (c0 >= p.N) continue;
+        uint8_t* const Qcg = Qw + (MODE == GLU_MODE_BOTH ? sub * 2 * kQcBytes : 0);
+        store2(&p.tm_qc, Qcg, Qcg + kQcBytes, int32_t(urow0), int32_t(c0), int32_t(urow0),
+               int32_t(p.N + c0), lane);
+      }
     }
   }
   if (failed && lane == 0) {
