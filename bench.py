@@ -500,7 +500,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=16384)
+    ap.add_argument("--cpu-rows", type=int, default=131072)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--sweep", default=None)
     ap.add_argument("--rows", type=int, default=M_FULL,
