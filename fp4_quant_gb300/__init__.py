@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "glu_quant_fwd", "glu_quant_bwd", "glu_quant_fwd_sizes", "glu_quant_bwd_sizes",
-    "glu_quant_status_str", "glu_quant_abi_version", "GluQuantFwdArgs", "GluQuantBwdArgs",
+    "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
+    "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
     "ACT_SILU", "ACT_GELU_TANH", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32",
     "MODE_ROW", "MODE_COL", "MODE_BOTH", "LAYOUT_SPLIT", "LAYOUT_INTERLEAVED",
@@ -86,6 +87,9 @@ def _load() -> ctypes.CDLL:
     lib.glu_quant_status_str.restype = ctypes.c_char_p
     lib.glu_quant_abi_version.argtypes = []
     lib.glu_quant_abi_version.restype = ctypes.c_int
+    lib.glu_quant_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32),
+                                            ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    lib.glu_quant_device_errors.restype = ctypes.c_int
     return lib
 
 
@@ -127,6 +131,13 @@ def glu_quant_status_str(status: int) -> str:
 
 def glu_quant_abi_version() -> int:
     return _lib().glu_quant_abi_version()
+
+
+def glu_quant_device_errors(clear: bool = False) -> tuple[int, int, int]:
+    """(status, forward error bits, backward error bits)."""
+    f, b = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    st = _lib().glu_quant_device_errors(ctypes.byref(f), ctypes.byref(b), int(clear))
+    return st, f.value, b.value
 
 
 # ---- tensor conveniences ------------------------------------------------------

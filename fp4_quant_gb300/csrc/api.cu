@@ -215,3 +215,10 @@ extern "C" const char* glu_quant_status_str(int status) {
 }
 
 extern "C" int glu_quant_abi_version(void) { return GLU_QUANT_ABI_VERSION; }
+
+extern "C" int glu_quant_device_errors(uint32_t* fwd_bits, uint32_t* bwd_bits, int clear) {
+  if (fwd_bits == nullptr || bwd_bits == nullptr) return GLU_EINVAL;
+  if (gq::read_err_fwd_mx(fwd_bits, clear != 0) != cudaSuccess) return GLU_EDEVICE;
+  if (gq::read_err_bwd_mx(bwd_bits, clear != 0) != cudaSuccess) return GLU_EDEVICE;
+  return GLU_OK;
+}

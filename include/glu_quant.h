@@ -162,6 +162,16 @@ GLU_API int glu_quant_bwd(const glu_quant_bwd_args* args, void* stream);
 GLU_API int glu_quant_fwd_sizes(const glu_quant_fwd_args* args, size_t sizes[4]);
 GLU_API int glu_quant_bwd_sizes(const glu_quant_bwd_args* args, size_t sizes[4]);
 
+/* Device-side error bits recorded since the last clear, on the current
+ * device (a bounded wait inside a kernel that gave up instead of spinning:
+ * 1 = a consumer waited too long for a tile, 4 = copies still in flight at
+ * exit; 0 = none).  *fwd_bits covers the forward MXFP8 kernels, *bwd_bits the
+ * backward MXFP8 kernels.  Copies from device memory, so it waits for the
+ * kernels launched before it; call it outside stream capture.  `clear`
+ * non-zero resets the bits afterwards.  Returns GLU_OK, GLU_EINVAL (NULL
+ * pointer) or GLU_EDEVICE. */
+GLU_API int glu_quant_device_errors(uint32_t* fwd_bits, uint32_t* bwd_bits, int clear);
+
 /* Static text for a status code. */
 GLU_API const char* glu_quant_status_str(int status);
 

@@ -441,3 +441,17 @@ def test_packed_gate_up_layout():
     b = G.fwd(g.contiguous(), u.contiguous(), mode=G.MODE_BOTH)
     for k in ("q_row", "s_row", "q_col", "s_col"):
         assert torch.equal(a[k], b[k])
+
+
+def test_device_error_bits_stay_clear():
+    """No bounded wait gave up during the calls above or a fresh set of
+    calls of every MXFP8 mode (the bits are read back and cleared)."""
+    st, f, b = G.glu_quant_device_errors(clear=True)
+    assert st == G.GLU_OK
+    g, u, d = _randn(256, 512, 81), _randn(256, 512, 82), _randn(256, 512, 83)
+    for mode in MODES:
+        G.fwd(g, u, mode=mode)
+        G.bwd(g, u, d, mode=mode)
+    torch.cuda.synchronize()
+    st, f, b = G.glu_quant_device_errors(clear=True)
+    assert (st, f, b) == (G.GLU_OK, 0, 0)
