@@ -261,7 +261,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // Measured over every bf16 gate of the fast range (SiLU |g| < 64, GELU
 // -7 < g < 64 forward, -6 < g < 64 backward), in units of 2^-24:
 //   fast_h2:   |act(g) u - h| / |act(g) u| <= 3.5 (SiLU), 33 (GELU)
-//   bwd_fast2: dUp 3.5 (SiLU), 31 (GELU); dGate 81 (SiLU), 56 (GELU)
+//   bwd_fast2: dUp 3.5 (SiLU), 31 (GELU); dGate 27 (SiLU), 47 (GELU)
 //              outside the cancellation run (below).
 // Gates outside the range take the exact path.
 
@@ -302,7 +302,7 @@ __device__ __forceinline__ bool fast_range_ok(uint32_t vmax) {
 //   x = g E S (SiLU) or 2 y'(g) g E S (GELU), y'(g) = sqrt(2/pi) (1 + 3 *
 //   0.044715 g^2), using 1 - S = E S; the products dY g and dY up are exact.
 // Near the zero of act' the sum 1 + x cancels and magnifies the errors of E
-// and S: for the run of bf16 gates where |1 + x| * 48 < |x| the backward
+// and S: for the run of bf16 gates where |1 + x| * 24 < |x| the backward
 // kernel takes act' from the cancellation table instead.
 template <int ACT>
 __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du) {
@@ -340,12 +340,12 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 // exact value and of the bracket products.
 //   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-17
 //   dUp = dY act(g):   same forms                             -> 2^-20, 2^-18
-//   dGate = dY up act'(g) off the cancellation run: SiLU 81, GELU 56
-//                                                             -> 2^-16, 2^-17
+//   dGate = dY up act'(g) off the cancellation run: SiLU 27, GELU 47
+//                                                             -> 2^-18, 2^-18
 template <int ACT> struct Bracket {
   static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-17f;
   static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
-  static constexpr float kDGate = ACT == 0 ? 0x1p-16f : 0x1p-17f;
+  static constexpr float kDGate = 0x1p-18f;
 };
 
 // ----------------------------------------------------------------- MXFP8 --

@@ -19,8 +19,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
 
 # half-widths (units of 2^-24) and measured-form ranges, per activation
-BRACKET = {0: {"act": 16.0, "dup": 16.0, "dgate": 256.0},
-           1: {"act": 128.0, "dup": 64.0, "dgate": 128.0}}
+BRACKET = {0: {"act": 16.0, "dup": 16.0, "dgate": 64.0},
+           1: {"act": 128.0, "dup": 64.0, "dgate": 64.0}}
 FWD_RANGE = {0: (-64.0, 64.0), 1: (-7.0, 64.0)}
 BWD_RANGE = {0: (-64.0, 64.0), 1: (-6.0, 64.0)}
 SLACK = 1.5  # final product rounding, exact-value rounding, bracket product
@@ -85,5 +85,5 @@ def test_backward_forms(probe, act):
     assert u_gate + SLACK <= BRACKET[act]["dgate"]
     # the run is where the fast dGate form cancels: it must be short and
     # sit around the zero of act'
-    assert 1 <= span <= 16
+    assert 1 <= span <= 16  # (the kernel copies at most 16 entries)
     assert np.all(np.abs(O.act_grad(act, g[run])) < 0.05)
