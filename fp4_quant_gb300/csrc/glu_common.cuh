@@ -338,12 +338,12 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 // error (measured over every bf16 gate of the fast range, in units of
 // 2^-24) plus one unit each for the rounding of the final product, of the
 // exact value and of the bracket products.
-//   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-17
+//   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-18
 //   dUp = dY act(g):   same forms                             -> 2^-20, 2^-18
 //   dGate = dY up act'(g) off the cancellation run: SiLU 27, GELU 47
 //                                                             -> 2^-18, 2^-18
 template <int ACT> struct Bracket {
-  static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-17f;
+  static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDGate = 0x1p-18f;
 };

@@ -20,7 +20,7 @@ CSRC = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
 
 # half-widths (units of 2^-24) and measured-form ranges, per activation
 BRACKET = {0: {"act": 16.0, "dup": 16.0, "dgate": 64.0},
-           1: {"act": 128.0, "dup": 64.0, "dgate": 64.0}}
+           1: {"act": 64.0, "dup": 64.0, "dgate": 64.0}}
 FWD_RANGE = {0: (-64.0, 64.0), 1: (-7.0, 64.0)}
 BWD_RANGE = {0: (-64.0, 64.0), 1: (-6.0, 64.0)}
 SLACK = 1.5  # final product rounding, exact-value rounding, bracket product
