@@ -1,8 +1,12 @@
-// Forward gated GLU fused with MXFP8 (E4M3 + E8M0 RCEIL) quantisation:
-// rowwise 1x32, colwise 32x1, or both from one read of gate/up.
-// "Add swiglu + MXFP8 fused CuTe DSL kernel", Summary ("gate/up are read
-// once, the bf16 activation tensor is never materialized, and rowwise (1x32),
-// colwise (32x1), or both scales come out of a single pass") and API.
+// Forward gated GLU fused with block-scaled quantisation:
+//   * MXFP8 (E4M3 + E8M0 RCEIL): rowwise 1x32, colwise 32x1, or both from one
+//     read of gate/up.  "Add swiglu + MXFP8 fused CuTe DSL kernel", Summary
+//     (gate/up read once, the bf16 activation never materialised, rowwise,
+//     colwise or both scales from a single pass) and API;
+//   * NVFP4 (packed E2M1, one E4M3 scale per 16 outputs, global scale 1,
+//     scales in the 128x4 layout).  "feat(phyai-kernel): add Thor NVFP4
+//     GeGLU kernel for pi0.5", Summary and Supported contract; the merged
+//     gate/up tile is read from memory instead of a GEMM epilogue.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
 //   * one persistent CTA per SM with two groups of eight warps (three groups
@@ -19,7 +23,7 @@
 //     of the same columns, rows first for rowwise) and rotate over the groups;
 //   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31.
 //     Rowwise: lane l takes row l, a 1x32 block (amax, scale and codes in
-//     registers).  Colwise: lane l reads column l straight from the stage.
+//     registers); NVFP4 is rowwise with two 16-output blocks per lane.  Colwise: lane l reads column l straight from the stage.
 //     Both: the row values also go through a private swizzled transpose
 //     buffer from which lane l reads column l.  Code boxes (32 x 32 bytes)
 //     leave through TMA stores; no barrier spans more than a warp;
@@ -32,6 +36,7 @@
 #include "glu_common.cuh"
 #include "kernels.h"
 #include "mx_block.cuh"
+#include "nv_block.cuh"
 #include "ring.cuh"
 #include "tma.cuh"
 
@@ -39,6 +44,9 @@ namespace gq {
 namespace {
 
 constexpr int kTR = 32;                       // tile rows
+// Internal mode of the NVFP4 format: walked and computed like rowwise MXFP8.
+constexpr int kModeNv = 4;
+__host__ __device__ constexpr bool row_walk(int mode) { return mode == GLU_MODE_ROW || mode == kModeNv; }
 constexpr int kWC = 32;                       // columns per warp sub-tile
 // Warps per group (one 32-column sub-tile each) and groups per CTA: two
 // groups of eight for rowwise and colwise (16 warps, up to 128 registers);
@@ -72,11 +80,15 @@ constexpr int kSlots = 2;
 // 20% slower than the rowwise pattern; so a group walks kSuper row tiles of
 // the same columns in a row and the warp fills a 32 x 128-byte box (128-byte
 // swizzle), stored once per kSuper tiles.
+// NVFP4: 32 rows x 16 bytes of packed codes per tile, two boxes so that a
+// store may still be reading one while the next is written.
 constexpr int kQBytes = 1024;
 constexpr int kSuper = 4;
 constexpr int kQcBytes = 32 * 32 * kSuper;
+constexpr int kQnBytes = 32 * 16;
 __host__ __device__ constexpr int qbytes_for(int mode) {
-  return (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
+  return mode == kModeNv ? 2 * kQnBytes
+                         : (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
 }
 
 using Ctl = RingCtl<3 * kSlots, 3>;
@@ -87,7 +99,7 @@ __host__ __device__ constexpr int smem_for(int mode) {
          groups_for(mode) * group_warps_for(mode) * qbytes_for(mode) + kCtlBytes;
 }
 static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
-                  smem_for(GLU_MODE_BOTH) <= 232448,
+                  smem_for(GLU_MODE_BOTH) <= 232448 && smem_for(kModeNv) <= 232448,
               "shared memory per CTA exceeds 227 KB");
 
 
@@ -101,7 +113,7 @@ __device__ uint32_t g_err_fwd_mx;
 struct FwdP {
   CUtensorMap tm_a;   // gate [M, N] bf16 (boxes 64 x 32) or X as (gate, up) pairs (32 x 32)
   CUtensorMap tm_b;   // up [M, N] bf16 (split layout)
-  CUtensorMap tm_qr;  // q_row [M, N] bytes, boxes 32 x 32
+  CUtensorMap tm_qr;  // q_row [M, N] bytes, boxes 32 x 32 (NVFP4: [M, N/2], boxes 16 x 32)
   CUtensorMap tm_qc;  // q_col [N, M] bytes, boxes 32 x 32
   const uint16_t* gate;  // the same operands in global memory, for the exact path
   const uint16_t* up;
@@ -113,7 +125,20 @@ struct FwdP {
   uint8_t* s_col;
   int64_t n_rt, n_ct, ntiles;
   int64_t n_rs;  // colwise: groups of kSuper row tiles
+  // NVFP4: 128x4 scale tiles per 128-row band (ceil(N/64)); codes written
+  // with plain stores when a code row is not a whole number of 16-byte
+  // chunks (N % 32 != 0), else through the code boxes
+  int64_t sc_tiles;
+  int32_t nv_direct;
 };
+
+// NVFP4 scale bytes of row (32 rt + lane), scale columns c0/16 and c0/16 + 1
+// in the 128x4 layout: 128-row x 4-column tiles of 512 bytes, row-band major;
+// inside a tile row r, column c at (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.
+// c0 is a multiple of 32, so the two columns are adjacent bytes of one tile.
+__device__ __forceinline__ uint8_t* nv_scale_at(const FwdP& p, int64_t rt, int64_t c0, int lane) {
+  return p.s_row + ((rt >> 2) * p.sc_tiles + (c0 >> 6)) * 512 + lane * 16 + (rt & 3) * 4 + ((c0 >> 4) & 3);
+}
 
 // Boxes have 32 rows of 128 bytes; the 128-byte swizzle stores the 16-byte
 // chunk k of row r at chunk k ^ (r & 7).  Split layout: a box holds 64 bf16
@@ -138,6 +163,65 @@ __device__ __forceinline__ float exact_at(const FwdP& p, const float2* hot, int6
   return exact_act_mul_hot<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, g, u);
 }
 
+// Exact values of elements e0 .. e0 + 7 of a block: element e at input row
+// r0 + dr * (e ^ rx), column c0 + dc * e.  All sixteen operand loads are
+// issued before the first value is formed.
+template <int ACT, int MODE, int LAYOUT>
+__device__ __forceinline__ void exact8_at(float (&x)[8], const FwdP& p, const float2* hot, int64_t r0,
+                                          int dr, int64_t c0, int dc, int e0, int rx) {
+  uint32_t gb[8], ub[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = e0 + i;
+    const int64_t row = r0 + dr * (e ^ rx), col = c0 + dc * e;
+    if (LAYOUT == GLU_LAYOUT_SPLIT) {
+      gb[i] = __ldg(p.gate + row * p.ld + col);
+      ub[i] = __ldg(p.up + row * p.ld + col);
+    } else {
+      gb[i] = __ldg(p.gate + row * p.ld + 2 * col);
+      ub[i] = __ldg(p.gate + row * p.ld + 2 * col + 1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    x[i] = exact_act_mul_hot<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(
+        hot, __uint_as_float(gb[i] << 16), __uint_as_float(ub[i] << 16));
+}
+
+// Raw bits of element (row r, column c) of warp w's 32 x 32 sub-tile in the
+// stage: gate in the low half, up in the high half.
+template <int LAYOUT, int UP_BOX>
+__device__ __forceinline__ uint32_t stage_pair(const uint8_t* st, int w, int r, int c) {
+  if (LAYOUT == GLU_LAYOUT_SPLIT) {
+    const uint8_t* A = st + (w >> 1) * kBoxBytes;
+    const int o = swz(r, 4 * (w & 1) + (c >> 3)) + 2 * (c & 7);
+    return uint32_t(*reinterpret_cast<const uint16_t*>(A + o)) |
+           (uint32_t(*reinterpret_cast<const uint16_t*>(A + UP_BOX * kBoxBytes + o)) << 16);
+  } else {
+    return *reinterpret_cast<const uint32_t*>(st + w * kBoxBytes + swz(r, c >> 2) + 4 * (c & 3));
+  }
+}
+
+// Gates outside the fast range (rare): exact values for those elements of
+// this lane's row (ROW) or column (!ROW) of the sub-tile, from the raw bits
+// still held in the stage.
+template <int ACT, int MODE, int LAYOUT, int UP_BOX, bool ROW>
+__device__ __forceinline__ void fix_range(float (&v)[32], const uint8_t* st, const float2* hot, int w,
+                                          int lane) {
+  uint32_t emask = 0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const uint32_t x = ROW ? stage_pair<LAYOUT, UP_BOX>(st, w, lane, e) : stage_pair<LAYOUT, UP_BOX>(st, w, e, lane);
+    emask |= uint32_t((x & 0xFFFFu) >= FastRange<ACT>::kNegLimit) << e;
+  }
+  while (emask != 0u) {
+    const int e = __ffs(emask) - 1;
+    emask &= emask - 1u;
+    const uint32_t x = ROW ? stage_pair<LAYOUT, UP_BOX>(st, w, lane, e) : stage_pair<LAYOUT, UP_BOX>(st, w, e, lane);
+    set_elem(v, e, exact_act_mul_hot<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, bf16_lo(x), bf16_hi(x)));
+  }
+}
+
 // Quantise one 32-value MXFP8 block held by this thread.  Element e sits at
 // input (row0 + (e ^ rx), c0 + lane) for a column block and at (row0 + lane,
 // c0 + e) for a row block.
@@ -145,10 +229,18 @@ template <int ACT, int MODE, int LAYOUT, bool COLUMN>
 __device__ __forceinline__ uint32_t quant_block(float (&v)[32], uint32_t (&q)[8], const FwdP& p,
                                                 const float2* hot, int64_t row0, int64_t c0,
                                                 int lane, int rx = 0) {
-  return mx_block(v, q, Bracket<ACT>::kAct, [&](int e) {
-    return COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
-                  : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
-  });
+  return mx_block(
+      v, q, Bracket<ACT>::kAct,
+      [&](int e) {
+        return COLUMN ? exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + (e ^ rx), c0 + lane)
+                      : exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e);
+      },
+      [&](float (&w)[32]) {
+        exact_fill<0, 4>(w, [&](int e0, float (&x)[8]) {
+          if (COLUMN) exact8_at<ACT, MODE, LAYOUT>(x, p, hot, row0, 1, c0 + lane, 0, e0, rx);
+          else exact8_at<ACT, MODE, LAYOUT>(x, p, hot, row0 + lane, 0, c0, 1, e0, 0);
+        });
+      });
 }
 
 // Colwise codes of row tile j of a unit into the warp's 32 x 128-byte box:
@@ -196,21 +288,21 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   // Work units: rowwise a tile, else kSuper row tiles of the same columns.
   // Unit u of the grid-stride sequence blockIdx.x + i * gridDim.x goes to
   // group i % kGroups; n_g counts the tiles of this warp's group.
-  constexpr int kPer = MODE == GLU_MODE_ROW ? 1 : kSuper;
-  const int64_t units = MODE == GLU_MODE_ROW ? p.ntiles : p.n_rs * p.n_ct;
+  constexpr int kPer = row_walk(MODE) ? 1 : kSuper;
+  const int64_t units = row_walk(MODE) ? p.ntiles : p.n_rs * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
   load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
-    if (MODE & GLU_MODE_ROW) prefetch_tensormap(&p.tm_qr);
+    if ((MODE & GLU_MODE_ROW) || (MODE == kModeNv && !p.nv_direct)) prefetch_tensormap(&p.tm_qr);
     if (MODE & GLU_MODE_COL) prefetch_tensormap(&p.tm_qc);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
     }
-    const int64_t n_minor = MODE == GLU_MODE_ROW ? p.n_ct : p.n_rs;
+    const int64_t n_minor = row_walk(MODE) ? p.n_ct : p.n_rs;
     for (int g = 0; g < kGroups; ++g) {
       const TileWalk tw(blockIdx.x + g * G, kGroups * G, n_minor);
       ctl->major[g] = tw.major;
@@ -235,8 +327,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     if (lane == 0) {
       const int64_t major = ctl->major[g], minor = ctl->minor[g];
       const int j = int(kk % kPer);
-      rt = MODE == GLU_MODE_ROW ? major : kSuper * minor + j;
-      ct = MODE == GLU_MODE_ROW ? minor : major;
+      rt = row_walk(MODE) ? major : kSuper * minor + j;
+      ct = row_walk(MODE) ? minor : major;
       ctl->rt[st] = rt;
       ctl->ct[st] = ct;
       if (j == kPer - 1) {
@@ -270,6 +362,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   uint8_t* Qr = Qbase + warp * kQPerWarp;                                 // row codes
   uint8_t* Qc = Qr + ((MODE == GLU_MODE_BOTH) ? kQBytes : 0);             // column codes
   const int64_t n_g = kPer * (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0);
+  uint32_t nst = 0;  // NVFP4: code boxes stored so far (selects the box)
 
   // Free stage s after this warp's last read of it; the last of the group's
   // warps to do so loads the group's tile k + kSlots into it.
@@ -337,6 +430,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           v[r] = h2.x;
           v[r + 1] = h2.y;
         }
+        if (!fast_range_ok<ACT>(gmax)) fix_range<ACT, MODE, LAYOUT, kUpBox, false>(v, st_base, hot, w, lane);
       }
       release(s, k);
       if (!active) continue;
@@ -345,20 +439,6 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         __syncwarp();
       }
       if (work) {
-        if (!fast_range_ok<ACT>(gmax)) {
-          uint32_t emask = 0;
-#pragma unroll 1
-          for (int r = 0; r < kTR; ++r) {
-            const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + r) * p.ld + c0 + lane)
-                                                            : __ldg(p.gate + (row0 + r) * p.ld + 2 * (c0 + lane));
-            emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << r;
-          }
-          while (emask != 0u) {
-            const int r = __ffs(emask) - 1;
-            emask &= emask - 1u;
-            set_elem(v, r, exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + r, c0 + lane));
-          }
-        }
         uint32_t q[8];
         const uint32_t sc = quant_block<ACT, MODE, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
         put_qc(Qc, lane, j, q);
@@ -414,29 +494,17 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
           h[16 * half + 2 * j + 1] = h2.y;
         }
       }
+      if (!fast_range_ok<ACT>(gmax)) fix_range<ACT, MODE, LAYOUT, kUpBox, true>(h, st_base, hot, w, lane);
     }
     // (both: the stage is kept for the transpose below)
     if (MODE != GLU_MODE_BOTH || !work) release(s, k);
     if (!work) {
       if (MODE == GLU_MODE_BOTH && active && j == kSuper - 1)
         store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+      // NVFP4 padding (rows past the last row tile up to the 128-row band,
+      // columns up to the 4-column tile): zero scales
+      if (MODE == kModeNv && c0 < 64 * p.sc_tiles) st_u16(nv_scale_at(p, rt, c0, lane), 0u);
       continue;
-    }
-
-    if (!fast_range_ok<ACT>(gmax)) {
-      // gates outside the fast range (rare): exact values for those
-      uint32_t emask = 0;
-#pragma unroll 1
-      for (int e = 0; e < 32; ++e) {
-        const uint32_t g16 = LAYOUT == GLU_LAYOUT_SPLIT ? __ldg(p.gate + (row0 + lane) * p.ld + c0 + e)
-                                                        : __ldg(p.gate + (row0 + lane) * p.ld + 2 * (c0 + e));
-        emask |= uint32_t(g16 >= FastRange<ACT>::kNegLimit) << e;
-      }
-      while (emask != 0u) {
-        const int e = __ffs(emask) - 1;
-        emask &= emask - 1u;
-        set_elem(h, e, exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e));
-      }
     }
 
     const bool row_ok = row0 + lane < p.M;
@@ -466,6 +534,43 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         *reinterpret_cast<float4*>(box + swz(lane, chunk)) =
             make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
       }
+    }
+
+    // ---- NVFP4: this lane's 32 values are two 16-output blocks
+    if (MODE == kModeNv) {
+      auto ex = [&](int e) { return exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e); };
+      auto ex8 = [&](int e0, float (&x)[8]) {
+        exact8_at<ACT, MODE, LAYOUT>(x, p, hot, row0 + lane, 0, c0, 1, e0, 0);
+      };
+      uint32_t c[4];
+      uint32_t s0 = nv_block<0>(h, c[0], c[1], Bracket<ACT>::kNv, ex, ex8);
+      uint32_t s1 = nv_block<16>(h, c[2], c[3], Bracket<ACT>::kNv, ex, ex8);
+      // rows past M and columns past N hold zero fill (zero scales already);
+      // explicit zeros keep the padding independent of it
+      if (!row_ok) s0 = 0u;
+      if (!row_ok || c0 + 16 >= p.N) s1 = 0u;
+      if (p.nv_direct) {
+        if (row_ok) {
+          uint8_t* dst = p.q_row + (row0 + lane) * (p.N / 2) + c0 / 2;
+          st_stream(dst, make_uint2(c[0], c[1]));
+          if (c0 + 16 < p.N) st_stream(dst + 8, make_uint2(c[2], c[3]));
+        }
+      } else {
+        uint8_t* Qn = Qr + (nst & 1u) * kQnBytes;
+        // the store issued two boxes ago (from this box) has read it out
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
+        *reinterpret_cast<uint4*>(Qn + lane * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tm_qr, int32_t(c0 / 2), int32_t(row0), Qn);  // rows >= M are clipped
+          bulk_commit();
+        }
+        ++nst;
+      }
+      st_u16(nv_scale_at(p, rt, c0, lane), s0 | (s1 << 8));
+      continue;
     }
 
     // ---- rowwise 1x32: this lane's 32 values
@@ -548,6 +653,9 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   }
   if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
     e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N, a.M, a.N, kWC, kTR, 32);
+  p.nv_direct = MODE == kModeNv && a.N % 32 != 0;
+  if (e == cudaSuccess && MODE == kModeNv && !p.nv_direct)
+    e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N / 2, a.M, a.N / 2, 16, kTR, 0);
   if (e == cudaSuccess && (MODE & GLU_MODE_COL))
     e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, a.N, a.M, kTR * kSuper, kWC, 128);
   if (e != cudaSuccess) return e;
@@ -559,9 +667,12 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + tc_for(MODE) - 1) / tc_for(MODE);
-  p.ntiles = p.n_rt * p.n_ct;
+  // NVFP4 walks the row tiles of whole 128-row scale bands (the tiles past
+  // M load nothing and write zero scales)
+  p.ntiles = (MODE == kModeNv ? (a.M + 127) / 128 * 4 : p.n_rt) * p.n_ct;
   p.n_rs = (p.n_rt + kSuper - 1) / kSuper;
-  const int64_t units = MODE == GLU_MODE_ROW ? p.ntiles : p.n_rs * p.n_ct;
+  p.sc_tiles = (a.N + 63) / 64;
+  const int64_t units = row_walk(MODE) ? p.ntiles : p.n_rs * p.n_ct;
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -590,6 +701,10 @@ cudaError_t by_mode(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& 
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   return a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+}
+
+cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
+  return a.act == GLU_ACT_SILU ? by_layout<0, kModeNv>(a, s, d) : by_layout<1, kModeNv>(a, s, d);
 }
 
 cudaError_t read_err_fwd_mx(uint32_t* v, bool clear) {

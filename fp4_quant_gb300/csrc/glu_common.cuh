@@ -68,6 +68,10 @@ __device__ __forceinline__ void st_byte(void* p, uint32_t v) {
   asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_u16(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(uint16_t(v)) : "memory");
+}
+
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void group_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -346,6 +350,9 @@ template <int ACT> struct Bracket {
   static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDGate = 0x1p-18f;
+  // NVFP4: the activation's width plus the roundings of 1/6, 1/s and the
+  // bracket products (4 units of 2^-24 at most)
+  static constexpr float kNv = 2.0f * kAct;
 };
 
 // ----------------------------------------------------------------- MXFP8 --

@@ -48,15 +48,29 @@ __device__ __forceinline__ void patch_code(uint32_t (&q)[8], int e, uint32_t c) 
     if (j == (e >> 2)) q[j] = __byte_perm(q[j], c, sel);
 }
 
+// v[B .. B + 8 * CHUNKS - 1] from exact values, eight at a time: exact8(e0, x)
+// writes the exact values of elements e0 .. e0 + 7 to x (so that their
+// operand loads can be issued together rather than one latency each).
+template <int B, int CHUNKS, class Exact8>
+__device__ __forceinline__ void exact_fill(float (&v)[32], Exact8&& exact8) {
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    float x[8];
+    exact8(B + 8 * c, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[B + 8 * c + i] = x[i];
+  }
+}
+
 // Quantise the block v (element e of 32).  `exact(e)` returns the exact
 // value of element e; it is called only for elements whose code the test
-// cannot decide (their code bytes are patched in place), and for the whole
-// block when its scale is undecided (or the block holds a NaN, an infinity
-// or a tiny amax).  Writes the 8 code words (element 4j + b in byte b of
-// q[j]) and returns the scale byte.
-template <class Exact>
+// cannot decide (their code bytes are patched in place).  `fill(v)` sets
+// the whole block to exact values, when its scale is undecided (or the
+// block holds a NaN, an infinity or a tiny amax).  Writes the 8 code words
+// (element 4j + b in byte b of q[j]) and returns the scale byte.
+template <class Exact, class Fill>
 __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], const float d,
-                                             Exact&& exact) {
+                                             Exact&& exact, Fill&& fill) {
   uint32_t sc = e8m0_checked(amax32(v), d);
   if (sc != 0x100u) {
     const float mul = e8m0_inv_scale(sc);
@@ -91,8 +105,7 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
     return sc;
   }
   // undecided scale (or a NaN/Inf/tiny block): the block from exact values
-#pragma unroll 1
-  for (int e = 0; e < 32; ++e) set_elem(v, e, exact(e));
+  fill(v);
   sc = e8m0_of(amax32(v));
   if (sc == 0xFFu) {
 #pragma unroll
@@ -101,6 +114,17 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
     codes32(v, e8m0_inv_scale(sc), q);
   }
   return sc;
+}
+
+// Same, with exact values that are cheap one at a time (operands in shared
+// memory): the block is filled by a plain loop.
+template <class Exact>
+__device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], const float d,
+                                             Exact&& exact) {
+  return mx_block(v, q, d, exact, [&](float (&w)[32]) {
+#pragma unroll 1
+    for (int e = 0; e < 32; ++e) set_elem(w, e, exact(e));
+  });
 }
 
 }  // namespace gq
