@@ -40,12 +40,14 @@ __device__ __forceinline__ uint32_t byte_mask(uint32_t x) {
 }
 
 // Replace byte b of word q[j] (j = e >> 2, b = e & 3) by the low byte of c.
+// Every word is rewritten (the identity selector for all but word j): a
+// conditional write of one word makes the compiler index q, which moves
+// the whole array to local memory.
 __device__ __forceinline__ void patch_code(uint32_t (&q)[8], int e, uint32_t c) {
   const int b = e & 3;
   const uint32_t sel = 0x3210u ^ ((uint32_t(b) ^ 4u) << (4 * b));  // byte b from c
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (j == (e >> 2)) q[j] = __byte_perm(q[j], c, sel);
+  for (int j = 0; j < 8; ++j) q[j] = __byte_perm(q[j], c, j == (e >> 2) ? sel : 0x3210u);
 }
 
 // v[B .. B + 8 * CHUNKS - 1] from exact values, eight at a time: exact8(e0, x)
