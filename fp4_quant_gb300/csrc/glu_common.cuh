@@ -265,8 +265,8 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // Measured over every bf16 gate of the fast range (SiLU |g| < 64, GELU
 // -7 < g < 64 forward, -6 < g < 64 backward), in units of 2^-24:
 //   fast_h2:   |act(g) u - h| / |act(g) u| <= 3.5 (SiLU), 33 (GELU)
-//   bwd_fast2: dUp 3.5 (SiLU), 31 (GELU); dGate 27 (SiLU), 47 (GELU)
-//              outside the cancellation run (below).
+//   bwd_fast2: dUp 3.5 (SiLU), 31 (GELU); dGate below 2^-14 (the closed
+//              form below, magnified near the zero of act').
 // Gates outside the range take the exact path.
 
 // act(g) * u for a pair.
@@ -302,38 +302,43 @@ __device__ __forceinline__ bool fast_range_ok(uint32_t vmax) {
 }
 
 // Fast dGate and dUp for a pair of elements:
-//   dUp = (dY g) S,  dGate = (dY up) act'(g),  act'(g) = S (1 + x),
-//   x = g E S (SiLU) or 2 y'(g) g E S (GELU), y'(g) = sqrt(2/pi) (1 + 3 *
-//   0.044715 g^2), using 1 - S = E S; the products dY g and dY up are exact.
-// Near the zero of act' the sum 1 + x cancels and magnifies the errors of E
-// and S: for the run of bf16 gates where |1 + x| * 24 < |x| the backward
-// kernel takes act' from the cancellation table instead.
+//   dUp = (dY g) S,  dGate = (dY up) act'(g),  the products dY g and dY up
+//   exact.  With 1 - S = E S the derivative has the closed form
+//     act'(g) = S (1 + t (1 - S)) = N S^2,   N = 1 + E t,
+//   t = g (SiLU) or 2 g y'(g) (GELU), y'(g) = sqrt(2/pi) (1 + 3 * 0.044715
+//   g^2); here 1 + t is formed first (exact for a bf16 SiLU gate; one
+//   rounding by fma for GELU) and N by one fma, so near the zero of act'
+//   (SiLU g ~ -1.278, GELU ~ -0.752) the only error N magnifies is that of
+//   E.  Over the bf16 gates the magnification |E (1 + t)| / |N| peaks at 79
+//   (SiLU, g = -1.28125) and 83 (GELU, g = -0.75390625); it is at most
+//   1.1 / |N| wherever |N| < 1/8, so the half-width of a dGate block's
+//   rounding test follows the smallest |N| among its elements
+//   (dgate_bracket).  N S is formed before the second factor S, so that S^2
+//   never underflows (E up to 2^92).
+// n returns N, whose magnitude sets the dGate half-width (dgate_bracket).
 template <int ACT>
-__device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du) {
-  float2 E, q;
+__device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du,
+                                          float2& n) {
+  float2 E, t1;
   if (ACT == 0) {
     const float2 th = mul2(g, splat2(-0x1.7154p+0f));            // exact
     const float2 tl = mul2(g, splat2(-4.888495368504664e-06f));  // tail * ln2
     const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
     E = fma2(e0, tl, e0);
+    t1 = add2(g, splat2(1.0f));  // 1 + g, exact
   } else {
-    q = mul2(g, g);
+    const float2 q = mul2(g, g);
     const float2 g3 = mul2(q, g);  // exact
     const float2 w = fma2(splat2(-0.10294324159622192f), g3, mul2(g, splat2(-2.3139550575201895e-05f)));
     const float2 t = add2(mul2(g, splat2(-0x1.26aep+1f)), w);
     E = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    const float2 y2 = fma2(splat2(0.21406444881780073f), q, splat2(1.5957691216057308f));  // 2 y'
+    t1 = fma2(g, y2, splat2(1.0f));  // 1 + 2 g y'
   }
   const float2 den = add2(E, splat2(1.0f));
   const float2 S = make_float2(rcp_approx(den.x), rcp_approx(den.y));
-  const float2 es = mul2(E, S);
-  float2 x;
-  if (ACT == 0) {
-    x = mul2(g, es);
-  } else {
-    const float2 y2 = fma2(splat2(0.21406444881780073f), q, splat2(1.5957691216057308f));
-    x = mul2(mul2(g, es), y2);
-  }
-  const float2 ap = fma2(S, x, S);
+  n = fma2(E, t1, splat2(1.0f));
+  const float2 ap = mul2(mul2(n, S), S);
   du = mul2(mul2(d, g), S);
   dg = mul2(mul2(d, u), ap);
 }
@@ -344,16 +349,45 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 // exact value and of the bracket products.
 //   forward act(g) u:  SiLU 3.5 (two-word exponent), GELU 33  -> 2^-20, 2^-18
 //   dUp = dY act(g):   same forms                             -> 2^-20, 2^-18
-//   dGate = dY up act'(g) off the cancellation run: SiLU 27, GELU 47
-//                                                             -> 2^-18, 2^-18
+//   dGate = dY up act'(g): 6.7 units, plus the error of E (below 3.3
+//                          units) times 1.1 / |N| near the zero of act'
+//                          -> per block from the smallest |N| (dgate_bracket)
 template <int ACT> struct Bracket {
   static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
-  static constexpr float kDGate = 0x1p-18f;
+  static constexpr float kDGate = 0x1p-14f;  // the widest dgate_bracket step
   // NVFP4: the activation's width plus the roundings of 1/6, 1/s and the
   // bracket products (4 units of 2^-24 at most)
   static constexpr float kNv = 2.0f * kAct;
 };
+
+// Half-width of the rounding test of a dGate block whose elements' |N| (see
+// bwd_fast2) are at least nmin: the error bound 10.2 + 3.63 / nmin units of
+// 2^-24 (6.7 units of the closed form, 3.3 units of E magnified 1.1 / |N|
+// times, 3.5 units of roundings) rounded up to a power of two.  Away from the
+// zero of act' (|N| >= 1/8) that is 2^-18, as for the other outputs; a NaN
+// nmin (a block of NaNs) takes the widest step.
+__device__ __forceinline__ float dgate_bracket(float nmin) {
+  return nmin >= 0x1p-3f ? 0x1p-18f
+       : nmin >= 0x1p-4f ? 0x1p-17f
+       : nmin >= 0x1p-5f ? 0x1p-16f
+       : nmin >= 0x1p-6f ? 0x1p-15f
+                          : 0x1p-14f;
+}
+
+// min |x| of three values (three-input min, sm_100+; NaNs ignored).
+__device__ __forceinline__ float absmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
+// min |x| over the 32 lanes of the warp (all lanes take part; NaNs ignored).
+__device__ __forceinline__ float warp_absmin(float x) {
+  float r;
+  asm volatile("redux.sync.min.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 // ----------------------------------------------------------------- MXFP8 --
 

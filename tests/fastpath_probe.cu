@@ -9,7 +9,8 @@
 namespace {
 
 // out[4 i .. 4 i + 3] for gate pattern i: forward act(g) (u = 1), backward
-// dGate = act'(g) and dUp = act(g) (dY = up = 1).
+// dGate = act'(g) and dUp = act(g) (dY = up = 1), and the backward form's N
+// (the factor whose magnitude sets the dGate half-width).
 template <int ACT>
 __global__ void probe_kernel(float* out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -17,20 +18,19 @@ __global__ void probe_kernel(float* out) {
   const float g = __uint_as_float(uint32_t(i) << 16);
   const float2 g2 = make_float2(g, g), one = make_float2(1.0f, 1.0f);
   const float2 h = gq::fast_h2<ACT>(g2, one);
-  float2 dg, du;
-  gq::bwd_fast2<ACT>(g2, one, one, dg, du);
+  float2 dg, du, n;
+  gq::bwd_fast2<ACT>(g2, one, one, dg, du, n);
   out[4 * i] = h.x;
   out[4 * i + 1] = dg.x;
   out[4 * i + 2] = du.x;
-  out[4 * i + 3] = 0.0f;
+  out[4 * i + 3] = n.x;
 }
 
 }  // namespace
 
 // Fills host[4 * 65536] for activation `act` (0 SiLU, 1 GELU tanh); returns a
-// cudaError_t value.  cancel[0..1] receives the first bf16 pattern and the
-// length of the cancellation run the backward kernel takes from its table.
-extern "C" __attribute__((visibility("default"))) int gq_probe_fast(int act, float* host, unsigned* cancel) {
+// cudaError_t value.
+extern "C" __attribute__((visibility("default"))) int gq_probe_fast(int act, float* host) {
   float* d = nullptr;
   cudaError_t e = cudaMalloc(&d, 4 * 65536 * sizeof(float));
   if (e != cudaSuccess) return int(e);
@@ -41,7 +41,5 @@ extern "C" __attribute__((visibility("default"))) int gq_probe_fast(int act, flo
   e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaMemcpy(host, d, 4 * 65536 * sizeof(float), cudaMemcpyDeviceToHost);
   cudaFree(d);
-  cancel[0] = act == 0 ? GQ_CANCEL_P0_0 : GQ_CANCEL_P0_1;
-  cancel[1] = act == 0 ? GQ_CANCEL_SPAN_0 : GQ_CANCEL_SPAN_1;
   return int(e);
 }
