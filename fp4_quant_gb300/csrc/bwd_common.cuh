@@ -67,6 +67,26 @@ struct StageView {
   __device__ uint32_t d16(int r, int c) const {
     return *reinterpret_cast<const uint16_t*>(st + (4 + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
   }
+  // Column `lane` of the sub-tile as bf16 pairs (word i: rows 2i, 2i + 1).
+  // For a fixed row the warp reads 64 contiguous bytes of a box (one
+  // wavefront); rows 8 i + j sit 1024 i bytes after row j.
+  __device__ void col(int lane, uint32_t (&gw)[16], uint32_t (&uw)[16], uint32_t (&dw)[16]) const {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r0 = 2 * i, r1 = 2 * i + 1;
+      if (LAYOUT == GLU_LAYOUT_SPLIT) {
+        gw[i] = g16(r0, lane) | (g16(r1, lane) << 16);
+        uw[i] = u16(r0, lane) | (u16(r1, lane) << 16);
+      } else {
+        const uint8_t* A = st + w * kBoxBytes + 4 * (lane & 3);
+        const uint32_t p0 = *reinterpret_cast<const uint32_t*>(A + swz128(r0, lane >> 2));
+        const uint32_t p1 = *reinterpret_cast<const uint32_t*>(A + swz128(r1, lane >> 2));
+        gw[i] = __byte_perm(p0, p1, 0x5410);
+        uw[i] = __byte_perm(p0, p1, 0x7632);
+      }
+      dw[i] = d16(r0, lane) | (d16(r1, lane) << 16);
+    }
+  }
   // Row `lane` of the sub-tile as bf16 pairs (word i: elements 2i, 2i + 1).
   __device__ void row(int lane, uint32_t (&gw)[16], uint32_t (&uw)[16], uint32_t (&dw)[16]) const {
 #pragma unroll

@@ -16,6 +16,7 @@ struct DevInfo {
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
+cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);  // both directions
 cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_fwd_plain(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_plain(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
@@ -27,6 +28,7 @@ cudaError_t make_tile_map(CUtensorMap* map, const void* base, int elem_bytes, in
 
 // Error bits recorded by a kernel family (bounded waits that gave up).
 cudaError_t read_err_fwd_mx(uint32_t* v, bool clear);
-cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);
+cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);  // (includes the both-directions kernel's bits)
+cudaError_t read_err_bwd_cb(uint32_t* v, bool clear);
 
 }  // namespace gq
