@@ -493,16 +493,6 @@ __device__ __forceinline__ uint32_t e4m3x4_bracket(float a, float b, float c, fl
   return ql;
 }
 
-// Same test on two pairs with packed multiplies.
-__device__ __forceinline__ uint32_t e4m3x4_bracket2(float2 a, float2 b, float2 mlo, float2 mhi,
-                                                    bool& bad) {
-  const float2 al = mul2(a, mlo), bl = mul2(b, mlo), ah = mul2(a, mhi), bh = mul2(b, mhi);
-  const uint32_t ql = e4m3x4(al.x, al.y, bl.x, bl.y);
-  const uint32_t qh = e4m3x4(ah.x, ah.y, bh.x, bh.y);
-  bad |= ql != qh;
-  return ql;
-}
-
 // E8M0 byte from a float amax (NaN/Inf -> 0xFF).
 __device__ __forceinline__ uint32_t e8m0_of(float amax) {
   return e8m0_from_amax_bits(__float_as_uint(amax) & 0x7FFFFFFFu);

@@ -77,21 +77,22 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
   if (sc != 0x100u) {
     const float mul = e8m0_inv_scale(sc);
     const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-    uint32_t wbad = 0;
+    // codes from the low bracket end; any byte where the high end differs
+    // leaves a bit in `diff`
+    uint32_t diff = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      bool bad = false;
-      q[j] = e4m3x4_bracket2(make_float2(v[4 * j], v[4 * j + 1]), make_float2(v[4 * j + 2], v[4 * j + 3]),
-                             splat2(mlo), splat2(mhi), bad);
-      wbad |= uint32_t(bad) << j;
+      const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
+      const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
+      const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
+      q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
+      diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
     }
-    if (wbad != 0u) {
-      // rare: the straddling elements of the undecided words get codes from
-      // their exact values
+    if (diff != 0u) {
+      // rare: the straddling elements get codes from their exact values
       uint32_t emask = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (!((wbad >> j) & 1u)) continue;
         const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
                                    v[4 * j + 3] * mlo);
         const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
