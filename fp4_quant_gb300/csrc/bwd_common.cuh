@@ -87,6 +87,46 @@ struct StageView {
       dw[i] = d16(r0, lane) | (d16(r1, lane) << 16);
     }
   }
+  // Half h of row r (columns 16h .. 16h + 15) as bf16 pairs.
+  __device__ void row_half(int r, int h, uint32_t (&gw)[8], uint32_t (&uw)[8], uint32_t (&dw)[8]) const {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int o = swz128(r, 4 * (w & 1) + 2 * h + c);
+      if (LAYOUT == GLU_LAYOUT_SPLIT) {
+        const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
+        const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+        gw[4 * c] = a.x; gw[4 * c + 1] = a.y; gw[4 * c + 2] = a.z; gw[4 * c + 3] = a.w;
+        uw[4 * c] = b.x; uw[4 * c + 1] = b.y; uw[4 * c + 2] = b.z; uw[4 * c + 3] = b.w;
+      } else {  // pairs: chunks 4 h + 2 c and 4 h + 2 c + 1 of the warp's box
+        const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(r, 4 * h + 2 * c));
+        const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(r, 4 * h + 2 * c + 1));
+        gw[4 * c] = __byte_perm(a.x, a.y, 0x5410); uw[4 * c] = __byte_perm(a.x, a.y, 0x7632);
+        gw[4 * c + 1] = __byte_perm(a.z, a.w, 0x5410); uw[4 * c + 1] = __byte_perm(a.z, a.w, 0x7632);
+        gw[4 * c + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c + 2] = __byte_perm(b.x, b.y, 0x7632);
+        gw[4 * c + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c + 3] = __byte_perm(b.z, b.w, 0x7632);
+      }
+      const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes + o);
+      dw[4 * c] = dd.x; dw[4 * c + 1] = dd.y; dw[4 * c + 2] = dd.z; dw[4 * c + 3] = dd.w;
+    }
+  }
+  // Half h of column c (rows 16h .. 16h + 15) as bf16 pairs.
+  __device__ void col_half(int c, int h, uint32_t (&gw)[8], uint32_t (&uw)[8], uint32_t (&dw)[8]) const {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r0 = 16 * h + 2 * i, r1 = r0 + 1;
+      if (LAYOUT == GLU_LAYOUT_SPLIT) {
+        gw[i] = g16(r0, c) | (g16(r1, c) << 16);
+        uw[i] = u16(r0, c) | (u16(r1, c) << 16);
+      } else {
+        const uint8_t* A = st + w * kBoxBytes + 4 * (c & 3);
+        const uint32_t p0 = *reinterpret_cast<const uint32_t*>(A + swz128(r0, c >> 2));
+        const uint32_t p1 = *reinterpret_cast<const uint32_t*>(A + swz128(r1, c >> 2));
+        gw[i] = __byte_perm(p0, p1, 0x5410);
+        uw[i] = __byte_perm(p0, p1, 0x7632);
+      }
+      dw[i] = d16(r0, c) | (d16(r1, c) << 16);
+    }
+  }
   // Row `lane` of the sub-tile as bf16 pairs (word i: elements 2i, 2i + 1).
   __device__ void row(int lane, uint32_t (&gw)[16], uint32_t (&uw)[16], uint32_t (&dw)[16]) const {
 #pragma unroll

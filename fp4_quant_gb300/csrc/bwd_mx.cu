@@ -7,19 +7,22 @@
 // kernel of both directions.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
-//   * one persistent CTA per SM with three groups of four warps (twelve
-//     warps: three per SM sub-partition, up to 168 registers per thread).
+//   * one persistent CTA per SM with groups of four warps (rowwise: three
+//     groups, up to 168 registers per thread; colwise: four, up to 128).
 //     Tiles are 32 rows x 128 columns of N; each group has a private
 //     two-slot ring of 24 KB stages filled by 2-D TMA loads of 32-row boxes
 //     with 128-byte rows and the 128-byte swizzle (gate, up and dY: two
 //     boxes each, or four boxes of (gate, up) pairs and two of dY).  The
 //     warp that frees a stage last issues the group's next load into it;
 //   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31 of
-//     the tile: rowwise, lane l reads row l of the sub-tile (16-byte
-//     chunks); colwise, column l (one 64-byte line of a box per row across
-//     the warp).  The lane forms its 32 dGate and 32 dUp values in registers
-//     and quantises its two blocks, the rare exact path reading its
-//     operands from the stage (held until the codes are decided);
+//     the tile.  Rowwise: lane l reads row l of the sub-tile (16-byte
+//     chunks), forms its 32 dGate and 32 dUp values in registers and
+//     quantises its two 1x32 blocks.  Colwise: two passes of 16 columns;
+//     lanes 2i and 2i + 1 share column 16 pass + i (rows 0..15 and 16..31,
+//     read straight from the swizzled stage), each forming and encoding 16
+//     values per output, one shuffle joining the halves' amax.  The rare
+//     exact path reads its operands from the stage (held until the codes
+//     are decided);
 //   * rowwise walks the tiles of a row band first, colwise down the column
 //     strips (the CTAs working at once then store neighbouring 32-byte
 //     pieces of the same [2N, M] code rows);
@@ -27,10 +30,10 @@
 //     rounding test deciding codes and scales (dGate's half-width set by
 //     the distance to the zero of act') and the activation table settling
 //     the rest;
-//   * code boxes (32 x 32 bytes, 32-byte swizzle) go to the warp's 4 KB box
-//     area, two pairs used in turn, and leave through TMA stores: rowwise at
-//     columns c and N + c of [M, 2N], colwise at rows c and N + c of [2N, M]
-//     (box row c holding column c).
+//   * code boxes (32 x 32 bytes, 32-byte swizzle) go to the warp's box area
+//     (rowwise: two pairs used in turn) and leave through TMA stores:
+//     rowwise at columns c and N + c of [M, 2N], colwise at rows c and
+//     N + c of [2N, M] (box row c holding column c).
 #include <cstring>
 
 #include "bwd_common.cuh"
@@ -75,36 +78,45 @@ namespace {
 
 using namespace bwd;
 
-constexpr int kGroups = 3;
+// Rowwise: three groups of four warps (up to 168 registers: a lane holds a
+// whole row's 64 values), two box pairs per warp used in turn, the hot slice
+// of the backward table in shared memory.  Colwise: four groups of four
+// warps (up to 128 registers: two lanes share a column, 16 rows each), one
+// box pair per warp, the exact path reading the table from global memory.
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_COL ? 4 : 3; }
+__host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
+__host__ __device__ constexpr int tbytes_for(int mode) { return mode == GLU_MODE_COL ? 2048 : 4096; }
+__host__ __device__ constexpr int hot_for(int mode) { return mode == GLU_MODE_COL ? 0 : kHotBytes; }
 constexpr int kSlots = 2;
-constexpr int kStages = kGroups * kSlots;
-constexpr int kThreads = kGroups * kGroupWarps * 32;
-constexpr int kTBytes = 4096;  // per warp: two pairs of code boxes
 
-using Ctl = RingCtl<kStages, kGroups>;
+using Ctl = RingCtl<4 * kSlots, 4>;
 
-constexpr int kSmem = 1024 + kStages * kStageBytes + kGroups * kGroupWarps * kTBytes + kHotBytes +
-                      int(sizeof(Ctl));
-static_assert(kSmem <= 232448, "shared memory per CTA exceeds 227 KB");
+__host__ __device__ constexpr int smem_for(int mode) {
+  return 1024 + groups_for(mode) * kSlots * kStageBytes + groups_for(mode) * kGroupWarps * tbytes_for(mode) +
+         hot_for(mode) + int(sizeof(Ctl));
+}
+static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448,
+              "shared memory per CTA exceeds 227 KB");
 
 __device__ uint32_t g_err_bwd_dir;
 
 template <int ACT, int MODE, int LAYOUT>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dir_kernel(const __grid_constant__ BwdP p) {
+__global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __grid_constant__ BwdP p) {
   constexpr bool kCol = MODE == GLU_MODE_COL;
+  constexpr int kGroups = groups_for(MODE), kStages = kGroups * kSlots, kTBytes = tbytes_for(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
   uint8_t* Tbase = stages + kStages * kStageBytes;
   uint8_t* hot_raw = Tbase + kGroups * kGroupWarps * kTBytes;
-  const float4* hot = reinterpret_cast<const float4*>(hot_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(hot_raw + kHotBytes);
+  const float4* hot = hot_for(MODE) ? reinterpret_cast<const float4*>(hot_raw) : nullptr;
+  Ctl* ctl = reinterpret_cast<Ctl*>(hot_raw + hot_for(MODE));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   const int64_t units = p.n_rt * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+  if (hot_for(MODE)) load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -188,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dir_kernel(const __grid_const
     const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;
     const StageView<LAYOUT> sv{stages + s * kStageBytes, w};
 
-    if (c0 < p.N) {
+    if (!kCol && c0 < p.N) {
       // ---- row (colwise: column) `lane` of the sub-tile: dGate and dUp in
       // registers; element e of the lane's blocks sits at (lane, e) of the
       // sub-tile (colwise: (e, lane))
@@ -263,6 +275,104 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dir_kernel(const __grid_const
         bulk_commit();
       }
       ++nst;
+    } else if (kCol && c0 < p.N) {
+      // two passes of 16 lines (rows; colwise: columns): lane l takes line
+      // 16 pass + l / 2, elements 16 (l % 2) .. 16 (l % 2) + 15 of it
+      const int hf = lane & 1;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        const int L = 16 * pass + (lane >> 1);
+        // element e of the lane's half sits at (L, 16 hf + e) of the sub-tile
+        // (colwise: (16 hf + e, L))
+        auto at_r = [&](int e) { return kCol ? 16 * hf + e : L; };
+        auto at_c = [&](int e) { return kCol ? L : 16 * hf + e; };
+        float dg[16], du[16];
+        float nmin = __int_as_float(0x7F800000);
+        {
+          uint32_t gw[8], uw[8], dw[8];
+          if (kCol)
+            sv.col_half(L, hf, gw, uw, dw);
+          else
+            sv.row_half(L, hf, gw, uw, dw);
+          uint32_t gmax = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float2 dg2, du2, n2;
+            bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, n2);
+            gmax = vmax_u16x2(gmax, gw[i]);
+            nmin = absmin3(nmin, n2.x, n2.y);
+            dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;
+            du[2 * i] = du2.x; du[2 * i + 1] = du2.y;
+          }
+          if (!range_ok<ACT>(gmax)) {  // rare: gates below the fast range
+#pragma unroll 1
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t gb = sv.g16(at_r(e), at_c(e));
+              if (gb >= FastRangeAcc<ACT>::kNegLimit) {
+                const uint32_t ub = sv.u16(at_r(e), at_c(e)), db = sv.d16(at_r(e), at_c(e));
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2)
+                  if (k2 == e) {
+                    dg[k2] = exact_bwd<ACT>(hot, gb, ub, db, 0);
+                    du[k2] = exact_bwd<ACT>(hot, gb, ub, db, 1);
+                  }
+              }
+            }
+          }
+        }
+        nmin = fminf(nmin, __shfl_xor_sync(0xFFFFFFFFu, nmin, 1));
+        auto ex = [&](int e, int which) {
+          return exact_bwd<ACT>(hot, sv.g16(at_r(e), at_c(e)), sv.u16(at_r(e), at_c(e)), sv.d16(at_r(e), at_c(e)), which);
+        };
+        uint32_t qg[4], qu[4];
+        const uint32_t sg = mx_half(dg, qg, dgate_bracket(nmin), [&](int e) { return ex(e, 0); },
+                                    [&](float (&x)[16]) {
+#pragma unroll 1
+                                      for (int e = 0; e < 16; ++e) {
+                                        const float y = ex(e, 0);
+#pragma unroll
+                                        for (int k2 = 0; k2 < 16; ++k2) if (k2 == e) x[k2] = y;
+                                      }
+                                    });
+        const uint32_t su = mx_half(du, qu, Bracket<ACT>::kDUp, [&](int e) { return ex(e, 1); },
+                                    [&](float (&x)[16]) {
+#pragma unroll 1
+                                      for (int e = 0; e < 16; ++e) {
+                                        const float y = ex(e, 1);
+#pragma unroll
+                                        for (int k2 = 0; k2 < 16; ++k2) if (k2 == e) x[k2] = y;
+                                      }
+                                    });
+        if (pass == 0) {  // the previous tile's boxes have been read out
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+        }
+        *reinterpret_cast<uint4*>(T + swz32(L, hf)) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
+        *reinterpret_cast<uint4*>(T + kQBytes + swz32(L, hf)) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+        if (hf == 0) {
+          if (kCol) {
+            st_byte(p.s_col + (c0 + L) * (p.M / 32) + row0 / 32, sg);
+            st_byte(p.s_col + (p.N + c0 + L) * (p.M / 32) + row0 / 32, su);
+          } else if (row0 + L < p.M) {
+            st_byte(p.s_row + (row0 + L) * (W / 32) + c0 / 32, sg);
+            st_byte(p.s_row + (row0 + L) * (W / 32) + (p.N + c0) / 32, su);
+          }
+        }
+      }
+      // the tile's codes are decided: the stage is free
+      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (kCol) {
+          tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(c0), T);
+          tma_store_2d(&p.tm_qc, int32_t(row0), int32_t(p.N + c0), T + kQBytes);
+        } else {
+          tma_store_2d(&p.tm_qr, int32_t(c0), int32_t(row0), T);  // rows >= M are clipped
+          tma_store_2d(&p.tm_qr, int32_t(p.N + c0), int32_t(row0), T + kQBytes);
+        }
+        bulk_commit();
+      }
     } else {
       // no columns for this warp in the tile
       if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
@@ -283,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dir_kernel(const __grid_const
 template <int ACT, int MODE, int LAYOUT>
 cudaError_t launch_dir(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
   auto kern = bwd_dir_kernel<ACT, MODE, LAYOUT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  const int smem = smem_for(MODE);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   BwdP p;
   e = make_params(p, a);
@@ -292,8 +403,8 @@ cudaError_t launch_dir(const glu_quant_bwd_args& a, cudaStream_t s, const DevInf
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.blockDim = dim3(threads_for(MODE));
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }

@@ -130,4 +130,84 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
   });
 }
 
+// ---------------------------------------------------------- half blocks --
+// A 32-element block held by two neighbouring lanes (lane 2i + h holds
+// elements 16h .. 16h + 15): one shuffle joins the two halves' amax, each
+// lane encodes its 16 codes.  Both lanes of a pair take every decision
+// alike, since both see the same amax.
+
+__device__ __forceinline__ float amax16(const float (&v)[16]) {
+  const float a = amax3(v[0], v[1], v[2]), b = amax3(v[3], v[4], v[5]), c = amax3(v[6], v[7], v[8]);
+  const float e = amax3(v[9], v[10], v[11]), f = amax3(v[12], v[13], v[14]);
+  return amax2(amax3(a, b, c), amax3(e, f, v[15]));
+}
+
+// max of the amax of this lane's half and of its neighbour's (whole warp)
+__device__ __forceinline__ float pair_amax(float a) {
+  return amax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+}
+
+__device__ __forceinline__ void patch_code4(uint32_t (&q)[4], int e, uint32_t c) {
+  const int b = e & 3;
+  const uint32_t sel = 0x3210u ^ ((uint32_t(b) ^ 4u) << (4 * b));  // byte b from c
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = __byte_perm(q[j], c, j == (e >> 2) ? sel : 0x3210u);
+}
+
+// Quantise the half block v (element e of 16) with the rounding test; all
+// lanes of the warp call it together.  `exact(e)` returns the exact value of
+// element e, called only for elements whose code the test cannot decide;
+// `fill(v)` sets this lane's half to exact values, for blocks whose scale is
+// undecided (or that hold a NaN, an infinity or a tiny amax).  Writes the 4
+// code words (element 4j + b in byte b of q[j]) and returns the scale byte.
+template <class Exact, class Fill>
+__device__ __forceinline__ uint32_t mx_half(float (&v)[16], uint32_t (&q)[4], const float d, Exact&& exact,
+                                            Fill&& fill) {
+  uint32_t sc = e8m0_checked(pair_amax(amax16(v)), d);
+  const bool undecided = sc == 0x100u;
+  if (!undecided) {
+    const float mul = e8m0_inv_scale(sc);
+    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+    uint32_t diff = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
+      const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
+      const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
+      q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
+      diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
+    }
+    if (diff != 0u) {
+      // rare: the straddling elements get codes from their exact values
+      uint32_t emask = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo,
+                                   v[4 * j + 3] * mlo);
+        const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi,
+                                   v[4 * j + 3] * mhi);
+        emask |= byte_mask(ql ^ qh) << (4 * j);
+      }
+      while (emask != 0u) {
+        const int e = __ffs(emask) - 1;
+        emask &= emask - 1u;
+        patch_code4(q, e, e4m3(exact(e) * mul));
+      }
+    }
+  }
+  // rare, taken by the whole warp: the undecided blocks from exact values
+  if (__any_sync(0xFFFFFFFFu, undecided)) {
+    if (undecided) fill(v);
+    const float a = pair_amax(amax16(v));
+    if (undecided) {
+      sc = e8m0_of(a);
+      const float m = e8m0_inv_scale(sc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        q[j] = sc == 0xFFu ? 0x7F7F7F7Fu : e4m3x4(v[4 * j] * m, v[4 * j + 1] * m, v[4 * j + 2] * m, v[4 * j + 3] * m);
+    }
+  }
+  return sc;
+}
+
 }  // namespace gq
