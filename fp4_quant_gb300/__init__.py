@@ -21,12 +21,12 @@ __all__ = [
     "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
     "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
-    "ACT_SILU", "ACT_GELU_TANH", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32",
+    "ACT_SILU", "ACT_GELU_TANH", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
     "MODE_ROW", "MODE_COL", "MODE_BOTH", "LAYOUT_SPLIT", "LAYOUT_INTERLEAVED",
 ]
 
 ACT_SILU, ACT_GELU_TANH = 0, 1
-FMT_MXFP8, FMT_NVFP4, FMT_BF16, FMT_FP32 = 0, 1, 2, 3
+FMT_MXFP8, FMT_NVFP4, FMT_BF16, FMT_FP32, FMT_MXFP8_128X4 = 0, 1, 2, 3, 4
 MODE_ROW, MODE_COL, MODE_BOTH = 1, 2, 3
 LAYOUT_SPLIT, LAYOUT_INTERLEAVED = 0, 1
 
@@ -160,6 +160,15 @@ def _out_tensors(fmt, mode, M, W, device):
                 "s_row": e((M, W // 32), dtype=u8, device=device) if mode & MODE_ROW else None,
                 "q_col": e((W, M), dtype=u8, device=device) if mode & MODE_COL else None,
                 "s_col": e((W, M // 32), dtype=u8, device=device) if mode & MODE_COL else None,
+                "out": None}
+    if fmt == FMT_MXFP8_128X4:
+        # scale matrices [M, W/32] and [W, M/32] in the padded 128x4 layout
+        def sw(r, c):
+            return (-(-r // 128) * 128) * (-(-c // 4) * 4)
+        return {"q_row": e((M, W), dtype=u8, device=device) if mode & MODE_ROW else None,
+                "s_row": e((sw(M, W // 32),), dtype=u8, device=device) if mode & MODE_ROW else None,
+                "q_col": e((W, M), dtype=u8, device=device) if mode & MODE_COL else None,
+                "s_col": e((sw(W, M // 32),), dtype=u8, device=device) if mode & MODE_COL else None,
                 "out": None}
     if fmt == FMT_NVFP4:
         rp, cp = -(-M // 128) * 128, -(-W // 64) * 4

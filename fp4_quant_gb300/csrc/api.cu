@@ -29,22 +29,23 @@ int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t
                  int64_t ld_in, const void* gate, const void* up, const void* q_row,
                  const void* s_row, const void* q_col, const void* s_col, const void* out) {
   if (act != GLU_ACT_SILU && act != GLU_ACT_GELU_TANH) return GLU_EINVAL;
-  if (fmt < GLU_FMT_MXFP8_E4M3 || fmt > GLU_FMT_FP32) return GLU_EINVAL;
+  if (fmt < GLU_FMT_MXFP8_E4M3 || fmt > GLU_FMT_MXFP8_E4M3_128X4) return GLU_EINVAL;
   if (mode < GLU_MODE_ROW || mode > GLU_MODE_BOTH) return GLU_EINVAL;
   if (layout != GLU_LAYOUT_SPLIT && layout != GLU_LAYOUT_INTERLEAVED) return GLU_EINVAL;
-  if (fmt != GLU_FMT_MXFP8_E4M3 && mode != GLU_MODE_ROW) return GLU_EINVAL;
+  const bool mx = fmt == GLU_FMT_MXFP8_E4M3 || fmt == GLU_FMT_MXFP8_E4M3_128X4;
+  if (!mx && mode != GLU_MODE_ROW) return GLU_EINVAL;
   if (M <= 0 || N <= 0) return GLU_EINVAL;
   if (gate == nullptr) return GLU_EINVAL;
   if ((layout == GLU_LAYOUT_SPLIT) != (up != nullptr)) return GLU_EINVAL;
   // exactly the outputs the format/mode produces are given
-  const bool want_qr = fmt == GLU_FMT_NVFP4_E2M1 || (fmt == GLU_FMT_MXFP8_E4M3 && (mode & GLU_MODE_ROW));
-  const bool want_qc = fmt == GLU_FMT_MXFP8_E4M3 && (mode & GLU_MODE_COL);
+  const bool want_qr = fmt == GLU_FMT_NVFP4_E2M1 || (mx && (mode & GLU_MODE_ROW));
+  const bool want_qc = mx && (mode & GLU_MODE_COL);
   const bool want_out = fmt == GLU_FMT_BF16 || fmt == GLU_FMT_FP32;
   if ((q_row != nullptr) != want_qr || (s_row != nullptr) != want_qr) return GLU_EINVAL;
   if ((q_col != nullptr) != want_qc || (s_col != nullptr) != want_qc) return GLU_EINVAL;
   if ((out != nullptr) != want_out) return GLU_EINVAL;
   // geometry
-  if (fmt == GLU_FMT_MXFP8_E4M3) {
+  if (mx) {
     if (N % 32 != 0) return GLU_ESHAPE;
     if ((mode & GLU_MODE_COL) && M % 32 != 0) return GLU_ESHAPE;
   }
@@ -92,6 +93,16 @@ void sizes_for(int32_t fmt, int32_t mode, int64_t M, int64_t W, size_t s[4]) {
     if (mode & GLU_MODE_COL) {
       s[2] = size_t(W) * size_t(M);
       s[3] = size_t(W) * size_t(M / 32);
+    }
+  } else if (fmt == GLU_FMT_MXFP8_E4M3_128X4) {
+    // scale matrices [M, W/32] and [W, M/32] in the 128x4 layout (padded)
+    if (mode & GLU_MODE_ROW) {
+      s[0] = size_t(M) * size_t(W);
+      s[1] = size_t((M + 127) / 128 * 128) * size_t((W / 32 + 3) / 4 * 4);
+    }
+    if (mode & GLU_MODE_COL) {
+      s[2] = size_t(W) * size_t(M);
+      s[3] = size_t((W + 127) / 128 * 128) * size_t((M / 32 + 3) / 4 * 4);
     }
   } else if (fmt == GLU_FMT_NVFP4_E2M1) {
     s[0] = size_t(M) * size_t(W / 2);
@@ -148,7 +159,8 @@ extern "C" int glu_quant_fwd(const glu_quant_fwd_args* a, void* stream) {
   if (st != GLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (a->fmt) {
-    case GLU_FMT_MXFP8_E4M3: return launched(gq::launch_fwd_mx(*a, s, d));
+    case GLU_FMT_MXFP8_E4M3:
+    case GLU_FMT_MXFP8_E4M3_128X4: return launched(gq::launch_fwd_mx(*a, s, d));
     case GLU_FMT_NVFP4_E2M1: return launched(gq::launch_fwd_nvfp4(*a, s, d));
     default: return launched(gq::launch_fwd_plain(*a, s, d));
   }
@@ -161,7 +173,8 @@ extern "C" int glu_quant_bwd(const glu_quant_bwd_args* a, void* stream) {
   st = device_info(&d);
   if (st != GLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a->fmt == GLU_FMT_MXFP8_E4M3) return launched(gq::launch_bwd_mx(*a, s, d));
+  if (a->fmt == GLU_FMT_MXFP8_E4M3 || a->fmt == GLU_FMT_MXFP8_E4M3_128X4)
+    return launched(gq::launch_bwd_mx(*a, s, d));
   return launched(gq::launch_bwd_plain(*a, s, d));
 }
 
@@ -174,7 +187,7 @@ extern "C" int glu_quant_fwd_sizes(const glu_quant_fwd_args* a, size_t sizes[4])
   void* phw = reinterpret_cast<void*>(uintptr_t(256));
   c.gate = ph;
   c.up = (c.layout == GLU_LAYOUT_SPLIT) ? ph : nullptr;
-  const bool mx = c.fmt == GLU_FMT_MXFP8_E4M3;
+  const bool mx = c.fmt == GLU_FMT_MXFP8_E4M3 || c.fmt == GLU_FMT_MXFP8_E4M3_128X4;
   c.q_row = c.s_row = (c.fmt == GLU_FMT_NVFP4_E2M1 || (mx && (c.mode & GLU_MODE_ROW))) ? phw : nullptr;
   c.q_col = c.s_col = (mx && (c.mode & GLU_MODE_COL)) ? phw : nullptr;
   c.out = (c.fmt == GLU_FMT_BF16 || c.fmt == GLU_FMT_FP32) ? phw : nullptr;
@@ -192,7 +205,7 @@ extern "C" int glu_quant_bwd_sizes(const glu_quant_bwd_args* a, size_t sizes[4])
   c.gate = ph;
   c.dy = ph;
   c.up = (c.layout == GLU_LAYOUT_SPLIT) ? ph : nullptr;
-  const bool mx = c.fmt == GLU_FMT_MXFP8_E4M3;
+  const bool mx = c.fmt == GLU_FMT_MXFP8_E4M3 || c.fmt == GLU_FMT_MXFP8_E4M3_128X4;
   c.q_row = c.s_row = (mx && (c.mode & GLU_MODE_ROW)) ? phw : nullptr;
   c.q_col = c.s_col = (mx && (c.mode & GLU_MODE_COL)) ? phw : nullptr;
   c.out = (c.fmt == GLU_FMT_BF16 || c.fmt == GLU_FMT_FP32) ? phw : nullptr;

@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
           });
       put_box(Q + (MODE == GLU_MODE_BOTH ? j : o) * kQBytes, lane, q);
       if (colj)
-        st_byte(p.s_col + (o * p.N + c0 + lane) * (p.M / 32) + row0 / 32, sc);
+        st_byte(p.s_col + p.sl_col.at(o * p.N + c0 + lane, row0 / 32), sc);
       else
-        st_byte(p.s_row + (row0 + lane) * (W / 32) + (o * p.N + c0) / 32, sc);
+        st_byte(p.s_row + p.sl_row.at(row0 + lane, (o * p.N + c0) / 32), sc);
     }
     fence_proxy_async();
     __syncwarp();

@@ -37,6 +37,7 @@ struct BwdP {
   int64_t M, N;
   uint8_t* s_row;
   uint8_t* s_col;
+  ScaleLayout sl_row, sl_col;  // scale matrices [M, 2N/32] and [2N, M/32]
   int64_t n_rt, n_ct;
 };
 

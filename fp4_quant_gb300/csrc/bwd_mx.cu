@@ -67,6 +67,8 @@ cudaError_t make_params(BwdP& p, const glu_quant_bwd_args& a) {
   p.N = a.N;
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.s_col = static_cast<uint8_t*>(a.s_col);
+  p.sl_row = scale_layout(2 * a.N / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
+  p.sl_col = scale_layout(a.M / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
   return cudaSuccess;
@@ -256,11 +258,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
       put_box(Q, lane, qg);
       put_box(Q + kQBytes, lane, qu);
       if (kCol) {
-        st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sg);
-        st_byte(p.s_col + (p.N + c0 + lane) * (p.M / 32) + row0 / 32, su);
+        st_byte(p.s_col + p.sl_col.at(c0 + lane, row0 / 32), sg);
+        st_byte(p.s_col + p.sl_col.at(p.N + c0 + lane, row0 / 32), su);
       } else if (row0 + lane < p.M) {
-        st_byte(p.s_row + (row0 + lane) * (W / 32) + c0 / 32, sg);
-        st_byte(p.s_row + (row0 + lane) * (W / 32) + (p.N + c0) / 32, su);
+        st_byte(p.s_row + p.sl_row.at(row0 + lane, c0 / 32), sg);
+        st_byte(p.s_row + p.sl_row.at(row0 + lane, (p.N + c0) / 32), su);
       }
       fence_proxy_async();
       __syncwarp();
@@ -351,11 +353,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
         *reinterpret_cast<uint4*>(T + kQBytes + swz32(L, hf)) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
         if (hf == 0) {
           if (kCol) {
-            st_byte(p.s_col + (c0 + L) * (p.M / 32) + row0 / 32, sg);
-            st_byte(p.s_col + (p.N + c0 + L) * (p.M / 32) + row0 / 32, su);
+            st_byte(p.s_col + p.sl_col.at(c0 + L, row0 / 32), sg);
+            st_byte(p.s_col + p.sl_col.at(p.N + c0 + L, row0 / 32), su);
           } else if (row0 + L < p.M) {
-            st_byte(p.s_row + (row0 + L) * (W / 32) + c0 / 32, sg);
-            st_byte(p.s_row + (row0 + L) * (W / 32) + (p.N + c0) / 32, su);
+            st_byte(p.s_row + p.sl_row.at(row0 + L, c0 / 32), sg);
+            st_byte(p.s_row + p.sl_row.at(row0 + L, (p.N + c0) / 32), su);
           }
         }
       }
@@ -423,8 +425,16 @@ cudaError_t by_mode(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& 
 }  // namespace
 
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
-  if (a.mode == GLU_MODE_BOTH) return launch_bwd_cb(a, s, d);
-  return a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+  cudaError_t e = a.mode == GLU_MODE_BOTH ? launch_bwd_cb(a, s, d)
+                  : a.act == GLU_ACT_SILU  ? by_mode<0>(a, s, d)
+                                           : by_mode<1>(a, s, d);
+  if (e == cudaSuccess && a.fmt == GLU_FMT_MXFP8_E4M3_128X4) {
+    // the padding of the 128x4 scale layouts (no tile writes it)
+    if (a.mode & GLU_MODE_ROW) e = launch_scale_pad(static_cast<uint8_t*>(a.s_row), a.M, 2 * a.N / 32, s);
+    if (e == cudaSuccess && (a.mode & GLU_MODE_COL))
+      e = launch_scale_pad(static_cast<uint8_t*>(a.s_col), 2 * a.N, a.M / 32, s);
+  }
+  return e;
 }
 
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear) {

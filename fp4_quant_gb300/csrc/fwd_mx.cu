@@ -130,6 +130,7 @@ struct FwdP {
   // chunks (N % 32 != 0), else through the code boxes
   int64_t sc_tiles;
   int32_t nv_direct;
+  ScaleLayout sl_row, sl_col;  // MXFP8 scale matrices [M, N/32] and [N, M/32]
 };
 
 // NVFP4 scale bytes of row (32 rt + lane), scale columns c0/16 and c0/16 + 1
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         uint32_t q[8];
         const uint32_t sc = quant_block<ACT, MODE, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
         put_qc(Qc, lane, j, q);
-        st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+        st_byte(p.s_col + p.sl_col.at(c0 + lane, row0 / 32), sc);
       }
       if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
       continue;
@@ -588,7 +589,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         tma_store_2d(&p.tm_qr, int32_t(c0), int32_t(row0), Qr);  // rows >= M are clipped
         bulk_commit();
       }
-      if (row_ok) st_byte(p.s_row + (row0 + lane) * (p.N / 32) + c0 / 32, sc);
+      if (row_ok) st_byte(p.s_row + p.sl_row.at(row0 + lane, c0 / 32), sc);
     }
 
     // ---- colwise 32x1 (both): lane l takes column l of the staged values
@@ -618,7 +619,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
       // (the wait before the row box above covered the previous unit's store)
       put_qc(Qc, lane, j, q);
-      st_byte(p.s_col + (c0 + lane) * (p.M / 32) + row0 / 32, sc);
+      st_byte(p.s_col + p.sl_col.at(c0 + lane, row0 / 32), sc);
       if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
     }
   }
@@ -665,6 +666,8 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.q_col = static_cast<uint8_t*>(a.q_col);
   p.s_col = static_cast<uint8_t*>(a.s_col);
+  p.sl_row = scale_layout(a.N / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
+  p.sl_col = scale_layout(a.M / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + tc_for(MODE) - 1) / tc_for(MODE);
   // NVFP4 walks the row tiles of whole 128-row scale bands (the tiles past
@@ -700,7 +703,14 @@ cudaError_t by_mode(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& 
 }  // namespace
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
-  return a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+  cudaError_t e = a.act == GLU_ACT_SILU ? by_mode<0>(a, s, d) : by_mode<1>(a, s, d);
+  if (e == cudaSuccess && a.fmt == GLU_FMT_MXFP8_E4M3_128X4) {
+    // the padding of the 128x4 scale layouts (no tile writes it)
+    if (a.mode & GLU_MODE_ROW) e = launch_scale_pad(static_cast<uint8_t*>(a.s_row), a.M, a.N / 32, s);
+    if (e == cudaSuccess && (a.mode & GLU_MODE_COL))
+      e = launch_scale_pad(static_cast<uint8_t*>(a.s_col), a.N, a.M / 32, s);
+  }
+  return e;
 }
 
 cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {

@@ -82,6 +82,24 @@ __device__ __forceinline__ void group_sync(int id, int nthreads) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ----------------------------------------------------------- scale layout --
+
+// Where a kernel writes the scale S[r][c] of a scale matrix with `cols`
+// columns: row-major, or the 128x4 layout (tiles of 128 rows x 4 columns,
+// row-tile-major, 512 bytes each; S[r][c] at (r % 32) * 16 + ((r % 128) /
+// 32) * 4 + c % 4 inside its tile; cols_p = cols rounded up to 4).
+struct ScaleLayout {
+  int64_t cols, cols_p;
+  int32_t swz;
+  __device__ __forceinline__ int64_t at(int64_t r, int64_t c) const {
+    return swz ? ((r >> 7) * (cols_p >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3)
+               : r * cols + c;
+  }
+};
+__host__ __device__ inline ScaleLayout scale_layout(int64_t cols, bool swz) {
+  return ScaleLayout{cols, (cols + 3) / 4 * 4, swz ? 1 : 0};
+}
+
 // ---------------------------------------------------------------- tables --
 
 // Table slot of a bf16 pattern (16 bits): in-range magnitudes map to

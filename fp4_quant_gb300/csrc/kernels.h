@@ -21,6 +21,11 @@ cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const 
 cudaError_t launch_fwd_plain(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_plain(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
 
+// Zero the padding of a scale matrix [rows, cols] stored in the 128x4
+// layout (rows up to a multiple of 128, columns up to a multiple of 4);
+// nothing is launched when there is none (plain.cu).
+cudaError_t launch_scale_pad(uint8_t* s, int64_t rows, int64_t cols, cudaStream_t st);
+
 // 2-D TMA descriptor of a row-major matrix (tmap.cu).
 cudaError_t make_tile_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t cols,
                           int64_t rows, int64_t row_stride_bytes, int box_cols, int box_rows,

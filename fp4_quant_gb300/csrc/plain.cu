@@ -205,7 +205,38 @@ cudaError_t dispatch(const PlainP& p, int act, int fmt, int layout, cudaStream_t
   return bf ? launch_t<1, BWD, 1, uint16_t>(p, s, d) : launch_t<1, BWD, 1, float>(p, s, d);
 }
 
+// Zero the padding of a [rows, cols] scale matrix in the 128x4 layout: the
+// rows from `rows` up to a multiple of 128 (every padded column), then the
+// columns from `cols` up to a multiple of 4 of the real rows.  One thread
+// per padding byte.
+__global__ void scale_pad_kernel(uint8_t* s, int64_t rows, int64_t cols, int64_t rows_p, int64_t cols_p) {
+  const int64_t n_tail = (rows_p - rows) * cols_p, n_side = rows * (cols_p - cols);
+  const ScaleLayout sl = scale_layout(cols, true);
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_tail + n_side;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    int64_t r, c;
+    if (i < n_tail) {
+      r = rows + i / cols_p;
+      c = i % cols_p;
+    } else {
+      const int64_t j = i - n_tail;
+      r = j / (cols_p - cols);
+      c = cols + j % (cols_p - cols);
+    }
+    s[sl.at(r, c)] = 0;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_scale_pad(uint8_t* s, int64_t rows, int64_t cols, cudaStream_t st) {
+  const int64_t rows_p = (rows + 127) / 128 * 128, cols_p = (cols + 3) / 4 * 4;
+  const int64_t n = (rows_p - rows) * cols_p + rows * (cols_p - cols);
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256;
+  scale_pad_kernel<<<unsigned(blocks < 1024 ? blocks : 1024), 256, 0, st>>>(s, rows, cols, rows_p, cols_p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fwd_plain(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   PlainP p = {};

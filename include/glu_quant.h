@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define GLU_QUANT_ABI_VERSION 1
+#define GLU_QUANT_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define GLU_API __attribute__((visibility("default")))
@@ -78,7 +78,10 @@ enum glu_fmt {
   GLU_FMT_MXFP8_E4M3 = 0, /* E4M3 codes + E8M0 scales (row/col/both)      */
   GLU_FMT_NVFP4_E2M1 = 1, /* packed E2M1 + E4M3 scales, 128x4 (row only)  */
   GLU_FMT_BF16 = 2,       /* unquantised bf16 output (row only)          */
-  GLU_FMT_FP32 = 3        /* unquantised fp32 output (row only)          */
+  GLU_FMT_FP32 = 3,       /* unquantised fp32 output (row only)          */
+  GLU_FMT_MXFP8_E4M3_128X4 = 4 /* MXFP8 codes as GLU_FMT_MXFP8_E4M3, the
+                                  scale matrices in the 128x4 layout that a
+                                  block-scaled GEMM reads directly (ABI 2) */
 };
 enum glu_mode { GLU_MODE_ROW = 1, GLU_MODE_COL = 2, GLU_MODE_BOTH = 3 };
 enum glu_layout {
@@ -97,10 +100,20 @@ enum glu_layout {
  *   MXFP8, mode & ROW:  q_row [M, N] codes, s_row [M, N/32] scales
  *   MXFP8, mode & COL:  q_col [N, M] codes (column j's rows are contiguous),
  *                       s_col [N, M/32] scales
+ *   MXFP8_128X4:        the same codes; each scale matrix S [R, C] (rowwise
+ *                       R = M, C = N/32; colwise R = N, C = M/32) stored in
+ *                       the 128x4 layout below, ceil(R/128)*128 *
+ *                       ceil(C/4)*4 bytes, padding = 0
  *   NVFP4 (ROW):        q_row [M, N/2] packed codes (element 2i in the low
- *                       nibble), s_row the 128x4-layout E4M3 scales,
- *                       ceil(M/128)*128 * ceil(N/64)*4 bytes; padding = 0
+ *                       nibble), s_row the 128x4-layout E4M3 scales of the
+ *                       [M, N/16] scale matrix, ceil(M/128)*128 *
+ *                       ceil(N/64)*4 bytes; padding = 0
  *   BF16 / FP32 (ROW):  out [M, N] bf16 / fp32
+ * The 128x4 layout ("feat(phyai-kernel): add Thor NVFP4 GeGLU kernel for
+ * pi0.5", Supported contract, names it): S padded to Rp = ceil(R/128)*128
+ * rows and Cp = ceil(C/4)*4 columns, cut into 128 x 4 tiles stored
+ * row-tile-major (512 bytes each); S[r][c] sits at byte
+ *   ((r/128) * (Cp/4) + c/4) * 512 + (r%32) * 16 + ((r%128)/32) * 4 + c%4.
  * Alignment: every pointer 16-byte aligned; ld_in a multiple of 8.
  */
 typedef struct glu_quant_fwd_args {
@@ -124,6 +137,7 @@ typedef struct glu_quant_fwd_args {
  * 8).  The output is the logical matrix [dGate | dUp] of shape [M, 2N]:
  *   MXFP8 ROW: q_row [M, 2N], s_row [M, 2N/32]
  *   MXFP8 COL: q_col [2N, M], s_col [2N, M/32]
+ *   MXFP8_128X4: the same codes, the scale matrices in the 128x4 layout
  *   BF16/FP32: out [M, 2N]
  * NVFP4 backward is not provided (GLU_EINVAL).
  */

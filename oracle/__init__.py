@@ -22,7 +22,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 
 SILU, GELU_TANH = 0, 1
-MXFP8, NVFP4, BF16, FP32 = 0, 1, 2, 3
+MXFP8, NVFP4, BF16, FP32, MXFP8_128X4 = 0, 1, 2, 3, 4
 ROW, COL, BOTH = 1, 2, 3
 SPLIT, INTERLEAVED = 0, 1
 
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             l.orc_e8m0_decode.restype = ctypes.c_float
             l.orc_swizzle_offset.argtypes = [i64, i64, i64]
             l.orc_swizzle_offset.restype = i64
+            l.orc_scales_128x4.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p]
+            l.orc_scales_128x4.restype = None
             l.orc_glu_fwd.argtypes = [ctypes.POINTER(FwdArgs), ctypes.c_int]
             l.orc_glu_fwd.restype = ctypes.c_int
             l.orc_glu_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.c_int]
@@ -192,6 +194,24 @@ def swizzle_offset(r: int, c: int, scale_cols_padded: int) -> int:
     return lib().orc_swizzle_offset(r, c, scale_cols_padded)
 
 
+def scales_128x4(S: np.ndarray) -> np.ndarray:
+    """A row-major scale matrix [R, C] in the padded 128x4 layout (flat)."""
+    S = np.ascontiguousarray(S, dtype=np.uint8)
+    R, C = S.shape
+    out = np.empty((-(-R // 128) * 128) * (-(-C // 4) * 4), np.uint8)
+    lib().orc_scales_128x4(_ptr(S), R, C, _ptr(out))
+    return out
+
+
+def _mx_128x4(res: dict) -> dict:
+    """MXFP8_128X4 results from plain MXFP8 ones: the same codes, the scale
+    matrices re-laid in the 128x4 layout."""
+    for k in ("s_row", "s_col"):
+        if res.get(k) is not None:
+            res[k] = scales_128x4(res[k])
+    return res
+
+
 # ---- the path ---------------------------------------------------------------
 
 def _bits(x: np.ndarray) -> np.ndarray:
@@ -221,6 +241,9 @@ def glu_fwd(gate, up=None, *, act: int, fmt: int, mode: int = ROW,
             nthreads: int | None = None) -> dict:
     """Run the oracle forward.  ``gate`` is [M, ld] bf16 bits; for the
     interleaved layout ``gate`` is X [M, >=2N] and ``up`` is None."""
+    if fmt == MXFP8_128X4:
+        return _mx_128x4(glu_fwd(gate, up, act=act, fmt=MXFP8, mode=mode, layout=layout, N=N,
+                                 want_h=want_h, nthreads=nthreads))
     g = np.ascontiguousarray(_bits(gate))
     u = None if up is None else np.ascontiguousarray(_bits(up))
     M, ld = g.shape
@@ -255,6 +278,9 @@ def glu_bwd(gate, up, dy, *, act: int, fmt: int, mode: int = ROW,
             layout: int = SPLIT, N: int | None = None, want_h: bool = False,
             nthreads: int | None = None) -> dict:
     """Run the oracle backward: logical output [M, 2N] = [dGate | dUp]."""
+    if fmt == MXFP8_128X4:
+        return _mx_128x4(glu_bwd(gate, up, dy, act=act, fmt=MXFP8, mode=mode, layout=layout, N=N,
+                                 want_h=want_h, nthreads=nthreads))
     g = np.ascontiguousarray(_bits(gate))
     u = None if up is None else np.ascontiguousarray(_bits(up))
     d = np.ascontiguousarray(_bits(dy))

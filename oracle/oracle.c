@@ -204,6 +204,17 @@ int64_t orc_swizzle_offset(int64_t r, int64_t c, int64_t scale_cols_padded) {
   return tile * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4);
 }
 
+/* The scale matrix S [rows, cols] (row-major) re-laid in the 128x4 layout
+ * above: padded to ceil(rows/128)*128 rows and ceil(cols/4)*4 columns,
+ * padding bytes 0.  This is the MXFP8 scale output of the 128x4 format; the
+ * codes are those of plain MXFP8. */
+void orc_scales_128x4(const uint8_t* S, int64_t rows, int64_t cols, uint8_t* out) {
+  int64_t rp = (rows + 127) / 128 * 128, cp = (cols + 3) / 4 * 4;
+  for (int64_t r = 0; r < rp; ++r)
+    for (int64_t c = 0; c < cp; ++c)
+      out[orc_swizzle_offset(r, c, cp)] = (r < rows && c < cols) ? S[r * cols + c] : 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Boundary distance (the code-window rule)                                 */
 /* ------------------------------------------------------------------------ */

@@ -53,6 +53,8 @@ uint8_t orc_e8m0_rceil(float amax);
 float orc_e8m0_decode(uint8_t s);
 uint8_t orc_nvfp4_scale(float amax);
 int64_t orc_swizzle_offset(int64_t r, int64_t c, int64_t scale_cols_padded);
+/* S [rows, cols] row-major -> the padded 128x4 layout (padding 0). */
+void orc_scales_128x4(const uint8_t* S, int64_t rows, int64_t cols, uint8_t* out);
 
 /* Distance, in fp32 ulps, from |v| to the nearest code rounding boundary of
  * the given format (ORC_MXFP8 -> E4M3 midpoints, ORC_NVFP4 -> E2M1

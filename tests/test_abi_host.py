@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert G.glu_quant_abi_version() == 1
+    assert G.glu_quant_abi_version() == 2
     for st in (0, -1, -2, -3, -4, -5):
         assert G.glu_quant_status_str(st) != "unknown status"
     assert G.glu_quant_status_str(7) == "unknown status"
@@ -62,7 +62,7 @@ def _no_gpu():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(act=2), G.GLU_EINVAL),
-    (dict(fmt=4), G.GLU_EINVAL),
+    (dict(fmt=5), G.GLU_EINVAL),
     (dict(mode=0), G.GLU_EINVAL),
     (dict(mode=4), G.GLU_EINVAL),
     (dict(layout=2), G.GLU_EINVAL),
@@ -119,3 +119,10 @@ def test_sizes():
     assert st == 0 and s == (8 * 1001 * 2, 0, 0, 0)
     st, _ = G.glu_quant_fwd_sizes(fwd_args(N=250, ld_in=256))
     assert st == G.GLU_ESHAPE
+    # MXFP8 with 128x4 scales: [R, C] padded to ceil(R/128)*128 x ceil(C/4)*4
+    st, s = G.glu_quant_fwd_sizes(fwd_args(fmt=4, mode=3, q_col=P, s_col=P, M=160, N=800, ld_in=800))
+    assert st == 0 and s == (160 * 800, 256 * 28, 800 * 160, 896 * 8)
+    st, s = G.glu_quant_bwd_sizes(bwd_args(fmt=4, mode=1, M=96, N=416, ld_in=416, ld_dy=416))
+    assert st == 0 and s == (96 * 832, 128 * 28, 0, 0)
+    st, _ = G.glu_quant_fwd_sizes(fwd_args(fmt=5))
+    assert st == G.GLU_EINVAL

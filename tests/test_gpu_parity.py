@@ -103,6 +103,60 @@ def test_mx_bwd_small(act, mode, layout):
     check(gpu, ref, G.FMT_MXFP8, mode, M, 2 * N, "bwd")
 
 
+def _relaid_to_plain(flat, R, C):
+    """128x4 layout -> plain [R, C] scale matrix (padding dropped)."""
+    cp = -(-C // 4) * 4
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * (cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    return flat[off]
+
+
+def check_mx_128x4(gpu, ref_plain, mode, M, W, what):
+    """MXFP8 with 128x4 scales: the whole padded scale buffers equal the
+    oracle's plain scales re-laid (padding zero), and the codes and scales
+    pass the MXFP8 rules against the plain oracle."""
+    st = Stats()
+    plain = dict(gpu)
+    if mode & G.MODE_ROW:
+        assert np.array_equal(gpu["s_row"], O.scales_128x4(ref_plain["s_row"])), what + ".row scales"
+        plain["s_row"] = _relaid_to_plain(gpu["s_row"], M, W // 32)
+    if mode & G.MODE_COL:
+        assert np.array_equal(gpu["s_col"], O.scales_128x4(ref_plain["s_col"])), what + ".col scales"
+        plain["s_col"] = _relaid_to_plain(gpu["s_col"], W, M // 32)
+    check_mx(plain, ref_plain, mode, st, what)
+    return st
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_mx_128x4_scales(act, mode, direction):
+    """MXFP8 with scales in the 128x4 layout: padded rows (M, 2N not
+    multiples of 128) and padded scale columns (N/32, M/32 not multiples
+    of 4); the scale buffers are filled with garbage first so that the
+    padding must be written."""
+    M, N = (160, 800) if direction == "fwd" else (96, 416)
+    W = N if direction == "fwd" else 2 * N
+    g, u, d = _randn(M, N, 41, 2.0), _randn(M, N, 42), _randn(M, N, 43)
+    sizes = {"s_row": (-(-M // 128) * 128) * (-(-(W // 32) // 4) * 4),
+             "s_col": (-(-W // 128) * 128) * (-(-(M // 32) // 4) * 4)}
+    out = {"q_row": torch.empty((M, W), dtype=torch.uint8, device=DEV) if mode & G.MODE_ROW else None,
+           "s_row": torch.full((sizes["s_row"],), 0xA5, dtype=torch.uint8, device=DEV) if mode & G.MODE_ROW else None,
+           "q_col": torch.empty((W, M), dtype=torch.uint8, device=DEV) if mode & G.MODE_COL else None,
+           "s_col": torch.full((sizes["s_col"],), 0xA5, dtype=torch.uint8, device=DEV) if mode & G.MODE_COL else None,
+           "out": None}
+    if direction == "fwd":
+        G.fwd(g, u, act=act[0], fmt=G.FMT_MXFP8_128X4, mode=mode, out=out)
+        ref = O.glu_fwd(host_bits(g), host_bits(u), act=act[1], fmt=O.MXFP8, mode=mode, want_h=True)
+    else:
+        G.bwd(g, u, d, act=act[0], fmt=G.FMT_MXFP8_128X4, mode=mode, out=out)
+        ref = O.glu_bwd(host_bits(g), host_bits(u), host_bits(d), act=act[1], fmt=O.MXFP8, mode=mode,
+                        want_h=True)
+    torch.cuda.synchronize()
+    check_mx_128x4({k: host(v) for k, v in out.items()}, ref, mode, M, W, direction)
+
+
 @pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 @pytest.mark.parametrize("shape", [(200, 1296), (128, 64), (1, 16)], ids=["ragged", "one_tile", "tiny"])

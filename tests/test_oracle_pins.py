@@ -486,3 +486,45 @@ def test_oracle_rejects_unsupported_arguments():
         O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.COL)     # M % 32
     with pytest.raises(ValueError):
         O.glu_fwd(g, u, act=O.SILU, fmt=O.NVFP4, mode=O.BOTH)
+
+
+def test_scales_128x4_layout():
+    """The MXFP8 128x4 scale output: S [R, C] re-laid with zero padding.
+    Offsets worked by hand from the layout's definition (128 x 4 tiles,
+    row-tile-major, 512 bytes; (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4
+    inside a tile)."""
+    R, C = 160, 25                      # padded to 256 x 28: 2 x 7 tiles
+    rng = np.random.default_rng(5)
+    S = rng.integers(1, 256, size=(R, C), dtype=np.uint8)
+    out = O.scales_128x4(S)
+    assert out.shape == (256 * 28,)
+    hand = {(0, 0): 0, (1, 0): 16, (31, 0): 496, (32, 0): 4, (96, 0): 12, (0, 1): 1,
+            (0, 3): 3, (0, 4): 512, (0, 24): 6 * 512, (127, 3): 31 * 16 + 12 + 3,
+            (128, 0): 7 * 512, (159, 24): (7 + 6) * 512 + 31 * 16 + 0 * 4 + 0}
+    for (r, c), off in hand.items():
+        assert out[off] == S[r, c], (r, c)
+    # every real scale lands once, every other byte is padding (zero)
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * 7 + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    assert len(np.unique(off)) == R * C
+    assert np.array_equal(out[off], S)
+    mask = np.ones(out.shape, bool)
+    mask[off.ravel()] = False
+    assert not out[mask].any()
+
+
+def test_mxfp8_128x4_is_mxfp8_with_relaid_scales():
+    """The oracle's 128x4 format: codes equal plain MXFP8's, scales equal
+    the plain scale matrices re-laid (rowwise [M, W/32], colwise [W, M/32])."""
+    rng = np.random.default_rng(9)
+    M, N = 96, 160
+    g = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    u = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    a = O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.BOTH)
+    b = O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8_128X4, mode=O.BOTH)
+    assert np.array_equal(a["q_row"], b["q_row"]) and np.array_equal(a["q_col"], b["q_col"])
+    assert b["s_row"].shape == (128 * 8,) and b["s_col"].shape == (256 * 4,)
+    assert np.array_equal(b["s_row"], O.scales_128x4(a["s_row"]))
+    assert np.array_equal(b["s_col"], O.scales_128x4(a["s_col"]))
+
