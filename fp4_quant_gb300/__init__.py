@@ -17,7 +17,7 @@ import ctypes
 import os
 
 __all__ = [
-    "glu_quant_fwd", "glu_quant_bwd", "glu_quant_fwd_sizes", "glu_quant_bwd_sizes",
+    "glu_quant_fwd", "glu_quant_bwd", "glu_quant_fwd_nvfp4_gs", "glu_quant_fwd_sizes", "glu_quant_bwd_sizes",
     "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
     "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(_LIB_PATH)
     lib.glu_quant_fwd.argtypes = [ctypes.POINTER(GluQuantFwdArgs), ctypes.c_void_p]
     lib.glu_quant_fwd.restype = ctypes.c_int
+    lib.glu_quant_fwd_nvfp4_gs.argtypes = [ctypes.POINTER(GluQuantFwdArgs), ctypes.c_void_p, ctypes.c_void_p]
+    lib.glu_quant_fwd_nvfp4_gs.restype = ctypes.c_int
     lib.glu_quant_bwd.argtypes = [ctypes.POINTER(GluQuantBwdArgs), ctypes.c_void_p]
     lib.glu_quant_bwd.restype = ctypes.c_int
     lib.glu_quant_fwd_sizes.argtypes = [ctypes.POINTER(GluQuantFwdArgs), ctypes.POINTER(ctypes.c_size_t)]
@@ -107,6 +109,10 @@ def _lib() -> ctypes.CDLL:
 
 def glu_quant_fwd(args: GluQuantFwdArgs, stream: int | None) -> int:
     return _lib().glu_quant_fwd(ctypes.byref(args), stream)
+
+
+def glu_quant_fwd_nvfp4_gs(args: GluQuantFwdArgs, amax: int | None, stream: int | None) -> int:
+    return _lib().glu_quant_fwd_nvfp4_gs(ctypes.byref(args), amax, stream)
 
 
 def glu_quant_bwd(args: GluQuantBwdArgs, stream: int | None) -> int:
@@ -191,11 +197,13 @@ def _check_input(t, name):
 
 
 def fwd(gate, up=None, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
-        layout=LAYOUT_SPLIT, N=None, out=None, stream=None) -> dict:
+        layout=LAYOUT_SPLIT, N=None, out=None, stream=None, amax=None) -> dict:
     """Forward.  ``gate``/``up``: bf16 [M, N] (split) or ``gate`` = X [M, 2N]
     (interleaved, ``up`` None).  Returns the output dict (q_row, s_row,
-    q_col, s_col, out); disabled outputs are None.  Raises GluQuantError on a
-    nonzero status (nothing was launched then)."""
+    q_col, s_col, out); disabled outputs are None.  ``amax`` (NVFP4 only): a
+    one-element fp32 CUDA tensor holding the tensor amax for the global
+    scale (``glu_quant_fwd_nvfp4_gs``).  Raises GluQuantError on a nonzero
+    status (nothing was launched then)."""
     _check_input(gate, "gate")
     if up is not None:
         _check_input(up, "up")
@@ -208,7 +216,13 @@ def fwd(gate, up=None, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
     a = GluQuantFwdArgs(act, fmt, mode, layout, M, N, gate.stride(0), _ptr(gate), _ptr(up),
                         _ptr(o["q_row"]), _ptr(o["s_row"]), _ptr(o["q_col"]), _ptr(o["s_col"]),
                         _ptr(o["out"]))
-    st = glu_quant_fwd(a, stream if stream is not None else _stream_handle(gate.device))
+    sh = stream if stream is not None else _stream_handle(gate.device)
+    if amax is not None:
+        st = glu_quant_fwd_nvfp4_gs(a, _ptr(amax), sh)
+        if st != GLU_OK:
+            raise GluQuantError(st, "glu_quant_fwd_nvfp4_gs")
+        return o
+    st = glu_quant_fwd(a, sh)
     if st != GLU_OK:
         raise GluQuantError(st, "glu_quant_fwd")
     return o

@@ -161,9 +161,20 @@ extern "C" int glu_quant_fwd(const glu_quant_fwd_args* a, void* stream) {
   switch (a->fmt) {
     case GLU_FMT_MXFP8_E4M3:
     case GLU_FMT_MXFP8_E4M3_128X4: return launched(gq::launch_fwd_mx(*a, s, d));
-    case GLU_FMT_NVFP4_E2M1: return launched(gq::launch_fwd_nvfp4(*a, s, d));
+    case GLU_FMT_NVFP4_E2M1: return launched(gq::launch_fwd_nvfp4(*a, nullptr, s, d));
     default: return launched(gq::launch_fwd_plain(*a, s, d));
   }
+}
+
+extern "C" int glu_quant_fwd_nvfp4_gs(const glu_quant_fwd_args* a, const float* amax, void* stream) {
+  if (a == nullptr || a->fmt != GLU_FMT_NVFP4_E2M1 || amax == nullptr) return GLU_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) != 0) return GLU_EALIGN;
+  int st = check_fwd(a);
+  if (st != GLU_OK) return st;
+  gq::DevInfo d;
+  st = device_info(&d);
+  if (st != GLU_OK) return st;
+  return launched(gq::launch_fwd_nvfp4(*a, amax, static_cast<cudaStream_t>(stream), d));
 }
 
 extern "C" int glu_quant_bwd(const glu_quant_bwd_args* a, void* stream) {

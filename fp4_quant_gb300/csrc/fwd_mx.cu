@@ -130,6 +130,7 @@ struct FwdP {
   // chunks (N % 32 != 0), else through the code boxes
   int64_t sc_tiles;
   int32_t nv_direct;
+  const float* nv_amax;  // NVFP4: the tensor amax for the global scale, or NULL (scale 1)
   ScaleLayout sl_row, sl_col;  // MXFP8 scale matrices [M, N/32] and [N, M/32]
 };
 
@@ -294,6 +295,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
   load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  // NVFP4 global encode scale 2688 / amax (448 * 6 over the tensor amax,
+  // IEEE division); 1 without an amax, or for a zero or non-finite one
+  float nv_gs = 1.0f;
+  if (MODE == kModeNv && p.nv_amax != nullptr) {
+    const float a = __ldg(p.nv_amax);
+    if (a > 0.0f && a < __int_as_float(0x7F800000)) nv_gs = __fdiv_rn(2688.0f, a);
+  }
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -537,11 +545,18 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
     }
 
-    // ---- NVFP4: this lane's 32 values are two 16-output blocks
+    // ---- NVFP4: this lane's 32 values are two 16-output blocks, scaled by
+    // the global encode scale first (one rounding; 1 when none is given)
     if (MODE == kModeNv) {
-      auto ex = [&](int e) { return exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e); };
+      if (nv_gs != 1.0f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) h[i] = __fmul_rn(h[i], nv_gs);
+      }
+      auto ex = [&](int e) { return __fmul_rn(exact_at<ACT, MODE, LAYOUT>(p, hot, row0 + lane, c0 + e), nv_gs); };
       auto ex8 = [&](int e0, float (&x)[8]) {
         exact8_at<ACT, MODE, LAYOUT>(x, p, hot, row0 + lane, 0, c0, 1, e0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], nv_gs);
       };
       uint32_t c[4];
       uint32_t s0 = nv_block<0>(h, c[0], c[1], Bracket<ACT>::kNv, ex, ex8);
@@ -636,7 +651,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
 }
 
 template <int ACT, int MODE, int LAYOUT>
-cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
+cudaError_t launch_t(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s, const DevInfo& d) {
   auto kern = fwd_mx_kernel<ACT, MODE, LAYOUT>;
   const int smem = smem_for(MODE);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -655,6 +670,7 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
   if (e == cudaSuccess && (MODE & GLU_MODE_ROW))
     e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N, a.M, a.N, kWC, kTR, 32);
   p.nv_direct = MODE == kModeNv && a.N % 32 != 0;
+  p.nv_amax = amax;
   if (e == cudaSuccess && MODE == kModeNv && !p.nv_direct)
     e = make_tile_map(&p.tm_qr, a.q_row, 1, a.N / 2, a.M, a.N / 2, 16, kTR, 0);
   if (e == cudaSuccess && (MODE & GLU_MODE_COL))
@@ -686,17 +702,17 @@ cudaError_t launch_t(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo&
 }
 
 template <int ACT, int MODE>
-cudaError_t by_layout(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
-  return a.layout == GLU_LAYOUT_SPLIT ? launch_t<ACT, MODE, GLU_LAYOUT_SPLIT>(a, s, d)
-                                      : launch_t<ACT, MODE, GLU_LAYOUT_INTERLEAVED>(a, s, d);
+cudaError_t by_layout(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s, const DevInfo& d) {
+  return a.layout == GLU_LAYOUT_SPLIT ? launch_t<ACT, MODE, GLU_LAYOUT_SPLIT>(a, amax, s, d)
+                                      : launch_t<ACT, MODE, GLU_LAYOUT_INTERLEAVED>(a, amax, s, d);
 }
 
 template <int ACT>
 cudaError_t by_mode(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   switch (a.mode) {
-    case GLU_MODE_ROW: return by_layout<ACT, GLU_MODE_ROW>(a, s, d);
-    case GLU_MODE_COL: return by_layout<ACT, GLU_MODE_COL>(a, s, d);
-    default: return by_layout<ACT, GLU_MODE_BOTH>(a, s, d);
+    case GLU_MODE_ROW: return by_layout<ACT, GLU_MODE_ROW>(a, nullptr, s, d);
+    case GLU_MODE_COL: return by_layout<ACT, GLU_MODE_COL>(a, nullptr, s, d);
+    default: return by_layout<ACT, GLU_MODE_BOTH>(a, nullptr, s, d);
   }
 }
 
@@ -713,8 +729,9 @@ cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const Dev
   return e;
 }
 
-cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
-  return a.act == GLU_ACT_SILU ? by_layout<0, kModeNv>(a, s, d) : by_layout<1, kModeNv>(a, s, d);
+cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
+                             const DevInfo& d) {
+  return a.act == GLU_ACT_SILU ? by_layout<0, kModeNv>(a, amax, s, d) : by_layout<1, kModeNv>(a, amax, s, d);
 }
 
 cudaError_t read_err_fwd_mx(uint32_t* v, bool clear) {

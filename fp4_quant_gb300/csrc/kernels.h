@@ -17,7 +17,9 @@ struct DevInfo {
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);  // both directions
-cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
+// amax: device pointer to the tensor amax for the global scale, or NULL
+cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
+                             const DevInfo& d);
 cudaError_t launch_fwd_plain(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_plain(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
 

@@ -163,6 +163,22 @@ typedef struct glu_quant_bwd_args {
  * Summary (bf16 GeGLU).  Returns GLU_OK or a negative status. */
 GLU_API int glu_quant_fwd(const glu_quant_fwd_args* args, void* stream);
 
+/* NVFP4 forward with a per-tensor global scale (two-level NVFP4 scaling;
+ * "feat(phyai-kernel): add Thor NVFP4 GeGLU kernel for pi0.5", Supported
+ * contract and Known limits, fixes the global scale at 1; this is the
+ * general case).  `amax` is a DEVICE pointer (4-byte aligned) to the fp32
+ * amax of the tensor being quantised, read on the device, so that it may be
+ * produced by an earlier kernel on the same stream.  The global encode scale
+ * is G = 2688 / amax (448 * 6 / amax, IEEE division; G = 1 when amax is
+ * zero, negative, infinite or NaN); every value is scaled once, v =
+ * RN_fp32(h * G), and v is quantised exactly like GLU_FMT_NVFP4_E2M1 (scale
+ * E4M3(amax_block(v) / 6), codes E2M1(v / scale)).  Dequantisation is
+ * code * scale / G.  args->fmt must be GLU_FMT_NVFP4_E2M1, and the outputs
+ * are the same as glu_quant_fwd's.  Returns GLU_OK, GLU_EINVAL (NULL amax
+ * or another format), GLU_EALIGN (amax not 4-byte aligned) or the statuses
+ * of glu_quant_fwd (ABI 2). */
+GLU_API int glu_quant_fwd_nvfp4_gs(const glu_quant_fwd_args* args, const float* amax, void* stream);
+
 /* Backward: dGate = dY*up*act'(gate), dUp = dY*act(gate), quantised like
  * the forward ("Add swiglu + MXFP8 fused CuTe DSL kernel", API: backward
  * returns concatenated [dGate | dUp]).  Returns GLU_OK or a negative

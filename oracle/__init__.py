@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
             l.orc_swizzle_offset.restype = i64
             l.orc_scales_128x4.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p]
             l.orc_scales_128x4.restype = None
+            l.orc_nvfp4_matrix.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p, ctypes.c_void_p]
+            l.orc_nvfp4_matrix.restype = None
             l.orc_glu_fwd.argtypes = [ctypes.POINTER(FwdArgs), ctypes.c_int]
             l.orc_glu_fwd.restype = ctypes.c_int
             l.orc_glu_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.c_int]
@@ -201,6 +203,29 @@ def scales_128x4(S: np.ndarray) -> np.ndarray:
     out = np.empty((-(-R // 128) * 128) * (-(-C // 4) * 4), np.uint8)
     lib().orc_scales_128x4(_ptr(S), R, C, _ptr(out))
     return out
+
+
+def nvfp4_global_scale(amax: float) -> np.float32:
+    """The global encode scale G = 2688 / amax in fp32 (IEEE division);
+    1 for a zero, negative or non-finite amax."""
+    a = np.float32(amax)
+    if not (np.isfinite(a) and a > 0):
+        return np.float32(1.0)
+    return np.float32(np.float32(2688.0) / a)
+
+
+def glu_fwd_nvfp4_gs(gate, up=None, *, act: int, amax: float, layout: int = SPLIT,
+                     N: int | None = None, nthreads: int | None = None) -> dict:
+    """NVFP4 with a global scale: v = RN_fp32(h * G), h the path's exact fp32
+    values, then the unit-global-scale NVFP4 rule on v.  Returns out (codes),
+    s_nvfp4 (padded 128x4 scales), h and v."""
+    h = glu_fwd(gate, up, act=act, fmt=FP32, layout=layout, N=N, nthreads=nthreads)["out"]
+    v = np.ascontiguousarray((h * nvfp4_global_scale(amax)).astype(np.float32))
+    M, W = v.shape
+    q = np.zeros((M, W // 2), np.uint8)
+    s = np.zeros((-(-M // 128) * 128) * (-(-(W // 16) // 4) * 4), np.uint8)
+    lib().orc_nvfp4_matrix(_ptr(v), M, W, _ptr(q), _ptr(s))
+    return {"out": q, "s_nvfp4": s, "h": h, "v": v}
 
 
 def _mx_128x4(res: dict) -> dict:

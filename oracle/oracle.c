@@ -317,6 +317,8 @@ static uint8_t nvfp4_block(const float* x, uint8_t* c) {
 /* Quantising a computed row chunk                                         */
 /* ------------------------------------------------------------------------ */
 
+enum { CHUNK_ROWS_NV = 128 }; /* NVFP4 chunks own whole 128-row scale tiles */
+
 typedef struct {
   int32_t fmt, mode;
   int64_t M, W;          /* logical output matrix [M, W] */
@@ -374,6 +376,24 @@ static void emit_chunk(const sink_t* k, const float* h, int64_t r0, int64_t nr) 
       for (int64_t j = 0; j < W; ++j)
         mx_block(h + g * W + j, W, k->q_col + j * M + r0 + g, 1,
                  k->s_col + j * (M / 32) + (r0 + g) / 32);
+  }
+}
+
+/* NVFP4 of a given fp32 matrix v [M, W] (W % 16 == 0): codes [M, W/2] and
+ * the padded 128x4 scale buffer, by the same block rule as the path's NVFP4
+ * output.  With a global encode scale G, the path quantises v = RN(h * G)
+ * this way (two-level scaling; G = 1 gives the unit-global-scale output). */
+void orc_nvfp4_matrix(const float* v, int64_t M, int64_t W, uint8_t* q, uint8_t* s) {
+  sink_t k;
+  memset(&k, 0, sizeof k);
+  k.fmt = ORC_NVFP4;
+  k.M = M;
+  k.W = W;
+  k.out = q;
+  k.s_nvfp4 = s;
+  for (int64_t r0 = 0; r0 < M; r0 += CHUNK_ROWS_NV) {
+    int64_t nr = M - r0 < CHUNK_ROWS_NV ? M - r0 : CHUNK_ROWS_NV;
+    emit_chunk(&k, v + r0 * W, r0, nr);
   }
 }
 

@@ -55,6 +55,8 @@ uint8_t orc_nvfp4_scale(float amax);
 int64_t orc_swizzle_offset(int64_t r, int64_t c, int64_t scale_cols_padded);
 /* S [rows, cols] row-major -> the padded 128x4 layout (padding 0). */
 void orc_scales_128x4(const uint8_t* S, int64_t rows, int64_t cols, uint8_t* out);
+/* NVFP4 of a given fp32 matrix v [M, W] (codes [M, W/2], padded 128x4 scales). */
+void orc_nvfp4_matrix(const float* v, int64_t M, int64_t W, uint8_t* q, uint8_t* s);
 
 /* Distance, in fp32 ulps, from |v| to the nearest code rounding boundary of
  * the given format (ORC_MXFP8 -> E4M3 midpoints, ORC_NVFP4 -> E2M1

@@ -25,7 +25,7 @@ def _declared():
 
 def test_every_declared_symbol_is_exported():
     names = _declared()
-    assert len(names) == 7, names
+    assert len(names) == 8, names
     lib = ctypes.CDLL(G.library_path())
     for n in names:
         assert hasattr(lib, n), n
@@ -100,6 +100,14 @@ def test_fwd_rejections(kw, status):
 ])
 def test_bwd_rejections(kw, status):
     assert G.glu_quant_bwd(bwd_args(**kw), None) == status
+
+
+def test_nvfp4_global_scale_rejections():
+    nv = dict(fmt=1, layout=1, up=None, ld_in=512)
+    assert G.glu_quant_fwd_nvfp4_gs(fwd_args(), P, None) == G.GLU_EINVAL        # not NVFP4
+    assert G.glu_quant_fwd_nvfp4_gs(fwd_args(**nv), None, None) == G.GLU_EINVAL  # no amax
+    assert G.glu_quant_fwd_nvfp4_gs(fwd_args(**nv), P + 2, None) == G.GLU_EALIGN
+    assert G.glu_quant_fwd_nvfp4_gs(fwd_args(fmt=1, layout=1, up=None, ld_in=256), P, None) == G.GLU_ESHAPE
 
 
 @pytest.mark.skipif(not _no_gpu(), reason="checks the no-device status")

@@ -231,6 +231,35 @@ def _special_inputs(M, N, seed):
 
 
 @pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+@pytest.mark.parametrize("amax", ["tensor", 100.0, 0.75], ids=["tensor_amax", "amax_100", "amax_small"])
+def test_nvfp4_global_scale(act, layout, amax):
+    """NVFP4 with a global scale (glu_quant_fwd_nvfp4_gs): the amax read from
+    device memory; the tensor's own amax (the spike row makes the other
+    values tiny after scaling), and two smaller ones (saturating codes, and
+    infinite scaled values in the spike row, which take the NaN/Inf block
+    rule)."""
+    M, N = 200, 1296
+    g, u = _randn(M, N, 71, 2.0), _randn(M, N, 72)
+    u[5, :40] = 1.0e37  # spikes: h near 1e37, so v overflows for the smaller amaxes
+    if amax == "tensor":
+        h = O.glu_fwd(host_bits(g), host_bits(u), act=act[1], fmt=O.FP32)["out"]
+        amax = float(np.abs(h).max())
+    amax_t = torch.tensor([amax], dtype=torch.float32, device=DEV)
+    if layout == G.LAYOUT_SPLIT:
+        out = G.fwd(g, u, act=act[0], fmt=G.FMT_NVFP4, amax=amax_t)
+        ref = O.glu_fwd_nvfp4_gs(host_bits(g), host_bits(u), act=act[1], amax=amax)
+    else:
+        x = _interleave(g, u)
+        out = G.fwd(x, None, act=act[0], fmt=G.FMT_NVFP4, layout=layout, amax=amax_t)
+        ref = O.glu_fwd_nvfp4_gs(host_bits(x), act=act[1], amax=amax, layout=O.INTERLEAVED)
+    torch.cuda.synchronize()
+    st = Stats()
+    check_nvfp4({k: host(v) for k, v in out.items()}, {"out": ref["out"], "s_nvfp4": ref["s_nvfp4"], "h": ref["v"]},
+                M, N, st, "nvfp4_gs")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
                          ids=["fp32", "bf16", "mxfp8", "nvfp4"])
 def test_special_values_fwd(act, fmt):

@@ -528,3 +528,50 @@ def test_mxfp8_128x4_is_mxfp8_with_relaid_scales():
     assert np.array_equal(b["s_row"], O.scales_128x4(a["s_row"]))
     assert np.array_equal(b["s_col"], O.scales_128x4(a["s_col"]))
 
+
+def test_nvfp4_global_scale_hand_worked():
+    """Global encode scale G = 2688 / amax, values scaled once, then the
+    unit-global-scale rule.  gate = 32 makes h = 32 * up exactly; with the
+    tensor amax 96 (up = 3), G = 28: v = 2688 and 896 -> block scale
+    E4M3(2688 / 6) = 448 (0x7E), codes 6 (0x7) and 2 (0x4)."""
+    assert O.nvfp4_global_scale(96.0) == np.float32(28.0)
+    assert O.nvfp4_global_scale(0.0) == 1.0 and O.nvfp4_global_scale(float("inf")) == 1.0
+    M, N = 1, 16
+    g = np.full((M, N), 0x4200, np.uint16)            # bf16 32.0
+    u = np.zeros((M, N), np.uint16)
+    u[0, 0] = 0x4040                                  # 3.0 -> h = 96
+    u[0, 1] = 0x3F80                                  # 1.0 -> h = 32
+    r = O.glu_fwd_nvfp4_gs(g, u, act=O.SILU, amax=96.0)
+    assert r["v"][0, 0] == 2688.0 and r["v"][0, 1] == 896.0
+    assert r["s_nvfp4"][0] == 0x7E
+    assert r["out"][0, 0] == 0x7 | (0x4 << 4)          # element 0 low nibble, 1 high
+    assert not r["out"][0, 1:].any()
+
+
+def test_nvfp4_power_of_two_global_scale():
+    """G = 2 (tensor amax 1344) scales every value exactly: blocks whose unit
+    scale is a normal E4M3 below 224 get the scale one binade up (byte + 8)
+    and the same codes (v / (2 s) = h / s); G = 1 (amax 2688) is the
+    unit-global-scale output itself."""
+    rng = np.random.default_rng(3)
+    M, N = 256, 128
+    g = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    u = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    plain = O.glu_fwd(g, u, act=O.GELU_TANH, fmt=O.NVFP4)
+    one = O.glu_fwd_nvfp4_gs(g, u, act=O.GELU_TANH, amax=2688.0)
+    assert np.array_equal(plain["out"], one["out"]) and np.array_equal(plain["s_nvfp4"], one["s_nvfp4"])
+    two = O.glu_fwd_nvfp4_gs(g, u, act=O.GELU_TANH, amax=1344.0)
+    sp, s2 = plain["s_nvfp4"].astype(int), two["s_nvfp4"].astype(int)
+    normal = (sp >= 0x08) & (sp < 0x76)
+    assert normal.sum() > 1000
+    assert np.array_equal(s2[normal], sp[normal] + 8)
+    # codes of those blocks: block (r, c) holds elements 16c .. 16c + 15 of row r
+    C = N // 16
+    cp = -(-C // 4) * 4
+    r = np.arange(M)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * (cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    ok = normal[off]                                   # [M, C] blocks with a normal unit scale
+    qb = lambda q: q.reshape(M, C, 8)
+    assert np.array_equal(qb(two["out"])[ok], qb(plain["out"])[ok])
+
