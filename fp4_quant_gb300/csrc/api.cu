@@ -28,7 +28,8 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow
 int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t M, int64_t N,
                  int64_t ld_in, const void* gate, const void* up, const void* q_row,
                  const void* s_row, const void* q_col, const void* s_col, const void* out) {
-  if (act != GLU_ACT_SILU && act != GLU_ACT_GELU_TANH) return GLU_EINVAL;
+  const int32_t act_kind = act & ~GLU_ACT_BF16_STEPS;
+  if (act_kind != GLU_ACT_SILU && act_kind != GLU_ACT_GELU_TANH) return GLU_EINVAL;
   if (fmt < GLU_FMT_MXFP8_E4M3 || fmt > GLU_FMT_MXFP8_E4M3_128X4) return GLU_EINVAL;
   if (mode < GLU_MODE_ROW || mode > GLU_MODE_BOTH) return GLU_EINVAL;
   if (layout != GLU_LAYOUT_SPLIT && layout != GLU_LAYOUT_INTERLEAVED) return GLU_EINVAL;
@@ -71,6 +72,7 @@ int check_fwd(const glu_quant_fwd_args* a) {
 int check_bwd(const glu_quant_bwd_args* a) {
   if (a == nullptr) return GLU_EINVAL;
   if (a->fmt == GLU_FMT_NVFP4_E2M1) return GLU_EINVAL;
+  if (a->act & GLU_ACT_BF16_STEPS) return GLU_EINVAL;  // the bf16-step values are forward only
   int st = check_common(a->act, a->fmt, a->mode, a->layout, a->M, a->N, a->ld_in, a->gate,
                         a->up, a->q_row, a->s_row, a->q_col, a->s_col, a->out);
   if (st != GLU_OK) return st;

@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
   uint8_t* const V = Vbase + warp * kVBytes;
   uint8_t* const T = Tbase + warp * kTBytes;
   const int64_t n_g = my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0;
-  const int64_t W = 2 * p.N;
   uint32_t nst = 0;  // bulk groups this warp has committed (colwise: selects the half)
 
   if (w == 0) {

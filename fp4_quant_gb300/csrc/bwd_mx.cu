@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
   uint8_t* const T = Tbase + warp * kTBytes;
   const int64_t n_g = my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0;
-  const int64_t W = 2 * p.N;
   uint32_t nst = 0;  // bulk groups this warp has committed (selects the box pair)
 
   if (w == 0) {

@@ -177,6 +177,51 @@ __device__ __forceinline__ float exact_grad_mul(float g, float dy, float u) {
   return tab_cold(h) ? slow_grad_mul(ACT, g, dy, u) : h;
 }
 
+// ------------------------------------------------------ bf16-step values --
+// With the bf16-steps flag (act | 16, forward only) the path takes the
+// values an eager bf16 evaluation of act(gate) * up gives: a = RN_bf16(act(g))
+// and h = RN_bf16(a * u) ("Add swiglu + MXFP8 fused CuTe DSL kernel",
+// Numerics and tests: forward data bitwise identical to the eager activation
+// followed by the quantiser).  a * u is exact in fp32 (two 8-bit
+// significands; where it would fall below fp32's subnormal resolution it
+// rounds to a bf16 zero either way).
+
+// Round an fp32 value to bf16 (nearest, ties to even), returned as fp32.
+__device__ __forceinline__ float bf16_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return __uint_as_float(uint32_t(r) << 16);
+}
+
+// Round a double to bf16 with one rounding: truncate to fp32, make the
+// result odd when bits were dropped (round to odd keeps every bit a later
+// rounding needs: fp32 has 16 more than bf16), then round to nearest even.
+__device__ __forceinline__ float bf16_from_double(double x) {
+  const float t = __double2float_rz(x);
+  uint32_t b = __float_as_uint(t);
+  if ((double)t != x && !isnan(x)) b |= 1u;
+  return bf16_rn(__uint_as_float(b));
+}
+
+// RN_bf16 of act(g) from a table pair: hi is act(g) rounded toward zero
+// and lo the remainder (|lo| < one ulp of hi, of hi's sign), so act(g)
+// rounds like hi, except when hi sits exactly on a bf16 midpoint and lo is
+// not zero: act(g) is then past the midpoint, away from zero.
+__device__ __forceinline__ float bf16_of_pair(float hi, float lo) {
+  const uint32_t b = __float_as_uint(hi);
+  if ((b & 0xFFFFu) == 0x8000u && lo != 0.0f) return __uint_as_float((b & 0xFFFF0000u) + 0x10000u);
+  return bf16_rn(hi);
+}
+
+// Exact RN_bf16(act(g)) from a forward table entry (a NaN entry: the gate
+// is outside the table or act(g) too small for it; the fp64 form decides).
+template <int ACT>
+__device__ __forceinline__ float act_bf16_of_entry(float2 e, float g) {
+  if (isnan(e.x) && !isnan(g)) return bf16_from_double(act_f64(ACT, (double)g));
+  if (isnan(g)) return g;
+  return bf16_of_pair(e.x, e.y);
+}
+
 // Hot slice of a table kept in shared memory: bf16 exponent fields
 // LO .. LO + BIN - 1, positive gates then negative gates.  It serves the
 // exact path of the kernels, whose undecided blocks are rare but otherwise
@@ -222,6 +267,18 @@ __device__ __forceinline__ float exact_act_mul_hot(const float2* hot, float g, f
   if (k < 0) return exact_act_mul<ACT>(g, u);
   const float h = tab_mul(hot[k], u);
   return tab_cold(h) ? slow_act_mul(ACT, g, u) : h;
+}
+
+// Exact forward value of one element for ACT = activation | 16 * bf16-steps
+// flag: act(g) * u rounded once to fp32, or RN_bf16(RN_bf16(act(g)) * u).
+template <int ACT, uint32_t LO = kHotExpLo, uint32_t BIN = kHotBinades>
+__device__ __forceinline__ float exact_h(const float2* hot, float g, float u) {
+  constexpr int A = ACT & 1;
+  if (!(ACT & 16)) return exact_act_mul_hot<A, LO, BIN>(hot, g, u);
+  const int k = hot_index<LO, BIN>(__float_as_uint(g) >> 16);
+  const float2* tab = reinterpret_cast<const float2*>(A == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  const float2 e = k >= 0 ? hot[k] : __ldg(tab + tab_index(__float_as_uint(g) >> 16));
+  return bf16_rn(__fmul_rn(act_bf16_of_entry<A>(e, g), u));
 }
 
 // ---------------------------------------------------- packed fp32 pairs --
@@ -303,6 +360,24 @@ __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
   }
   const float2 d = add2(E, splat2(1.0f));
   return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// bf16-steps values of a pair from the fast form: act(g) (fast_h2 with u = 1)
+// is rounded to bf16 at both ends of the rounding-test bracket (the ACT
+// half-width); `bad` is set when they differ (the caller then takes exact
+// values), else h = RN_bf16(a * u) is exact.
+template <int ACT>
+__device__ __forceinline__ float2 fast_h2_bf16(float2 g, float2 u, float d, bool& bad) {
+  const float2 a = fast_h2<ACT>(g, splat2(1.0f));
+  const float2 lo = mul2(a, splat2(1.0f - d)), hi = mul2(a, splat2(1.0f + d));
+  uint32_t bl, bh;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(bl) : "f"(lo.y), "f"(lo.x));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(bh) : "f"(hi.y), "f"(hi.x));
+  bad = bl != bh;
+  const float2 h = mul2(make_float2(__uint_as_float(bl << 16), __uint_as_float(bl & 0xFFFF0000u)), u);
+  uint32_t hb;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb) : "f"(h.y), "f"(h.x));
+  return make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
 }
 
 // Largest raw bf16 pattern of the gates (two per word, unsigned per half):

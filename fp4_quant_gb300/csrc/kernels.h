@@ -34,7 +34,12 @@ cudaError_t make_tile_map(CUtensorMap* map, const void* base, int elem_bytes, in
                           int swizzle_bytes = 0);
 
 // Error bits recorded by a kernel family (bounded waits that gave up).
-cudaError_t read_err_fwd_mx(uint32_t* v, bool clear);
+cudaError_t read_err_fwd_mx(uint32_t* v, bool clear);  // (includes the bf16-step kernels' bits)
+// The forward kernels for the bf16-step values (fwd_mx_b16.cu).
+cudaError_t launch_fwd_mx_b16(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
+cudaError_t launch_fwd_nvfp4_b16(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
+                                 const DevInfo& d);
+cudaError_t read_err_fwd_b16(uint32_t* v, bool clear);
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);  // (includes the both-directions kernel's bits)
 cudaError_t read_err_bwd_cb(uint32_t* v, bool clear);
 

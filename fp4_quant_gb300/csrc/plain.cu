@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
   constexpr int kEntry = BWD ? 16 : 8;
   {
     const uint4* src = reinterpret_cast<const uint4*>(
-        BWD ? (ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1) : (ACT == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1));
+        BWD ? ((ACT & 1) == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1) : ((ACT & 1) == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1));
     uint4* dst = reinterpret_cast<uint4*>(smem);
     for (int i = threadIdx.x; i < int(kTabEntries) * kEntry / 16; i += blockDim.x) dst[i] = src[i];
   }
@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
           b[k] = tab_mul(make_float2(e.x, e.y), dv);
           a[k] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
           cold |= is_cold(a[k]) | is_cold(b[k]);
+        } else if (ACT & 16) {  // bf16 steps: RN_bf16(RN_bf16(act(g)) * u)
+          const float2 e = reinterpret_cast<const float2*>(smem)[idx];
+          a[k] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(e, __uint_as_float(g16 << 16)), u));
         } else {
           a[k] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
           cold |= is_cold(a[k]);
@@ -143,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
         b[0] = tab_mul(make_float2(e.x, e.y), dv);
         a[0] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
         cold = is_cold(a[0]) | is_cold(b[0]);
+      } else if (ACT & 16) {
+        a[0] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(reinterpret_cast<const float2*>(smem)[idx], g), u));
       } else {
         a[0] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
         cold = is_cold(a[0]);
@@ -157,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
         if (BWD) {
           const float dv = __uint_as_float(
               uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0 + k]) << 16);
-          if (is_cold(a[k])) a[k] = slow_grad_mul(ACT, g, dv, u);
-          if (is_cold(b[k])) b[k] = slow_act_mul(ACT, g, dv);
+          if (is_cold(a[k])) a[k] = slow_grad_mul(ACT & 1, g, dv, u);
+          if (is_cold(b[k])) b[k] = slow_act_mul(ACT & 1, g, dv);
         } else if (is_cold(a[k])) {
-          a[k] = slow_act_mul(ACT, g, u);
+          a[k] = slow_act_mul(ACT & 1, g, u);
         }
       }
     }
@@ -193,16 +198,22 @@ cudaError_t launch_t(PlainP p, cudaStream_t s, const DevInfo& d) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int ACT, int BWD>
+cudaError_t by_out(const PlainP& p, int fmt, int layout, cudaStream_t s, const DevInfo& d) {
+  const bool bf = fmt == GLU_FMT_BF16;
+  if (layout == GLU_LAYOUT_SPLIT)
+    return bf ? launch_t<ACT, BWD, 0, uint16_t>(p, s, d) : launch_t<ACT, BWD, 0, float>(p, s, d);
+  return bf ? launch_t<ACT, BWD, 1, uint16_t>(p, s, d) : launch_t<ACT, BWD, 1, float>(p, s, d);
+}
+
 template <int BWD>
 cudaError_t dispatch(const PlainP& p, int act, int fmt, int layout, cudaStream_t s, const DevInfo& d) {
-  const bool bf = fmt == GLU_FMT_BF16;
-  const bool split = layout == GLU_LAYOUT_SPLIT;
-  if (act == GLU_ACT_SILU) {
-    if (split) return bf ? launch_t<0, BWD, 0, uint16_t>(p, s, d) : launch_t<0, BWD, 0, float>(p, s, d);
-    return bf ? launch_t<0, BWD, 1, uint16_t>(p, s, d) : launch_t<0, BWD, 1, float>(p, s, d);
+  switch (act) {
+    case GLU_ACT_SILU: return by_out<0, BWD>(p, fmt, layout, s, d);
+    case GLU_ACT_GELU_TANH: return by_out<1, BWD>(p, fmt, layout, s, d);
+    case GLU_ACT_SILU | GLU_ACT_BF16_STEPS: return by_out<16, 0>(p, fmt, layout, s, d);  // forward only
+    default: return by_out<17, 0>(p, fmt, layout, s, d);
   }
-  if (split) return bf ? launch_t<1, BWD, 0, uint16_t>(p, s, d) : launch_t<1, BWD, 0, float>(p, s, d);
-  return bf ? launch_t<1, BWD, 1, uint16_t>(p, s, d) : launch_t<1, BWD, 1, float>(p, s, d);
 }
 
 // Zero the padding of a [rows, cols] scale matrix in the 128x4 layout: the

@@ -73,7 +73,17 @@ extern "C" {
 #define GLU_ELAUNCH (-5) /* the CUDA launch returned an error            */
 
 /* ---- enums ---------------------------------------------------------- */
-enum glu_act { GLU_ACT_SILU = 0, GLU_ACT_GELU_TANH = 1 };
+enum glu_act {
+  GLU_ACT_SILU = 0,
+  GLU_ACT_GELU_TANH = 1,
+  /* OR-ed into act, forward only (ABI 2): the eager bf16 values
+   * h = RN_bf16(RN_bf16(act(gate)) * up) in place of act(gate) * up in
+   * fp32 ("Add swiglu + MXFP8 fused CuTe DSL kernel", Numerics and tests:
+   * forward data bitwise identical to the eager activation followed by the
+   * standalone quantiser).  Every output format takes these values; the
+   * backward rejects the flag (GLU_EINVAL). */
+  GLU_ACT_BF16_STEPS = 16
+};
 enum glu_fmt {
   GLU_FMT_MXFP8_E4M3 = 0, /* E4M3 codes + E8M0 scales (row/col/both)      */
   GLU_FMT_NVFP4_E2M1 = 1, /* packed E2M1 + E4M3 scales, 128x4 (row only)  */

@@ -22,6 +22,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 
 SILU, GELU_TANH = 0, 1
+BF16_STEPS = 16  # OR-ed into act (forward): h = RN_bf16(RN_bf16(act(g)) * u)
 MXFP8, NVFP4, BF16, FP32, MXFP8_128X4 = 0, 1, 2, 3, 4
 ROW, COL, BOTH = 1, 2, 3
 SPLIT, INTERLEAVED = 0, 1
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
             l.orc_e8m0_decode.restype = ctypes.c_float
             l.orc_swizzle_offset.argtypes = [i64, i64, i64]
             l.orc_swizzle_offset.restype = i64
+            l.orc_round_bf16.argtypes = [ctypes.c_double]
+            l.orc_round_bf16.restype = ctypes.c_double
             l.orc_scales_128x4.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p]
             l.orc_scales_128x4.restype = None
             l.orc_nvfp4_matrix.argtypes = [ctypes.c_void_p, i64, i64, ctypes.c_void_p, ctypes.c_void_p]
@@ -203,6 +206,11 @@ def scales_128x4(S: np.ndarray) -> np.ndarray:
     out = np.empty((-(-R // 128) * 128) * (-(-C // 4) * 4), np.uint8)
     lib().orc_scales_128x4(_ptr(S), R, C, _ptr(out))
     return out
+
+
+def round_bf16(x: float) -> float:
+    """The nearest bf16 value of a double (ties to even), as a double."""
+    return lib().orc_round_bf16(float(x))
 
 
 def nvfp4_global_scale(amax: float) -> np.float32:

@@ -43,6 +43,25 @@ uint16_t orc_f32_to_bf16_rne(float f) {
   return (uint16_t)kept;
 }
 
+static double round_half_even(double q);
+
+/* Round a double to the nearest bf16 value (ties to even), returned as a
+ * double; one rounding, from the definition: the bf16 grid has 8 significant
+ * bits for |x| >= 2^-126 and the fixed step 2^-133 below; magnitudes at or
+ * above the midpoint between the largest bf16 (0x7F7F) and 2^128 become
+ * infinite.  NaN stays NaN. */
+double orc_round_bf16(double x) {
+  if (isnan(x) || isinf(x) || x == 0.0) return x;
+  double a = fabs(x), step;
+  int e;
+  frexp(a, &e);                       /* a = m * 2^e, 0.5 <= m < 1 */
+  step = (e - 1 >= -126) ? ldexp(1.0, e - 1 - 7) : ldexp(1.0, -133);
+  double q = a / step;                /* exact: step is a power of two */
+  double r = round_half_even(q) * step;
+  if (r >= ldexp(255.0, 120) + ldexp(1.0, 119)) r = INFINITY; /* 0x7F7F = 255 * 2^120 */
+  return copysign(r, x);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Activations, in double                                                  */
 /* ------------------------------------------------------------------------ */
@@ -411,7 +430,15 @@ static void fwd_values(const orc_fwd_args* a, int64_t r0, int64_t nr, float* h) 
       if (a->layout == ORC_SPLIT) { gb = grow[j]; ub = urow[j]; }
       else { gb = grow[2 * j]; ub = grow[2 * j + 1]; } /* gate_j, up_j pairs */
       double g = orc_bf16_to_f32(gb), u = orc_bf16_to_f32(ub);
-      h[r * N + j] = (float)(orc_act(a->act, g) * u);
+      if (a->act & ORC_BF16_STEPS) {
+        /* eager bf16 semantics: act(gate) rounded to bf16, then the product
+         * with up rounded to bf16 (the product of two bf16 values is exact
+         * in double) */
+        double ab = orc_round_bf16(orc_act(a->act & ~ORC_BF16_STEPS, g));
+        h[r * N + j] = (float)orc_round_bf16(ab * u);
+      } else {
+        h[r * N + j] = (float)(orc_act(a->act, g) * u);
+      }
     }
   }
 }
@@ -470,6 +497,7 @@ static void* worker(void* p) {
 
 static int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t M,
                         int64_t W) {
+  act &= ~ORC_BF16_STEPS;
   if (act != ORC_SILU && act != ORC_GELU_TANH) return -1;
   if (layout != ORC_SPLIT && layout != ORC_INTERLEAVED) return -1;
   if (M <= 0 || W <= 0) return -1;
@@ -531,6 +559,7 @@ int orc_glu_fwd(const orc_fwd_args* a, int nthreads) {
 
 int orc_glu_bwd(const orc_bwd_args* a, int nthreads) {
   if (a->fmt == ORC_NVFP4) return -1; /* NVFP4 backward is not on the path */
+  if (a->act & ORC_BF16_STEPS) return -1; /* the bf16-step values are forward only */
   if (check_common(a->act, a->fmt, a->mode, a->layout, a->M, 2 * a->N)) return -1;
   if (a->ld_in < (a->layout == ORC_SPLIT ? a->N : 2 * a->N) || a->ld_dy < a->N) return -1;
   job_t j;

@@ -34,6 +34,12 @@ extern "C" {
 #endif
 
 enum { ORC_SILU = 0, ORC_GELU_TANH = 1 };
+/* OR-ed into act (forward only): h = RN_bf16(RN_bf16(act(g)) * u), the
+ * values an eager bf16 evaluation of act(gate) * up gives ("Add swiglu +
+ * MXFP8 fused CuTe DSL kernel", Numerics and tests: forward data bitwise
+ * identical to the eager activation followed by the quantiser). */
+enum { ORC_BF16_STEPS = 16 };
+double orc_round_bf16(double x);
 enum { ORC_MXFP8 = 0, ORC_NVFP4 = 1, ORC_BF16 = 2, ORC_FP32 = 3 };
 enum { ORC_ROW = 1, ORC_COL = 2, ORC_BOTH = 3 };
 enum { ORC_SPLIT = 0, ORC_INTERLEAVED = 1 };

@@ -62,6 +62,8 @@ def _no_gpu():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(act=2), G.GLU_EINVAL),
+    (dict(act=18), G.GLU_EINVAL),
+    (dict(act=32), G.GLU_EINVAL),
     (dict(fmt=5), G.GLU_EINVAL),
     (dict(mode=0), G.GLU_EINVAL),
     (dict(mode=4), G.GLU_EINVAL),
@@ -91,6 +93,7 @@ def test_fwd_rejections(kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(act=16), G.GLU_EINVAL),                          # bf16 steps: forward only
     (dict(dy=None), G.GLU_EINVAL),
     (dict(fmt=1), G.GLU_EINVAL),                           # no NVFP4 backward
     (dict(ld_dy=128), G.GLU_ESHAPE),

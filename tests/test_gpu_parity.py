@@ -262,6 +262,40 @@ def test_nvfp4_global_scale(act, layout, amax):
 @pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
                          ids=["fp32", "bf16", "mxfp8", "nvfp4"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+def test_bf16_steps_fwd(act, fmt, layout):
+    """act | GLU_ACT_BF16_STEPS: the eager bf16 values RN_bf16(RN_bf16(act(g))
+    * up) in every output format (MXFP8 both directions), ragged shapes."""
+    M, N = (160, 800) if fmt == G.FMT_MXFP8 else (200, 1296)
+    g, u = _randn(M, N, 81, 2.0), _randn(M, N, 82)
+    mode = G.MODE_BOTH if fmt == G.FMT_MXFP8 else G.MODE_ROW
+    gpu, ref = run_fwd(g, u, act[0] | G.ACT_BF16_STEPS, fmt, mode, layout)
+    assert not np.any(ref["h"].view(np.uint32) & 0xFFFF)  # the values are bf16 values
+    check(gpu, ref, fmt, mode, M, N, "bf16_steps")
+    if fmt in (G.FMT_FP32, G.FMT_BF16):  # exact values: bit for bit
+        assert np.array_equal(gpu["out"], ref["out"])
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+def test_every_bf16_gate_bf16_steps(act):
+    """All 65536 gate patterns through the bf16-step values (MXFP8 both and
+    the BF16 output), so that every gate's bf16 rounding of act(g) is
+    exercised, decided fast or exactly."""
+    M, N = 256, 256
+    pats = torch.arange(65536, dtype=torch.int32)
+    perm = torch.randperm(65536, generator=torch.Generator().manual_seed(91))
+    g = pats[perm].to(torch.int16).view(torch.bfloat16).reshape(M, N).to(DEV)
+    u = _randn(M, N, 92)
+    a = act[0] | G.ACT_BF16_STEPS
+    gpu, ref = run_fwd(g, u, a, G.FMT_MXFP8, G.MODE_BOTH, G.LAYOUT_SPLIT)
+    check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, N, "all_gates_bf16_steps")
+    gpu, ref = run_fwd(g, u, a, G.FMT_BF16, G.MODE_ROW, G.LAYOUT_SPLIT)
+    check(gpu, ref, G.FMT_BF16, G.MODE_ROW, M, N, "all_gates_bf16_steps_out")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
+                         ids=["fp32", "bf16", "mxfp8", "nvfp4"])
 def test_special_values_fwd(act, fmt):
     M, N = 64, 256
     g, u = _special_inputs(M, N, 51)

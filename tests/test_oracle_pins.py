@@ -575,3 +575,83 @@ def test_nvfp4_power_of_two_global_scale():
     qb = lambda q: q.reshape(M, C, 8)
     assert np.array_equal(qb(two["out"])[ok], qb(plain["out"])[ok])
 
+
+def _bf16_grid():
+    """Every finite non-negative bf16 value, ascending, as float64."""
+    pats = np.arange(0x0000, 0x7F81, dtype=np.uint32)  # +0 .. +inf
+    return (pats << 16).view(np.float32).astype(np.float64)
+
+
+def _nearest_bf16_brute(x: float) -> float:
+    """Nearest bf16 by search over the grid, ties to the even pattern."""
+    grid = _bf16_grid()
+    a = abs(x)
+    i = int(np.searchsorted(grid, a))
+    if i < len(grid) and grid[i] == a:
+        r = a
+    else:
+        lo, hi = grid[i - 1], grid[i]
+        if hi == np.inf:  # beyond the largest finite bf16: the half-way point is 2^128 - 2^119
+            r = np.inf if a >= lo + 2.0 ** 119 else lo
+        else:
+            dl, dh = a - lo, hi - a
+            r = lo if dl < dh else hi if dh < dl else (lo if (i - 1) % 2 == 0 else hi)
+    return float(np.copysign(r, x))
+
+
+def test_round_bf16_against_brute_force():
+    rng = np.random.default_rng(17)
+    grid = _bf16_grid()
+    xs = list(rng.standard_normal(300) * 10.0 ** rng.integers(-45, 38, 300))
+    mids = (grid[1:-1] + grid[2:]) / 2                 # every midpoint is a tie
+    xs += list(mids[rng.integers(0, len(mids) - 1, 300)])
+    xs += list(np.nextafter(mids[:50], 0)) + list(np.nextafter(mids[:50], 1))
+    xs += [1e-41, 9.2e-41 / 2, 2.0 ** -134, 3.3895e38, 3.396e38, 3.3966e38, 3.4e38, -2.859375, 0.0]
+    for x in xs:
+        assert O.round_bf16(x) == _nearest_bf16_brute(x) or (np.isnan(x)), x
+
+
+def test_bf16_steps_values():
+    """act | 16: h = RN_bf16(RN_bf16(act(g)) * up).  Hand-worked: silu(3) =
+    2.8577224 -> bf16 2.859375 (step 1/64 in [2, 4)); times up = 3 gives
+    8.578125 -> bf16 8.5625 (step 1/16 in [8, 16)), where the fp32 value is
+    8.5731672."""
+    g = np.array([[0x4040]], np.uint16)  # 3.0
+    u = np.array([[0x4040]], np.uint16)
+    h = O.glu_fwd(g, u, act=O.SILU | O.BF16_STEPS, fmt=O.FP32)["out"][0, 0]
+    assert h == np.float32(8.5625)
+    h32 = O.glu_fwd(g, u, act=O.SILU, fmt=O.FP32)["out"][0, 0]
+    assert abs(h32 - 8.5731672) < 1e-6
+    # every value is a bf16 value, and equals the two roundings done on the
+    # host from the oracle's double activation
+    rng = np.random.default_rng(4)
+    M, N = 8, 64
+    g = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    u = (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for act in (O.SILU, O.GELU_TANH):
+        h = O.glu_fwd(g, u, act=act | O.BF16_STEPS, fmt=O.FP32)["out"]
+        gf = (g.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        uf = (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        a = np.array([O.round_bf16(x) for x in O.act(act, gf.ravel())]).reshape(M, N)
+        ref = np.array([O.round_bf16(x) for x in (a * uf).ravel()]).reshape(M, N)
+        assert np.array_equal(h.astype(np.float64), ref)
+        assert np.all((h.view(np.uint32) & 0xFFFF) == 0)
+    # the backward has no bf16-step form
+    with pytest.raises(ValueError):
+        O.glu_bwd(g, u, g, act=O.SILU | O.BF16_STEPS, fmt=O.FP32)
+
+
+def test_bf16_steps_agree_with_torch_eager():
+    """torch's CPU bf16 silu rounds its own fp32 evaluation: it can differ
+    from the correctly rounded bf16 of silu(g) only where silu(g) lies
+    within a few fp32 ulps of a bf16 midpoint, i.e. almost nowhere."""
+    torch = pytest.importorskip("torch")
+    pats = np.arange(0, 0x10000, dtype=np.uint32)
+    gf = (pats << 16).view(np.float32)
+    ok = np.isfinite(gf) & (np.abs(gf) < 60)
+    gb = torch.from_numpy(gf[ok].copy()).to(torch.bfloat16)
+    eager = torch.nn.functional.silu(gb).float().numpy().astype(np.float64)
+    ours = np.array([O.round_bf16(x) for x in O.act(O.SILU, gf[ok].astype(np.float64))])
+    mism = np.sum(eager != ours)
+    assert mism <= 10, mism
+
