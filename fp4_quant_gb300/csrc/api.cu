@@ -71,7 +71,6 @@ int check_fwd(const glu_quant_fwd_args* a) {
 
 int check_bwd(const glu_quant_bwd_args* a) {
   if (a == nullptr) return GLU_EINVAL;
-  if (a->fmt == GLU_FMT_NVFP4_E2M1) return GLU_EINVAL;
   if (a->act & GLU_ACT_BF16_STEPS) return GLU_EINVAL;  // the bf16-step values are forward only
   int st = check_common(a->act, a->fmt, a->mode, a->layout, a->M, a->N, a->ld_in, a->gate,
                         a->up, a->q_row, a->s_row, a->q_col, a->s_col, a->out);
@@ -186,7 +185,7 @@ extern "C" int glu_quant_bwd(const glu_quant_bwd_args* a, void* stream) {
   st = device_info(&d);
   if (st != GLU_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a->fmt == GLU_FMT_MXFP8_E4M3 || a->fmt == GLU_FMT_MXFP8_E4M3_128X4)
+  if (a->fmt == GLU_FMT_MXFP8_E4M3 || a->fmt == GLU_FMT_MXFP8_E4M3_128X4 || a->fmt == GLU_FMT_NVFP4_E2M1)
     return launched(gq::launch_bwd_mx(*a, s, d));
   return launched(gq::launch_bwd_plain(*a, s, d));
 }
@@ -219,7 +218,7 @@ extern "C" int glu_quant_bwd_sizes(const glu_quant_bwd_args* a, size_t sizes[4])
   c.dy = ph;
   c.up = (c.layout == GLU_LAYOUT_SPLIT) ? ph : nullptr;
   const bool mx = c.fmt == GLU_FMT_MXFP8_E4M3 || c.fmt == GLU_FMT_MXFP8_E4M3_128X4;
-  c.q_row = c.s_row = (mx && (c.mode & GLU_MODE_ROW)) ? phw : nullptr;
+  c.q_row = c.s_row = (c.fmt == GLU_FMT_NVFP4_E2M1 || (mx && (c.mode & GLU_MODE_ROW))) ? phw : nullptr;
   c.q_col = c.s_col = (mx && (c.mode & GLU_MODE_COL)) ? phw : nullptr;
   c.out = (c.fmt == GLU_FMT_BF16 || c.fmt == GLU_FMT_FP32) ? phw : nullptr;
   int st = check_bwd(&c);

@@ -35,6 +35,7 @@ struct BwdP {
   const uint16_t* dy;
   int64_t ld, ld_dy;
   int64_t M, N;
+  uint8_t* q_row;  // NVFP4 codes [M, N] (stored directly; MXFP8 codes leave by TMA)
   uint8_t* s_row;
   uint8_t* s_col;
   ScaleLayout sl_row, sl_col;  // scale matrices [M, 2N/32] and [2N, M/32]

@@ -37,6 +37,7 @@
 #include <cstring>
 
 #include "bwd_common.cuh"
+#include "nv_block.cuh"
 #include "ring.cuh"
 #include "tma.cuh"
 
@@ -53,7 +54,7 @@ cudaError_t make_params(BwdP& p, const glu_quant_bwd_args& a) {
     e = make_tile_map(&p.tm_a, a.gate, 4, a.N, a.M, a.ld_in * 2, kWC, kTR, 128);
   }
   if (e == cudaSuccess) e = make_tile_map(&p.tm_d, a.dy, 2, a.N, a.M, a.ld_dy * 2, 64, kTR, 128);
-  if (e == cudaSuccess && (a.mode & GLU_MODE_ROW))
+  if (e == cudaSuccess && (a.mode & GLU_MODE_ROW) && a.fmt != GLU_FMT_NVFP4_E2M1)
     e = make_tile_map(&p.tm_qr, a.q_row, 1, 2 * a.N, a.M, 2 * a.N, kWC, kTR, 32);
   if (e == cudaSuccess && (a.mode & GLU_MODE_COL))
     e = make_tile_map(&p.tm_qc, a.q_col, 1, a.M, 2 * a.N, a.M, kTR, kWC, 32);
@@ -65,9 +66,11 @@ cudaError_t make_params(BwdP& p, const glu_quant_bwd_args& a) {
   p.ld_dy = a.ld_dy;
   p.M = a.M;
   p.N = a.N;
+  p.q_row = static_cast<uint8_t*>(a.q_row);
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.s_col = static_cast<uint8_t*>(a.s_col);
-  p.sl_row = scale_layout(2 * a.N / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
+  p.sl_row = a.fmt == GLU_FMT_NVFP4_E2M1 ? scale_layout(2 * a.N / 16, true)
+                                        : scale_layout(2 * a.N / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
   p.sl_col = scale_layout(a.M / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
   p.n_rt = (a.M + kTR - 1) / kTR;
   p.n_ct = (a.N + kTC - 1) / kTC;
@@ -85,6 +88,7 @@ using namespace bwd;
 // of the backward table in shared memory.  Colwise: four groups of four
 // warps (up to 128 registers: two lanes share a column, 16 rows each), one
 // box pair per warp, the exact path reading the table from global memory.
+constexpr int kModeNvB = 4;  // internal mode: NVFP4 (rowwise walk, like GLU_MODE_ROW)
 __host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_COL ? 4 : 3; }
 __host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * kGroupWarps * 32; }
 __host__ __device__ constexpr int tbytes_for(int mode) { return mode == GLU_MODE_COL ? 2048 : 4096; }
@@ -97,7 +101,8 @@ __host__ __device__ constexpr int smem_for(int mode) {
   return 1024 + groups_for(mode) * kSlots * kStageBytes + groups_for(mode) * kGroupWarps * tbytes_for(mode) +
          hot_for(mode) + int(sizeof(Ctl));
 }
-static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448,
+static_assert(smem_for(GLU_MODE_ROW) <= 232448 && smem_for(GLU_MODE_COL) <= 232448 &&
+                  smem_for(kModeNvB) <= 232448,
               "shared memory per CTA exceeds 227 KB");
 
 __device__ uint32_t g_err_bwd_dir;
@@ -105,6 +110,7 @@ __device__ uint32_t g_err_bwd_dir;
 template <int ACT, int MODE, int LAYOUT>
 __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __grid_constant__ BwdP p) {
   constexpr bool kCol = MODE == GLU_MODE_COL;
+  constexpr bool kNv = MODE == kModeNvB;  // NVFP4: rowwise 1x16 blocks, codes and scales stored directly
   constexpr int kGroups = groups_for(MODE), kStages = kGroups * kSlots, kTBytes = tbytes_for(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
     prefetch_tensormap(&p.tm_d);
-    prefetch_tensormap(kCol ? &p.tm_qc : &p.tm_qr);
+    if (!kNv) prefetch_tensormap(kCol ? &p.tm_qc : &p.tm_qr);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
@@ -236,6 +242,47 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
             }
           }
         }
+      }
+
+      if constexpr (kNv) {
+        // ---- NVFP4: two 16-element blocks per output; codes (element 2i in
+        // the low nibble) and E4M3 scales (128x4 layout) stored directly
+        auto ex = [&](int which) {
+          return [&, which](int e) {
+            return exact_bwd<ACT>(hot, sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), which);
+          };
+        };
+        auto ex8 = [&](int which) {
+          return [&, which](int e0, float (&x)[8]) {
+#pragma unroll 1
+            for (int i = 0; i < 8; ++i)
+              x[i] = exact_bwd<ACT>(hot, sv.g16(lane, e0 + i), sv.u16(lane, e0 + i), sv.d16(lane, e0 + i), which);
+          };
+        };
+        const float dgd = 2.0f * dgate_bracket(nrow), dud = Bracket<ACT>::kNv;
+        uint32_t c[8], sc[4];
+        sc[0] = nv_block<0>(dg, c[0], c[1], dgd, ex(0), ex8(0));
+        sc[1] = nv_block<16>(dg, c[2], c[3], dgd, ex(0), ex8(0));
+        sc[2] = nv_block<0>(du, c[4], c[5], dud, ex(1), ex8(1));
+        sc[3] = nv_block<16>(du, c[6], c[7], dud, ex(1), ex8(1));
+        if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+        const int64_t r = row0 + lane;
+        if (r < p.M) {
+          const bool two = c0 + 16 < p.N;  // N % 32 == 16 leaves a half sub-tile at the end
+          uint8_t* qg = p.q_row + r * p.N + c0 / 2;
+          uint8_t* qu = p.q_row + r * p.N + (p.N + c0) / 2;
+          st_stream(qg, make_uint2(c[0], c[1]));
+          st_stream(qu, make_uint2(c[4], c[5]));
+          st_byte(p.s_row + p.sl_row.at(r, c0 / 16), sc[0]);
+          st_byte(p.s_row + p.sl_row.at(r, (p.N + c0) / 16), sc[2]);
+          if (two) {
+            st_stream(qg + 8, make_uint2(c[2], c[3]));
+            st_stream(qu + 8, make_uint2(c[6], c[7]));
+            st_byte(p.s_row + p.sl_row.at(r, c0 / 16 + 1), sc[1]);
+            st_byte(p.s_row + p.sl_row.at(r, (p.N + c0) / 16 + 1), sc[3]);
+          }
+        }
+        continue;
       }
 
       // ---- the lane's two blocks
@@ -418,6 +465,7 @@ cudaError_t by_layout(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo
 
 template <int ACT>
 cudaError_t by_mode(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
+  if (a.fmt == GLU_FMT_NVFP4_E2M1) return by_layout<ACT, kModeNvB>(a, s, d);
   return a.mode == GLU_MODE_COL ? by_layout<ACT, GLU_MODE_COL>(a, s, d) : by_layout<ACT, GLU_MODE_ROW>(a, s, d);
 }
 
@@ -427,6 +475,8 @@ cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
   cudaError_t e = a.mode == GLU_MODE_BOTH ? launch_bwd_cb(a, s, d)
                   : a.act == GLU_ACT_SILU  ? by_mode<0>(a, s, d)
                                            : by_mode<1>(a, s, d);
+  if (e == cudaSuccess && a.fmt == GLU_FMT_NVFP4_E2M1)  // scale padding (rows to 128, columns to 4)
+    e = launch_scale_pad(static_cast<uint8_t*>(a.s_row), a.M, 2 * a.N / 16, s);
   if (e == cudaSuccess && a.fmt == GLU_FMT_MXFP8_E4M3_128X4) {
     // the padding of the 128x4 scale layouts (no tile writes it)
     if (a.mode & GLU_MODE_ROW) e = launch_scale_pad(static_cast<uint8_t*>(a.s_row), a.M, 2 * a.N / 32, s);

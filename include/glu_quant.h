@@ -148,8 +148,9 @@ typedef struct glu_quant_fwd_args {
  *   MXFP8 ROW: q_row [M, 2N], s_row [M, 2N/32]
  *   MXFP8 COL: q_col [2N, M], s_col [2N, M/32]
  *   MXFP8_128X4: the same codes, the scale matrices in the 128x4 layout
+ *   NVFP4 (ROW, ABI 2): q_row [M, N] packed codes of the [M, 2N] matrix,
+ *              s_row the 128x4-layout scales of [M, 2N/16], padding 0
  *   BF16/FP32: out [M, 2N]
- * NVFP4 backward is not provided (GLU_EINVAL).
  */
 typedef struct glu_quant_bwd_args {
   int32_t act, fmt, mode, layout;

@@ -326,14 +326,14 @@ def glu_bwd(gate, up, dy, *, act: int, fmt: int, mode: int = ROW,
         if shp is None:
             res[k] = None
         elif k == "out":
-            res[k] = np.zeros(shp, {BF16: np.uint16, FP32: np.float32}[fmt])
+            res[k] = np.zeros(shp, {BF16: np.uint16, FP32: np.float32, NVFP4: np.uint8}[fmt])
         else:
             res[k] = np.zeros(shp, np.uint8)
     h = np.zeros((M, W), np.float32) if want_h else None
+    keys = ("q_row", "s_nvfp4" if fmt == NVFP4 else "s_row", "q_col", "s_col", "out")
     a = BwdArgs(act, fmt, mode, layout, M, N, ld, d.shape[1], _ptr(g).value,
                 None if u is None else _ptr(u).value, _ptr(d).value,
-                *(None if res.get(k) is None else _ptr(res[k]).value
-                  for k in ("q_row", "s_row", "q_col", "s_col", "out")),
+                *(None if res.get(k) is None else _ptr(res[k]).value for k in keys),
                 None if h is None else _ptr(h).value)
     rc = lib().orc_glu_bwd(ctypes.byref(a), nthreads or os.cpu_count() or 1)
     if rc != 0:

@@ -558,7 +558,6 @@ int orc_glu_fwd(const orc_fwd_args* a, int nthreads) {
 }
 
 int orc_glu_bwd(const orc_bwd_args* a, int nthreads) {
-  if (a->fmt == ORC_NVFP4) return -1; /* NVFP4 backward is not on the path */
   if (a->act & ORC_BF16_STEPS) return -1; /* the bf16-step values are forward only */
   if (check_common(a->act, a->fmt, a->mode, a->layout, a->M, 2 * a->N)) return -1;
   if (a->ld_in < (a->layout == ORC_SPLIT ? a->N : 2 * a->N) || a->ld_dy < a->N) return -1;
@@ -572,6 +571,7 @@ int orc_glu_bwd(const orc_bwd_args* a, int nthreads) {
   j.sink.q_row = a->q_row; j.sink.s_row = a->s_row;
   j.sink.q_col = a->q_col; j.sink.s_col = a->s_col;
   j.sink.out = a->out;
+  if (a->fmt == ORC_NVFP4) j.sink.s_nvfp4 = a->s_row; /* codes in out, 128x4 scales in s_row */
   return run(&j, nthreads);
 }
 

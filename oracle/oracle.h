@@ -92,10 +92,10 @@ typedef struct {
   const uint16_t* up;
   const uint16_t* dy;   /* [M, N] with row stride ld_dy */
   uint8_t* q_row;       /* [M, 2N]          */
-  uint8_t* s_row;       /* [M, 2N/32]       */
+  uint8_t* s_row;       /* [M, 2N/32]; NVFP4: the padded 128x4 scales of [M, 2N/16] */
   uint8_t* q_col;       /* [2N, M]          */
   uint8_t* s_col;       /* [2N, M/32]       */
-  void* out;            /* BF16/FP32: [M, 2N] */
+  void* out;            /* BF16/FP32: [M, 2N]; NVFP4: packed codes [M, N] */
   float* h;             /* optional [M, 2N]: fp32 [dGate | dUp] */
 } orc_bwd_args;
 

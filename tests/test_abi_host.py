@@ -95,7 +95,7 @@ def test_fwd_rejections(kw, status):
 @pytest.mark.parametrize("kw,status", [
     (dict(act=16), G.GLU_EINVAL),                          # bf16 steps: forward only
     (dict(dy=None), G.GLU_EINVAL),
-    (dict(fmt=1), G.GLU_EINVAL),                           # no NVFP4 backward
+    (dict(fmt=1, mode=2, q_row=None, s_row=None, q_col=P, s_col=P), G.GLU_EINVAL),  # NVFP4 is row only
     (dict(ld_dy=128), G.GLU_ESHAPE),
     (dict(ld_dy=260), G.GLU_EALIGN),
     (dict(dy=P + 4), G.GLU_EALIGN),
@@ -137,3 +137,6 @@ def test_sizes():
     assert st == 0 and s == (96 * 832, 128 * 28, 0, 0)
     st, _ = G.glu_quant_fwd_sizes(fwd_args(fmt=5))
     assert st == G.GLU_EINVAL
+    # NVFP4 backward: codes of [M, 2N] packed, scales of [M, 2N/16] in 128x4
+    st, s = G.glu_quant_bwd_sizes(bwd_args(fmt=1, M=200, N=48, ld_in=48, ld_dy=48))
+    assert st == 0 and s == (200 * 48, 256 * 8, 0, 0)

@@ -260,6 +260,20 @@ def test_nvfp4_global_scale(act, layout, amax):
 
 
 @pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+@pytest.mark.parametrize("shape", [(200, 416), (96, 400), (1, 16)], ids=["ragged", "half_subtile", "tiny"])
+def test_nvfp4_bwd(act, layout, shape):
+    """NVFP4 backward: [dGate | dUp] as packed E2M1 [M, N] with 128x4 E4M3
+    scales of [M, 2N/16]; ragged rows (padding rows of the scale layout), N
+    a multiple of 32 plus 16 (a half sub-tile at the end of each output)."""
+    M, N = shape
+    g, u, d = _randn(M, N, 101, 2.0), _randn(M, N, 102), _randn(M, N, 103)
+    gpu, ref = run_bwd(g, u, d, act[0], G.FMT_NVFP4, G.MODE_ROW, layout)
+    check(gpu, {"out": ref["out"], "s_nvfp4": ref["s_nvfp4"], "h": ref["h"]}, G.FMT_NVFP4,
+          G.MODE_ROW, M, 2 * N, "nvfp4_bwd")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
                          ids=["fp32", "bf16", "mxfp8", "nvfp4"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])

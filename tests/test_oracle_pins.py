@@ -655,3 +655,19 @@ def test_bf16_steps_agree_with_torch_eager():
     mism = np.sum(eager != ours)
     assert mism <= 10, mism
 
+
+def test_nvfp4_backward_is_nvfp4_of_the_backward_values():
+    """NVFP4 backward: the [M, 2N] = [dGate | dUp] fp32 values quantised by
+    the NVFP4 block rule (codes [M, N] packed, 128x4 scales of [M, 2N/16])."""
+    rng = np.random.default_rng(6)
+    M, N = 200, 48
+    mk = lambda: (rng.standard_normal((M, N)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    g, u, d = mk(), mk(), mk()
+    for act in (O.SILU, O.GELU_TANH):
+        r = O.glu_bwd(g, u, d, act=act, fmt=O.NVFP4)
+        f = np.ascontiguousarray(O.glu_bwd(g, u, d, act=act, fmt=O.FP32)["out"])
+        q = np.zeros((M, N), np.uint8)
+        s = np.zeros(256 * 8, np.uint8)
+        O.lib().orc_nvfp4_matrix(O._ptr(f), M, 2 * N, O._ptr(q), O._ptr(s))
+        assert np.array_equal(q, r["out"]) and np.array_equal(s, r["s_nvfp4"])
+
