@@ -60,6 +60,8 @@ def algo_bytes(direction: str, mode: int, M: int, N: int, fmt: str = "mxfp8") ->
         read = 6 * MN
         if fmt == "mxfp8":
             write = dirs * 2 * (MN + MN // 32)
+        elif fmt == "nvfp4":
+            write = MN + MN // 8
         elif fmt == "bf16":
             write = 4 * MN
         else:
@@ -484,6 +486,34 @@ def sweep(path: str):
         o = G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1)
         record("geglu_nvfp4", "fwd", 1, "nvfp4", "gelu_tanh", M, 16384,
                lambda s, o=o: G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1, out=o, stream=s))
+    # the formats and flags beyond the headline calls, on the same shapes
+    x = synth.make(synth.spec("swiglu_131072"), dev, with_dy=True)
+    M5, N5 = x["gate"].shape
+    for direction, mode in (("fwd", 3), ("bwd", 1)):
+        f = lambda s, o, dr=direction, m=mode: (
+            G.fwd(x["gate"], x["up"], fmt=G.FMT_MXFP8_128X4, mode=m, out=o, stream=s) if dr == "fwd" else
+            G.bwd(x["gate"], x["up"], x["dy"], fmt=G.FMT_MXFP8_128X4, mode=m, out=o, stream=s))
+        o = f(None, None)
+        record("swiglu_131072_mxfp8_128x4", direction, mode, "mxfp8", "silu", M5, N5,
+               lambda s, f=f, o=o: f(s, o))
+    for mode in (1, 3):
+        o = G.fwd(x["gate"], x["up"], act=G.ACT_SILU | G.ACT_BF16_STEPS, mode=mode)
+        record("swiglu_131072_bf16_steps", "fwd", mode, "mxfp8", "silu", M5, N5,
+               lambda s, m=mode, o=o: G.fwd(x["gate"], x["up"], act=G.ACT_SILU | G.ACT_BF16_STEPS,
+                                            mode=m, out=o, stream=s))
+    del x
+    for N in (14336,):
+        x = synth.make(synth.spec("geglu_8192", N=N), dev, with_dy=True)
+        o = G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=G.FMT_NVFP4)
+        record("geglu_8192_nvfp4_bwd", "bwd", 1, "nvfp4", "gelu_tanh", 8192, N,
+               lambda s, o=o: G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=G.FMT_NVFP4, out=o, stream=s))
+        del x
+    for M in (784, 968):
+        X = synth.make(synth.spec("geglu_nvfp4", M=M), dev)["x"]
+        amax = torch.tensor([50.0], dtype=torch.float32, device=dev)
+        o = G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1, amax=amax)
+        record("geglu_nvfp4_global_scale", "fwd", 1, "nvfp4", "gelu_tanh", M, 16384,
+               lambda s, o=o: G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1, out=o, stream=s, amax=amax))
     with open(path, "w") as f:
         for r in recs:
             f.write(json.dumps(r) + "\n")
