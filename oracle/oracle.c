@@ -80,8 +80,15 @@ static const double GELU_A = 0.044715;
  *     gelu(x) = 0.5 x (1 + tanh(y)),  y = sqrt(2/pi) (x + 0.044715 x^3),
  *   evaluated through the identity 0.5 (1 + tanh(y)) = sigmoid(2y), which
  *   keeps full relative precision in the negative tail where 1 + tanh(y)
- *   cancels. */
+ *   cancels.
+ *   ReLU and the identity (further gated activations, "Add swiglu + MXFP8
+ *   fused CuTe DSL kernel", Follow-ups): relu(x) = x for x > 0, else +0, so
+ *   that h = relu(g) * up is a signed zero with the sign of up where g <= 0;
+ *   identity(x) = x.  With bf16 operands both products are exact in double
+ *   and in fp32. */
 double orc_act(int act, double x) {
+  if (act == ORC_RELU) return x > 0.0 ? x : 0.0; /* ReLU: +0 for x <= 0 */
+  if (act == ORC_IDENTITY) return x;
   if (act == ORC_SILU) return x * sigmoid(x);
   double y = GELU_C * (x + GELU_A * x * x * x);
   return x * sigmoid(2.0 * y);
@@ -96,6 +103,9 @@ double orc_act(int act, double x) {
  *  0.5(1 + tanh y) + 0.5 x (1 - tanh^2 y) y').  1 - s is taken as
  *  sigmoid(-t), the same quantity without cancellation. */
 double orc_act_grad(int act, double x) {
+  /* ReLU: 1 for x > 0, else 0 (the derivative at 0 taken as 0); identity 1 */
+  if (act == ORC_RELU) return x > 0.0 ? 1.0 : 0.0;
+  if (act == ORC_IDENTITY) return 1.0;
   if (act == ORC_SILU) {
     double s = sigmoid(x), one_minus_s = sigmoid(-x);
     return s * (1.0 + x * one_minus_s);
@@ -498,7 +508,7 @@ static void* worker(void* p) {
 static int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t M,
                         int64_t W) {
   act &= ~ORC_BF16_STEPS;
-  if (act != ORC_SILU && act != ORC_GELU_TANH) return -1;
+  if (act < ORC_SILU || act > ORC_IDENTITY) return -1;
   if (layout != ORC_SPLIT && layout != ORC_INTERLEAVED) return -1;
   if (M <= 0 || W <= 0) return -1;
   if (fmt == ORC_MXFP8) {

@@ -33,7 +33,11 @@
 extern "C" {
 #endif
 
-enum { ORC_SILU = 0, ORC_GELU_TANH = 1 };
+/* Activations.  SiLU and GELU (tanh) are the pages' own; ReLU (ReGLU,
+ * relu(g) = g for g > 0, else +0) and the identity (the bilinear GLU, h = g *
+ * up) are the further gated activations that "Add swiglu + MXFP8 fused CuTe
+ * DSL kernel", Follow-ups (item 1) leaves open, in their textbook form. */
+enum { ORC_SILU = 0, ORC_GELU_TANH = 1, ORC_RELU = 2, ORC_IDENTITY = 3 };
 /* OR-ed into act (forward only): h = RN_bf16(RN_bf16(act(g)) * u), the
  * values an eager bf16 evaluation of act(gate) * up gives ("Add swiglu +
  * MXFP8 fused CuTe DSL kernel", Numerics and tests: forward data bitwise

@@ -671,3 +671,115 @@ def test_nvfp4_backward_is_nvfp4_of_the_backward_values():
         O.lib().orc_nvfp4_matrix(O._ptr(f), M, 2 * N, O._ptr(q), O._ptr(s))
         assert np.array_equal(q, r["out"]) and np.array_equal(s, r["s_nvfp4"])
 
+
+
+# ------------------------------------------- ReLU and identity gates --
+# ReGLU (relu(g) = g for g > 0, else +0) and the bilinear GLU (act = identity):
+# the gated activations beyond SiLU and GELU.  With bf16 operands their values
+# are exact products, so the oracle is pinned against torch's own fp32 and
+# autograd results bit for bit, and against the other activations where
+# they coincide.
+
+def _bf16_f32(b):
+    return (np.asarray(b, np.uint32) << 16).view(np.float32)
+
+
+def test_relu_identity_vs_torch_float64():
+    x = torch.linspace(-5, 5, 10001, dtype=torch.float64)
+    x = torch.cat([x, torch.tensor([0.0, -0.0, 1e-300, -1e-300, 3e38, -3e38], dtype=torch.float64)])
+    assert np.array_equal(O.act(O.RELU, x.numpy()), torch.relu(x).numpy())
+    assert np.array_equal(O.act(O.IDENTITY, x.numpy()), x.numpy())
+    t = x.clone().requires_grad_(True)
+    torch.relu(t).sum().backward()
+    assert np.array_equal(O.act_grad(O.RELU, x.numpy()), t.grad.numpy())
+    assert np.all(O.act_grad(O.IDENTITY, x.numpy()) == 1.0)
+    # relu is +0 (not -0) at and below zero: h then takes the sign of up
+    assert all(math.copysign(1, v) == 1 for v in O.act(O.RELU, [-2.0, -0.0, 0.0]))
+
+
+def _spiky_inputs(M, N, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(3):
+        v = rng.standard_normal((M, N)).astype(np.float32)
+        v[rng.random((M, N)) < 0.01] = 60.0
+        v[rng.random((M, N)) < 0.01] = 0.0
+        out.append(_bf16_bits(v))
+    return out
+
+
+@pytest.mark.parametrize("kind", [O.RELU, O.IDENTITY])
+def test_exact_product_activations_vs_torch(kind):
+    # forward fp32 values are torch's fp32 relu(g) * u (exact products), the
+    # backward ones torch's autograd of relu(g) * u * dY in float64, rounded
+    g, u, d = _spiky_inputs(64, 96, 31 + kind)
+    gf, uf, df = (torch.from_numpy(_bf16_f32(b)) for b in (g, u, d))
+    fn = torch.relu if kind == O.RELU else (lambda t: t)
+    h = O.glu_fwd(g, u, act=kind, fmt=O.FP32)["out"]
+    assert np.array_equal(h, (fn(gf) * uf).numpy())
+    gg = gf.double().requires_grad_(True)
+    uu = uf.double().requires_grad_(True)
+    (fn(gg) * uu * df.double()).sum().backward()
+    ref = torch.cat([gg.grad, uu.grad], dim=1).float().numpy()
+    assert np.array_equal(O.glu_bwd(g, u, d, act=kind, fmt=O.FP32)["out"], ref)
+
+
+def test_relu_signed_zeros_hand_worked():
+    # g = -1: relu = +0, so h = (+0) * up carries the sign of up; one MXFP8
+    # block of such values has scale 0 and codes 0x00 / 0x80
+    g = _bf16_bits(np.full((1, 32), -1.0))
+    u = _bf16_bits(np.where(np.arange(32) % 2 == 0, 2.0, -2.0).reshape(1, 32))
+    r = O.glu_fwd(g, u, act=O.RELU, fmt=O.MXFP8, mode=O.ROW)
+    assert r["s_row"].tolist() == [[0]]
+    assert r["q_row"][0].tolist() == [0x00, 0x80] * 16
+    # backward, dY = 1: dGate = (dY * up) * 0 keeps the sign of up, dUp = dY * (+0) = +0
+    d = _bf16_bits(np.ones((1, 32)))
+    out = O.glu_bwd(g, u, d, act=O.RELU, fmt=O.FP32)["out"][0]
+    assert [math.copysign(1, v) for v in out[:32]] == [1.0, -1.0] * 16
+    assert all(v == 0 and math.copysign(1, v) == 1 for v in out[32:])
+    # dY = -1 flips both
+    d = _bf16_bits(-np.ones((1, 32)))
+    out = O.glu_bwd(g, u, d, act=O.RELU, fmt=O.FP32)["out"][0]
+    assert [math.copysign(1, v) for v in out[:32]] == [-1.0, 1.0] * 16
+    assert all(math.copysign(1, v) == -1 for v in out[32:])
+
+
+@pytest.mark.parametrize("fmt,mode", [(O.MXFP8, O.BOTH), (O.NVFP4, O.ROW), (O.BF16, O.ROW)],
+                         ids=["mxfp8_both", "nvfp4", "bf16"])
+def test_relu_equals_identity_on_positive_gates(fmt, mode):
+    rng = np.random.default_rng(41)
+    M, N = 64, 128
+    g = _bf16_bits(np.abs(rng.standard_normal((M, N))) + 2.0 ** -8)
+    u, d = _bf16_bits(rng.standard_normal((M, N))), _bf16_bits(rng.standard_normal((M, N)))
+    a = O.glu_fwd(g, u, act=O.RELU, fmt=fmt, mode=mode)
+    b = O.glu_fwd(g, u, act=O.IDENTITY, fmt=fmt, mode=mode)
+    assert all(np.array_equal(a[k], b[k]) for k in a)
+    a = O.glu_bwd(g, u, d, act=O.RELU, fmt=fmt, mode=mode)
+    b = O.glu_bwd(g, u, d, act=O.IDENTITY, fmt=fmt, mode=mode)
+    assert all(np.array_equal(a[k], b[k]) for k in a)
+
+
+def test_all_activations_agree_at_gate_32():
+    # act(32) = 32 and act'(32) = 1 after rounding to fp32 for all four
+    # activations, so every output of every format coincides
+    rng = np.random.default_rng(42)
+    M, N = 64, 64
+    g = _bf16_bits(np.full((M, N), 32.0))
+    u, d = _bf16_bits(rng.standard_normal((M, N))), _bf16_bits(rng.standard_normal((M, N)))
+    for fmt, mode in ((O.MXFP8, O.BOTH), (O.NVFP4, O.ROW), (O.FP32, O.ROW)):
+        ref_f = O.glu_fwd(g, u, act=O.SILU, fmt=fmt, mode=mode)
+        ref_b = O.glu_bwd(g, u, d, act=O.SILU, fmt=fmt, mode=mode)
+        for kind in (O.GELU_TANH, O.RELU, O.IDENTITY):
+            f = O.glu_fwd(g, u, act=kind, fmt=fmt, mode=mode)
+            b = O.glu_bwd(g, u, d, act=kind, fmt=fmt, mode=mode)
+            assert all(np.array_equal(f[k], ref_f[k]) for k in f), (kind, fmt)
+            assert all(np.array_equal(b[k], ref_b[k]) for k in b), (kind, fmt)
+
+
+def test_relu_bf16_steps_is_one_rounding():
+    # relu(g) of a bf16 gate is already bf16, so the bf16-step value is the
+    # bf16 rounding of the exact product
+    g, u, _ = _spiky_inputs(32, 64, 43)
+    h = O.glu_fwd(g, u, act=O.RELU | O.BF16_STEPS, fmt=O.FP32)["out"]
+    ref = (torch.relu(torch.from_numpy(_bf16_f32(g))) * torch.from_numpy(_bf16_f32(u))).to(torch.bfloat16)
+    assert np.array_equal(h, ref.float().numpy())
