@@ -82,12 +82,13 @@ static const double GELU_A = 0.044715;
  *   keeps full relative precision in the negative tail where 1 + tanh(y)
  *   cancels.
  *   ReLU and the identity (further gated activations, "Add swiglu + MXFP8
- *   fused CuTe DSL kernel", Follow-ups): relu(x) = x for x > 0, else +0, so
- *   that h = relu(g) * up is a signed zero with the sign of up where g <= 0;
+ *   fused CuTe DSL kernel", Follow-ups): relu(x) = +0 for x <= 0, else x
+ *   (so a NaN stays NaN), and h = relu(g) * up is a signed zero with the
+ *   sign of up where g <= 0;
  *   identity(x) = x.  With bf16 operands both products are exact in double
  *   and in fp32. */
 double orc_act(int act, double x) {
-  if (act == ORC_RELU) return x > 0.0 ? x : 0.0; /* ReLU: +0 for x <= 0 */
+  if (act == ORC_RELU) return x <= 0.0 ? 0.0 : x; /* ReLU: +0 for x <= 0, NaN kept */
   if (act == ORC_IDENTITY) return x;
   if (act == ORC_SILU) return x * sigmoid(x);
   double y = GELU_C * (x + GELU_A * x * x * x);
@@ -103,8 +104,9 @@ double orc_act(int act, double x) {
  *  0.5(1 + tanh y) + 0.5 x (1 - tanh^2 y) y').  1 - s is taken as
  *  sigmoid(-t), the same quantity without cancellation. */
 double orc_act_grad(int act, double x) {
-  /* ReLU: 1 for x > 0, else 0 (the derivative at 0 taken as 0); identity 1 */
-  if (act == ORC_RELU) return x > 0.0 ? 1.0 : 0.0;
+  /* ReLU: 0 for x <= 0 (the derivative at 0 taken as 0), else 1 (a NaN
+   * gate too, as its gradient passes dY through); identity 1 */
+  if (act == ORC_RELU) return x <= 0.0 ? 0.0 : 1.0;
   if (act == ORC_IDENTITY) return 1.0;
   if (act == ORC_SILU) {
     double s = sigmoid(x), one_minus_s = sigmoid(-x);

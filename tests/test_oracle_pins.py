@@ -686,12 +686,14 @@ def _bf16_f32(b):
 
 def test_relu_identity_vs_torch_float64():
     x = torch.linspace(-5, 5, 10001, dtype=torch.float64)
-    x = torch.cat([x, torch.tensor([0.0, -0.0, 1e-300, -1e-300, 3e38, -3e38], dtype=torch.float64)])
-    assert np.array_equal(O.act(O.RELU, x.numpy()), torch.relu(x).numpy())
-    assert np.array_equal(O.act(O.IDENTITY, x.numpy()), x.numpy())
+    x = torch.cat([x, torch.tensor([0.0, -0.0, 1e-300, -1e-300, 3e38, -3e38, math.inf, -math.inf, math.nan],
+                                   dtype=torch.float64)])
+    # NaN kept, as torch.relu keeps it
+    assert np.array_equal(O.act(O.RELU, x.numpy()), torch.relu(x).numpy(), equal_nan=True)
+    assert np.array_equal(O.act(O.IDENTITY, x.numpy()), x.numpy(), equal_nan=True)
     t = x.clone().requires_grad_(True)
     torch.relu(t).sum().backward()
-    assert np.array_equal(O.act_grad(O.RELU, x.numpy()), t.grad.numpy())
+    assert np.array_equal(O.act_grad(O.RELU, x.numpy()), t.grad.numpy())  # 1 at NaN: dY passes
     assert np.all(O.act_grad(O.IDENTITY, x.numpy()) == 1.0)
     # relu is +0 (not -0) at and below zero: h then takes the sign of up
     assert all(math.copysign(1, v) == 1 for v in O.act(O.RELU, [-2.0, -0.0, 0.0]))
