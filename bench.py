@@ -496,6 +496,16 @@ def sweep(path: str):
         o = f(None, None)
         record("swiglu_131072_mxfp8_128x4", direction, mode, "mxfp8", "silu", M5, N5,
                lambda s, f=f, o=o: f(s, o))
+    # the exact-product gates (ReLU, identity) on the same shape
+    for act, name in ((G.ACT_RELU, "reglu_131072"), (G.ACT_IDENTITY, "bilinear_131072")):
+        for direction, mode in (("fwd", 1), ("fwd", 3), ("bwd", 1), ("bwd", 3)):
+            f = lambda s, o, dr=direction, m=mode, a=act: (
+                G.fwd(x["gate"], x["up"], act=a, mode=m, out=o, stream=s) if dr == "fwd" else
+                G.bwd(x["gate"], x["up"], x["dy"], act=a, mode=m, out=o, stream=s))
+            o = f(None, None)
+            record(name, direction, mode, "mxfp8", "relu" if act == G.ACT_RELU else "identity", M5, N5,
+                   lambda s, f=f, o=o: f(s, o))
+            del o
     for mode in (1, 3):
         o = G.fwd(x["gate"], x["up"], act=G.ACT_SILU | G.ACT_BF16_STEPS, mode=mode)
         record("swiglu_131072_bf16_steps", "fwd", mode, "mxfp8", "silu", M5, N5,

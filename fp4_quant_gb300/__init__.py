@@ -21,11 +21,11 @@ __all__ = [
     "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
     "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
-    "ACT_SILU", "ACT_GELU_TANH", "ACT_BF16_STEPS", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
+    "ACT_SILU", "ACT_GELU_TANH", "ACT_RELU", "ACT_IDENTITY", "ACT_BF16_STEPS", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
     "MODE_ROW", "MODE_COL", "MODE_BOTH", "LAYOUT_SPLIT", "LAYOUT_INTERLEAVED",
 ]
 
-ACT_SILU, ACT_GELU_TANH = 0, 1
+ACT_SILU, ACT_GELU_TANH, ACT_RELU, ACT_IDENTITY = 0, 1, 2, 3  # SiLU, GELU (tanh), ReLU (ReGLU), identity (bilinear)
 ACT_BF16_STEPS = 16  # OR-ed into act (forward): the eager bf16 values RN_bf16(RN_bf16(act(g)) * up)
 FMT_MXFP8, FMT_NVFP4, FMT_BF16, FMT_FP32, FMT_MXFP8_128X4 = 0, 1, 2, 3, 4
 MODE_ROW, MODE_COL, MODE_BOTH = 1, 2, 3

@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
         }
       }
       const float d = o ? Bracket<ACT>::kDUp
-                        : (colj ? (((near_cols >> lane) & 1u) ? Bracket<ACT>::kDGate : 0x1p-18f)
-                                : dgate_bracket(nrow));
+                        : (colj ? (((near_cols >> lane) & 1u) ? Bracket<ACT>::kDGate : Bracket<ACT>::kDGateFar)
+                                : dgate_width<ACT>(nrow));
       // element e of the block: (r0 + dr e, cb + dc e)
       const int64_t r0 = colj ? row0 : row0 + lane, cb = colj ? c0 + lane : c0;
       const int dr = colj ? 1 : 0, dc = colj ? 0 : 1;
@@ -307,7 +307,12 @@ cudaError_t by_layout(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo
 }  // namespace
 
 cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
-  return a.act == GLU_ACT_SILU ? by_layout<0, GLU_MODE_BOTH>(a, s, d) : by_layout<1, GLU_MODE_BOTH>(a, s, d);
+  switch (a.act) {
+    case GLU_ACT_SILU: return by_layout<0, GLU_MODE_BOTH>(a, s, d);
+    case GLU_ACT_GELU_TANH: return by_layout<1, GLU_MODE_BOTH>(a, s, d);
+    case GLU_ACT_RELU: return by_layout<2, GLU_MODE_BOTH>(a, s, d);
+    default: return by_layout<3, GLU_MODE_BOTH>(a, s, d);
+  }
 }
 
 cudaError_t read_err_bwd_cb(uint32_t* v, bool clear) {

@@ -159,8 +159,8 @@ __device__ __forceinline__ float bf(uint32_t b16) { return __uint_as_float(b16 <
 // Gates at or below the fast path's lower limit (raw bf16 patterns, the
 // sign bit set): SiLU -64, GELU -6.
 template <int ACT>
-struct FastRangeAcc {
-  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC280u : 0xC0C0u;
+struct FastRangeAcc {  // exact-product gates: no limit (above every pattern)
+  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u : ACT == 0 ? 0xC280u : 0xC0C0u;
 };
 template <int ACT>
 __device__ __forceinline__ bool range_ok(uint32_t vmax) {
@@ -179,6 +179,8 @@ template <int ACT>
 __device__ __forceinline__ float exact_bwd(const float4* hot, uint32_t gb, uint32_t ub, uint32_t db,
                                            int which) {
   const float g = bf(gb), u = bf(ub), d = bf(db);
+  if constexpr (kExactAct<ACT>)
+    return which == 0 ? __fmul_rn(d, __fmul_rn(u, xact_grad<ACT>(g))) : __fmul_rn(d, xact<ACT>(g));
   const int k = hot != nullptr ? hot_index<kHotLo, kHotBin>(gb) : -1;
   if (k >= 0) {
     const float4 e = hot[k];

@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
   const int64_t units = p.n_rt * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  if (hot_for(MODE)) load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+  if (hot_for(MODE) && !kExactAct<ACT>)
+    load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
               x[i] = exact_bwd<ACT>(hot, sv.g16(lane, e0 + i), sv.u16(lane, e0 + i), sv.d16(lane, e0 + i), which);
           };
         };
-        const float dgd = 2.0f * dgate_bracket(nrow), dud = Bracket<ACT>::kNv;
+        const float dgd = Bracket<ACT>::kExact ? Bracket<ACT>::kNv : 2.0f * dgate_bracket(nrow), dud = Bracket<ACT>::kNv;
         uint32_t c[8], sc[4];
         sc[0] = nv_block<0>(dg, c[0], c[1], dgd, ex(0), ex8(0));
         sc[1] = nv_block<16>(dg, c[2], c[3], dgd, ex(0), ex8(0));
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
 
       // ---- the lane's two blocks
       uint32_t qg[8], qu[8];
-      const uint32_t sg = mx_block(dg, qg, dgate_bracket(nrow), [&](int e) {
+      const uint32_t sg = mx_block(dg, qg, dgate_width<ACT>(nrow), [&](int e) {
         return exact_bwd<ACT>(hot, sv.g16(at_r(e), at_c(e)), sv.u16(at_r(e), at_c(e)), sv.d16(at_r(e), at_c(e)), 0);
       });
       const uint32_t su = mx_block(du, qu, Bracket<ACT>::kDUp, [&](int e) {
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
           return exact_bwd<ACT>(hot, sv.g16(at_r(e), at_c(e)), sv.u16(at_r(e), at_c(e)), sv.d16(at_r(e), at_c(e)), which);
         };
         uint32_t qg[4], qu[4];
-        const uint32_t sg = mx_half(dg, qg, dgate_bracket(nmin), [&](int e) { return ex(e, 0); },
+        const uint32_t sg = mx_half(dg, qg, dgate_width<ACT>(nmin), [&](int e) { return ex(e, 0); },
                                     [&](float (&x)[16]) {
 #pragma unroll 1
                                       for (int e = 0; e < 16; ++e) {
@@ -472,9 +473,17 @@ cudaError_t by_mode(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& 
 }  // namespace
 
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
-  cudaError_t e = a.mode == GLU_MODE_BOTH ? launch_bwd_cb(a, s, d)
-                  : a.act == GLU_ACT_SILU  ? by_mode<0>(a, s, d)
-                                           : by_mode<1>(a, s, d);
+  cudaError_t e;
+  if (a.mode == GLU_MODE_BOTH) {
+    e = launch_bwd_cb(a, s, d);
+  } else {
+    switch (a.act) {
+      case GLU_ACT_SILU: e = by_mode<0>(a, s, d); break;
+      case GLU_ACT_GELU_TANH: e = by_mode<1>(a, s, d); break;
+      case GLU_ACT_RELU: e = by_mode<2>(a, s, d); break;
+      default: e = by_mode<3>(a, s, d); break;
+    }
+  }
   if (e == cudaSuccess && a.fmt == GLU_FMT_NVFP4_E2M1)  // scale padding (rows to 128, columns to 4)
     e = launch_scale_pad(static_cast<uint8_t*>(a.s_row), a.M, 2 * a.N / 16, s);
   if (e == cudaSuccess && a.fmt == GLU_FMT_MXFP8_E4M3_128X4) {

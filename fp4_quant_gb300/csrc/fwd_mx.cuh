@@ -153,26 +153,35 @@ __device__ __forceinline__ uint8_t* nv_scale_at(const FwdP& p, int64_t rt, int64
 constexpr int kBoxBytes = 4096;
 __device__ __forceinline__ int swz(int r, int chunk) { return r * 128 + 16 * (chunk ^ (r & 7)); }
 
-// ACT is the activation (bit 0) plus 16 for the bf16-step values.  The
-// rounding-test half-widths: the fast form's for fp32 values; for bf16-step
-// values, which are exact, none for MXFP8 (scaling by 2^-e is exact) and the
-// roundings of 1/6, 1/s and the bracket products for NVFP4.
+// ACT is the activation (ACT & 15) plus 16 for the bf16-step values.  The
+// rounding-test half-widths: the fast form's for fp32 values; for exact
+// values (bf16 steps, or the exact-product gates), none for MXFP8 (scaling
+// by 2^-e is exact) and the roundings of 1/6, 1/s and the bracket products
+// for NVFP4.
 template <int ACT>
-constexpr float kDQuant = (ACT & 16) ? 0.0f : Bracket<ACT & 1>::kAct;
+constexpr bool kExactVals = (ACT & 16) || kExactAct<ACT>;
 template <int ACT>
-constexpr float kDNv = (ACT & 16) ? 0x1p-21f : Bracket<ACT & 1>::kNv;
+constexpr float kDQuant = kExactVals<ACT> ? 0.0f : Bracket<ACT & 1>::kAct;
+template <int ACT>
+constexpr float kDNv = kExactVals<ACT> ? 0x1p-21f : Bracket<ACT & 1>::kNv;
 
-// Values of a pair from the fast form (fp32, or the bf16 steps; a pair
-// whose bf16 rounding of act(g) is undecided takes exact values).
-template <int ACT, int MODE>
-__device__ __forceinline__ float2 fast_vals(float2 g, float2 u, const float2* hot) {
-  if (!(ACT & 16)) return fast_h2<ACT & 1>(g, u);
-  bool bad;
-  float2 h = fast_h2_bf16<ACT & 1>(g, u, Bracket<ACT & 1>::kAct, bad);
-  if (bad) {
-    h.x = exact_h<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, g.x, u.x);
-    h.y = exact_h<ACT, hot_lo_for(MODE), hot_bin_for(MODE)>(hot, g.y, u.y);
+// Values of a pair (elements e, e + 1 of a block) from the fast form: fp32,
+// or the bf16 steps, where a pair whose bf16 rounding of act(g) is undecided
+// sets its two bits in `bad` (fix_range then gives them exact values, one
+// copy of that code outside the unrolled loops).
+template <int ACT>
+__device__ __forceinline__ float2 fast_vals(float2 g, float2 u, uint32_t& bad, int e) {
+  if constexpr (kExactAct<ACT>) {
+    const float2 h = mul2(make_float2(xact<ACT>(g.x), xact<ACT>(g.y)), u);  // exact products
+    if (!(ACT & 16)) return h;
+    uint32_t hb;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb) : "f"(h.y), "f"(h.x));
+    return make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
   }
+  if (!(ACT & 16)) return fast_h2<ACT & 1>(g, u);
+  bool b;
+  const float2 h = fast_h2_bf16<ACT & 1>(g, u, Bracket<ACT & 1>::kAct, b);
+  bad |= uint32_t(b) * (3u << e);
   return h;
 }
 
@@ -231,13 +240,13 @@ __device__ __forceinline__ uint32_t stage_pair(const uint8_t* st, int w, int r, 
   }
 }
 
-// Gates outside the fast range (rare): exact values for those elements of
-// this lane's row (ROW) or column (!ROW) of the sub-tile, from the raw bits
-// still held in the stage.
+// Gates outside the fast range, and the elements flagged in `extra` (rare):
+// exact values for those elements of this lane's row (ROW) or column (!ROW)
+// of the sub-tile, from the raw bits still held in the stage.
 template <int ACT, int MODE, int LAYOUT, int UP_BOX, bool ROW>
 __device__ __forceinline__ void fix_range(float (&v)[32], const uint8_t* st, const float2* hot, int w,
-                                          int lane) {
-  uint32_t emask = 0;
+                                          int lane, uint32_t extra) {
+  uint32_t emask = extra;
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const uint32_t x = ROW ? stage_pair<LAYOUT, UP_BOX>(st, w, lane, e) : stage_pair<LAYOUT, UP_BOX>(st, w, e, lane);
@@ -321,7 +330,8 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   const int64_t units = row_walk(MODE) ? p.ntiles : p.n_rs * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, (ACT & 1) == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
+  if (!kExactAct<ACT>)
+    load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, (ACT & 1) == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
   // NVFP4 global encode scale 2688 / amax (448 * 6 over the tensor amax,
   // IEEE division); 1 without an amax, or for a zero or non-finite one
   float nv_gs = 1.0f;
@@ -434,7 +444,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       // ---- column `lane` of the warp's box: 32 rows, read straight from the
       // swizzled stage (for a fixed row the warp reads one 128-byte line)
       float v[32];
-      uint32_t gmax = 0;
+      uint32_t gmax = 0, bad = 0;  // gate range; undecided bf16-step pairs
       if (work) {
         const uint8_t* st_base = stages + s * kStageBytes;
 #pragma unroll
@@ -462,11 +472,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             u2 = make_float2(bf16_hi(pa), bf16_hi(pb));
           }
           gmax = vmax_u16x2(gmax, g16a | (g16b << 16));
-          const float2 h2 = fast_vals<ACT, MODE>(g2, u2, hot);
+          const float2 h2 = fast_vals<ACT>(g2, u2, bad, r);
           v[r] = h2.x;
           v[r + 1] = h2.y;
         }
-        if (!fast_range_ok<ACT & 1>(gmax)) fix_range<ACT, MODE, LAYOUT, kUpBox, false>(v, st_base, hot, w, lane);
+        if (!fast_range_ok<ACT & 15>(gmax) || bad != 0u)
+          fix_range<ACT, MODE, LAYOUT, kUpBox, false>(v, st_base, hot, w, lane, bad);
       }
       release(s, k);
       if (!active) continue;
@@ -488,6 +499,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // free the stage; fast activation in pairs
     float h[32];
     uint32_t gmax = 0;  // running max of the raw gate patterns (range check)
+    uint32_t bad = 0;   // undecided bf16-step pairs
     if (work) {
       const uint8_t* st_base = stages + s * kStageBytes;
 #pragma unroll
@@ -525,12 +537,13 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
             u2 = make_float2(bf16_hi(p0), bf16_hi(p1));
             gmax = vmax_u16x2(gmax, (p0 & 0xFFFFu) | (p1 << 16));
           }
-          const float2 h2 = fast_vals<ACT, MODE>(g2, u2, hot);
+          const float2 h2 = fast_vals<ACT>(g2, u2, bad, 16 * half + 2 * j);
           h[16 * half + 2 * j] = h2.x;
           h[16 * half + 2 * j + 1] = h2.y;
         }
       }
-      if (!fast_range_ok<ACT & 1>(gmax)) fix_range<ACT, MODE, LAYOUT, kUpBox, true>(h, st_base, hot, w, lane);
+      if (!fast_range_ok<ACT & 15>(gmax) || bad != 0u)
+        fix_range<ACT, MODE, LAYOUT, kUpBox, true>(h, st_base, hot, w, lane, bad);
     }
     // (both: the stage is kept for the transpose below)
     if (MODE != GLU_MODE_BOTH || !work) release(s, k);

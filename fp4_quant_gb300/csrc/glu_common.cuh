@@ -100,6 +100,28 @@ __host__ __device__ inline ScaleLayout scale_layout(int64_t cols, bool swz) {
   return ScaleLayout{cols, (cols + 3) / 4 * 4, swz ? 1 : 0};
 }
 
+// ------------------------------------------------- exact-product gates --
+// ACT & 15 is the activation: 0 SiLU, 1 GELU (tanh), 2 ReLU (ReGLU), 3 the
+// identity (bilinear GLU); ACT & 16 asks for the bf16-step values.  ReLU and
+// the identity are exact in fp32 for a bf16 gate (relu(g) = g for g > 0,
+// else +0), and their products with a bf16 operand are exact (8 x 8
+// significant bits), so every value of theirs is the rounded exact value
+// with no test at all.  relu(NaN) is NaN (g <= 0 is false), relu' is 0 for
+// g <= 0 and 1 elsewhere.  dGate = dY (up act'(g)): the exact value of
+// dY up act'(g) rounded once, which is a signed zero where act' = 0 even when
+// dY up would overflow fp32.
+template <int ACT>
+constexpr bool kExactAct = (ACT & 15) >= 2;
+
+template <int ACT>
+__device__ __forceinline__ float xact(float g) {
+  return (ACT & 15) == 2 ? (g <= 0.0f ? 0.0f : g) : g;
+}
+template <int ACT>
+__device__ __forceinline__ float xact_grad(float g) {
+  return (ACT & 15) == 2 ? (g <= 0.0f ? 0.0f : 1.0f) : 1.0f;
+}
+
 // ---------------------------------------------------------------- tables --
 
 // Table slot of a bf16 pattern (16 bits): in-range magnitudes map to
@@ -273,6 +295,10 @@ __device__ __forceinline__ float exact_act_mul_hot(const float2* hot, float g, f
 // flag: act(g) * u rounded once to fp32, or RN_bf16(RN_bf16(act(g)) * u).
 template <int ACT, uint32_t LO = kHotExpLo, uint32_t BIN = kHotBinades>
 __device__ __forceinline__ float exact_h(const float2* hot, float g, float u) {
+  if constexpr (kExactAct<ACT>) {
+    const float h = __fmul_rn(xact<ACT>(g), u);  // act(g) is bf16 already
+    return (ACT & 16) ? bf16_rn(h) : h;
+  }
   constexpr int A = ACT & 1;
   if (!(ACT & 16)) return exact_act_mul_hot<A, LO, BIN>(hot, g, u);
   const int k = hot_index<LO, BIN>(__float_as_uint(g) >> 16);
@@ -385,8 +411,8 @@ __device__ __forceinline__ float2 fast_h2_bf16(float2 g, float2 u, float d, bool
 // patterns reaches kNegLimit exactly when some gate is at or below the fast
 // path's lower limit.  Positive gates never reach it.
 template <int ACT>
-struct FastRange {
-  static constexpr uint32_t kNegLimit = ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
+struct FastRange {  // exact-product gates: no limit (above every pattern)
+  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u : ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
 };
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
 template <int ACT>
@@ -412,6 +438,14 @@ __device__ __forceinline__ bool fast_range_ok(uint32_t vmax) {
 template <int ACT>
 __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& dg, float2& du,
                                           float2& n) {
+  if constexpr (kExactAct<ACT>) {
+    // exact: dUp = dY act(g) and dGate = dY (up act'(g)); act' is 0 or 1, so
+    // up act'(g) is exact and dY up never overflows where act' = 0
+    dg = mul2(d, mul2(u, make_float2(xact_grad<ACT>(g.x), xact_grad<ACT>(g.y))));
+    du = mul2(d, make_float2(xact<ACT>(g.x), xact<ACT>(g.y)));
+    n = splat2(__int_as_float(0x7F800000));  // no zero of act' to widen for
+    return;
+  }
   float2 E, t1;
   if (ACT == 0) {
     const float2 th = mul2(g, splat2(-0x1.7154p+0f));            // exact
@@ -445,13 +479,17 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 //   dGate = dY up act'(g): 6.7 units, plus the error of E (below 3.3
 //                          units) times 1.1 / |N| near the zero of act'
 //                          -> per block from the smallest |N| (dgate_bracket)
+// Exact-product gates (ReLU, identity) need no width for their values;
+// NVFP4 keeps 2^-21 for the roundings of 1/6, 1/s and the bracket products.
 template <int ACT> struct Bracket {
-  static constexpr float kAct = ACT == 0 ? 0x1p-20f : 0x1p-18f;
-  static constexpr float kDUp = ACT == 0 ? 0x1p-20f : 0x1p-18f;
-  static constexpr float kDGate = 0x1p-14f;  // the widest dgate_bracket step
+  static constexpr bool kExact = kExactAct<ACT>;
+  static constexpr float kAct = kExact ? 0.0f : ACT == 0 ? 0x1p-20f : 0x1p-18f;
+  static constexpr float kDUp = kAct;
+  static constexpr float kDGate = kExact ? 0.0f : 0x1p-14f;     // the widest dgate_bracket step
+  static constexpr float kDGateFar = kExact ? 0.0f : 0x1p-18f;  // |N| >= 1/8
   // NVFP4: the activation's width plus the roundings of 1/6, 1/s and the
   // bracket products (4 units of 2^-24 at most)
-  static constexpr float kNv = 2.0f * kAct;
+  static constexpr float kNv = kExact ? 0x1p-21f : 2.0f * kAct;
 };
 
 // Half-width of the rounding test of a dGate block whose elements' |N| (see
@@ -466,6 +504,12 @@ __device__ __forceinline__ float dgate_bracket(float nmin) {
        : nmin >= 0x1p-5f ? 0x1p-16f
        : nmin >= 0x1p-6f ? 0x1p-15f
                           : 0x1p-14f;
+}
+
+// dgate_bracket for the activation (zero for the exact-product gates).
+template <int ACT>
+__device__ __forceinline__ float dgate_width(float nmin) {
+  return Bracket<ACT>::kExact ? 0.0f : dgate_bracket(nmin);
 }
 
 // min |x| of three values (three-input min, sm_100+; NaNs ignored).

@@ -15,7 +15,10 @@
  *     - BF16 or FP32: the unquantised activation ("perf: tile wide GeGLU rows
  *       on SM103", Summary; FP32 is the checking mode).
  *   act is SiLU (x * sigmoid(x)) or GELU with the tanh approximation
- *   (0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))).
+ *   (0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))); ABI 3 adds ReLU
+ *   (ReGLU) and the identity (bilinear GLU), the further gated activations
+ *   that "Add swiglu + MXFP8 fused CuTe DSL kernel", Follow-ups (item 1)
+ *   leaves open.
  * The operation (backward), "Add swiglu + MXFP8 fused CuTe DSL kernel", API:
  *   dGate = dY * up * act'(gate),  dUp = dY * act(gate), emitted as one
  *   logical [M, 2N] matrix [dGate | dUp] in the same formats.
@@ -50,7 +53,7 @@
 extern "C" {
 #endif
 
-#define GLU_QUANT_ABI_VERSION 2
+#define GLU_QUANT_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define GLU_API __attribute__((visibility("default")))
@@ -76,6 +79,14 @@ extern "C" {
 enum glu_act {
   GLU_ACT_SILU = 0,
   GLU_ACT_GELU_TANH = 1,
+  /* ABI 3: relu(x) = x for x > 0, else +0 (relu' = 1 for x > 0, else 0; a
+   * NaN gate stays NaN), and the identity act(x) = x.  With bf16 operands
+   * every value of theirs (h, dGate, dUp, the bf16 steps) is an exact
+   * product rounded once, so their outputs match the rounded exact values
+   * with no tolerance; where relu(gate) is +0, h and dUp are zeros with the
+   * sign of up and dY, and dGate a zero with the sign of dY * up. */
+  GLU_ACT_RELU = 2,
+  GLU_ACT_IDENTITY = 3,
   /* OR-ed into act, forward only (ABI 2): the eager bf16 values
    * h = RN_bf16(RN_bf16(act(gate)) * up) in place of act(gate) * up in
    * fp32 ("Add swiglu + MXFP8 fused CuTe DSL kernel", Numerics and tests:

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert G.glu_quant_abi_version() == 2
+    assert G.glu_quant_abi_version() == 3
     for st in (0, -1, -2, -3, -4, -5):
         assert G.glu_quant_status_str(st) != "unknown status"
     assert G.glu_quant_status_str(7) == "unknown status"
@@ -61,8 +61,8 @@ def _no_gpu():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(act=2), G.GLU_EINVAL),
-    (dict(act=18), G.GLU_EINVAL),
+    (dict(act=4), G.GLU_EINVAL),
+    (dict(act=20), G.GLU_EINVAL),
     (dict(act=32), G.GLU_EINVAL),
     (dict(fmt=5), G.GLU_EINVAL),
     (dict(mode=0), G.GLU_EINVAL),

@@ -23,7 +23,9 @@ if not torch.cuda.is_available():
 import fp4_quant_gb300 as G  # noqa: E402  (raises if the library is missing)
 
 DEV = torch.device("cuda:0")
-ACTS = [(G.ACT_SILU, O.SILU), (G.ACT_GELU_TANH, O.GELU_TANH)]
+ACTS = [(G.ACT_SILU, O.SILU), (G.ACT_GELU_TANH, O.GELU_TANH), (G.ACT_RELU, O.RELU),
+        (G.ACT_IDENTITY, O.IDENTITY)]
+ACT_IDS = ["silu", "gelu", "relu", "identity"]
 MODES = [G.MODE_ROW, G.MODE_COL, G.MODE_BOTH]
 
 
@@ -81,7 +83,7 @@ def check(gpu, ref, fmt, mode, M, W, what):
 
 # ------------------------------------------------------------ small, ragged --
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 def test_mx_fwd_small(act, mode, layout):
@@ -92,7 +94,7 @@ def test_mx_fwd_small(act, mode, layout):
     check(gpu, ref, G.FMT_MXFP8, mode, M, N, "fwd")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 def test_mx_bwd_small(act, mode, layout):
@@ -128,7 +130,7 @@ def check_mx_128x4(gpu, ref_plain, mode, M, W, what):
     return st
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("mode", MODES, ids=["row", "col", "both"])
 @pytest.mark.parametrize("direction", ["fwd", "bwd"])
 def test_mx_128x4_scales(act, mode, direction):
@@ -157,7 +159,7 @@ def test_mx_128x4_scales(act, mode, direction):
     check_mx_128x4({k: host(v) for k, v in out.items()}, ref, mode, M, W, direction)
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 @pytest.mark.parametrize("shape", [(200, 1296), (128, 64), (1, 16)], ids=["ragged", "one_tile", "tiny"])
 def test_nvfp4_small(act, layout, shape):
@@ -167,7 +169,7 @@ def test_nvfp4_small(act, layout, shape):
     check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, N, "nvfp4")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("fmt", [G.FMT_BF16, G.FMT_FP32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 @pytest.mark.parametrize("N", [1024, 1001], ids=["vec", "ragged"])
@@ -230,7 +232,7 @@ def _special_inputs(M, N, seed):
     return g.contiguous(), u.contiguous()
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 @pytest.mark.parametrize("amax", ["tensor", 100.0, 0.75], ids=["tensor_amax", "amax_100", "amax_small"])
 def test_nvfp4_global_scale(act, layout, amax):
@@ -259,7 +261,7 @@ def test_nvfp4_global_scale(act, layout, amax):
                 M, N, st, "nvfp4_gs")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 @pytest.mark.parametrize("shape", [(200, 416), (96, 400), (1, 16)], ids=["ragged", "half_subtile", "tiny"])
 def test_nvfp4_bwd(act, layout, shape):
@@ -273,7 +275,7 @@ def test_nvfp4_bwd(act, layout, shape):
           G.MODE_ROW, M, 2 * N, "nvfp4_bwd")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
                          ids=["fp32", "bf16", "mxfp8", "nvfp4"])
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
@@ -290,7 +292,7 @@ def test_bf16_steps_fwd(act, fmt, layout):
         assert np.array_equal(gpu["out"], ref["out"])
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 def test_every_bf16_gate_bf16_steps(act):
     """All 65536 gate patterns through the bf16-step values (MXFP8 both and
     the BF16 output), so that every gate's bf16 rounding of act(g) is
@@ -307,7 +309,7 @@ def test_every_bf16_gate_bf16_steps(act):
     check(gpu, ref, G.FMT_BF16, G.MODE_ROW, M, N, "all_gates_bf16_steps_out")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_BF16, G.FMT_MXFP8, G.FMT_NVFP4],
                          ids=["fp32", "bf16", "mxfp8", "nvfp4"])
 def test_special_values_fwd(act, fmt):
@@ -318,7 +320,7 @@ def test_special_values_fwd(act, fmt):
     check(gpu, ref, fmt, mode, M, N, "special")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("fmt", [G.FMT_FP32, G.FMT_MXFP8], ids=["fp32", "mxfp8"])
 def test_special_values_bwd(act, fmt):
     M, N = 64, 256
@@ -331,7 +333,7 @@ def test_special_values_bwd(act, fmt):
     check(gpu, ref, fmt, mode, M, 2 * N, "special_bwd")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("direction", ["fwd", "bwd"])
 def test_every_bf16_gate(act, direction):
     """All 65536 bf16 gate patterns (NaN, infinities, subnormals, the run
@@ -352,7 +354,7 @@ def test_every_bf16_gate(act, direction):
         check(gpu, ref, G.FMT_MXFP8, G.MODE_BOTH, M, 2 * N, "all_gates_bwd")
 
 
-@pytest.mark.parametrize("act", ACTS, ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", ACTS, ids=ACT_IDS)
 @pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
 def test_every_bf16_gate_nvfp4(act, layout):
     """All 65536 bf16 gate patterns through the NVFP4 forward (shuffled, up
@@ -365,6 +367,51 @@ def test_every_bf16_gate_nvfp4(act, layout):
     u[::5] *= 1e-3
     gpu, ref = run_fwd(g, u, act[0], G.FMT_NVFP4, G.MODE_ROW, layout)
     check(gpu, ref, G.FMT_NVFP4, G.MODE_ROW, M, N, "all_gates_nvfp4")
+
+
+def _bits_equal(gpu, ref, fmt):
+    """Every output byte equal (the NVFP4 codes and scales are "out" and
+    "s_nvfp4" on the oracle's side)."""
+    if fmt == G.FMT_NVFP4:
+        pairs = [("q_row", "out"), ("s_row", "s_nvfp4")]
+    elif fmt == G.FMT_MXFP8:
+        pairs = [(k, k) for k in ("q_row", "s_row", "q_col", "s_col") if gpu.get(k) is not None]
+    else:
+        pairs = [("out", "out")]
+    assert pairs
+    for kg, kr in pairs:
+        a, b = np.ascontiguousarray(gpu[kg]), np.ascontiguousarray(ref[kr])
+        assert a.nbytes == b.nbytes and np.array_equal(a.reshape(-1).view(np.uint8),
+                                                       b.reshape(-1).view(np.uint8)), (kg, fmt)
+
+
+@pytest.mark.parametrize("act", [G.ACT_RELU, G.ACT_IDENTITY], ids=["relu", "identity"])
+@pytest.mark.parametrize("steps", [0, G.ACT_BF16_STEPS], ids=["fp32", "bf16_steps"])
+@pytest.mark.parametrize("layout", [G.LAYOUT_SPLIT, G.LAYOUT_INTERLEAVED], ids=["split", "inter"])
+def test_exact_gates_bit_for_bit(act, steps, layout):
+    """ReLU and identity gates: every value is an exact product rounded once,
+    so every output byte (codes, scales, signed zeros, fp32/bf16 bits)
+    equals the oracle's, with no tolerance window; ragged shapes, +-0 and
+    spiked operands, forward (every format) and backward (MXFP8 row, col,
+    both; NVFP4; FP32)."""
+    M, N = 160, 800
+    g, u, d = _randn(M, N, 301, 2.0), _randn(M, N, 302), _randn(M, N, 303)
+    g[::9, ::4] = 0.0
+    g[::13, 1::4] = -0.0
+    u[::7, ::6] = -0.0
+    g[::31, ::17] = 60.0
+    d[::5, ::11] = 0.0
+    a = act | steps
+    for fmt, mode in ((G.FMT_MXFP8, G.MODE_BOTH), (G.FMT_NVFP4, G.MODE_ROW), (G.FMT_FP32, G.MODE_ROW),
+                      (G.FMT_BF16, G.MODE_ROW)):
+        gpu, ref = run_fwd(g, u, a, fmt, mode, layout)
+        _bits_equal(gpu, ref, fmt)
+    if steps:
+        return
+    for fmt, mode in ((G.FMT_MXFP8, G.MODE_ROW), (G.FMT_MXFP8, G.MODE_COL), (G.FMT_MXFP8, G.MODE_BOTH),
+                      (G.FMT_NVFP4, G.MODE_ROW), (G.FMT_FP32, G.MODE_ROW)):
+        gpu, ref = run_bwd(g, u, d, act, fmt, mode, layout)
+        _bits_equal(gpu, ref, fmt)
 
 
 def test_exact_activation_blocks_on_gpu():
