@@ -7,10 +7,12 @@
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
 //   * one persistent CTA per SM with three groups of four warps (twelve
 //     warps, up to 168 registers per thread).  Tiles are 32 rows x 128
-//     columns of N, walked down the column strips (so that the CTAs working
-//     at once store neighbouring 32-byte pieces of the same [2N, M] code
-//     rows); each group has one 24 KB stage, filled by 2-D TMA loads of
-//     32-row boxes with 128-byte rows and the 128-byte swizzle;
+//     columns of N; a group takes units of four consecutive row tiles of one
+//     column strip (one tile where the row tiles do not come in fours), the
+//     units walked down the column strips (so that the CTAs working at once
+//     store neighbouring pieces of the same [2N, M] code rows); each group
+//     has one 24 KB stage, filled by 2-D TMA loads of 32-row boxes with
+//     128-byte rows and the 128-byte swizzle;
 //   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31:
 //     lane l copies row l of its gate, up and dY into registers, and the
 //     group's stage is released at once (the warp that releases it last
@@ -27,7 +29,14 @@
 //   * code boxes (32 x 32 bytes, 32-byte swizzle; box row c of a colwise box
 //     holds column c) go to the warp's 4 KB box area and leave through TMA
 //     stores: rowwise at columns c and N + c of [M, 2N], colwise at rows c
-//     and N + c of [2N, M].
+//     and N + c of [2N, M];
+//   * scale bytes are stored four at a time where the layout puts four
+//     side by side (one lane's byte per lane store scatters a 32-byte sector
+//     per lane): a lane's colwise scales of a unit's four row tiles are one
+//     word, and the four warps' rowwise scales of a row (its four column
+//     blocks) are gathered in shared memory and stored as one word by the
+//     warp that finishes the tile last.  Both the row-major and the 128x4
+//     scale layouts hold these four bytes contiguous and 4-byte aligned.
 #include <cstring>
 
 #include "bwd_common.cuh"
@@ -46,10 +55,20 @@ constexpr int kThreads = kGroups * kGroupWarps * 32;
 constexpr int kVBytes = 8192;  // per warp: dGate and dUp of the sub-tile
 constexpr int kTBytes = 4096;  // per warp: code boxes
 
+constexpr int kSup = 4;        // row tiles per unit
 using Ctl = RingCtl<kStages, kGroups>;
 
+// Rowwise scales of a tile, gathered across the group's warps: word [o][r]
+// holds the four column blocks of row r (byte w from warp w), two tiles in
+// flight per group; cnt counts the warps done with a slot (mod 4).
+struct Gather {
+  uint32_t rs[kGroups][2][2][32];
+  uint32_t cnt[kGroups][2];
+  int32_t sub[kGroups];  // next tile of the group's current unit
+};
+
 constexpr int kSmem = 1024 + kStages * kStageBytes + kGroups * kGroupWarps * (kVBytes + kTBytes) +
-                      int(sizeof(Ctl));
+                      int(sizeof(Ctl)) + int(sizeof(Gather));
 static_assert(kSmem <= 232448, "shared memory per CTA exceeds 227 KB");
 
 __device__ uint32_t g_err_bwd_cb;
@@ -63,10 +82,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
   uint8_t* Vbase = stages + kStages * kStageBytes;
   uint8_t* Tbase = Vbase + kGroups * kGroupWarps * kVBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(Tbase + kGroups * kGroupWarps * kTBytes);
+  Gather* gat = reinterpret_cast<Gather*>(ctl + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
-  const int64_t units = p.n_rt * p.n_ct;
+  const int sup = p.n_rt % kSup == 0 ? kSup : 1;  // row tiles per unit
+  const int64_t n_su = p.n_rt / sup;
+  const int64_t units = n_su * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
+  // four-byte scale stores: colwise with whole units, rowwise with whole
+  // column strips (every warp of a group active)
+  const bool word_col = sup == kSup, word_row = p.N % kTC == 0;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
@@ -78,16 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
     }
-    // down the column strips: tile t is (row t % n_rt, column strip t / n_rt)
+    // major[g]: the group's next unit (grid stride kGroups * G)
     for (int g = 0; g < kGroups; ++g) {
-      const TileWalk tw(blockIdx.x + g * G, kGroups * G, p.n_rt);
-      ctl->major[g] = tw.major;
-      ctl->minor[g] = tw.minor;
-      if (g == 0) {
-        ctl->n_minor = tw.n_minor;
-        ctl->dmaj = tw.dmaj;
-        ctl->dmin = tw.dmin;
-      }
+      gat->cnt[g][0] = gat->cnt[g][1] = 0;
+      gat->sub[g] = 0;
+      ctl->major[g] = blockIdx.x + g * G;
     }
     fence_barrier_init();
   }
@@ -98,18 +118,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
   auto issue = [&](int st, int g) {
     int64_t rt = 0, ct = 0;
     if (lane == 0) {
-      const int64_t major = ctl->major[g], minor = ctl->minor[g];
-      rt = minor;
-      ct = major;
+      const int64_t u = ctl->major[g];
+      const int sub = gat->sub[g];
+      // down the column strips: unit u is (row tiles sup * (u % n_su) ..,
+      // column strip u / n_su)
+      ct = u / n_su;
+      rt = (u - ct * n_su) * sup + sub;
       ctl->rt[st] = rt;
       ctl->ct[st] = ct;
-      int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
-      if (mn >= ctl->n_minor) {
-        mn -= ctl->n_minor;
-        ++mj;
+      if (sub + 1 < sup) {
+        gat->sub[g] = sub + 1;
+      } else {  // the unit's last tile: on to the group's next unit
+        gat->sub[g] = 0;
+        ctl->major[g] = u + kGroups * G;
       }
-      ctl->major[g] = mj;
-      ctl->minor[g] = mn;
       mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
     }
     rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
@@ -131,8 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
   uint8_t* const V = Vbase + warp * kVBytes;
   uint8_t* const T = Tbase + warp * kTBytes;
-  const int64_t n_g = my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0;
+  const int64_t n_g = (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0) * sup;  // tiles
   uint32_t nst = 0;  // bulk groups this warp has committed (colwise: selects the half)
+  uint32_t cw0 = 0, cw1 = 0;  // colwise scale bytes of the unit so far (dGate, dUp)
 
   if (w == 0) {
     for (int j = 0; j < kSlots; ++j)
@@ -249,10 +272,44 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_cb_kernel(const __grid_consta
             });
           });
       put_box(Q + (MODE == GLU_MODE_BOTH ? j : o) * kQBytes, lane, q);
-      if (colj)
-        st_byte(p.s_col + p.sl_col.at(o * p.N + c0 + lane, row0 / 32), sc);
-      else
-        st_byte(p.s_row + p.sl_row.at(row0 + lane, (o * p.N + c0) / 32), sc);
+      if (colj) {
+        if (!word_col) {
+          st_byte(p.s_col + p.sl_col.at(o * p.N + c0 + lane, row0 / 32), sc);
+        } else {
+          const uint32_t b = sc << (8 * int(rt & (kSup - 1)));
+          if (o) cw1 |= b;
+          else cw0 |= b;
+        }
+      } else {
+        if (!word_row)
+          st_byte(p.s_row + p.sl_row.at(row0 + lane, (o * p.N + c0) / 32), sc);
+        else
+          reinterpret_cast<volatile uint8_t*>(&gat->rs[grp][k & 1][o][lane])[w] = uint8_t(sc);
+      }
+    }
+    if (word_col && (rt & (kSup - 1)) == kSup - 1) {  // the unit's four row blocks of column c0 + lane
+      const int64_t rb = (row0 - (kSup - 1) * kTR) / 32;
+      st_stream(p.s_col + p.sl_col.at(c0 + lane, rb), cw0);
+      st_stream(p.s_col + p.sl_col.at(p.N + c0 + lane, rb), cw1);
+      cw0 = cw1 = 0;
+    }
+    if ((MODE & GLU_MODE_ROW) && word_row) {
+      // the warp that completes the tile stores row row0 + lane's four
+      // column blocks of each output (byte w from warp w)
+      __syncwarp();
+      uint32_t done = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        done = atomicAdd(&gat->cnt[grp][k & 1], 1u);
+      }
+      if ((__shfl_sync(0xFFFFFFFFu, done, 0) & 3u) == 3u) {
+        __threadfence_block();
+        const uint32_t r0w = reinterpret_cast<volatile uint32_t*>(&gat->rs[grp][k & 1][0][lane])[0];
+        const uint32_t r1w = reinterpret_cast<volatile uint32_t*>(&gat->rs[grp][k & 1][1][lane])[0];
+        const int64_t cb = ct * (kTC / 32);
+        st_stream(p.s_row + p.sl_row.at(row0 + lane, cb), r0w);
+        st_stream(p.s_row + p.sl_row.at(row0 + lane, p.N / 32 + cb), r1w);
+      }
     }
     fence_proxy_async();
     __syncwarp();
@@ -288,7 +345,7 @@ cudaError_t launch_t(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo&
   BwdP p;
   e = make_params(p, a);
   if (e != cudaSuccess) return e;
-  const int64_t units = p.n_rt * p.n_ct;
+  const int64_t units = (p.n_rt % kSup == 0 ? p.n_rt / kSup : p.n_rt) * p.n_ct;
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
