@@ -426,6 +426,21 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       if (j < n_g) issue(grp * kSlots + j, grp, j);
   }
 
+  // Colwise scales of a unit (byte i: row block rb0 + i of column c), stored
+  // as one word where the unit is whole and the layout holds its four bytes
+  // side by side and 4-byte aligned (one lane's byte per lane store would
+  // scatter a 32-byte sector per lane), else byte by byte.
+  uint32_t cw = 0;
+  auto flush_cs = [&](int64_t rb0, int64_t c) {
+    if (rb0 + kSuper <= p.n_rt && (p.sl_col.swz || (p.n_rt & (kSuper - 1)) == 0)) {
+      st_stream(p.s_col + p.sl_col.at(c, rb0), cw);
+    } else {
+      for (int i = 0; i < kSuper; ++i)
+        if (rb0 + i < p.n_rt) st_byte(p.s_col + p.sl_col.at(c, rb0 + i), (cw >> (8 * i)) & 0xFFu);
+    }
+    cw = 0;
+  };
+
   int64_t k = 0;
   bool failed = false;
   for (; k < n_g; ++k) {
@@ -489,9 +504,12 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         uint32_t q[8];
         const uint32_t sc = quant_block<ACT, MODE, LAYOUT, true>(v, q, p, hot, row0, c0, lane);
         put_qc(Qc, lane, j, q);
-        st_byte(p.s_col + p.sl_col.at(c0 + lane, row0 / 32), sc);
+        cw |= sc << (8 * j);
       }
-      if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+      if (j == kSuper - 1) {
+        store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+        flush_cs(rt - j, c0 + lane);
+      }
       continue;
     }
 
@@ -548,8 +566,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     // (both: the stage is kept for the transpose below)
     if (MODE != GLU_MODE_BOTH || !work) release(s, k);
     if (!work) {
-      if (MODE == GLU_MODE_BOTH && active && j == kSuper - 1)
+      if (MODE == GLU_MODE_BOTH && active && j == kSuper - 1) {
         store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+        flush_cs(rt - j, c0 + lane);
+      }
       // NVFP4 padding (rows past the last row tile up to the 128-row band,
       // columns up to the 4-column tile): zero scales
       if (MODE == kModeNv && c0 < 64 * p.sc_tiles) st_u16(nv_scale_at(p, rt, c0, lane), 0u);
@@ -674,8 +694,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       }
       // (the wait before the row box above covered the previous unit's store)
       put_qc(Qc, lane, j, q);
-      st_byte(p.s_col + p.sl_col.at(c0 + lane, row0 / 32), sc);
-      if (j == kSuper - 1) store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+      cw |= sc << (8 * j);
+      if (j == kSuper - 1) {
+        store_qc(&p.tm_qc, Qc, row0 - j * kTR, c0, lane);
+        flush_cs(rt - j, c0 + lane);
+      }
     }
   }
   if (failed && lane == 0) {
