@@ -94,6 +94,7 @@ __host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode
 __host__ __device__ constexpr int tbytes_for(int mode) { return mode == GLU_MODE_COL ? 2048 : 4096; }
 __host__ __device__ constexpr int hot_for(int mode) { return mode == GLU_MODE_COL ? 0 : kHotBytes; }
 constexpr int kSlots = 2;
+constexpr int kColSup = 4;  // colwise: row tiles per unit
 
 using Ctl = RingCtl<4 * kSlots, 4>;
 
@@ -121,7 +122,11 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
   Ctl* ctl = reinterpret_cast<Ctl*>(hot_raw + hot_for(MODE));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
-  const int64_t units = p.n_rt * p.n_ct;
+  // colwise: units of sup consecutive row tiles of one column strip, so that
+  // a lane's scales of a unit (four row blocks of its column) are one word
+  const int sup = kCol && p.n_rt % kColSup == 0 ? kColSup : 1;
+  const int64_t n_su = p.n_rt / sup;
+  const int64_t units = n_su * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
   if (hot_for(MODE) && !kExactAct<ACT>)
@@ -135,9 +140,10 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
     }
-    // rowwise: the tiles of a row band first; colwise: down the column strips
+    // rowwise: the tiles of a row band first; colwise: units (column strip,
+    // row tiles sup * minor ..) down the column strips
     for (int g = 0; g < kGroups; ++g) {
-      const TileWalk tw(blockIdx.x + g * G, kGroups * G, kCol ? p.n_rt : p.n_ct);
+      const TileWalk tw(blockIdx.x + g * G, kGroups * G, kCol ? n_su : p.n_ct);
       ctl->major[g] = tw.major;
       ctl->minor[g] = tw.minor;
       if (g == 0) {
@@ -152,21 +158,24 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
 
   // Load the group's next tile into stage st (whole warp; lanes 0..5 issue
   // one box each).
-  auto issue = [&](int st, int g) {
+  auto issue = [&](int st, int g, int64_t kk) {  // kk: the group's tile index
     int64_t rt = 0, ct = 0;
     if (lane == 0) {
       const int64_t major = ctl->major[g], minor = ctl->minor[g];
-      rt = kCol ? minor : major;
+      const int sub = int(kk & (sup - 1));  // tile of the unit (sup is 1 or 4)
+      rt = kCol ? minor * sup + sub : major;
       ct = kCol ? major : minor;
       ctl->rt[st] = rt;
       ctl->ct[st] = ct;
-      int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
-      if (mn >= ctl->n_minor) {
-        mn -= ctl->n_minor;
-        ++mj;
+      if (sub == sup - 1) {  // the unit's last tile: on to the group's next unit
+        int64_t mj = major + ctl->dmaj, mn = minor + ctl->dmin;
+        if (mn >= ctl->n_minor) {
+          mn -= ctl->n_minor;
+          ++mj;
+        }
+        ctl->major[g] = mj;
+        ctl->minor[g] = mn;
       }
-      ctl->major[g] = mj;
-      ctl->minor[g] = mn;
       mbar_arrive_expect_tx(&ctl->full[st], kStageBytes);
     }
     rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
@@ -187,12 +196,17 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
 
   const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
   uint8_t* const T = Tbase + warp * kTBytes;
-  const int64_t n_g = my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0;
+  const int64_t n_g = (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0) * sup;  // tiles
   uint32_t nst = 0;  // bulk groups this warp has committed (selects the box pair)
+  // colwise: dGate and dUp scale bytes of the unit so far (byte i: its row
+  // tile i) of column 16 (lane % 2) + lane / 2 of the sub-tile (lane 2i
+  // keeps the column of pass 0, lane 2i + 1 that of pass 1; both lanes of a
+  // pair hold the same scales)
+  uint32_t cg = 0, cu = 0;
 
   if (w == 0) {
     for (int j = 0; j < kSlots; ++j)
-      if (j < n_g) issue(grp * kSlots + j, grp);
+      if (j < n_g) issue(grp * kSlots + j, grp, j);
   }
 
   int64_t k = 0;
@@ -266,7 +280,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
         sc[1] = nv_block<16>(dg, c[2], c[3], dgd, ex(0), ex8(0));
         sc[2] = nv_block<0>(du, c[4], c[5], dud, ex(1), ex8(1));
         sc[3] = nv_block<16>(du, c[6], c[7], dud, ex(1), ex8(1));
-        if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+        if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
         const int64_t r = row0 + lane;
         if (r < p.M) {
           const bool two = c0 + 16 < p.N;  // N % 32 == 16 leaves a half sub-tile at the end
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
         return exact_bwd<ACT>(hot, sv.g16(at_r(e), at_c(e)), sv.u16(at_r(e), at_c(e)), sv.d16(at_r(e), at_c(e)), 1);
       });
       // the tile's codes are decided: the stage is free
-      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
 
       // ---- codes out: box pairs in turn; the store committed two groups
       // ago (from this pair) has read it out
@@ -398,18 +412,36 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
         }
         *reinterpret_cast<uint4*>(T + swz32(L, hf)) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
         *reinterpret_cast<uint4*>(T + kQBytes + swz32(L, hf)) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
-        if (hf == 0) {
-          if (kCol) {
-            st_byte(p.s_col + p.sl_col.at(c0 + L, row0 / 32), sg);
-            st_byte(p.s_col + p.sl_col.at(p.N + c0 + L, row0 / 32), su);
-          } else if (row0 + L < p.M) {
+        if (kCol) {
+          if (hf == pass) {
+            const int sh = sup == kColSup ? 8 * int(rt & (kColSup - 1)) : 0;
+            cg |= sg << sh;
+            cu |= su << sh;
+          }
+        } else if (hf == 0) {
+          if (row0 + L < p.M) {
             st_byte(p.s_row + p.sl_row.at(row0 + L, c0 / 32), sg);
             st_byte(p.s_row + p.sl_row.at(row0 + L, (p.N + c0) / 32), su);
           }
         }
       }
+      if (kCol && (sup == 1 || (rt & (kColSup - 1)) == kColSup - 1)) {
+        // the unit's scales of the lane's column: one word each (row-major
+        // rows of M / 32 bytes hold four row blocks side by side and
+        // aligned when sup is 4; so does 128x4)
+        const int64_t rb0 = rt - (sup - 1);
+        const int64_t c = c0 + 16 * hf + (lane >> 1);
+        if (sup == kColSup) {
+          st_stream(p.s_col + p.sl_col.at(c, rb0), cg);
+          st_stream(p.s_col + p.sl_col.at(p.N + c, rb0), cu);
+        } else {
+          st_byte(p.s_col + p.sl_col.at(c, rb0), cg);
+          st_byte(p.s_col + p.sl_col.at(p.N + c, rb0), cu);
+        }
+        cg = cu = 0;
+      }
       // the tile's codes are decided: the stage is free
-      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
@@ -424,7 +456,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
       }
     } else {
       // no columns for this warp in the tile
-      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp);
+      if (ring_free<kGroupWarps>(&ctl->freed[s], lane) && k + kSlots < n_g) issue(s, grp, k + kSlots);
     }
   }
   if (failed && lane == 0) {
@@ -448,7 +480,8 @@ cudaError_t launch_dir(const glu_quant_bwd_args& a, cudaStream_t s, const DevInf
   BwdP p;
   e = make_params(p, a);
   if (e != cudaSuccess) return e;
-  const int64_t units = p.n_rt * p.n_ct;
+  const int64_t units =
+      (MODE == GLU_MODE_COL && p.n_rt % kColSup == 0 ? p.n_rt / kColSup : p.n_rt) * p.n_ct;
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
