@@ -272,12 +272,7 @@ def gpu_arm(args, rank, world, dist):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"swiglu_{M}x{N}_mxfp8_" + "+".join(
-                       f"{c[0]}_{MODE_NAME[c[1]]}" for c in calls),
-                   "M": M, "N": N, "act": "silu", "fmt": "mxfp8_e4m3_e8m0_rceil",
-                   "calls_per_step": len(calls), "global_batch_rows": world * M,
-                   "parallelism": f"dp{world}" if world > 1 else "single",
-                   "l2": "inputs 6 GB >> 129 MB L2; no flush"},
+        "config": bench_config(M, N, calls, world),
         "modes": modes,
         "roofline": {"bound": "hbm", "achieved": dom_gbps, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(dom_gbps / peaks["hbm_gbs"], 4),
@@ -384,6 +379,15 @@ def cpu_baseline(rows: int):
             "sample": f"{rows} of 131072 rows, all six calls, {dt:.1f} s wall"}
 
 
+def bench_config(M, N, calls, world):
+    """The workload description both arms report."""
+    return {"workload": f"swiglu_{M}x{N}_mxfp8_" + "+".join(f"{c[0]}_{MODE_NAME[c[1]]}" for c in calls),
+            "M": M, "N": N, "act": "silu", "fmt": "mxfp8_e4m3_e8m0_rceil",
+            "calls_per_step": len(calls), "global_batch_rows": world * M,
+            "parallelism": f"dp{world}" if world > 1 else "single",
+            "l2": f"inputs {6 * M * N / 1e9:.2g} GB (gate, up, dY) vs 129 MB L2; no flush"}
+
+
 def reference_arm(args, rank, world):
     rows = args.ref_rows
     for _ in range(max(args.warmup, 1)):
@@ -399,8 +403,7 @@ def reference_arm(args, rank, world):
             "ms_per_step": round(statistics.median(times) * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "swiglu_131072x8192_mxfp8_fwd+bwd_row+col+both",
-                       "M": M_FULL, "N": N_FULL, "sample_rows": rows},
+            "config": dict(bench_config(M_FULL, N_FULL, CALLS, world), sample_rows=rows),
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": n,
                              "kind": "oracle",
                              "sample": f"{rows} of 131072 rows per step, all six calls"},
