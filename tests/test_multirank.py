@@ -63,3 +63,18 @@ def test_algorithmic_byte_model_matches_the_page_figures():
     assert bench.algo_bytes("fwd", 1, M, N) / 904.19e-6 / 1e9 == pytest.approx(5974.7, abs=0.1)
     assert bench.algo_bytes("bwd", 3, M, N) / 1859.09e-6 / 1e9 == pytest.approx(5847.8, abs=0.1)
     assert bench.algo_bytes("fwd", 3, 16384, 7168) / 143.36e-6 / 1e9 == pytest.approx(4966.4, abs=0.1)
+
+
+def test_algorithmic_bytes_per_format():
+    # per output element: forward reads 4 B and writes 1 + 1/32 B per MXFP8
+    # direction, 1/2 + 1/16 B NVFP4, 2 B bf16; backward reads 6 B and writes
+    # twice that per (gate, up) element
+    assert bench.algo_bytes("fwd", 1, 128, 128) == 65536 + 16896
+    M, N = 131072, 8192
+    assert bench.algo_bytes("fwd", 2, M, N) == bench.algo_bytes("fwd", 1, M, N) == 5402263552
+    assert bench.algo_bytes("fwd", 3, M, N) == 4 * M * N + 2 * (M * N + M * N // 32)
+    assert bench.algo_bytes("bwd", 1, M, N) == 6 * M * N + 2 * (M * N + M * N // 32)
+    # NVFP4, interleaved GeGLU 784 x 16384 outputs: 51.38 MB read, 7.225 MB written
+    assert bench.algo_bytes("fwd", 1, 784, 16384, "nvfp4") == 51380224 + 7225344
+    assert bench.algo_bytes("bwd", 1, 8192, 14336, "nvfp4") == 6 * 8192 * 14336 + 8192 * 14336 * 9 // 8
+    assert bench.algo_bytes("fwd", 1, 8192, 11008, "bf16") == 6 * 8192 * 11008
