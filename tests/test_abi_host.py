@@ -140,3 +140,42 @@ def test_sizes():
     # NVFP4 backward: codes of [M, 2N] packed, scales of [M, 2N/16] in 128x4
     st, s = G.glu_quant_bwd_sizes(bwd_args(fmt=1, M=200, N=48, ld_in=48, ld_dy=48))
     assert st == 0 and s == (200 * 48, 256 * 8, 0, 0)
+
+
+def test_binding_mirrors_the_header(tmp_path):
+    """The ctypes structs and constants of the binding against the header as
+    a C compiler sees it: struct sizes, every field offset, every enum and
+    status value."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    fields = {"glu_quant_fwd_args": G.GluQuantFwdArgs, "glu_quant_bwd_args": G.GluQuantBwdArgs}
+    consts = {"GLU_ACT_SILU": G.ACT_SILU, "GLU_ACT_GELU_TANH": G.ACT_GELU_TANH, "GLU_ACT_RELU": G.ACT_RELU,
+              "GLU_ACT_IDENTITY": G.ACT_IDENTITY, "GLU_ACT_BF16_STEPS": G.ACT_BF16_STEPS,
+              "GLU_FMT_MXFP8_E4M3": G.FMT_MXFP8, "GLU_FMT_NVFP4_E2M1": G.FMT_NVFP4, "GLU_FMT_BF16": G.FMT_BF16,
+              "GLU_FMT_FP32": G.FMT_FP32, "GLU_FMT_MXFP8_E4M3_128X4": G.FMT_MXFP8_128X4,
+              "GLU_MODE_ROW": G.MODE_ROW, "GLU_MODE_COL": G.MODE_COL, "GLU_MODE_BOTH": G.MODE_BOTH,
+              "GLU_LAYOUT_SPLIT": G.LAYOUT_SPLIT, "GLU_LAYOUT_INTERLEAVED": G.LAYOUT_INTERLEAVED,
+              "GLU_OK": G.GLU_OK, "GLU_EINVAL": G.GLU_EINVAL, "GLU_ESHAPE": G.GLU_ESHAPE,
+              "GLU_EALIGN": G.GLU_EALIGN, "GLU_EDEVICE": G.GLU_EDEVICE, "GLU_ELAUNCH": G.GLU_ELAUNCH}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "glu_quant.h"', "int main(void) {"]
+    for st, cls in fields.items():
+        lines.append(f'  printf("size {st} %zu\\n", sizeof({st}));')
+        for name, _ in cls._fields_:
+            lines.append(f'  printf("off {st}.{name} %zu\\n", offsetof({st}, {name}));')
+    for c in consts:
+        lines.append(f'  printf("const {c} %d\\n", (int)({c}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                               check=True).stdout.splitlines())
+    for st, cls in fields.items():
+        assert int(got[f"size {st}"]) == ctypes.sizeof(cls), st
+        for name, _ in cls._fields_:
+            assert int(got[f"off {st}.{name}"]) == getattr(cls, name).offset, (st, name)
+    for c, v in consts.items():
+        assert int(got[f"const {c}"]) == v, c
