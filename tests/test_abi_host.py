@@ -179,3 +179,17 @@ def test_binding_mirrors_the_header(tmp_path):
             assert int(got[f"off {st}.{name}"]) == getattr(cls, name).offset, (st, name)
     for c, v in consts.items():
         assert int(got[f"const {c}"]) == v, c
+
+
+@pytest.mark.parametrize("act", [0, 1, 2, 3, 16, 17, 18, 19])
+def test_every_activation_is_accepted_forward(act):
+    st, s = G.glu_quant_fwd_sizes(fwd_args(act=act))
+    assert st == G.GLU_OK and s == (64 * 256, 64 * 8, 0, 0)
+
+
+@pytest.mark.parametrize("act,status", [(0, G.GLU_OK), (1, G.GLU_OK), (2, G.GLU_OK), (3, G.GLU_OK),
+                                        (18, G.GLU_EINVAL), (19, G.GLU_EINVAL), (4, G.GLU_EINVAL)])
+def test_backward_activations(act, status):
+    # the bf16 steps are a forward-only flag for every activation
+    st, _ = G.glu_quant_bwd_sizes(bwd_args(act=act))
+    assert st == status
