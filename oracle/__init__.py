@@ -21,7 +21,7 @@ _HDR = os.path.join(_HERE, "oracle.h")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 
-SILU, GELU_TANH, RELU, IDENTITY = 0, 1, 2, 3
+SILU, GELU_TANH, RELU, IDENTITY, GELU_ERF = 0, 1, 2, 3, 4
 BF16_STEPS = 16  # OR-ed into act (forward): h = RN_bf16(RN_bf16(act(g)) * u)
 MXFP8, NVFP4, BF16, FP32, MXFP8_128X4 = 0, 1, 2, 3, 4
 ROW, COL, BOTH = 1, 2, 3

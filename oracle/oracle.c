@@ -90,6 +90,10 @@ static const double GELU_A = 0.044715;
 double orc_act(int act, double x) {
   if (act == ORC_RELU) return x <= 0.0 ? 0.0 : x; /* ReLU: +0 for x <= 0, NaN kept */
   if (act == ORC_IDENTITY) return x;
+  /* GELU (erf): x * Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2, which keeps full
+   * relative precision in the negative tail where 1 + erf(x / sqrt 2)
+   * cancels */
+  if (act == ORC_GELU_ERF) return x * (0.5 * erfc(-x * 0.70710678118654752440));
   if (act == ORC_SILU) return x * sigmoid(x);
   double y = GELU_C * (x + GELU_A * x * x * x);
   return x * sigmoid(2.0 * y);
@@ -108,6 +112,9 @@ double orc_act_grad(int act, double x) {
    * gate too, as its gradient passes dY through); identity 1 */
   if (act == ORC_RELU) return x <= 0.0 ? 0.0 : 1.0;
   if (act == ORC_IDENTITY) return 1.0;
+  /* GELU (erf): Phi(x) + x phi(x), phi(x) = exp(-x^2 / 2) / sqrt(2 pi) */
+  if (act == ORC_GELU_ERF)
+    return 0.5 * erfc(-x * 0.70710678118654752440) + x * (exp(-0.5 * x * x) * 0.39894228040143267793994605993438);
   if (act == ORC_SILU) {
     double s = sigmoid(x), one_minus_s = sigmoid(-x);
     return s * (1.0 + x * one_minus_s);
@@ -510,7 +517,7 @@ static void* worker(void* p) {
 static int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t M,
                         int64_t W) {
   act &= ~ORC_BF16_STEPS;
-  if (act < ORC_SILU || act > ORC_IDENTITY) return -1;
+  if (act < ORC_SILU || act > ORC_GELU_ERF) return -1;
   if (layout != ORC_SPLIT && layout != ORC_INTERLEAVED) return -1;
   if (M <= 0 || W <= 0) return -1;
   if (fmt == ORC_MXFP8) {

@@ -38,6 +38,10 @@ extern "C" {
  * up) are the further gated activations that "Add swiglu + MXFP8 fused CuTe
  * DSL kernel", Follow-ups (item 1) leaves open, in their textbook form. */
 enum { ORC_SILU = 0, ORC_GELU_TANH = 1, ORC_RELU = 2, ORC_IDENTITY = 3 };
+/* GELU with the exact normal CDF, x * Phi(x) (GeGLU in its erf form), the
+ * next gated activation of the same template; the oracle defines it ahead of
+ * a GPU path. */
+enum { ORC_GELU_ERF = 4 };
 /* OR-ed into act (forward only): h = RN_bf16(RN_bf16(act(g)) * u), the
  * values an eager bf16 evaluation of act(gate) * up gives ("Add swiglu +
  * MXFP8 fused CuTe DSL kernel", Numerics and tests: forward data bitwise

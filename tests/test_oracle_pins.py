@@ -466,6 +466,14 @@ def test_fp32_mode_is_rounded_exact_value():
         X = mpmath.mpf(float(x))
         exact = X / (1 + mpmath.exp(-X)) * mpmath.mpf(float(y))
         assert o == np.float32(float(exact))
+    # GELU (erf) through the whole forward path, fp32 and bf16-step values
+    r = O.glu_fwd(g, u, act=O.GELU_ERF, fmt=O.FP32)
+    rb = O.glu_fwd(g, u, act=O.GELU_ERF | O.BF16_STEPS, fmt=O.FP32)
+    for x, y, o, ob in zip(gv.ravel(), uv.ravel(), r["out"].ravel(), rb["out"].ravel()):
+        X = mpmath.mpf(float(x))
+        a = X * mpmath.ncdf(X)
+        assert o == np.float32(float(a * mpmath.mpf(float(y))))
+        assert ob == O.round_bf16(O.round_bf16(float(a)) * float(y))
 
 
 def test_boundary_distance():
@@ -785,3 +793,51 @@ def test_relu_bf16_steps_is_one_rounding():
     h = O.glu_fwd(g, u, act=O.RELU | O.BF16_STEPS, fmt=O.FP32)["out"]
     ref = (torch.relu(torch.from_numpy(_bf16_f32(g))) * torch.from_numpy(_bf16_f32(u))).to(torch.bfloat16)
     assert np.array_equal(h, ref.float().numpy())
+
+
+# ------------------------------------------------------------ GELU (erf) --
+# x * Phi(x), the erf form of GELU: defined in the oracle ahead of a GPU path.
+
+def test_gelu_erf_vs_mpmath():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+
+    def f(x):
+        return x * mpmath.ncdf(x)
+
+    xs = _all_bf16_in(-30.0, 30.0)[::5]
+    ours, ours_d = O.act(O.GELU_ERF, xs), O.act_grad(O.GELU_ERF, xs)
+    for x, y, dy in zip(xs, ours, ours_d):
+        X = mpmath.mpf(float(x))
+        ref, dref = f(X), mpmath.ncdf(X) + X * mpmath.npdf(X)
+        # erfc's relative condition number grows like x^2 in the negative tail
+        cond = 1.0 + float(x) ** 2
+        assert abs(y - float(ref)) <= 1e-15 * cond * abs(float(ref)) + 1e-300, (x, y, float(ref))
+        scale = abs(float(mpmath.ncdf(X))) + abs(float(X * mpmath.npdf(X)))  # act' has a zero near -0.75
+        assert abs(dy - float(dref)) <= 1e-15 * cond * scale + 1e-300, (x, dy, float(dref))
+
+
+def test_gelu_erf_vs_torch_float64():
+    # torch evaluates 0.5 x (1 + erf(x / sqrt 2)), which cancels for x << 0;
+    # stay where that library form is itself accurate (the tail is pinned
+    # against mpmath above)
+    x = torch.linspace(-3, 20, 20001, dtype=torch.float64)
+    assert np.allclose(O.act(O.GELU_ERF, x.numpy()), torch.nn.functional.gelu(x).numpy(), rtol=1e-12, atol=1e-300)
+    t = x.clone().requires_grad_(True)
+    torch.nn.functional.gelu(t).sum().backward()
+    assert np.allclose(O.act_grad(O.GELU_ERF, x.numpy()), t.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_gelu_erf_special_values_and_differences():
+    assert O.act(O.GELU_ERF, [0.0])[0] == 0.0
+    assert O.act_grad(O.GELU_ERF, [0.0])[0] == 0.5
+    assert np.float32(O.act(O.GELU_ERF, [60.0])[0]) == np.float32(60.0)
+    assert np.float32(O.act_grad(O.GELU_ERF, [60.0])[0]) == np.float32(1.0)
+    assert math.copysign(1, O.act(O.GELU_ERF, [-30.0])[0]) == -1  # a tiny negative value, not 0
+    assert math.copysign(1, O.act(O.GELU_ERF, [-40.0])[0]) == -1  # Phi underflows: -0
+    xs = np.linspace(-9, 9, 1801)
+    h = 1e-5
+    fd = (O.act(O.GELU_ERF, xs + h) - O.act(O.GELU_ERF, xs - h)) / (2 * h)
+    assert np.allclose(O.act_grad(O.GELU_ERF, xs), fd, rtol=0, atol=1e-8)
+    # close to the tanh approximation it was built to approximate (|diff| < 5e-4)
+    assert np.max(np.abs(O.act(O.GELU_ERF, xs) - O.act(O.GELU_TANH, xs))) < 5e-4
