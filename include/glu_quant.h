@@ -79,8 +79,9 @@ extern "C" {
 enum glu_act {
   GLU_ACT_SILU = 0,
   GLU_ACT_GELU_TANH = 1,
-  /* ABI 3: relu(x) = x for x > 0, else +0 (relu' = 1 for x > 0, else 0; a
-   * NaN gate stays NaN), and the identity act(x) = x.  With bf16 operands
+  /* ABI 3: relu(x) = +0 for x <= 0, else x (a NaN gate stays NaN), relu'
+   * = 0 for x <= 0, else 1 (at a NaN gate too, so dY passes through), and
+   * the identity act(x) = x.  With bf16 operands
    * every value of theirs (h, dGate, dUp, the bf16 steps) is an exact
    * product rounded once, so their outputs match the rounded exact values
    * with no tolerance; where relu(gate) is +0, h and dUp are zeros with the
