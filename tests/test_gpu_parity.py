@@ -633,3 +633,32 @@ def test_device_error_bits_stay_clear():
     torch.cuda.synchronize()
     st, f, b = G.glu_quant_device_errors(clear=True)
     assert (st, f, b) == (G.GLU_OK, 0, 0)
+
+
+@pytest.mark.parametrize("shape", [(128, 416), (96, 384), (256, 1024), (160, 640)],
+                         ids=["units_ragged_strip", "tiles_full_strips", "units_full_strips", "ragged_unit"])
+@pytest.mark.parametrize("fmt", [G.FMT_MXFP8, G.FMT_MXFP8_128X4], ids=["rowmajor", "128x4"])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_scale_word_paths(shape, fmt, direction):
+    """Every combination of the four-byte scale stores and their byte
+    fallbacks: row tiles in whole units of four or not (colwise words), whole
+    128-column strips or a ragged last strip (rowwise words across a group's
+    warps), in both scale layouts, for the colwise and both-direction calls."""
+    M, N = shape
+    g, u, d = _randn(M, N, 111, 2.0), _randn(M, N, 112), _randn(M, N, 113)
+    W = N if direction == "fwd" else 2 * N
+    for mode in (G.MODE_COL, G.MODE_BOTH):
+        if direction == "fwd":
+            out = G.fwd(g, u, fmt=fmt, mode=mode)
+            torch.cuda.synchronize()
+            ref = O.glu_fwd(host_bits(g), host_bits(u), act=O.SILU, fmt=O.MXFP8, mode=mode, want_h=True)
+        else:
+            out = G.bwd(g, u, d, fmt=fmt, mode=mode)
+            torch.cuda.synchronize()
+            ref = O.glu_bwd(host_bits(g), host_bits(u), host_bits(d), act=O.SILU, fmt=O.MXFP8, mode=mode,
+                            want_h=True)
+        gpu = {k: host(v) for k, v in out.items()}
+        if fmt == G.FMT_MXFP8:
+            check(gpu, ref, G.FMT_MXFP8, mode, M, W, f"{direction}_{mode}")
+        else:
+            check_mx_128x4(gpu, ref, mode, M, W, f"{direction}_{mode}_128x4")
