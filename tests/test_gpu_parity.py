@@ -176,12 +176,15 @@ def test_nvfp4_small(act, layout, shape):
 @pytest.mark.parametrize("bwd", [False, True], ids=["fwd", "bwd"])
 def test_plain_small(act, fmt, layout, N, bwd):
     M = 67
-    if layout == G.LAYOUT_INTERLEAVED and N % 8:
-        pytest.skip("interleaved rows of 2N elements need ld % 8 == 0")
-    # pad the row stride to a multiple of 8 for the ragged split case
+    # pad the row strides to a multiple of 8 for the ragged cases (split: ld
+    # >= N; interleaved: ld >= 2N)
     ld = -(-N // 8) * 8
     base_g, base_u, base_d = _randn(M, ld, 41, 2.0), _randn(M, ld, 42), _randn(M, ld, 43)
     g, u, d = base_g[:, :N], base_u[:, :N], base_d[:, :N]
+    if layout == G.LAYOUT_INTERLEAVED:
+        ldx = -(-2 * N // 8) * 8
+        x = torch.zeros(M, ldx, dtype=torch.bfloat16, device=DEV)
+        x[:, :2 * N] = _interleave(g.contiguous(), u.contiguous())
     if bwd:
         if layout == G.LAYOUT_SPLIT:
             out = G.bwd(g, u, d, act=act[0], fmt=fmt, N=N)
@@ -189,11 +192,10 @@ def test_plain_small(act, fmt, layout, N, bwd):
             ref = O.glu_bwd(host_bits(base_g), host_bits(base_u), host_bits(base_d), act=act[0],
                             fmt=fmt, N=N, want_h=True)
         else:
-            x = _interleave(g.contiguous(), u.contiguous())
-            out = G.bwd(x, None, d.contiguous(), act=act[0], fmt=fmt, layout=layout)
+            out = G.bwd(x, None, d, act=act[0], fmt=fmt, layout=layout, N=N)
             torch.cuda.synchronize()
-            ref = O.glu_bwd(host_bits(x), None, host_bits(d), act=act[0], fmt=fmt,
-                            layout=O.INTERLEAVED, want_h=True)
+            ref = O.glu_bwd(host_bits(x), None, host_bits(base_d), act=act[0], fmt=fmt,
+                            layout=O.INTERLEAVED, N=N, want_h=True)
     else:
         if layout == G.LAYOUT_SPLIT:
             out = G.fwd(g, u, act=act[0], fmt=fmt, N=N)
@@ -201,10 +203,9 @@ def test_plain_small(act, fmt, layout, N, bwd):
             ref = O.glu_fwd(host_bits(base_g), host_bits(base_u), act=act[0], fmt=fmt, N=N,
                             want_h=True)
         else:
-            x = _interleave(g.contiguous(), u.contiguous())
-            out = G.fwd(x, None, act=act[0], fmt=fmt, layout=layout)
+            out = G.fwd(x, None, act=act[0], fmt=fmt, layout=layout, N=N)
             torch.cuda.synchronize()
-            ref = O.glu_fwd(host_bits(x), act=act[0], fmt=fmt, layout=O.INTERLEAVED, want_h=True)
+            ref = O.glu_fwd(host_bits(x), act=act[0], fmt=fmt, layout=O.INTERLEAVED, N=N, want_h=True)
     st = Stats()
     check_plain(host(out["out"]), ref, fmt, st, "plain")
 
