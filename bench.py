@@ -1,21 +1,38 @@
-"""Benchmark of the fused gated-GLU + MXFP8 quantisation path on GB300.
+"""Benchmark of the fused gated-GLU + block-scaled quantisation path on GB300.
 
-Workload (one "step"): SwiGLU at M=131072, N=8192 (gate, up, dY bf16
-N(0,1) with 0.1% of elements set to +-60), MXFP8 E4M3/E8M0 outputs, the six
-calls forward {row, col, both} and backward {row, col, both}, each its own
-kernel launch.  The metric is effective bandwidth: algorithmic bytes read +
-written (4 B/elem read forward, 6 B/elem backward; 1 + 1/32 B written per
-element and direction) divided by device time, reported against the measured
-HBM copy bandwidth.  Inputs (6 GB) are far larger than L2, so nothing is
-flushed between steps.
+Headline workload (one "step"): SwiGLU at M=131072, N=8192 (gate, up, dY
+bf16 N(0,1) with 0.1% of elements set to +-60), MXFP8 E4M3/E8M0 outputs, the
+six calls forward {row, col, both} and backward {row, col, both}, each its
+own kernel launch.  The metric is effective bandwidth: algorithmic bytes
+read + written (4 B/elem read forward, 6 B/elem backward; 1 + 1/32 B written
+per element and direction) divided by device time, reported against the
+measured HBM copy bandwidth.  Inputs (6 GB) are far larger than L2, so
+nothing is flushed between steps.
+
+Beside the headline line's timed steps (CUDA events around each call):
+  * ``modes``: every call also timed as a CUDA graph of 20 calls per replay
+    (25 warm-up replays, median and min of 30);
+  * ``configs``: the other workloads (SwiGLU 128x128; SwiGLU 4096x7168 all
+    six calls; GeGLU 8192 x {11008, 14336, 18944, 29568} MXFP8 rowwise and
+    BF16 forward and backward; GeGLU NVFP4 interleaved at 784 and 968 rows),
+    graph-timed the same way, with a cold-L2 figure (a graph rotating
+    through buffer sets totalling more than twice L2) for the L2-resident
+    ones;
+  * ``parity``: every output of every call above compared with the CPU
+    oracle on the same input bytes (the headline workload on all 131072
+    rows): scale mismatches and out-of-window code mismatches must be 0,
+    code mismatches inside the 2-ulp window are counted;
+  * ``cpu_baseline``: the oracle's own time for the headline step on all
+    host cores (and on one core, on a sample).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--no-e2e] [--no-cpu] [--sweep FILE]
+                    [--no-e2e] [--no-cpu] [--no-configs] [--sweep FILE]
 
 One JSON line on stdout (rank 0).  ``--impl reference`` times the CPU oracle
 (the only reference implementation that exists for this path) on a bounded
-sample of the same workload.  ``--sweep FILE`` additionally writes one JSONL
-record per workload/mode/direction (CUDA-graph timing, 20 calls per replay).
+sample of the same workload.  ``--sweep FILE`` also writes one JSONL record
+per extra format and activation (128x4 scales, ReLU, identity, GELU-erf,
+bf16 steps, NVFP4 backward and global scale).
 """
 from __future__ import annotations
 
@@ -40,6 +57,7 @@ MODE_NAME = {1: "row", 2: "col", 3: "both"}
 PAGE_GB200_US = {("fwd", 1): 904.19, ("fwd", 2): 1022.98, ("fwd", 3): 1216.08,
                  ("bwd", 1): 1321.98, ("bwd", 2): 1710.08, ("bwd", 3): 1859.09}
 L2_BYTES = 129 * 2 ** 20
+GRAPH_REPS, GRAPH_WARM, GRAPH_SAMPLES = 20, 25, 30
 
 
 def algo_bytes(direction: str, mode: int, M: int, N: int, fmt: str = "mxfp8") -> int:
@@ -179,6 +197,92 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(load)}
 
 
+# ------------------------------------------------------------ GPU timing --
+
+def graph_time(fns, dev, reps=GRAPH_REPS, warm=GRAPH_WARM, samples=GRAPH_SAMPLES):
+    """Median and min µs per call of a CUDA graph that runs the calls
+    ``fns`` (each takes a stream handle) in turn until it holds ``reps``
+    calls (a list longer than ``reps`` is captured whole)."""
+    import torch
+    n = max(reps, len(fns))
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for f in fns:  # eager warm-up on the capture stream (lazy set-up)
+            f(s.cuda_stream)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(n):
+                fns[i % len(fns)](s.cuda_stream)
+    torch.cuda.synchronize(dev)
+    for _ in range(warm):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    out = []
+    for _ in range(samples):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        out.append(a.elapsed_time(b) * 1e3 / n)
+    del graph
+    return statistics.median(out), min(out)
+
+
+def device_error_bits(G) -> dict:
+    """Error bits the kernels' bounded waits recorded (then cleared): a wait
+    that gave up leaves partial output behind, so any bit voids the timing."""
+    st, f, b = G.glu_quant_device_errors(clear=True)
+    return {"status": st, "fwd": f, "bwd": b, "ok": st == 0 and f == 0 and b == 0}
+
+
+# ----------------------------------------------------------- parity (host) --
+
+def _parity_util():
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity_util
+    return parity_util
+
+
+def oracle_call(O, direction, mode, fmt, act, bits, layout=0, N=None, nthreads=None):
+    """The oracle's outputs of one call on host bit arrays (gate, up, dy)."""
+    gb, ub, db = bits
+    ofmt = {"mxfp8": O.MXFP8, "nvfp4": O.NVFP4, "bf16": O.BF16, "fp32": O.FP32}[fmt]
+    if direction == "fwd":
+        return O.glu_fwd(gb, ub, act=act, fmt=ofmt, mode=mode, layout=layout, N=N, nthreads=nthreads)
+    return O.glu_bwd(gb, ub, db, act=act, fmt=ofmt, mode=mode, layout=layout, N=N, nthreads=nthreads)
+
+
+def parity_of(O, PU, direction, mode, fmt, act, bits, gpu_host, M, N, layout=0, ref=None):
+    """Counts of one call's comparison with the oracle (PU.compare_counts)."""
+    ofmt = {"mxfp8": O.MXFP8, "nvfp4": O.NVFP4, "bf16": O.BF16}[fmt]
+    if ref is None:
+        ref = oracle_call(O, direction, mode, fmt, act, bits, layout, N)
+    W = N if direction == "fwd" else 2 * N
+
+    def h_rows(rows):
+        gb, ub, db = bits
+        sub = lambda x: None if x is None else x[rows]
+        return oracle_call(O, direction, 1, "fp32", act, (sub(gb), sub(ub), sub(db)), layout, N)["out"]
+    return PU.compare_counts(gpu_host, ref, ofmt, mode, M, W, h_rows)
+
+
+def host_outputs(o: dict) -> dict:
+    """Host numpy copies of a call's output tensors."""
+    import torch
+    r = {}
+    for k, t in o.items():
+        if t is None:
+            r[k] = None
+        elif t.dtype == torch.bfloat16:
+            r[k] = t.contiguous().view(torch.int16).cpu().numpy().view("uint16")
+        else:
+            r[k] = t.cpu().numpy()
+    return r
+
+
 # ------------------------------------------------------------------ GPU arm --
 
 def gpu_arm(args, rank, world, dist):
@@ -212,17 +316,19 @@ def gpu_arm(args, rank, world, dist):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def call(c):
+    def call(c, s=None):
         direction, mode = c
+        s = sh if s is None else s
         if direction == "fwd":
-            G.fwd(g, u, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+            G.fwd(g, u, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=s)
         else:
-            G.bwd(g, u, d, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=sh)
+            G.bwd(g, u, d, act=G.ACT_SILU, fmt=G.FMT_MXFP8, mode=mode, out=bufs[c], stream=s)
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
+    G.glu_quant_device_errors(clear=True)
     for _ in range(args.warmup):
         for c in calls:
             call(c)
@@ -246,6 +352,7 @@ def gpu_arm(args, rank, world, dist):
         t1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
+    errs = device_error_bits(G)
     total_ms = t0.elapsed_time(t1)
     per_call_ms = {c: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)]
                    for i, c in enumerate(calls)}
@@ -285,11 +392,34 @@ def gpu_arm(args, rank, world, dist):
             "note": "the pages' GB200 per-call times for the same six calls (context, not a target)"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "device_errors": errs,
     }
+
+    # every call also as a CUDA graph of 20 calls per replay
+    if not args.no_graph:
+        for c in calls:
+            med, mn = graph_time([lambda s, c=c: call(c, s)], dev)
+            r = modes[f"{c[0]}_{MODE_NAME[c[1]]}"]
+            r["us_graph"] = round(med, 2)
+            r["us_graph_min"] = round(mn, 2)
+            r["frac_hbm_graph"] = round(algo_bytes(c[0], c[1], M, N) / (med * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)
+        res["device_errors_graph"] = device_error_bits(G)
+
+    host_in = gpu_out = None
+    if rank == 0 and (not args.no_parity or (not args.no_cpu and world == 1)):
+        host_in = [synth.to_host_bits(t) for t in (g, u, d)]
+        if not args.no_parity:
+            gpu_out = {c: host_outputs(bufs[c]) for c in calls}
 
     if not args.no_e2e:
         res["e2e"] = e2e_leg(args, G, g, u, d, bufs, calls, dev, stream, dist, world, step_bytes)
-    return res
+    del x, g, u, d, bufs
+    torch.cuda.empty_cache()
+
+    if not args.no_configs and rank == 0:
+        res["configs"] = configs_block(args, G, dev, peaks, parity=not args.no_parity)
+        res["device_errors_configs"] = device_error_bits(G)
+    return res, host_in, gpu_out, (M, N, calls)
 
 
 def e2e_leg(args, G, g, u, d, bufs, calls, dev, stream, dist, world, step_bytes):
@@ -343,6 +473,102 @@ def e2e_leg(args, G, g, u, d, bufs, calls, dev, stream, dist, world, step_bytes)
             "ms_per_step": round(ms / K, 3)}
 
 
+# ------------------------------------------------------ the other configs --
+
+def config_calls(G):
+    """(config, workload spec args, [(direction, mode, fmt, act, layout)]),
+    the shapes and calls of the non-headline workloads."""
+    S, GE = G.ACT_SILU, G.ACT_GELU_TANH
+    c3 = [("fwd", 1, "mxfp8", GE, 0), ("bwd", 1, "mxfp8", GE, 0),
+          ("fwd", 1, "bf16", GE, 0), ("bwd", 1, "bf16", GE, 0)]
+    return ([("C1", ("swiglu_128", {}), [("fwd", 1, "mxfp8", S, 0)])]
+            + [("C2", ("swiglu_4096", {}), [(dr, m, "mxfp8", S, 0) for dr in ("fwd", "bwd") for m in (1, 2, 3)])]
+            + [("C3", ("geglu_8192", {"N": n}), c3) for n in (11008, 14336, 18944, 29568)]
+            + [("C4", ("geglu_nvfp4", {"M": m}), [("fwd", 1, "nvfp4", GE, 1)]) for m in (784, 968)])
+
+
+def configs_block(args, G, dev, peaks, parity=True):
+    """Graph-timed µs, GB/s and fraction of HBM per call of every config,
+    cold-L2 figures where the working set fits in L2, parity counts."""
+    import torch
+
+    import oracle as O
+    import synth
+    PU = _parity_util() if parity else None
+    fmts = {"mxfp8": G.FMT_MXFP8, "nvfp4": G.FMT_NVFP4, "bf16": G.FMT_BF16}
+    oact = {G.ACT_SILU: O.SILU, G.ACT_GELU_TANH: O.GELU_TANH}
+    recs = []
+    for cname, (wl, kw), cl in config_calls(G):
+        sp = synth.spec(wl, **kw)
+        x = synth.make(sp, dev, with_dy=any(dr == "bwd" for dr, *_ in cl))
+        interleaved = sp.interleaved
+        gin, uin = (x["x"], None) if interleaved else (x["gate"], x["up"])
+        din = x.get("dy")
+        M, N = sp.M, sp.N
+        bits = None
+        if parity:
+            tb = lambda t: None if t is None else synth.to_host_bits(t)
+            bits = (tb(gin), tb(uin), tb(din))
+        for (dr, mode, fmt, act, layout) in cl:
+            f = fmts[fmt]
+            mk = lambda s, o=None, dr=dr, mode=mode, f=f, act=act, layout=layout, gin=gin, uin=uin, din=din: (
+                G.fwd(gin, uin, act=act, fmt=f, mode=mode, layout=layout, out=o, stream=s) if dr == "fwd"
+                else G.bwd(gin, uin, din, act=act, fmt=f, mode=mode, layout=layout, out=o, stream=s))
+            o = mk(None)
+            med, mn = graph_time([lambda s, o=o, mk=mk: mk(s, o)], dev)
+            nbytes = algo_bytes(dr, mode, M, N, fmt)
+            gbps = nbytes / (med * 1e-6) / 1e9
+            r = {"config": cname, "workload": wl, "direction": dr, "mode": MODE_NAME[mode], "fmt": fmt,
+                 "act": "silu" if act == G.ACT_SILU else "gelu_tanh",
+                 "layout": "interleaved" if layout else "split", "M": M, "N": N,
+                 "us_graph": round(med, 3), "us_graph_min": round(mn, 3), "bytes": nbytes,
+                 "gbps": round(gbps, 1), "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
+                 "l2_resident": nbytes < L2_BYTES}
+            if nbytes < L2_BYTES:
+                r.update(cold_l2(G, dev, sp, dr, mode, f, act, layout, nbytes, peaks))
+            torch.cuda.synchronize(dev)
+            if parity:
+                gpu_host = host_outputs(o)
+                r["parity"] = parity_of(O, PU, dr, mode, fmt, oact[act], bits, gpu_host, M, N, layout=layout)
+            recs.append(r)
+            print(json.dumps(r), file=sys.stderr, flush=True)
+            del o
+        del x, gin, uin, din
+        torch.cuda.empty_cache()
+    return recs
+
+
+def cold_l2(G, dev, sp, dr, mode, f, act, layout, nbytes, peaks):
+    """µs per call with every call of the graph on its own input/output set,
+    at least 4 sets and more than 2x L2 in all, so that no call finds its
+    data in L2."""
+    import torch
+
+    import synth
+    sets = max(4, -(-2 * L2_BYTES // nbytes) + 1)
+    ins = []
+    base = synth.make(sp, dev, with_dy=dr == "bwd")
+    for i in range(sets):
+        # one copy per set (the values do not matter for the timing)
+        ins.append({k: v.clone() for k, v in base.items()})
+    fns = []
+    for xi in ins:
+        gin, uin = (xi["x"], None) if sp.interleaved else (xi["gate"], xi["up"])
+        din = xi.get("dy")
+        mk = lambda s, o=None, gin=gin, uin=uin, din=din: (
+            G.fwd(gin, uin, act=act, fmt=f, mode=mode, layout=layout, out=o, stream=s) if dr == "fwd"
+            else G.bwd(gin, uin, din, act=act, fmt=f, mode=mode, layout=layout, out=o, stream=s))
+        o = mk(None)
+        fns.append(lambda s, mk=mk, o=o: mk(s, o))
+    med, mn = graph_time(fns, dev, reps=len(fns), warm=5, samples=15)
+    del ins, fns, base
+    torch.cuda.empty_cache()
+    gbps = nbytes / (med * 1e-6) / 1e9
+    return {"cold_l2": {"us": round(med, 3), "us_min": round(mn, 3), "gbps": round(gbps, 1),
+                        "frac_hbm": round(gbps / peaks["hbm_gbs"], 4), "buffer_sets": sets,
+                        "bytes_all_sets": sets * nbytes}}
+
+
 # ------------------------------------------------------------- CPU (oracle) --
 
 _SAMPLE_CACHE = {}
@@ -373,10 +599,44 @@ def oracle_sample(rows: int, seed_offset: int = 0, nthreads: int | None = None):
     return nbytes / dt / 1e9, dt, nthreads
 
 
-def cpu_baseline(rows: int):
-    v, dt, n = oracle_sample(rows)
-    return {"value": round(v, 3), "unit": "GB/s", "cores": n, "kind": "oracle",
-            "sample": f"{rows} of 131072 rows, all six calls, {dt:.1f} s wall"}
+def cpu_leg(host_in, gpu_out, shape, parity: bool, one_thread_rows: int):
+    """The oracle on the GPU run's own input bytes: the headline step on all
+    host cores, timed call by call (cpu_baseline), each call's outputs
+    compared with the GPU's (parity); then a one-core sample."""
+    import oracle as O
+    PU = _parity_util() if parity else None
+    M, N, calls = shape
+    n = os.cpu_count() or 1
+    O.lib()
+    total, par = 0.0, {}
+    for c in calls:
+        dr, mode = c
+        t0 = time.perf_counter()
+        ref = oracle_call(O, dr, mode, "mxfp8", O.SILU, host_in, nthreads=n)
+        total += time.perf_counter() - t0
+        if parity:
+            par[f"{dr}_{MODE_NAME[mode]}"] = parity_of(O, PU, dr, mode, "mxfp8", O.SILU, host_in,
+                                                       gpu_out[c], M, N, ref=ref)
+        del ref
+    nbytes = sum(algo_bytes(dr, m, M, N) for dr, m in calls)
+    cpu = {"value": round(nbytes / total / 1e9, 3), "unit": "GB/s", "cores": n, "kind": "oracle",
+           "sample": f"all {M} rows of the timed workload's own inputs, all {len(calls)} calls, "
+                     f"{total:.1f} s wall"}
+    # one core, on the first rows
+    r1 = min(one_thread_rows, M)
+    sub = tuple(x[:r1] for x in host_in)
+    t0 = time.perf_counter()
+    for dr, mode in calls:
+        oracle_call(O, dr, mode, "mxfp8", O.SILU, sub, nthreads=1)
+    dt = time.perf_counter() - t0
+    cpu["one_core"] = {"value": round(sum(algo_bytes(dr, m, r1, N) for dr, m in calls) / dt / 1e9, 3),
+                       "unit": "GB/s", "cores": 1, "sample": f"first {r1} rows, all {len(calls)} calls, "
+                                                             f"{dt:.1f} s wall"}
+    if parity:
+        par["all_ok"] = all(v["ok"] for v in par.values())
+        par["rule"] = ("scales bit-exact; codes bit-exact except within 2 fp32 ulps of a rounding "
+                       "boundary (one code step, counted as window)")
+    return cpu, (par if parity else None)
 
 
 def bench_config(M, N, calls, world):
@@ -414,8 +674,8 @@ def reference_arm(args, rank, world):
 # ---------------------------------------------------------------- sweep --
 
 def sweep(path: str):
-    """Per-workload, per-mode records (CUDA graph of 20 calls per replay, 25
-    warm-up replays, 30 samples; median and min us per call)."""
+    """Per-format and per-activation records beyond the configs (CUDA graph
+    of 20 calls per replay, 25 warm-up replays, 30 samples)."""
     import torch
 
     import fp4_quant_gb300 as G
@@ -424,31 +684,8 @@ def sweep(path: str):
     peaks = measured_peaks()
     recs = []
 
-    def time_graph(fn, reps=20, warm=25, samples=30):
-        s = torch.cuda.Stream(dev)
-        s.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(s):
-            fn(s.cuda_stream)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=s):
-                for _ in range(reps):
-                    fn(s.cuda_stream)
-        torch.cuda.synchronize(dev)
-        for _ in range(warm):
-            graph.replay()
-        torch.cuda.synchronize(dev)
-        out = []
-        for _ in range(samples):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            graph.replay()
-            b.record()
-            b.synchronize()
-            out.append(a.elapsed_time(b) * 1e3 / reps)
-        return statistics.median(out), min(out)
-
     def record(workload, direction, mode, fmt, act, M, N, fn):
-        med, mn = time_graph(fn)
+        med, mn = graph_time([fn], dev)
         nbytes = algo_bytes(direction, mode, M, N, fmt)
         gbps = nbytes / (med * 1e-6) / 1e9
         r = {"workload": workload, "direction": direction, "mode": MODE_NAME.get(mode, "row"),
@@ -459,54 +696,24 @@ def sweep(path: str):
         recs.append(r)
         print(json.dumps(r), file=sys.stderr, flush=True)
 
-    fmts = {"mxfp8": G.FMT_MXFP8, "nvfp4": G.FMT_NVFP4, "bf16": G.FMT_BF16}
-    # workloads
-    x = synth.make(synth.spec("swiglu_128"), dev)
-    record("swiglu_128", "fwd", 1, "mxfp8", "silu", 128, 128,
-           lambda s: G.fwd(x["gate"], x["up"], mode=1, stream=s))
-    x = synth.make(synth.spec("swiglu_4096"), dev, with_dy=True)
-    for m in (1, 2, 3):
-        o = G.fwd(x["gate"], x["up"], mode=m)
-        record("swiglu_4096", "fwd", m, "mxfp8", "silu", 4096, 7168,
-               lambda s, m=m, o=o: G.fwd(x["gate"], x["up"], mode=m, out=o, stream=s))
-        o = G.bwd(x["gate"], x["up"], x["dy"], mode=m)
-        record("swiglu_4096", "bwd", m, "mxfp8", "silu", 4096, 7168,
-               lambda s, m=m, o=o: G.bwd(x["gate"], x["up"], x["dy"], mode=m, out=o, stream=s))
-    for N in (11008, 14336, 18944, 29568):
-        x = synth.make(synth.spec("geglu_8192", N=N), dev, with_dy=True)
-        for fname in ("mxfp8", "bf16"):
-            f = fmts[fname]
-            o = G.fwd(x["gate"], x["up"], act=1, fmt=f)
-            record("geglu_8192", "fwd", 1, fname, "gelu_tanh", 8192, N,
-                   lambda s, o=o, f=f: G.fwd(x["gate"], x["up"], act=1, fmt=f, out=o, stream=s))
-            o = G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=f)
-            record("geglu_8192", "bwd", 1, fname, "gelu_tanh", 8192, N,
-                   lambda s, o=o, f=f: G.bwd(x["gate"], x["up"], x["dy"], act=1, fmt=f, out=o,
-                                             stream=s))
-        del x
-    for M in (784, 968):
-        X = synth.make(synth.spec("geglu_nvfp4", M=M), dev)["x"]
-        o = G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1)
-        record("geglu_nvfp4", "fwd", 1, "nvfp4", "gelu_tanh", M, 16384,
-               lambda s, o=o: G.fwd(X, None, act=1, fmt=G.FMT_NVFP4, layout=1, out=o, stream=s))
-    # the formats and flags beyond the headline calls, on the same shapes
     x = synth.make(synth.spec("swiglu_131072"), dev, with_dy=True)
     M5, N5 = x["gate"].shape
-    for direction, mode in (("fwd", 3), ("bwd", 1)):
+    for direction, mode in (("fwd", 3), ("bwd", 1), ("bwd", 3)):
         f = lambda s, o, dr=direction, m=mode: (
             G.fwd(x["gate"], x["up"], fmt=G.FMT_MXFP8_128X4, mode=m, out=o, stream=s) if dr == "fwd" else
             G.bwd(x["gate"], x["up"], x["dy"], fmt=G.FMT_MXFP8_128X4, mode=m, out=o, stream=s))
         o = f(None, None)
         record("swiglu_131072_mxfp8_128x4", direction, mode, "mxfp8", "silu", M5, N5,
                lambda s, f=f, o=o: f(s, o))
-    # the exact-product gates (ReLU, identity) on the same shape
-    for act, name in ((G.ACT_RELU, "reglu_131072"), (G.ACT_IDENTITY, "bilinear_131072")):
+    for act, name in ((G.ACT_RELU, "reglu_131072"), (G.ACT_IDENTITY, "bilinear_131072"),
+                      (G.ACT_GELU_ERF, "geglu_erf_131072")):
         for direction, mode in (("fwd", 1), ("fwd", 3), ("bwd", 1), ("bwd", 3)):
             f = lambda s, o, dr=direction, m=mode, a=act: (
                 G.fwd(x["gate"], x["up"], act=a, mode=m, out=o, stream=s) if dr == "fwd" else
                 G.bwd(x["gate"], x["up"], x["dy"], act=a, mode=m, out=o, stream=s))
             o = f(None, None)
-            record(name, direction, mode, "mxfp8", "relu" if act == G.ACT_RELU else "identity", M5, N5,
+            record(name, direction, mode, "mxfp8",
+                   {G.ACT_RELU: "relu", G.ACT_IDENTITY: "identity"}.get(act, "gelu_erf"), M5, N5,
                    lambda s, f=f, o=o: f(s, o))
             del o
     for mode in (1, 3):
@@ -543,7 +750,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=131072)
+    ap.add_argument("--no-graph", action="store_true", help="skip the graph-timed per-call figures")
+    ap.add_argument("--no-configs", action="store_true", help="skip the non-headline configs")
+    ap.add_argument("--no-parity", action="store_true", help="skip the comparisons with the oracle")
+    ap.add_argument("--one-core-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--sweep", default=None)
     ap.add_argument("--rows", type=int, default=M_FULL,
@@ -563,18 +773,18 @@ def main():
             print(json.dumps(reference_arm(args, rank, world)), flush=True)
         return
 
-    # CPU baseline first (no GPU context yet), rank 0 at N=1 only
-    cpu = None
-    if not args.no_cpu and rank == 0 and world == 1:
-        cpu = cpu_baseline(args.cpu_rows)
-
     dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    res = gpu_arm(args, rank, world, dist)
-    if cpu is not None:
-        res["cpu_baseline"] = cpu
+    res, host_in, gpu_out, shape = gpu_arm(args, rank, world, dist)
+    if rank == 0 and (not args.no_parity or (not args.no_cpu and world == 1)):
+        cpu, par = cpu_leg(host_in, gpu_out, shape, parity=not args.no_parity,
+                           one_thread_rows=args.one_core_rows)
+        if not args.no_cpu and world == 1:
+            res["cpu_baseline"] = cpu
+        if par is not None:
+            res["parity"] = par
     if args.sweep and rank == 0:
         sweep(args.sweep)
     if rank == 0:

@@ -21,11 +21,11 @@ __all__ = [
     "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
     "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
-    "ACT_SILU", "ACT_GELU_TANH", "ACT_RELU", "ACT_IDENTITY", "ACT_BF16_STEPS", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
+    "ACT_SILU", "ACT_GELU_TANH", "ACT_RELU", "ACT_IDENTITY", "ACT_GELU_ERF", "ACT_BF16_STEPS", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
     "MODE_ROW", "MODE_COL", "MODE_BOTH", "LAYOUT_SPLIT", "LAYOUT_INTERLEAVED",
 ]
 
-ACT_SILU, ACT_GELU_TANH, ACT_RELU, ACT_IDENTITY = 0, 1, 2, 3  # SiLU, GELU (tanh), ReLU (ReGLU), identity (bilinear)
+ACT_SILU, ACT_GELU_TANH, ACT_RELU, ACT_IDENTITY, ACT_GELU_ERF = 0, 1, 2, 3, 4  # SiLU, GELU (tanh), ReLU (ReGLU), identity (bilinear), GELU (erf)
 ACT_BF16_STEPS = 16  # OR-ed into act (forward): the eager bf16 values RN_bf16(RN_bf16(act(g)) * up)
 FMT_MXFP8, FMT_NVFP4, FMT_BF16, FMT_FP32, FMT_MXFP8_128X4 = 0, 1, 2, 3, 4
 MODE_ROW, MODE_COL, MODE_BOTH = 1, 2, 3
@@ -195,6 +195,55 @@ def _check_input(t, name):
         raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:"
+                         f"{torch.cuda.current_device()} (the kernels run on the current device)")
+
+
+def _check_operands(M, N, layout, gate, up, dy=None):
+    """The C layer sees only pointers and strides: check here that the
+    tensors hold the rows and columns the arguments describe."""
+    need = N if layout == LAYOUT_SPLIT else 2 * N
+    if N <= 0 or gate.shape[1] < need:
+        raise ValueError(f"gate has {gate.shape[1]} columns; N = {N} needs at least {need}")
+    if layout == LAYOUT_SPLIT:
+        if up is None:
+            raise ValueError("the split layout needs `up`")
+        if tuple(up.shape) != tuple(gate.shape):
+            raise ValueError(f"up {tuple(up.shape)} and gate {tuple(gate.shape)} differ in shape")
+    elif up is not None:
+        raise ValueError("the interleaved layout takes gate = X and up = None")
+    if dy is not None and (dy.shape[0] != M or dy.shape[1] < N):
+        raise ValueError(f"dy {tuple(dy.shape)} does not hold [{M}, {N}]")
+
+
+_OUT_KEYS = ("q_row", "s_row", "q_col", "s_col")
+
+
+def _check_outputs(o, fmt, sizes, device):
+    """Every output the call writes must exist, be a contiguous CUDA tensor
+    on the inputs' device, have the format's dtype and hold the byte size
+    the library reports (glu_quant_*_sizes); disabled outputs must be None."""
+    import torch
+    want = {"out": sizes[0]} if fmt in (FMT_BF16, FMT_FP32) else dict(zip(_OUT_KEYS, sizes))
+    for k in ("q_row", "s_row", "q_col", "s_col", "out"):
+        t = o.get(k)
+        n = want.get(k, 0)
+        if n == 0:
+            if t is not None:
+                raise ValueError(f"output {k} is not produced by this call; pass None")
+            continue
+        if t is None:
+            raise ValueError(f"output {k} is required ({n} bytes)")
+        dt = (torch.bfloat16 if fmt == FMT_BF16 else torch.float32) if k == "out" else torch.uint8
+        if t.dtype != dt:
+            raise TypeError(f"output {k} must be {dt}, got {t.dtype}")
+        if not t.is_cuda or t.device != device:
+            raise ValueError(f"output {k} must be on {device}, got {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"output {k} must be contiguous")
+        if t.numel() * t.element_size() < n:
+            raise ValueError(f"output {k} holds {t.numel() * t.element_size()} bytes, needs {n}")
 
 
 def fwd(gate, up=None, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
@@ -213,12 +262,20 @@ def fwd(gate, up=None, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
     M = gate.shape[0]
     if N is None:
         N = gate.shape[1] if layout == LAYOUT_SPLIT else gate.shape[1] // 2
+    _check_operands(M, N, layout, gate, up)
     o = out if out is not None else _out_tensors(fmt, mode, M, N, gate.device)
     a = GluQuantFwdArgs(act, fmt, mode, layout, M, N, gate.stride(0), _ptr(gate), _ptr(up),
-                        _ptr(o["q_row"]), _ptr(o["s_row"]), _ptr(o["q_col"]), _ptr(o["s_col"]),
-                        _ptr(o["out"]))
+                        _ptr(o.get("q_row")), _ptr(o.get("s_row")), _ptr(o.get("q_col")),
+                        _ptr(o.get("s_col")), _ptr(o.get("out")))
+    st, sizes = glu_quant_fwd_sizes(a)
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_fwd_sizes")
+    _check_outputs(o, fmt, sizes, gate.device)
     sh = stream if stream is not None else _stream_handle(gate.device)
     if amax is not None:
+        import torch
+        if amax.dtype != torch.float32 or amax.numel() < 1 or amax.device != gate.device:
+            raise ValueError("amax must be a float32 tensor of at least one element on the inputs' device")
         st = glu_quant_fwd_nvfp4_gs(a, _ptr(amax), sh)
         if st != GLU_OK:
             raise GluQuantError(st, "glu_quant_fwd_nvfp4_gs")
@@ -241,10 +298,15 @@ def bwd(gate, up, dy, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
     M = gate.shape[0]
     if N is None:
         N = gate.shape[1] if layout == LAYOUT_SPLIT else gate.shape[1] // 2
+    _check_operands(M, N, layout, gate, up, dy)
     o = out if out is not None else _out_tensors(fmt, mode, M, 2 * N, gate.device)
     a = GluQuantBwdArgs(act, fmt, mode, layout, M, N, gate.stride(0), dy.stride(0), _ptr(gate),
-                        _ptr(up), _ptr(dy), _ptr(o["q_row"]), _ptr(o["s_row"]),
-                        _ptr(o["q_col"]), _ptr(o["s_col"]), _ptr(o["out"]))
+                        _ptr(up), _ptr(dy), _ptr(o.get("q_row")), _ptr(o.get("s_row")),
+                        _ptr(o.get("q_col")), _ptr(o.get("s_col")), _ptr(o.get("out")))
+    st, sizes = glu_quant_bwd_sizes(a)
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_bwd_sizes")
+    _check_outputs(o, fmt, sizes, gate.device)
     st = glu_quant_bwd(a, stream if stream is not None else _stream_handle(gate.device))
     if st != GLU_OK:
         raise GluQuantError(st, "glu_quant_bwd")

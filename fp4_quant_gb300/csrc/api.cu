@@ -29,7 +29,7 @@ int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t
                  int64_t ld_in, const void* gate, const void* up, const void* q_row,
                  const void* s_row, const void* q_col, const void* s_col, const void* out) {
   const int32_t act_kind = act & ~GLU_ACT_BF16_STEPS;
-  if (act_kind < GLU_ACT_SILU || act_kind > GLU_ACT_IDENTITY) return GLU_EINVAL;
+  if (act_kind < GLU_ACT_SILU || act_kind > GLU_ACT_GELU_ERF) return GLU_EINVAL;
   if (fmt < GLU_FMT_MXFP8_E4M3 || fmt > GLU_FMT_MXFP8_E4M3_128X4) return GLU_EINVAL;
   if (mode < GLU_MODE_ROW || mode > GLU_MODE_BOTH) return GLU_EINVAL;
   if (layout != GLU_LAYOUT_SPLIT && layout != GLU_LAYOUT_INTERLEAVED) return GLU_EINVAL;

@@ -368,7 +368,8 @@ cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
     case GLU_ACT_SILU: return by_layout<0, GLU_MODE_BOTH>(a, s, d);
     case GLU_ACT_GELU_TANH: return by_layout<1, GLU_MODE_BOTH>(a, s, d);
     case GLU_ACT_RELU: return by_layout<2, GLU_MODE_BOTH>(a, s, d);
-    default: return by_layout<3, GLU_MODE_BOTH>(a, s, d);
+    case GLU_ACT_IDENTITY: return by_layout<3, GLU_MODE_BOTH>(a, s, d);
+    default: return by_layout<4, GLU_MODE_BOTH>(a, s, d);
   }
 }
 

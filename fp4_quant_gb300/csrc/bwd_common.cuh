@@ -35,7 +35,8 @@ struct BwdP {
   const uint16_t* dy;
   int64_t ld, ld_dy;
   int64_t M, N;
-  uint8_t* q_row;  // NVFP4 codes [M, N] (stored directly; MXFP8 codes leave by TMA)
+  uint8_t* q_row;  // codes [M, 2N] (NVFP4 [M, N] packed), for the kernels that store them directly
+  uint8_t* q_col;  // codes [2N, M], likewise
   uint8_t* s_row;
   uint8_t* s_col;
   ScaleLayout sl_row, sl_col;  // scale matrices [M, 2N/32] and [2N, M/32]
@@ -160,7 +161,7 @@ __device__ __forceinline__ float bf(uint32_t b16) { return __uint_as_float(b16 <
 // sign bit set): SiLU -64, GELU -6.
 template <int ACT>
 struct FastRangeAcc {  // exact-product gates: no limit (above every pattern)
-  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u : ACT == 0 ? 0xC280u : 0xC0C0u;
+  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u : kErfAct<ACT> ? 0xC150u : ACT == 0 ? 0xC280u : 0xC0C0u;
 };
 template <int ACT>
 __device__ __forceinline__ bool range_ok(uint32_t vmax) {
@@ -181,6 +182,8 @@ __device__ __forceinline__ float exact_bwd(const float4* hot, uint32_t gb, uint3
   const float g = bf(gb), u = bf(ub), d = bf(db);
   if constexpr (kExactAct<ACT>)
     return which == 0 ? __fmul_rn(d, __fmul_rn(u, xact_grad<ACT>(g))) : __fmul_rn(d, xact<ACT>(g));
+  if constexpr (kErfAct<ACT>)  // fp64, rounded once
+    return which == 0 ? slow_grad_mul(4, g, d, u) : slow_act_mul(4, g, d);
   const int k = hot != nullptr ? hot_index<kHotLo, kHotBin>(gb) : -1;
   if (k >= 0) {
     const float4 e = hot[k];

@@ -67,6 +67,7 @@ cudaError_t make_params(BwdP& p, const glu_quant_bwd_args& a) {
   p.M = a.M;
   p.N = a.N;
   p.q_row = static_cast<uint8_t*>(a.q_row);
+  p.q_col = static_cast<uint8_t*>(a.q_col);
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.sl_row = a.fmt == GLU_FMT_NVFP4_E2M1 ? scale_layout(2 * a.N / 16, true)
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
   const int64_t units = n_su * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  if (hot_for(MODE) && !kExactAct<ACT>)
+  if (hot_for(MODE) && kTabAct<ACT>)
     load_hot_table<16, kHotLo, kHotBin>(hot_raw, ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
               x[i] = exact_bwd<ACT>(hot, sv.g16(lane, e0 + i), sv.u16(lane, e0 + i), sv.d16(lane, e0 + i), which);
           };
         };
-        const float dgd = Bracket<ACT>::kExact ? Bracket<ACT>::kNv : 2.0f * dgate_bracket(nrow), dud = Bracket<ACT>::kNv;
+        const float dgd = Bracket<ACT>::kExact ? Bracket<ACT>::kNv : 2.0f * dgate_width<ACT>(nrow), dud = Bracket<ACT>::kNv;
         uint32_t c[8], sc[4];
         sc[0] = nv_block<0>(dg, c[0], c[1], dgd, ex(0), ex8(0));
         sc[1] = nv_block<16>(dg, c[2], c[3], dgd, ex(0), ex8(0));
@@ -514,7 +515,8 @@ cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
       case GLU_ACT_SILU: e = by_mode<0>(a, s, d); break;
       case GLU_ACT_GELU_TANH: e = by_mode<1>(a, s, d); break;
       case GLU_ACT_RELU: e = by_mode<2>(a, s, d); break;
-      default: e = by_mode<3>(a, s, d); break;
+      case GLU_ACT_IDENTITY: e = by_mode<3>(a, s, d); break;
+      default: e = by_mode<4>(a, s, d); break;
     }
   }
   if (e == cudaSuccess && a.fmt == GLU_FMT_NVFP4_E2M1)  // scale padding (rows to 128, columns to 4)

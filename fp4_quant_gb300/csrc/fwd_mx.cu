@@ -8,7 +8,9 @@ namespace gq {
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d) {
   cudaError_t e;
-  if ((a.act & ~GLU_ACT_BF16_STEPS) >= GLU_ACT_RELU)
+  if ((a.act & ~GLU_ACT_BF16_STEPS) == GLU_ACT_GELU_ERF)
+    e = launch_fwd_mx_erf(a, s, d);
+  else if ((a.act & ~GLU_ACT_BF16_STEPS) >= GLU_ACT_RELU)
     e = launch_fwd_mx_x(a, s, d);
   else if (a.act & GLU_ACT_BF16_STEPS)
     e = launch_fwd_mx_b16(a, s, d);
@@ -25,15 +27,18 @@ cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const Dev
 
 cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
                              const DevInfo& d) {
+  if ((a.act & ~GLU_ACT_BF16_STEPS) == GLU_ACT_GELU_ERF) return launch_fwd_nvfp4_erf(a, amax, s, d);
   if ((a.act & ~GLU_ACT_BF16_STEPS) >= GLU_ACT_RELU) return launch_fwd_nvfp4_x(a, amax, s, d);
   if (a.act & GLU_ACT_BF16_STEPS) return launch_fwd_nvfp4_b16(a, amax, s, d);
   return a.act == GLU_ACT_SILU ? by_layout<0, kModeNv>(a, amax, s, d) : by_layout<1, kModeNv>(a, amax, s, d);
 }
 
 cudaError_t read_err_fwd_mx(uint32_t* v, bool clear) {
-  uint32_t b16 = 0, x = 0;
+  uint32_t b16 = 0, x = 0, er = 0;
   cudaError_t e = read_err_fwd_b16(&b16, clear);
   if (e == cudaSuccess) e = read_err_fwd_x(&x, clear);
+  if (e == cudaSuccess) e = read_err_fwd_erf(&er, clear);
+  x |= er;
   if (e == cudaSuccess) e = cudaMemcpyFromSymbol(v, g_err_fwd_mx, sizeof(uint32_t));
   if (e == cudaSuccess) *v |= b16 | x;
   if (e == cudaSuccess && clear) {

@@ -161,9 +161,9 @@ __device__ __forceinline__ int swz(int r, int chunk) { return r * 128 + 16 * (ch
 template <int ACT>
 constexpr bool kExactVals = (ACT & 16) || kExactAct<ACT>;
 template <int ACT>
-constexpr float kDQuant = kExactVals<ACT> ? 0.0f : Bracket<ACT & 1>::kAct;
+constexpr float kDQuant = kExactVals<ACT> ? 0.0f : Bracket<ACT & 15>::kAct;
 template <int ACT>
-constexpr float kDNv = kExactVals<ACT> ? 0x1p-21f : Bracket<ACT & 1>::kNv;
+constexpr float kDNv = kExactVals<ACT> ? 0x1p-21f : Bracket<ACT & 15>::kNv;
 
 // Values of a pair (elements e, e + 1 of a block) from the fast form: fp32,
 // or the bf16 steps, where a pair whose bf16 rounding of act(g) is undecided
@@ -178,9 +178,12 @@ __device__ __forceinline__ float2 fast_vals(float2 g, float2 u, uint32_t& bad, i
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb) : "f"(h.y), "f"(h.x));
     return make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
   }
-  if (!(ACT & 16)) return fast_h2<ACT & 1>(g, u);
+  if (!(ACT & 16)) {
+    if constexpr (kErfAct<ACT>) return erf_h2(g, u);
+    else return fast_h2<ACT & 1>(g, u);
+  }
   bool b;
-  const float2 h = fast_h2_bf16<ACT & 1>(g, u, Bracket<ACT & 1>::kAct, b);
+  const float2 h = fast_h2_bf16<ACT & 15>(g, u, Bracket<ACT & 15>::kAct, b);
   bad |= uint32_t(b) * (3u << e);
   return h;
 }
@@ -250,7 +253,7 @@ __device__ __forceinline__ void fix_range(float (&v)[32], const uint8_t* st, con
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const uint32_t x = ROW ? stage_pair<LAYOUT, UP_BOX>(st, w, lane, e) : stage_pair<LAYOUT, UP_BOX>(st, w, e, lane);
-    emask |= uint32_t((x & 0xFFFFu) >= FastRange<ACT & 1>::kNegLimit) << e;
+    emask |= uint32_t((x & 0xFFFFu) >= FastRange<ACT & 15>::kNegLimit) << e;
   }
   while (emask != 0u) {
     const int e = __ffs(emask) - 1;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
   const int64_t units = row_walk(MODE) ? p.ntiles : p.n_rs * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
-  if (!kExactAct<ACT>)
+  if (kTabAct<ACT>)
     load_hot_table<8, hot_lo_for(MODE), hot_bin_for(MODE)>(hot_raw, (ACT & 1) == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1);
   // NVFP4 global encode scale 2688 / amax (448 * 6 over the tensor amax,
   // IEEE division); 1 without an amax, or for a zero or non-finite one

@@ -111,7 +111,15 @@ __host__ __device__ inline ScaleLayout scale_layout(int64_t cols, bool swz) {
 // dY up act'(g) rounded once, which is a signed zero where act' = 0 even when
 // dY up would overflow fp32.
 template <int ACT>
-constexpr bool kExactAct = (ACT & 15) >= 2;
+constexpr bool kExactAct = (ACT & 15) == 2 || (ACT & 15) == 3;
+// ACT & 15 == 4: GELU with the exact normal CDF, act(x) = x Phi(x) (the erf
+// form of GeGLU).  Fast forms from normcdff and expf, exact values in fp64
+// (no activation tables).
+template <int ACT>
+constexpr bool kErfAct = (ACT & 15) == 4;
+// SiLU and GELU (tanh): fast forms plus exact activation tables
+template <int ACT>
+constexpr bool kTabAct = (ACT & 15) <= 1;
 
 template <int ACT>
 __device__ __forceinline__ float xact(float g) {
@@ -147,13 +155,18 @@ __device__ __forceinline__ float tab_mul(float2 e, float u) {
 constexpr double kGeluC = 0.79788456080286535587989211986876;  // sqrt(2/pi)
 constexpr double kGeluA = 0.044715;
 
+constexpr double kSqrtHalf = 0.70710678118654752440;       // 1/sqrt(2)
+constexpr double kInvSqrt2Pi = 0.39894228040143267793994605993438;  // 1/sqrt(2 pi)
+
 __device__ __forceinline__ double act_f64(int act, double x) {
+  if (act == 4) return x * (0.5 * erfc(-x * kSqrtHalf));  // x Phi(x), no cancellation for x << 0
   if (act == 0) return x / (1.0 + exp(-x));
   double y = kGeluC * (x + kGeluA * x * x * x);
   return x / (1.0 + exp(-2.0 * y));
 }
 
 __device__ __forceinline__ double act_grad_f64(int act, double x) {
+  if (act == 4) return 0.5 * erfc(-x * kSqrtHalf) + x * (exp(-0.5 * x * x) * kInvSqrt2Pi);
   if (act == 0) {
     double s = 1.0 / (1.0 + exp(-x)), sn = 1.0 / (1.0 + exp(x));
     return s * (1.0 + x * sn);
@@ -299,6 +312,10 @@ __device__ __forceinline__ float exact_h(const float2* hot, float g, float u) {
     const float h = __fmul_rn(xact<ACT>(g), u);  // act(g) is bf16 already
     return (ACT & 16) ? bf16_rn(h) : h;
   }
+  if constexpr (kErfAct<ACT>) {  // fp64 (rare: undecided codes and blocks, gates below the fast range)
+    if (ACT & 16) return bf16_rn(__fmul_rn(bf16_from_double(act_f64(4, (double)g)), u));
+    return slow_act_mul(4, g, u);
+  }
   constexpr int A = ACT & 1;
   if (!(ACT & 16)) return exact_act_mul_hot<A, LO, BIN>(hot, g, u);
   const int k = hot_index<LO, BIN>(__float_as_uint(g) >> 16);
@@ -388,13 +405,27 @@ __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
   return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
+// GELU (erf) forward for a pair: (g u) Phi(g), Phi from normcdff (at most 5
+// ulp by CUDA's documentation); measured over every bf16 gate of (-13, 64),
+// g Phi(g) is within 4.8 units of 2^-24 of the exact value.
+__device__ __forceinline__ float2 erf_h2(float2 g, float2 u) {
+  return mul2(mul2(g, u), make_float2(normcdff(g.x), normcdff(g.y)));
+}
+
+// act(g) of a pair from the activation's fast form (u = 1).
+template <int ACT>
+__device__ __forceinline__ float2 fast_act2(float2 g) {
+  if constexpr (kErfAct<ACT>) return erf_h2(g, splat2(1.0f));
+  else return fast_h2<ACT & 1>(g, splat2(1.0f));
+}
+
 // bf16-steps values of a pair from the fast form: act(g) (fast_h2 with u = 1)
 // is rounded to bf16 at both ends of the rounding-test bracket (the ACT
 // half-width); `bad` is set when they differ (the caller then takes exact
 // values), else h = RN_bf16(a * u) is exact.
 template <int ACT>
 __device__ __forceinline__ float2 fast_h2_bf16(float2 g, float2 u, float d, bool& bad) {
-  const float2 a = fast_h2<ACT>(g, splat2(1.0f));
+  const float2 a = fast_act2<ACT>(g);
   const float2 lo = mul2(a, splat2(1.0f - d)), hi = mul2(a, splat2(1.0f + d));
   uint32_t bl, bh;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(bl) : "f"(lo.y), "f"(lo.x));
@@ -412,7 +443,9 @@ __device__ __forceinline__ float2 fast_h2_bf16(float2 g, float2 u, float d, bool
 // path's lower limit.  Positive gates never reach it.
 template <int ACT>
 struct FastRange {  // exact-product gates: no limit (above every pattern)
-  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u : ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
+  static constexpr uint32_t kNegLimit = kExactAct<ACT> ? 0x10000u
+                                       : kErfAct<ACT> ? 0xC150u   // bf16 -13 (Phi subnormal below)
+                                       : ACT == 0 ? 0xC280u : 0xC0E0u;  // bf16 -64, -7
 };
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
 template <int ACT>
@@ -444,6 +477,20 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
     dg = mul2(d, mul2(u, make_float2(xact_grad<ACT>(g.x), xact_grad<ACT>(g.y))));
     du = mul2(d, make_float2(xact<ACT>(g.x), xact<ACT>(g.y)));
     n = splat2(__int_as_float(0x7F800000));  // no zero of act' to widen for
+    return;
+  }
+  if constexpr (kErfAct<ACT>) {
+    // act'(g) = A + B, A = Phi(g) (normcdff), B = g phi(g) with g^2 exact and
+    // expf; the sum cancels near g = -0.752, and n = (A + B) / (|A| + |B|)
+    // measures it: over every bf16 gate of (-13, 64) the error of A + B is
+    // within 4.4 / |n| units of 2^-24 (smallest |n| 0.0017, at g = -0.75)
+    const float2 A = make_float2(normcdff(g.x), normcdff(g.y));
+    const float2 q = mul2(splat2(-0.5f), mul2(g, g));
+    const float2 B = mul2(g, mul2(make_float2(expf(q.x), expf(q.y)), splat2(0.3989422804014327f)));
+    const float2 ap = add2(A, B);
+    n = make_float2(__fdiv_rn(ap.x, fabsf(A.x) + fabsf(B.x)), __fdiv_rn(ap.y, fabsf(A.y) + fabsf(B.y)));
+    du = mul2(mul2(d, g), A);
+    dg = mul2(mul2(d, u), ap);
     return;
   }
   float2 E, t1;
@@ -483,9 +530,10 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
 // NVFP4 keeps 2^-21 for the roundings of 1/6, 1/s and the bracket products.
 template <int ACT> struct Bracket {
   static constexpr bool kExact = kExactAct<ACT>;
-  static constexpr float kAct = kExact ? 0.0f : ACT == 0 ? 0x1p-20f : 0x1p-18f;
+  static constexpr float kAct = kExact ? 0.0f : (ACT == 0 || kErfAct<ACT>) ? 0x1p-20f : 0x1p-18f;
   static constexpr float kDUp = kAct;
-  static constexpr float kDGate = kExact ? 0.0f : 0x1p-14f;     // the widest dgate_bracket step
+  // the widest dgate_bracket / dgate_bracket_erf step
+  static constexpr float kDGate = kExact ? 0.0f : kErfAct<ACT> ? 0x1p-11f : 0x1p-14f;
   static constexpr float kDGateFar = kExact ? 0.0f : 0x1p-18f;  // |N| >= 1/8
   // NVFP4: the activation's width plus the roundings of 1/6, 1/s and the
   // bracket products (4 units of 2^-24 at most)
@@ -507,9 +555,22 @@ __device__ __forceinline__ float dgate_bracket(float nmin) {
 }
 
 // dgate_bracket for the activation (zero for the exact-product gates).
+// GELU (erf): error bound 2 + 4.4 / nmin units of 2^-24 (n the cancellation
+// ratio of act', see bwd_fast2), rounded up to a power of two.
+__device__ __forceinline__ float dgate_bracket_erf(float nmin) {
+  return nmin >= 0x1p-3f ? 0x1p-18f
+       : nmin >= 0x1p-4f ? 0x1p-17f
+       : nmin >= 0x1p-5f ? 0x1p-16f
+       : nmin >= 0x1p-6f ? 0x1p-15f
+       : nmin >= 0x1p-7f ? 0x1p-14f
+       : nmin >= 0x1p-8f ? 0x1p-13f
+       : nmin >= 0x1p-9f ? 0x1p-12f
+                          : 0x1p-11f;
+}
+
 template <int ACT>
 __device__ __forceinline__ float dgate_width(float nmin) {
-  return Bracket<ACT>::kExact ? 0.0f : dgate_bracket(nmin);
+  return Bracket<ACT>::kExact ? 0.0f : kErfAct<ACT> ? dgate_bracket_erf(nmin) : dgate_bracket(nmin);
 }
 
 // min |x| of three values (three-input min, sm_100+; NaNs ignored).

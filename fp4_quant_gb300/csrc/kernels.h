@@ -46,6 +46,12 @@ cudaError_t launch_fwd_mx_x(const glu_quant_fwd_args& a, cudaStream_t s, const D
 cudaError_t launch_fwd_nvfp4_x(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
                                const DevInfo& d);
 cudaError_t read_err_fwd_x(uint32_t* v, bool clear);
+// The forward kernels for GELU with the exact normal CDF, with or without the
+// bf16 steps (fwd_mx_erf.cu).
+cudaError_t launch_fwd_mx_erf(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
+cudaError_t launch_fwd_nvfp4_erf(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
+                                 const DevInfo& d);
+cudaError_t read_err_fwd_erf(uint32_t* v, bool clear);
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);  // (includes the both-directions kernel's bits)
 cudaError_t read_err_bwd_cb(uint32_t* v, bool clear);
 

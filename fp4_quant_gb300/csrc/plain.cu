@@ -79,7 +79,7 @@ template <int ACT, int BWD, int LAYOUT, typename OutT, int VEC>
 __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr int kEntry = BWD ? 16 : 8;
-  if (!kExactAct<ACT>) {
+  if (kTabAct<ACT>) {
     const uint4* src = reinterpret_cast<const uint4*>(
         BWD ? ((ACT & 1) == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1) : ((ACT & 1) == 0 ? gq_tab_fwd_0 : gq_tab_fwd_1));
     uint4* dst = reinterpret_cast<uint4*>(smem);
@@ -120,12 +120,17 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
           u = bf16_hi(w);
         }
         const uint32_t idx = tab_index(g16);
-        if (kExactAct<ACT>) {  // exact products, rounded once (the bf16 steps: to bf16)
+        if (!kTabAct<ACT>) {  // exact products (GELU erf: fp64), rounded once (the bf16 steps: to bf16)
           const float g = __uint_as_float(g16 << 16);
           if (BWD) {
             const float dv = (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
-            b[k] = __fmul_rn(dv, xact<ACT>(g));
-            a[k] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+            if constexpr (kErfAct<ACT>) {
+              b[k] = slow_act_mul(4, g, dv);
+              a[k] = slow_grad_mul(4, g, dv, u);
+            } else {
+              b[k] = __fmul_rn(dv, xact<ACT>(g));
+              a[k] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+            }
           } else {
             a[k] = exact_h<ACT>(nullptr, g, u);
           }
@@ -148,12 +153,17 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
       uint32_t g16;
       gu_at(p, LAYOUT, r, c0, g, g16, u);
       const uint32_t idx = tab_index(g16);
-      if (kExactAct<ACT>) {
+      if (!kTabAct<ACT>) {
         if (BWD) {
           const float dv =
               __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0]) << 16);
-          b[0] = __fmul_rn(dv, xact<ACT>(g));
-          a[0] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+          if constexpr (kErfAct<ACT>) {
+            b[0] = slow_act_mul(4, g, dv);
+            a[0] = slow_grad_mul(4, g, dv, u);
+          } else {
+            b[0] = __fmul_rn(dv, xact<ACT>(g));
+            a[0] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+          }
         } else {
           a[0] = exact_h<ACT>(nullptr, g, u);
         }
@@ -171,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
         cold = is_cold(a[0]);
       }
     }
-    if (!kExactAct<ACT> && cold) {
+    if (kTabAct<ACT> && cold) {
 #pragma unroll
       for (int k = 0; k < VEC; ++k) {
         float g, u;
@@ -200,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
 template <int ACT, int BWD, int LAYOUT, typename OutT>
 cudaError_t launch_t(PlainP p, cudaStream_t s, const DevInfo& d) {
   const bool vec = (p.N % 8) == 0;
-  const int smem = kExactAct<ACT> ? 0 : int(kTabEntries) * (BWD ? 16 : 8);
+  const int smem = kTabAct<ACT> ? int(kTabEntries) * (BWD ? 16 : 8) : 0;
   auto kern = vec ? plain_kernel<ACT, BWD, LAYOUT, OutT, 8> : plain_kernel<ACT, BWD, LAYOUT, OutT, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -231,11 +241,13 @@ cudaError_t dispatch(const PlainP& p, int act, int fmt, int layout, cudaStream_t
     case GLU_ACT_GELU_TANH: return by_out<1, BWD>(p, fmt, layout, s, d);
     case GLU_ACT_RELU: return by_out<2, BWD>(p, fmt, layout, s, d);
     case GLU_ACT_IDENTITY: return by_out<3, BWD>(p, fmt, layout, s, d);
+    case GLU_ACT_GELU_ERF: return by_out<4, BWD>(p, fmt, layout, s, d);
     // the bf16 steps: forward only
     case GLU_ACT_SILU | GLU_ACT_BF16_STEPS: return by_out<16, 0>(p, fmt, layout, s, d);
     case GLU_ACT_GELU_TANH | GLU_ACT_BF16_STEPS: return by_out<17, 0>(p, fmt, layout, s, d);
     case GLU_ACT_RELU | GLU_ACT_BF16_STEPS: return by_out<18, 0>(p, fmt, layout, s, d);
-    default: return by_out<19, 0>(p, fmt, layout, s, d);
+    case GLU_ACT_IDENTITY | GLU_ACT_BF16_STEPS: return by_out<19, 0>(p, fmt, layout, s, d);
+    default: return by_out<20, 0>(p, fmt, layout, s, d);
   }
 }
 

@@ -38,10 +38,17 @@
  * inputs are read and the outputs fully overwritten; outputs must not alias
  * inputs.
  *
- * Errors: every argument is checked before anything is launched.  A nonzero
- * return means nothing was launched and nothing was written (fail closed; no
- * fallback path exists).  GLU_ELAUNCH reports a CUDA error returned by the
- * launch itself.
+ * Errors: every argument is checked before anything is launched.  A status
+ * other than GLU_OK and GLU_ELAUNCH means nothing was launched and nothing
+ * was written (fail closed; no fallback path exists).  GLU_ELAUNCH reports a
+ * CUDA error returned by a launch itself; some calls launch two kernels (the
+ * main kernel, then one that zeroes the padding of a 128x4 scale buffer), so
+ * after GLU_ELAUNCH the outputs are undefined.  When a CUDA runtime call made
+ * by the library fails (GLU_ELAUNCH, GLU_EDEVICE), the library reports it
+ * through the status and resets the calling thread's CUDA last-error state
+ * (cudaGetLastError), so an earlier non-sticky error of the caller's own that
+ * was still pending is cleared with it; a successful call leaves that state
+ * alone.
  */
 #ifndef GLU_QUANT_H
 #define GLU_QUANT_H
@@ -53,7 +60,7 @@
 extern "C" {
 #endif
 
-#define GLU_QUANT_ABI_VERSION 3
+#define GLU_QUANT_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define GLU_API __attribute__((visibility("default")))
@@ -88,6 +95,9 @@ enum glu_act {
    * sign of up and dY, and dGate a zero with the sign of dY * up. */
   GLU_ACT_RELU = 2,
   GLU_ACT_IDENTITY = 3,
+  /* ABI 4: GELU with the exact normal CDF, act(x) = x Phi(x) = 0.5 x (1 +
+   * erf(x / sqrt 2)) (the erf form of GeGLU), act'(x) = Phi(x) + x phi(x). */
+  GLU_ACT_GELU_ERF = 4,
   /* OR-ed into act, forward only (ABI 2): the eager bf16 values
    * h = RN_bf16(RN_bf16(act(gate)) * up) in place of act(gate) * up in
    * fp32 ("Add swiglu + MXFP8 fused CuTe DSL kernel", Numerics and tests:
@@ -211,7 +221,10 @@ GLU_API int glu_quant_bwd(const glu_quant_bwd_args* args, void* stream);
 /* Byte sizes of the four outputs the arguments describe, in the order
  * q_row, s_row, q_col, s_col (for BF16/FP32, sizes[0] is the `out` size and
  * the rest are 0; disabled outputs are 0).  Checks the arguments like the
- * launch does (pointers are not looked at).  Touches no device. */
+ * launch does (pointers are not looked at).  Touches no device.  No page
+ * defines such a query; it is one function per argument struct (forward and
+ * backward) rather than one taking either, so that each keeps its own typed
+ * argument. */
 GLU_API int glu_quant_fwd_sizes(const glu_quant_fwd_args* args, size_t sizes[4]);
 GLU_API int glu_quant_bwd_sizes(const glu_quant_bwd_args* args, size_t sizes[4]);
 

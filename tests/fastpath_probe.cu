@@ -17,7 +17,7 @@ __global__ void probe_kernel(float* out) {
   if (i >= 65536) return;
   const float g = __uint_as_float(uint32_t(i) << 16);
   const float2 g2 = make_float2(g, g), one = make_float2(1.0f, 1.0f);
-  const float2 h = gq::fast_h2<ACT>(g2, one);
+  const float2 h = gq::fast_act2<ACT>(g2);
   float2 dg, du, n;
   gq::bwd_fast2<ACT>(g2, one, one, dg, du, n);
   out[4 * i] = h.x;
@@ -28,16 +28,18 @@ __global__ void probe_kernel(float* out) {
 
 }  // namespace
 
-// Fills host[4 * 65536] for activation `act` (0 SiLU, 1 GELU tanh); returns a
-// cudaError_t value.
+// Fills host[4 * 65536] for activation `act` (0 SiLU, 1 GELU tanh, 4 GELU
+// erf); returns a cudaError_t value.
 extern "C" __attribute__((visibility("default"))) int gq_probe_fast(int act, float* host) {
   float* d = nullptr;
   cudaError_t e = cudaMalloc(&d, 4 * 65536 * sizeof(float));
   if (e != cudaSuccess) return int(e);
   if (act == 0)
     probe_kernel<0><<<256, 256>>>(d);
-  else
+  else if (act == 1)
     probe_kernel<1><<<256, 256>>>(d);
+  else
+    probe_kernel<4><<<256, 256>>>(d);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaMemcpy(host, d, 4 * 65536 * sizeof(float), cudaMemcpyDeviceToHost);
   cudaFree(d);

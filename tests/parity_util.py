@@ -150,3 +150,83 @@ def host(t):
     if t.dtype == torch.bfloat16:
         return host_bits(t)
     return t.detach().cpu().numpy()
+
+
+# ---- full-size comparison with counts (pre-quant values only where needed) --
+
+def _nvfp4_scale_offsets(r, c, W):
+    """Byte offsets of scales (r, c) of a [*, W/16] NVFP4 scale matrix in the
+    128x4 layout."""
+    cp = -(-(W // 16) // 4) * 4
+    return ((r // 128) * (cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+
+
+def compare_counts(gpu: dict, ref: dict, fmt: int, mode: int, M: int, W: int, h_rows) -> dict:
+    """Compare one call's outputs with the oracle's under the rules above and
+    return counts instead of raising: compared elements and scales, scale
+    mismatches (the rules allow none), code mismatches inside the 2-ulp
+    window with one code step (allowed, counted) and outside it (none
+    allowed).  The oracle's exact values are needed only where codes differ;
+    ``h_rows(rows)`` returns them ([len(rows), W] fp32, the FP32-mode oracle
+    on those rows), so a full-size call needs no [M, W] array of them."""
+    res = {"elements": 0, "scales": 0, "scale_mismatches": 0, "code_mismatches": 0,
+           "window": 0, "out_of_window": 0}
+
+    def codes(q_g, q_r, to_rc, v_of, fmt_c):
+        bad = np.flatnonzero(q_g.ravel() != q_r.ravel())
+        res["elements"] += q_r.size
+        if bad.size == 0:
+            return
+        res["code_mismatches"] += bad.size
+        r, c = to_rc(bad)
+        rows, inv = np.unique(r, return_inverse=True)
+        h = np.asarray(h_rows(rows), np.float32)[inv, c]
+        v = v_of(h, r, c)
+        g, q = q_g.ravel()[bad], q_r.ravel()[bad]
+        if fmt_c == BF16_CODES:
+            isnan = lambda b: ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+            nan_ok = isnan(g) & isnan(q)
+            ok = nan_ok | ((O.boundary_ulps(O.BF16, v) <= WINDOW_ULPS)
+                           & (np.abs(g.astype(np.int32) - q.astype(np.int32)) == 1))
+        else:
+            adj = _adjacent_e4m3(g, q) if fmt_c == O.MXFP8 else _adjacent_e2m1(g, q)
+            ok = (O.boundary_ulps(fmt_c, v) <= WINDOW_ULPS) & adj
+        res["window"] += int(ok.sum())
+        res["out_of_window"] += int((~ok).sum())
+
+    def scales(s_g, s_r):
+        res["scales"] += s_r.size
+        res["scale_mismatches"] += int(np.count_nonzero(s_g != s_r))
+
+    if fmt in (O.MXFP8,):
+        if mode & O.ROW:
+            scales(gpu["s_row"], ref["s_row"])
+            s = ref["s_row"].astype(np.int32)
+            codes(gpu["q_row"], ref["q_row"], lambda i: (i // W, i % W),
+                  lambda h, r, c: (h.astype(np.float64) * np.exp2(127.0 - s[r, c // 32])).astype(np.float32),
+                  O.MXFP8)
+        if mode & O.COL:
+            scales(gpu["s_col"], ref["s_col"])
+            s = ref["s_col"].astype(np.int32)
+            codes(gpu["q_col"], ref["q_col"], lambda i: (i % M, i // M),
+                  lambda h, r, c: (h.astype(np.float64) * np.exp2(127.0 - s[c, r // 32])).astype(np.float32),
+                  O.MXFP8)
+    elif fmt == O.NVFP4:
+        scales(gpu["s_row"], ref["s_nvfp4"])
+        unpack = lambda q: np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[0], -1)
+        sb = ref["s_nvfp4"]
+
+        def v_nv(h, r, c):
+            s = O.e4m3_decode(sb[_nvfp4_scale_offsets(r, c // 16, W)]).astype(np.float32)
+            with np.errstate(divide="ignore", invalid="ignore"):
+                return np.where(s == 0, np.float32(0), h / np.where(s == 0, 1, s)).astype(np.float32)
+        codes(unpack(gpu["q_row"]), unpack(ref["out"]), lambda i: (i // W, i % W), v_nv, O.NVFP4)
+    elif fmt == O.BF16:
+        codes(gpu["out"], ref["out"], lambda i: (i // W, i % W), lambda h, r, c: h, BF16_CODES)
+    else:
+        raise ValueError("compare_counts covers MXFP8, NVFP4 and BF16 outputs")
+    res["ok"] = res["scale_mismatches"] == 0 and res["out_of_window"] == 0
+    return res
+
+
+BF16_CODES = -1  # compare_counts: the codes are bf16 bit patterns

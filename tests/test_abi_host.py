@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert G.glu_quant_abi_version() == 3
+    assert G.glu_quant_abi_version() == 4
     for st in (0, -1, -2, -3, -4, -5):
         assert G.glu_quant_status_str(st) != "unknown status"
     assert G.glu_quant_status_str(7) == "unknown status"
@@ -61,8 +61,8 @@ def _no_gpu():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(act=4), G.GLU_EINVAL),
-    (dict(act=20), G.GLU_EINVAL),
+    (dict(act=5), G.GLU_EINVAL),
+    (dict(act=21), G.GLU_EINVAL),
     (dict(act=32), G.GLU_EINVAL),
     (dict(fmt=5), G.GLU_EINVAL),
     (dict(mode=0), G.GLU_EINVAL),
@@ -152,7 +152,7 @@ def test_binding_mirrors_the_header(tmp_path):
         pytest.skip("no C compiler")
     fields = {"glu_quant_fwd_args": G.GluQuantFwdArgs, "glu_quant_bwd_args": G.GluQuantBwdArgs}
     consts = {"GLU_ACT_SILU": G.ACT_SILU, "GLU_ACT_GELU_TANH": G.ACT_GELU_TANH, "GLU_ACT_RELU": G.ACT_RELU,
-              "GLU_ACT_IDENTITY": G.ACT_IDENTITY, "GLU_ACT_BF16_STEPS": G.ACT_BF16_STEPS,
+              "GLU_ACT_IDENTITY": G.ACT_IDENTITY, "GLU_ACT_GELU_ERF": G.ACT_GELU_ERF, "GLU_ACT_BF16_STEPS": G.ACT_BF16_STEPS,
               "GLU_FMT_MXFP8_E4M3": G.FMT_MXFP8, "GLU_FMT_NVFP4_E2M1": G.FMT_NVFP4, "GLU_FMT_BF16": G.FMT_BF16,
               "GLU_FMT_FP32": G.FMT_FP32, "GLU_FMT_MXFP8_E4M3_128X4": G.FMT_MXFP8_128X4,
               "GLU_MODE_ROW": G.MODE_ROW, "GLU_MODE_COL": G.MODE_COL, "GLU_MODE_BOTH": G.MODE_BOTH,
@@ -181,14 +181,15 @@ def test_binding_mirrors_the_header(tmp_path):
         assert int(got[f"const {c}"]) == v, c
 
 
-@pytest.mark.parametrize("act", [0, 1, 2, 3, 16, 17, 18, 19])
+@pytest.mark.parametrize("act", [0, 1, 2, 3, 4, 16, 17, 18, 19, 20])
 def test_every_activation_is_accepted_forward(act):
     st, s = G.glu_quant_fwd_sizes(fwd_args(act=act))
     assert st == G.GLU_OK and s == (64 * 256, 64 * 8, 0, 0)
 
 
 @pytest.mark.parametrize("act,status", [(0, G.GLU_OK), (1, G.GLU_OK), (2, G.GLU_OK), (3, G.GLU_OK),
-                                        (18, G.GLU_EINVAL), (19, G.GLU_EINVAL), (4, G.GLU_EINVAL)])
+                                        (4, G.GLU_OK), (18, G.GLU_EINVAL), (20, G.GLU_EINVAL),
+                                        (5, G.GLU_EINVAL)])
 def test_backward_activations(act, status):
     # the bf16 steps are a forward-only flag for every activation
     st, _ = G.glu_quant_bwd_sizes(bwd_args(act=act))

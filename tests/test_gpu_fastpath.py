@@ -20,9 +20,12 @@ CSRC = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
 
 # half-widths (units of 2^-24) and measured-form ranges, per activation
 BRACKET = {0: {"act": 16.0, "dup": 16.0},
-           1: {"act": 64.0, "dup": 64.0}}
-FWD_RANGE = {0: (-64.0, 64.0), 1: (-7.0, 64.0)}
-BWD_RANGE = {0: (-64.0, 64.0), 1: (-6.0, 64.0)}
+           1: {"act": 64.0, "dup": 64.0},
+           4: {"act": 16.0, "dup": 16.0}}
+FWD_RANGE = {0: (-64.0, 64.0), 1: (-7.0, 64.0), 4: (-13.0, 64.0)}
+BWD_RANGE = {0: (-64.0, 64.0), 1: (-6.0, 64.0), 4: (-13.0, 64.0)}
+# the last (widest) step of the dGate ladder: 2^-14 (tables), 2^-11 (GELU erf)
+WIDEST_STEP = {0: 2.0 ** -14, 1: 2.0 ** -14, 4: 2.0 ** -11}
 SLACK = 1.5  # final product rounding, exact-value rounding, bracket product
 
 
@@ -38,7 +41,7 @@ def probe(tmp_path_factory):
     lib = ctypes.CDLL(out)
     lib.gq_probe_fast.argtypes = [ctypes.c_int, ctypes.c_void_p]
     res = {}
-    for act in (0, 1):
+    for act in (0, 1, 4):
         h = np.zeros(4 * 65536, np.float32)
         assert lib.gq_probe_fast(act, h.ctypes.data) == 0
         res[act] = h.reshape(65536, 4)
@@ -56,7 +59,7 @@ def _max_ulps(fast, exact, sel):
     return float(err.max() * 2.0 ** 24)
 
 
-@pytest.mark.parametrize("act", [0, 1], ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", [0, 1, 4], ids=["silu", "gelu", "gelu_erf"])
 def test_forward_form(probe, act):
     h = probe[act]
     pats, g = _gates()
@@ -69,18 +72,22 @@ def test_forward_form(probe, act):
     assert u + SLACK <= BRACKET[act]["act"]
 
 
-def _dgate_bracket_units(n):
-    """The kernels' dGate half-width (dgate_bracket in glu_common.cuh) from
-    |N|, in units of 2^-24: 2^-18 for |N| >= 1/8, doubling at each halving
-    of |N| down to 2^-14."""
+def _dgate_bracket_units(n, widest):
+    """The kernels' dGate half-width (dgate_bracket, dgate_bracket_erf in
+    glu_common.cuh) from |N| (GELU erf: the cancellation ratio n), in units
+    of 2^-24: 2^-18 for |N| >= 1/8, doubling at each halving of |N| down to
+    the widest step."""
     n = np.abs(n.astype(np.float64))
-    d = np.full(n.shape, 2.0 ** 10)
-    for lim, e in ((2.0 ** -3, 6), (2.0 ** -4, 7), (2.0 ** -5, 8), (2.0 ** -6, 9)):
-        d = np.where((n >= lim) & (d == 2.0 ** 10), 2.0 ** e, d)
+    top = widest * 2.0 ** 24
+    d = np.full(n.shape, top)
+    e, lim = 6, 2.0 ** -3
+    while 2.0 ** e < top:
+        d = np.where((n >= lim) & (d == top), 2.0 ** e, d)
+        e, lim = e + 1, lim / 2
     return d
 
 
-@pytest.mark.parametrize("act", [0, 1], ids=["silu", "gelu"])
+@pytest.mark.parametrize("act", [0, 1, 4], ids=["silu", "gelu", "gelu_erf"])
 def test_backward_forms(probe, act):
     h = probe[act]
     pats, g = _gates()
@@ -91,7 +98,7 @@ def test_backward_forms(probe, act):
         ex = O.act_grad(act, g)
         err = np.abs(h[:, 1].astype(np.float64) - ex) / np.abs(ex) * 2.0 ** 24
         # each gate's dGate error against the half-width its |N| selects
-        room = _dgate_bracket_units(h[:, 3]) - (err + SLACK)
+        room = _dgate_bracket_units(h[:, 3], WIDEST_STEP[act]) - (err + SLACK)
         worst = int(np.argmin(np.where(sel, room, np.inf)))
         u_gate = float(err[sel].max())
         # away from the zero of act' the closed form keeps the error of E
@@ -102,5 +109,5 @@ def test_backward_forms(probe, act):
           f"least room {room[worst]:.1f} units at g = {g[worst]}")
     assert u_up + SLACK <= BRACKET[act]["dup"]
     assert room[worst] >= 0.0
-    assert u_gate + SLACK <= 1024.0  # the widest step, 2^-14
+    assert u_gate + SLACK <= WIDEST_STEP[act] * 2.0 ** 24
     assert u_far + SLACK <= 64.0

@@ -24,8 +24,8 @@ import fp4_quant_gb300 as G  # noqa: E402  (raises if the library is missing)
 
 DEV = torch.device("cuda:0")
 ACTS = [(G.ACT_SILU, O.SILU), (G.ACT_GELU_TANH, O.GELU_TANH), (G.ACT_RELU, O.RELU),
-        (G.ACT_IDENTITY, O.IDENTITY)]
-ACT_IDS = ["silu", "gelu", "relu", "identity"]
+        (G.ACT_IDENTITY, O.IDENTITY), (G.ACT_GELU_ERF, O.GELU_ERF)]
+ACT_IDS = ["silu", "gelu", "relu", "identity", "gelu_erf"]
 MODES = [G.MODE_ROW, G.MODE_COL, G.MODE_BOTH]
 
 
