@@ -26,7 +26,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden"]
-UNITS = ["api.cu", "tmap.cu", "fwd_mx.cu", "fwd_mx_b16.cu", "fwd_mx_x.cu", "fwd_mx_erf.cu", "bwd_mx.cu", "bwd_cb.cu", "plain.cu"]
+UNITS = ["api.cu", "tmap.cu", "fwd_mx.cu", "fwd_mx_b16.cu", "fwd_mx_x.cu", "fwd_mx_erf.cu", "bwd_mx.cu", "bwd_both.cu", "plain.cu"]
 
 
 def _nvcc() -> str:

@@ -40,6 +40,7 @@ struct BwdP {
   uint8_t* s_row;
   uint8_t* s_col;
   ScaleLayout sl_row, sl_col;  // scale matrices [M, 2N/32] and [2N, M/32]
+  int32_t st32;                // q_row and q_col 32-byte aligned: codes stored 32 bytes at a time
   int64_t n_rt, n_ct;
 };
 
@@ -129,6 +130,26 @@ struct StageView {
       }
       dw[i] = d16(r0, c) | (d16(r1, c) << 16);
     }
+  }
+  // Columns 8 c8 .. 8 c8 + 7 of row `lane` of the sub-tile as bf16 pairs
+  // (word i: elements 8 c8 + 2i, 8 c8 + 2i + 1).
+  __device__ void row_chunk(int lane, int c8, uint32_t (&gw)[4], uint32_t (&uw)[4], uint32_t (&dw)[4]) const {
+    if (LAYOUT == GLU_LAYOUT_SPLIT) {
+      const int o = swz128(lane, 4 * (w & 1) + c8);
+      const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
+      const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+      gw[0] = a.x; gw[1] = a.y; gw[2] = a.z; gw[3] = a.w;
+      uw[0] = b.x; uw[1] = b.y; uw[2] = b.z; uw[3] = b.w;
+    } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
+      const uint4 a = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8));
+      const uint4 b = *reinterpret_cast<const uint4*>(st + w * kBoxBytes + swz128(lane, 2 * c8 + 1));
+      gw[0] = __byte_perm(a.x, a.y, 0x5410); uw[0] = __byte_perm(a.x, a.y, 0x7632);
+      gw[1] = __byte_perm(a.z, a.w, 0x5410); uw[1] = __byte_perm(a.z, a.w, 0x7632);
+      gw[2] = __byte_perm(b.x, b.y, 0x5410); uw[2] = __byte_perm(b.x, b.y, 0x7632);
+      gw[3] = __byte_perm(b.z, b.w, 0x5410); uw[3] = __byte_perm(b.z, b.w, 0x7632);
+    }
+    const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes + swz128(lane, 4 * (w & 1) + c8));
+    dw[0] = dd.x; dw[1] = dd.y; dw[2] = dd.z; dw[3] = dd.w;
   }
   // Row `lane` of the sub-tile as bf16 pairs (word i: elements 2i, 2i + 1).
   __device__ void row(int lane, uint32_t (&gw)[16], uint32_t (&uw)[16], uint32_t (&dw)[16]) const {

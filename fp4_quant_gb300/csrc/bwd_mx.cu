@@ -68,6 +68,7 @@ cudaError_t make_params(BwdP& p, const glu_quant_bwd_args& a) {
   p.N = a.N;
   p.q_row = static_cast<uint8_t*>(a.q_row);
   p.q_col = static_cast<uint8_t*>(a.q_col);
+  p.st32 = ((reinterpret_cast<uintptr_t>(a.q_row) | reinterpret_cast<uintptr_t>(a.q_col)) & 31u) == 0;
   p.s_row = static_cast<uint8_t*>(a.s_row);
   p.s_col = static_cast<uint8_t*>(a.s_col);
   p.sl_row = a.fmt == GLU_FMT_NVFP4_E2M1 ? scale_layout(2 * a.N / 16, true)

@@ -56,6 +56,13 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                : "memory");
 }
 
+// 32 bytes (one whole sector) in one 256-bit store; p 32-byte aligned.
+__device__ __forceinline__ void st_stream32(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_stream(void* p, uint2 v) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
@@ -177,12 +184,17 @@ __device__ __forceinline__ double act_grad_f64(int act, double x) {
   return s * (1.0 + 2.0 * x * sn * yp);
 }
 
-// Exact (fp64) forms of the three products, each rounded once to fp32.
-static __device__ __noinline__ float slow_act_mul(int act, float g, float u) {
+// Exact (fp64) forms of the three products, each rounded once to fp32:
+// inline, and as out-of-line calls for kernels that keep the rare path small.
+__device__ __forceinline__ float slow_act_mul_inl(int act, float g, float u) {
   return (float)(act_f64(act, (double)g) * (double)u);
 }
-static __device__ __noinline__ float slow_grad_mul(int act, float g, float dy, float u) {
+__device__ __forceinline__ float slow_grad_mul_inl(int act, float g, float dy, float u) {
   return (float)(((double)dy * (double)u) * act_grad_f64(act, (double)g));
+}
+static __device__ __noinline__ float slow_act_mul(int act, float g, float u) { return slow_act_mul_inl(act, g, u); }
+static __device__ __noinline__ float slow_grad_mul(int act, float g, float dy, float u) {
+  return slow_grad_mul_inl(act, g, dy, u);
 }
 
 // Result of the table combination that the table cannot vouch for: NaN

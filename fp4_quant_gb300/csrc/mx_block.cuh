@@ -119,6 +119,52 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
   return sc;
 }
 
+// The fast part of mx_block alone, for kernels that keep the exact path out
+// of line: returns the scale byte decided by the rounding test and sets
+// `mul` to 2^-e, or returns 0x100 when the scale is undecided (or the block
+// holds a NaN, an infinity or a tiny amax: every value must then be exact);
+// `emask` gets the elements whose codes the test cannot decide (bit e; the
+// caller patches them from exact values, code = E4M3(exact * mul)).
+__device__ __forceinline__ uint32_t mx_fast(const float (&v)[32], uint32_t (&q)[8], const float d, float& mul,
+                                            uint32_t& emask) {
+  emask = 0;
+  const uint32_t sc = e8m0_checked(amax32(v), d);
+  if (sc == 0x100u) return sc;
+  mul = e8m0_inv_scale(sc);
+  const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+  uint32_t diff = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
+    const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
+    const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
+    q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
+    diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  }
+  if (diff != 0u) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo, v[4 * j + 3] * mlo);
+      const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi, v[4 * j + 3] * mhi);
+      emask |= byte_mask(ql ^ qh) << (4 * j);
+    }
+  }
+  return sc;
+}
+
+// Scale byte and codes of a block of exact values (NaN/Inf -> 0xFF and
+// codes 0x7F).
+__device__ __forceinline__ uint32_t mx_exact(const float (&v)[32], uint32_t (&q)[8]) {
+  const uint32_t sc = e8m0_of(amax32(v));
+  if (sc == 0xFFu) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = 0x7F7F7F7Fu;
+  } else {
+    codes32(v, e8m0_inv_scale(sc), q);
+  }
+  return sc;
+}
+
 // Same, with exact values that are cheap one at a time (operands in shared
 // memory): the block is filled by a plain loop.
 template <class Exact>

@@ -37,6 +37,20 @@ struct TileWalk {
   }
 };
 
+// Unit u of a walk in bands of BAND column strips: the units of row unit
+// ru are the strips of its band, one after the other, so that units taken
+// at the same time by neighbouring CTAs cover up to BAND strips of the same
+// rows (the last band may be narrower).  n_ru row units, n_ct strips.
+template <int BAND>
+__device__ __forceinline__ void band_unit(int64_t u, int64_t n_ru, int64_t n_ct, int64_t& ru, int64_t& ct) {
+  const int64_t per_band = BAND * n_ru;
+  const int64_t b = u / per_band;
+  const int64_t rem = u - b * per_band;
+  const int64_t wb = n_ct - BAND * b < BAND ? n_ct - BAND * b : int64_t(BAND);
+  ru = rem / wb;
+  ct = BAND * b + (rem - ru * wb);
+}
+
 // Free a stage after this warp's last read of it (all lanes call).  Returns
 // true in every lane of the warp that freed it last.
 template <int GROUP_WARPS>
