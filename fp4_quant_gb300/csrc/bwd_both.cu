@@ -45,14 +45,26 @@ namespace {
 
 using namespace bwd;
 
+constexpr int kGW = 4;                 // warps per group
 constexpr int kGroups = 4;
-constexpr int kThreads = kGroups * kGroupWarps * 32;
+constexpr int kThreads = kGroups * kGW * 32;
+constexpr int kNB = kGW / 2;           // 64-column TMA boxes per operand
+constexpr int kTCw = kWC * kGW;        // tile columns
+constexpr int kStageB = 3 * kNB * kBoxBytes;
 constexpr int kVBytes = 8192;  // per warp: dGate and dUp of the sub-tile
 constexpr int kSup = 4;        // row tiles per unit
-constexpr int kBand = 8;       // column strips walked side by side
+constexpr int kBand = 1024 / kTCw;  // column strips walked side by side (1024 columns)
 using Ctl = RingCtl<kGroups, kGroups>;
 
-constexpr int kSmem = 1024 + kGroups * kStageBytes + kGroups * kGroupWarps * kVBytes + int(sizeof(Ctl));
+// act'(g) as (hi, lo) pairs for the negative gates of the binade that holds
+// the zero of act' (SiLU: -2 < g <= -1, GELU (tanh): -1 < g <= -0.5): the
+// dGate values next to that zero are made exact from this copy of the
+// backward table in shared memory
+constexpr int kBandBytes = 128 * 8;
+template <int ACT>
+constexpr uint32_t kBandExp = (ACT & 15) == 0 ? 127u : 126u;
+
+constexpr int kSmem = 1024 + kGroups * kStageB + kGroups * kGW * kVBytes + int(sizeof(Ctl)) + kBandBytes;
 static_assert(kSmem <= 232448, "shared memory per CTA exceeds 227 KB");
 
 __device__ uint32_t g_err_bwd_both;
@@ -100,8 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
-  uint8_t* Vbase = stages + kGroups * kStageBytes;
-  Ctl* ctl = reinterpret_cast<Ctl*>(Vbase + kGroups * kGroupWarps * kVBytes);
+  uint8_t* Vbase = stages + kGroups * kStageB;
+  Ctl* ctl = reinterpret_cast<Ctl*>(Vbase + kGroups * kGW * kVBytes);
+  float2* band = reinterpret_cast<float2*>(ctl + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   const int sup = p.n_rt % kSup == 0 ? kSup : 1;  // row tiles per unit
@@ -109,6 +122,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
   const int64_t units = n_ru * p.n_ct;
   const int64_t my_units = (units - blockIdx.x + G - 1) / G;
 
+  if constexpr (kTabAct<ACT>) {
+    if (threadIdx.x < 128) {
+      const float4* tab = reinterpret_cast<const float4*>(ACT == 0 ? gq_tab_bwd_0 : gq_tab_bwd_1);
+      const float4 e = __ldg(tab + tab_index(0x8000u | (kBandExp<ACT> << 7) | threadIdx.x));
+      band[threadIdx.x] = make_float2(e.z, e.w);
+    }
+  }
   if (threadIdx.x == 0) {
     prefetch_tensormap(&p.tm_a);
     if (LAYOUT == GLU_LAYOUT_SPLIT) prefetch_tensormap(&p.tm_b);
@@ -140,25 +160,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
         ctl->minor[g] = 0;
         ctl->major[g] = u + kGroups * G;
       }
-      mbar_arrive_expect_tx(&ctl->full[g], kStageBytes);
+      mbar_arrive_expect_tx(&ctl->full[g], kStageB);
     }
     rt = __shfl_sync(0xFFFFFFFFu, rt, 0);
     ct = __shfl_sync(0xFFFFFFFFu, ct, 0);
-    if (lane < 6) {
-      uint8_t* dst = stages + g * kStageBytes + lane * kBoxBytes;
+    // boxes: split: gate 0 .. kNB-1, up kNB .. 2kNB-1, dY 2kNB .. 3kNB-1
+    // (64 columns each); pairs: one box of 32 (gate, up) pairs per warp,
+    // then the dY boxes
+    if (lane < 3 * kNB) {
+      uint8_t* dst = stages + g * kStageB + lane * kBoxBytes;
       const int32_t y = int32_t(rt * kTR);
-      if (lane >= 4) {
-        tma_load_2d(dst, &p.tm_d, int32_t(ct * kTC + (lane - 4) * 64), y, &ctl->full[g]);
+      if (lane >= 2 * kNB) {
+        tma_load_2d(dst, &p.tm_d, int32_t(ct * kTCw + (lane - 2 * kNB) * 64), y, &ctl->full[g]);
       } else if (LAYOUT == GLU_LAYOUT_SPLIT) {
-        tma_load_2d(dst, lane < 2 ? &p.tm_a : &p.tm_b, int32_t(ct * kTC + (lane & 1) * 64), y,
+        tma_load_2d(dst, lane < kNB ? &p.tm_a : &p.tm_b, int32_t(ct * kTCw + (lane % kNB) * 64), y,
                     &ctl->full[g]);
       } else {
-        tma_load_2d(dst, &p.tm_a, int32_t(ct * kTC + lane * kWC), y, &ctl->full[g]);
+        tma_load_2d(dst, &p.tm_a, int32_t(ct * kTCw + lane * kWC), y, &ctl->full[g]);
       }
     }
   };
 
-  const int grp = warp / kGroupWarps, w = warp % kGroupWarps;
+  const int grp = warp / kGW, w = warp % kGW;
   uint8_t* const V = Vbase + warp * kVBytes;
   const int64_t n_g = (my_units > grp ? (my_units - grp + kGroups - 1) / kGroups : 0) * sup;  // tiles
   const int64_t W = 2 * p.N;    // columns of [dGate | dUp]
@@ -175,11 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
       break;
     }
     const int64_t rt = ctl->rt[grp], ct = ctl->ct[grp];
-    const int64_t row0 = rt * kTR, c0 = ct * kTC + w * kWC;
+    const int64_t row0 = rt * kTR, c0 = ct * kTCw + w * kWC;
     const bool active = c0 < p.N;
 
     if (!active) {
-      if (ring_free<kGroupWarps>(&ctl->freed[grp], lane) && k + 1 < n_g) issue(grp);
+      if (ring_free<kGW>(&ctl->freed[grp], lane) && k + 1 < n_g) issue(grp);
       continue;
     }
 
@@ -188,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
     // contents every lane has read: the column reads of the last tile
     // precede this point in every lane); then the stage is free
     __syncwarp();
-    const StageView<LAYOUT> sv{stages + grp * kStageBytes, w};
+    const StageView<LAYOUT, kNB> sv{stages + grp * kStageB, w};
     uint32_t near = 0;  // bit 31 - e: |N| < kNearN at element e (next to a zero of act')
     uint32_t gmax = 0;  // largest raw gate pattern (fast-range check)
 #pragma unroll 1
@@ -239,11 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
       while (m != 0u) {
         const int e = __clz(m);
         m &= ~(0x80000000u >> e);
-        const float x = exact_elem_bits<ACT>(sv.g16(lane, e), sv.u16(lane, e), sv.d16(lane, e), 0);
+        const uint32_t gb = sv.g16(lane, e), ub = sv.u16(lane, e), db = sv.d16(lane, e);
+        const uint32_t bi = gb - (0x8000u | (kBandExp<ACT> << 7));
+        float x = __int_as_float(0x7FC00000);
+        if (kTabAct<ACT> && bi < 128u) x = tab_mul(band[bi], __fmul_rn(bf(db), bf(ub)));
+        if (tab_cold(x)) x = exact_elem_bits<ACT>(gb, ub, db, 0);
         *reinterpret_cast<float*>(V + swz128(lane, e >> 2) + 4 * (e & 3)) = x;
       }
     }
-    if (ring_free<kGroupWarps>(&ctl->freed[grp], lane) && k + 1 < n_g) issue(grp);
+    if (ring_free<kGW>(&ctl->freed[grp], lane) && k + 1 < n_g) issue(grp);
 
     // ---- the four blocks of the lane, from the buffer: job 0, 1 the
     // rowwise dGate and dUp blocks of row row0 + lane (element e at (row0 +
@@ -360,6 +387,7 @@ cudaError_t launch_t(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo&
   BwdP p;
   e = make_params(p, a);
   if (e != cudaSuccess) return e;
+  p.n_ct = (a.N + kTCw - 1) / kTCw;  // this kernel's column strips
   const int64_t units = (p.n_rt % kSup == 0 ? p.n_rt / kSup : p.n_rt) * p.n_ct;
   const int grid = int(units < d.sms ? units : d.sms);
   cudaLaunchConfig_t cfg = {};

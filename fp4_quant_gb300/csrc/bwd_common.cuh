@@ -53,7 +53,7 @@ __device__ __forceinline__ int swz32(int r, int k) { return r * 32 + 16 * (k ^ (
 // c) of its 32 x 32 sub-tile.  Split layout: gate boxes 0-1, up 2-3, dY 4-5
 // (box b holds 64 columns, i.e. warps 2b' and 2b'+1); pairs: box w holds the
 // warp's 32 (gate, up) pairs, dY boxes 4-5.
-template <int LAYOUT>
+template <int LAYOUT, int NB = 2>
 struct StageView {
   const uint8_t* st;
   int w;
@@ -65,11 +65,11 @@ struct StageView {
   }
   __device__ uint32_t u16(int r, int c) const {
     if (LAYOUT == GLU_LAYOUT_SPLIT)
-      return *reinterpret_cast<const uint16_t*>(st + (2 + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
+      return *reinterpret_cast<const uint16_t*>(st + (NB + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
     return *reinterpret_cast<const uint16_t*>(st + w * kBoxBytes + swz128(r, c >> 2) + 4 * (c & 3) + 2);
   }
   __device__ uint32_t d16(int r, int c) const {
-    return *reinterpret_cast<const uint16_t*>(st + (4 + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
+    return *reinterpret_cast<const uint16_t*>(st + (2 * NB + (w >> 1)) * kBoxBytes + swz128(r, dchunk(c)) + 2 * (c & 7));
   }
   // Column `lane` of the sub-tile as bf16 pairs (word i: rows 2i, 2i + 1).
   // For a fixed row the warp reads 64 contiguous bytes of a box (one
@@ -98,7 +98,7 @@ struct StageView {
       const int o = swz128(r, 4 * (w & 1) + 2 * h + c);
       if (LAYOUT == GLU_LAYOUT_SPLIT) {
         const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-        const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+        const uint4 b = *reinterpret_cast<const uint4*>(st + (NB + (w >> 1)) * kBoxBytes + o);
         gw[4 * c] = a.x; gw[4 * c + 1] = a.y; gw[4 * c + 2] = a.z; gw[4 * c + 3] = a.w;
         uw[4 * c] = b.x; uw[4 * c + 1] = b.y; uw[4 * c + 2] = b.z; uw[4 * c + 3] = b.w;
       } else {  // pairs: chunks 4 h + 2 c and 4 h + 2 c + 1 of the warp's box
@@ -109,7 +109,7 @@ struct StageView {
         gw[4 * c + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c + 2] = __byte_perm(b.x, b.y, 0x7632);
         gw[4 * c + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c + 3] = __byte_perm(b.z, b.w, 0x7632);
       }
-      const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes + o);
+      const uint4 dd = *reinterpret_cast<const uint4*>(st + (2 * NB + (w >> 1)) * kBoxBytes + o);
       dw[4 * c] = dd.x; dw[4 * c + 1] = dd.y; dw[4 * c + 2] = dd.z; dw[4 * c + 3] = dd.w;
     }
   }
@@ -137,7 +137,7 @@ struct StageView {
     if (LAYOUT == GLU_LAYOUT_SPLIT) {
       const int o = swz128(lane, 4 * (w & 1) + c8);
       const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-      const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+      const uint4 b = *reinterpret_cast<const uint4*>(st + (NB + (w >> 1)) * kBoxBytes + o);
       gw[0] = a.x; gw[1] = a.y; gw[2] = a.z; gw[3] = a.w;
       uw[0] = b.x; uw[1] = b.y; uw[2] = b.z; uw[3] = b.w;
     } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
@@ -148,7 +148,7 @@ struct StageView {
       gw[2] = __byte_perm(b.x, b.y, 0x5410); uw[2] = __byte_perm(b.x, b.y, 0x7632);
       gw[3] = __byte_perm(b.z, b.w, 0x5410); uw[3] = __byte_perm(b.z, b.w, 0x7632);
     }
-    const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes + swz128(lane, 4 * (w & 1) + c8));
+    const uint4 dd = *reinterpret_cast<const uint4*>(st + (2 * NB + (w >> 1)) * kBoxBytes + swz128(lane, 4 * (w & 1) + c8));
     dw[0] = dd.x; dw[1] = dd.y; dw[2] = dd.z; dw[3] = dd.w;
   }
   // Row `lane` of the sub-tile as bf16 pairs (word i: elements 2i, 2i + 1).
@@ -158,7 +158,7 @@ struct StageView {
       if (LAYOUT == GLU_LAYOUT_SPLIT) {
         const int o = swz128(lane, 4 * (w & 1) + c8);
         const uint4 a = *reinterpret_cast<const uint4*>(st + (w >> 1) * kBoxBytes + o);
-        const uint4 b = *reinterpret_cast<const uint4*>(st + (2 + (w >> 1)) * kBoxBytes + o);
+        const uint4 b = *reinterpret_cast<const uint4*>(st + (NB + (w >> 1)) * kBoxBytes + o);
         gw[4 * c8] = a.x; gw[4 * c8 + 1] = a.y; gw[4 * c8 + 2] = a.z; gw[4 * c8 + 3] = a.w;
         uw[4 * c8] = b.x; uw[4 * c8 + 1] = b.y; uw[4 * c8 + 2] = b.z; uw[4 * c8 + 3] = b.w;
       } else {  // pairs: chunks 2 c8 and 2 c8 + 1 of the warp's box
@@ -169,7 +169,7 @@ struct StageView {
         gw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x5410); uw[4 * c8 + 2] = __byte_perm(b.x, b.y, 0x7632);
         gw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x5410); uw[4 * c8 + 3] = __byte_perm(b.z, b.w, 0x7632);
       }
-      const uint4 dd = *reinterpret_cast<const uint4*>(st + (4 + (w >> 1)) * kBoxBytes +
+      const uint4 dd = *reinterpret_cast<const uint4*>(st + (2 * NB + (w >> 1)) * kBoxBytes +
                                                        swz128(lane, 4 * (w & 1) + c8));
       dw[4 * c8] = dd.x; dw[4 * c8 + 1] = dd.y; dw[4 * c8 + 2] = dd.z; dw[4 * c8 + 3] = dd.w;
     }
