@@ -44,6 +44,17 @@ struct TileWalk {
 template <int BAND>
 __device__ __forceinline__ void band_unit(int64_t u, int64_t n_ru, int64_t n_ct, int64_t& ru, int64_t& ct) {
   const int64_t per_band = BAND * n_ru;
+  if (per_band * ((n_ct + BAND - 1) / BAND) < (int64_t(1) << 31)) {
+    // 32-bit division (every realistic walk): a few instructions instead of
+    // the 64-bit division routine, on the path of every load issue
+    const uint32_t u32 = uint32_t(u), pb = uint32_t(per_band);
+    const uint32_t b = u32 / pb, rem = u32 - b * pb;
+    const uint32_t wb = min(uint32_t(BAND), uint32_t(n_ct) - uint32_t(BAND) * b);
+    const uint32_t r = rem / wb;
+    ru = r;
+    ct = int64_t(BAND) * b + (rem - r * wb);
+    return;
+  }
   const int64_t b = u / per_band;
   const int64_t rem = u - b * per_band;
   const int64_t wb = n_ct - BAND * b < BAND ? n_ct - BAND * b : int64_t(BAND);
