@@ -418,6 +418,7 @@ def gpu_arm(args, rank, world, dist):
 
     if not args.no_configs and rank == 0:
         res["configs"] = configs_block(args, G, dev, peaks, parity=not args.no_parity)
+        res["gemm"] = gemm_block(G, dev, parity=not args.no_parity)
         res["device_errors_configs"] = device_error_bits(G)
     return res, host_in, gpu_out, (M, N, calls)
 
@@ -567,6 +568,69 @@ def cold_l2(G, dev, sp, dr, mode, f, act, layout, nbytes, peaks):
     return {"cold_l2": {"us": round(med, 3), "us_min": round(mn, 3), "gbps": round(gbps, 1),
                         "frac_hbm": round(gbps / peaks["hbm_gbs"], 4), "buffer_sets": sets,
                         "bytes_all_sets": sets * nbytes}}
+
+
+# ------------------------------------------- the gate/up GEMM with the quantiser --
+
+def measured_bf16_tflops() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"tflops": float(d["bf16_tflops"]), "source": "of measured (MEASURED_PEAKS.json bf16_tflops, burst)"}
+    return {"tflops": 1900.0, "source": "of fallback (1.9 PFLOP/s bf16 burst)"}
+
+
+def gemm_block(G, dev, parity=True):
+    """The pages' fused GEMM shapes (pi0.5 MLP: M in {784, 968}, K = 2048,
+    merged N = 32768, H = 16384), bf16 operands, GeGLU (tanh), NVFP4 output,
+    interleaved gate/up rows: CUDA-graph-timed µs per call and tensor
+    throughput (2 M 2H K flops) against the measured bf16 peak; parity on the
+    first row tile (the tensor cores' fp32 accumulation order may move a
+    value next to a rounding boundary by one step)."""
+    import numpy as np
+    import torch
+    peak = measured_bf16_tflops()
+    recs = []
+    for M in (784, 968):
+        H, K = 16384, 2048
+        g = torch.Generator(device=dev).manual_seed(5000 + M)
+        x = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn(2 * H, K, generator=g, device=dev) / 32).to(torch.bfloat16)
+        o = G.gemm(x, w, act=G.ACT_GELU_TANH, fmt=G.FMT_NVFP4, layout=G.LAYOUT_INTERLEAVED)
+        med, mn = graph_time([lambda st, o=o: G.gemm(x, w, act=G.ACT_GELU_TANH, fmt=G.FMT_NVFP4,
+                                                     layout=G.LAYOUT_INTERLEAVED, out=o, stream=st)], dev)
+        flops = 2 * M * 2 * H * K
+        tf = flops / (med * 1e-6) / 1e12
+        r = {"workload": f"geglu_gemm_nvfp4_{M}x{H}_k{K}", "M": M, "H": H, "K": K, "act": "gelu_tanh",
+             "fmt": "nvfp4", "layout": "interleaved", "operands": "bf16", "us_graph": round(med, 3),
+             "us_graph_min": round(mn, 3), "flops": flops, "tflops": round(tf, 1),
+             "frac_bf16_peak": round(tf / peak["tflops"], 4), "peak_source": peak["source"]}
+        if parity:
+            import oracle as O
+            torch.cuda.synchronize(dev)
+            xb = x[:128].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            wb = w.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            ref = O.gemm_glu_fwd(xb, wb, act=O.GELU_TANH, fmt=O.NVFP4, layout=O.INTERLEAVED)
+            q = o["q"][: 128 * H // 2].cpu().numpy().reshape(128, H // 2)
+            sg = o["s"][: 128 * H // 16].cpu().numpy()
+            un = lambda t: np.stack([t & 0xF, t >> 4], axis=-1).reshape(t.shape[0], -1)
+            cg, cr = un(q), un(ref["q"])
+            diff = cg != cr
+            a, b = cg[diff], cr[diff]
+            one_step = (((a & 8) == (b & 8)) & (np.abs((a & 7).astype(int) - (b & 7).astype(int)) == 1)) | \
+                       (((a & 7) == 0) & ((b & 7) == 0))
+            r["parity_first_row_tile"] = {
+                "elements": int(cg.size), "code_mismatches": int(diff.sum()),
+                "more_than_one_step": int((~one_step).sum()), "scales": int(sg.size),
+                "scale_mismatches": int((sg != ref["s"]).sum()),
+                "rule": "tensor-core fp32 accumulation vs the oracle's correctly rounded sums: "
+                        "codes may differ by one step next to a boundary"}
+        recs.append(r)
+        print(json.dumps(r), file=sys.stderr, flush=True)
+        del x, w, o
+        torch.cuda.empty_cache()
+    return recs
 
 
 # ------------------------------------------------------------- CPU (oracle) --
@@ -753,6 +817,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the graph-timed per-call figures")
     ap.add_argument("--no-configs", action="store_true", help="skip the non-headline configs")
     ap.add_argument("--no-parity", action="store_true", help="skip the comparisons with the oracle")
+    ap.add_argument("--gemm-only", action="store_true",
+                    help="only the fused gate/up GEMM block (no parity): for profiling its kernel")
     ap.add_argument("--one-core-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--sweep", default=None)
@@ -771,6 +837,13 @@ def main():
         # the oracle runs on host cores; under torchrun only rank 0 works
         if rank == 0:
             print(json.dumps(reference_arm(args, rank, world)), flush=True)
+        return
+
+    if args.gemm_only:
+        import torch
+
+        import fp4_quant_gb300 as G
+        print(json.dumps({"gemm": gemm_block(G, torch.device("cuda", 0), parity=False)}), flush=True)
         return
 
     dist = None

@@ -19,6 +19,7 @@ import os
 __all__ = [
     "glu_quant_fwd", "glu_quant_bwd", "glu_quant_fwd_nvfp4_gs", "glu_quant_fwd_sizes", "glu_quant_bwd_sizes",
     "glu_quant_status_str", "glu_quant_abi_version", "glu_quant_device_errors",
+    "glu_quant_gemm_fwd", "glu_quant_gemm_sizes", "GluQuantGemmArgs", "gemm",
     "GluQuantFwdArgs", "GluQuantBwdArgs",
     "GluQuantError", "fwd", "bwd", "library_path",
     "ACT_SILU", "ACT_GELU_TANH", "ACT_RELU", "ACT_IDENTITY", "ACT_GELU_ERF", "ACT_BF16_STEPS", "FMT_MXFP8", "FMT_NVFP4", "FMT_BF16", "FMT_FP32", "FMT_MXFP8_128X4",
@@ -64,6 +65,16 @@ class GluQuantBwdArgs(ctypes.Structure):
                 ("out", ctypes.c_void_p)]
 
 
+class GluQuantGemmArgs(ctypes.Structure):
+    """Mirror of ``glu_quant_gemm_args``."""
+    _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("ld_x", ctypes.c_int64), ("ld_w", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("s", ctypes.c_void_p)]
+
+
 class GluQuantError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: status {status} ({glu_quant_status_str(status)})")
@@ -90,6 +101,10 @@ def _load() -> ctypes.CDLL:
     lib.glu_quant_status_str.restype = ctypes.c_char_p
     lib.glu_quant_abi_version.argtypes = []
     lib.glu_quant_abi_version.restype = ctypes.c_int
+    lib.glu_quant_gemm_fwd.argtypes = [ctypes.POINTER(GluQuantGemmArgs), ctypes.c_void_p]
+    lib.glu_quant_gemm_fwd.restype = ctypes.c_int
+    lib.glu_quant_gemm_sizes.argtypes = [ctypes.POINTER(GluQuantGemmArgs), ctypes.POINTER(ctypes.c_size_t)]
+    lib.glu_quant_gemm_sizes.restype = ctypes.c_int
     lib.glu_quant_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32),
                                             ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.glu_quant_device_errors.restype = ctypes.c_int
@@ -129,6 +144,16 @@ def glu_quant_fwd_sizes(args: GluQuantFwdArgs) -> tuple[int, tuple[int, int, int
 def glu_quant_bwd_sizes(args: GluQuantBwdArgs) -> tuple[int, tuple[int, int, int, int]]:
     s = (ctypes.c_size_t * 4)()
     st = _lib().glu_quant_bwd_sizes(ctypes.byref(args), s)
+    return st, tuple(s)
+
+
+def glu_quant_gemm_fwd(args: GluQuantGemmArgs, stream: int | None) -> int:
+    return _lib().glu_quant_gemm_fwd(ctypes.byref(args), stream)
+
+
+def glu_quant_gemm_sizes(args: GluQuantGemmArgs) -> tuple[int, tuple[int, int]]:
+    s = (ctypes.c_size_t * 2)()
+    st = _lib().glu_quant_gemm_sizes(ctypes.byref(args), s)
     return st, tuple(s)
 
 
@@ -311,3 +336,36 @@ def bwd(gate, up, dy, *, act=ACT_SILU, fmt=FMT_MXFP8, mode=MODE_ROW,
     if st != GLU_OK:
         raise GluQuantError(st, "glu_quant_bwd")
     return o
+
+
+def gemm(x, w, *, act=ACT_GELU_TANH, fmt=FMT_NVFP4, layout=LAYOUT_INTERLEAVED, out=None,
+         stream=None) -> dict:
+    """The gate/up GEMM with the quantiser in its epilogue: ``x`` bf16
+    [M, K], ``w`` bf16 [2H, K] (gate/up rows interleaved or split); returns
+    {"q", "s"} (allocated unless ``out`` is given).  Raises GluQuantError on
+    a nonzero status (nothing was launched then)."""
+    import torch
+    _check_input(x, "x")
+    _check_input(w, "w")
+    M, K = x.shape
+    if w.shape[1] != K or w.shape[0] % 2 != 0:
+        raise ValueError(f"w {tuple(w.shape)} does not hold [2H, {K}]")
+    H = w.shape[0] // 2
+    a = GluQuantGemmArgs(act, fmt, layout, 0, M, H, K, x.stride(0), w.stride(0), _ptr(x), _ptr(w),
+                         None, None)
+    st, sizes = glu_quant_gemm_sizes(a)
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_gemm_sizes")
+    if out is None:
+        out = {"q": torch.empty(sizes[0], dtype=torch.uint8, device=x.device),
+               "s": torch.empty(sizes[1], dtype=torch.uint8, device=x.device)}
+    for k, n in zip(("q", "s"), sizes):
+        t = out.get(k)
+        if t is None or t.dtype != torch.uint8 or t.device != x.device or not t.is_contiguous() \
+                or t.numel() < n:
+            raise ValueError(f"output {k} must be a contiguous uint8 tensor of >= {n} bytes on {x.device}")
+    a.q, a.s = _ptr(out["q"]), _ptr(out["s"])
+    st = glu_quant_gemm_fwd(a, stream if stream is not None else _stream_handle(x.device))
+    if st != GLU_OK:
+        raise GluQuantError(st, "glu_quant_gemm_fwd")
+    return out

@@ -26,7 +26,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden"]
-UNITS = ["api.cu", "tmap.cu", "fwd_mx.cu", "fwd_mx_b16.cu", "fwd_mx_x.cu", "fwd_mx_erf.cu", "bwd_mx.cu", "bwd_both.cu", "plain.cu"]
+UNITS = ["api.cu", "tmap.cu", "fwd_mx.cu", "fwd_mx_b16.cu", "fwd_mx_x.cu", "fwd_mx_erf.cu", "bwd_mx.cu", "bwd_both.cu", "gemm_glu.cu", "plain.cu"]
 
 
 def _nvcc() -> str:
@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.replace(tmp, tables)
     # 2. translation units
     nvcc = _nvcc()
-    headers = [os.path.join(CSRC, h) for h in ("glu_common.cuh", "kernels.h", "tma.cuh", "mx_block.cuh", "nv_block.cuh", "ring.cuh", "bwd_common.cuh", "fwd_mx.cuh")]
+    headers = [os.path.join(CSRC, h) for h in ("glu_common.cuh", "kernels.h", "tma.cuh", "mx_block.cuh", "nv_block.cuh", "ring.cuh", "bwd_common.cuh", "fwd_mx.cuh", "tc.cuh")]
     headers += [tables, os.path.join(INCLUDE, "glu_quant.h")]
     objs, jobs = [], []
     for u in UNITS:

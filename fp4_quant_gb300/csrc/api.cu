@@ -83,6 +83,41 @@ int check_bwd(const glu_quant_bwd_args* a) {
   return GLU_OK;
 }
 
+// The GEMM entry point's checks (shapes of its tiles, formats it emits).
+int check_gemm(const glu_quant_gemm_args* a) {
+  if (a == nullptr) return GLU_EINVAL;
+  if (a->act < GLU_ACT_SILU || a->act > GLU_ACT_GELU_ERF) return GLU_EINVAL;  // no bf16-step flag
+  if (a->fmt != GLU_FMT_NVFP4_E2M1 && a->fmt != GLU_FMT_MXFP8_E4M3 && a->fmt != GLU_FMT_MXFP8_E4M3_128X4)
+    return GLU_EINVAL;
+  if (a->layout != GLU_LAYOUT_SPLIT && a->layout != GLU_LAYOUT_INTERLEAVED) return GLU_EINVAL;
+  if (a->reserved != 0) return GLU_EINVAL;
+  if (a->M <= 0 || a->H <= 0 || a->K <= 0) return GLU_EINVAL;
+  if (a->x == nullptr || a->w == nullptr || a->q == nullptr || a->s == nullptr) return GLU_EINVAL;
+  if (a->K % 64 != 0 || a->H % 128 != 0) return GLU_ESHAPE;
+  if (a->ld_x < a->K || a->ld_w < a->K) return GLU_ESHAPE;
+  // TMA coordinates are 32-bit: rows of X and W, K
+  if (a->M > INT32_MAX || 2 * a->H > INT32_MAX || a->K > INT32_MAX) return GLU_ESHAPE;
+  int64_t t;
+  if (!mul_ok(a->M, a->ld_x, &t) || !mul_ok(t, 2, &t)) return GLU_ESHAPE;
+  if (!mul_ok(2 * a->H, a->ld_w, &t) || !mul_ok(t, 2, &t)) return GLU_ESHAPE;
+  if (!mul_ok(a->M + 127, a->H, &t)) return GLU_ESHAPE;
+  if (a->ld_x % 8 != 0 || a->ld_w % 8 != 0) return GLU_EALIGN;
+  for (const void* p : {a->x, a->w, static_cast<const void*>(a->q), static_cast<const void*>(a->s)})
+    if (!aligned16(p)) return GLU_EALIGN;
+  return GLU_OK;
+}
+
+void gemm_sizes(const glu_quant_gemm_args* a, size_t s[2]) {
+  if (a->fmt == GLU_FMT_NVFP4_E2M1) {
+    s[0] = size_t(a->M) * size_t(a->H / 2);
+    s[1] = size_t((a->M + 127) / 128 * 128) * size_t(a->H / 16);
+  } else {
+    s[0] = size_t(a->M) * size_t(a->H);
+    s[1] = a->fmt == GLU_FMT_MXFP8_E4M3_128X4 ? size_t((a->M + 127) / 128 * 128) * size_t(a->H / 32)
+                                              : size_t(a->M) * size_t(a->H / 32);
+  }
+}
+
 // Output byte sizes for a logical [M, W] result.
 void sizes_for(int32_t fmt, int32_t mode, int64_t M, int64_t W, size_t s[4]) {
   s[0] = s[1] = s[2] = s[3] = 0;
@@ -190,6 +225,28 @@ extern "C" int glu_quant_bwd(const glu_quant_bwd_args* a, void* stream) {
   return launched(gq::launch_bwd_plain(*a, s, d));
 }
 
+extern "C" int glu_quant_gemm_fwd(const glu_quant_gemm_args* a, void* stream) {
+  int st = check_gemm(a);
+  if (st != GLU_OK) return st;
+  gq::DevInfo d;
+  st = device_info(&d);
+  if (st != GLU_OK) return st;
+  return launched(gq::launch_gemm_glu(*a, static_cast<cudaStream_t>(stream), d));
+}
+
+extern "C" int glu_quant_gemm_sizes(const glu_quant_gemm_args* a, size_t sizes[2]) {
+  if (sizes == nullptr || a == nullptr) return GLU_EINVAL;
+  glu_quant_gemm_args c = *a;
+  const void* ph = reinterpret_cast<const void*>(uintptr_t(256));
+  void* phw = reinterpret_cast<void*>(uintptr_t(256));
+  c.x = c.w = ph;
+  c.q = c.s = phw;
+  int st = check_gemm(&c);
+  if (st != GLU_OK) return st;
+  gemm_sizes(&c, sizes);
+  return GLU_OK;
+}
+
 extern "C" int glu_quant_fwd_sizes(const glu_quant_fwd_args* a, size_t sizes[4]) {
   if (sizes == nullptr || a == nullptr) return GLU_EINVAL;
   // validate shapes/enums with placeholder pointers standing in for the
@@ -244,6 +301,9 @@ extern "C" int glu_quant_abi_version(void) { return GLU_QUANT_ABI_VERSION; }
 extern "C" int glu_quant_device_errors(uint32_t* fwd_bits, uint32_t* bwd_bits, int clear) {
   if (fwd_bits == nullptr || bwd_bits == nullptr) return GLU_EINVAL;
   if (gq::read_err_fwd_mx(fwd_bits, clear != 0) != cudaSuccess) return GLU_EDEVICE;
+  uint32_t gemm_bits = 0;
+  if (gq::read_err_gemm(&gemm_bits, clear != 0) != cudaSuccess) return GLU_EDEVICE;
+  *fwd_bits |= gemm_bits;
   if (gq::read_err_bwd_mx(bwd_bits, clear != 0) != cudaSuccess) return GLU_EDEVICE;
   return GLU_OK;
 }

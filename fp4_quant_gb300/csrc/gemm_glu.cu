@@ -1,0 +1,392 @@
+// The gate/up projection GEMM with the gated activation and the
+// block-scaled quantiser in its epilogue ("feat(phyai-kernel): add Thor
+// NVFP4 GeGLU kernel for pi0.5", Summary and Review map: the merged gate/up
+// projection, the GeGLU fold and the compact NVFP4 store in one kernel, with
+// pairwise-interleaved gate/up weight rows; here on GB300's tcgen05 tensor
+// cores with bf16 operands).
+//
+//   C = X W^T,  X [M, K] bf16, W [2H, K] bf16 (both K-contiguous), fp32
+//   accumulators in tensor memory; gate_j / up_j are the columns of W rows
+//   2j, 2j + 1 (interleaved) or j, H + j (split); h = act(gate) * up is
+//   quantised to NVFP4 (packed E2M1 [M, H/2], E4M3 scales per 16 in the
+//   128x4 layout, global scale 1) or MXFP8 rowwise (E4M3 [M, H], E8M0 scales
+//   per 32, row-major or 128x4).  Neither C nor h is ever stored.
+//
+// Work decomposition (GB300: 152 SMs, 227 KB shared memory and 512 TMEM
+// columns per SM): a persistent CTA per SM walks output tiles of 128 rows x
+// 128 hidden columns (256 columns of C: the gate and up halves), row tiles
+// first so that the CTAs working at once share W's column tile in L2.  Six
+// warps: warp 0 issues the TMA loads of X (128 x 64) and W (2 x 128 x 64)
+// K-slices into a four-stage ring (128-byte swizzle, the K-major layout the
+// MMA reads); warp 1 allocates TMEM and one of its lanes issues the
+// 128 x 256 x 16 tcgen05.mma instructions into one of two accumulators;
+// warps 2-5 (one TMEM lane quarter each, so one output row per thread) read
+// the other accumulator 64 columns at a time, form 32 values of h and
+// quantise them while the next tile accumulates.  Every wait is bounded; a
+// wait that gives up records an error bit and the kernel winds down, TMEM
+// freed.
+//
+// Numerics: h from the fast activation forms on the fp32 accumulators,
+// every code and scale decided by the rounding test with a half-width above
+// their error for fp32 gates, the undecided ones from h evaluated in fp64 (so
+// the result is that of the exactly rounded h of the fp32 accumulators).
+#include <cstring>
+
+#include "kernels.h"
+#include "mx_block.cuh"
+#include "nv_block.cuh"
+#include "tc.cuh"
+#include "tma.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 6 * 32;
+constexpr int kEpiThreads = 4 * 32;
+constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN);
+constexpr int kScratch = 64 * 4;  // per epilogue thread: the 64 accumulator values of a step
+
+struct Ctl {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t done;
+  uint32_t tmem;
+};
+
+constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiThreads * kScratch + int(sizeof(Ctl));
+static_assert(kSmem <= 232448, "shared memory per CTA exceeds 227 KB");
+
+__device__ uint32_t g_err_gemm;
+
+struct GemmP {
+  CUtensorMap tm_x;  // X [M, K], boxes 64 x 128
+  CUtensorMap tm_w;  // W [2H, K], boxes 64 x 128
+  uint8_t* q;
+  uint8_t* s;
+  int64_t M, H, K;
+  int64_t n_mt, n_nt, tiles;
+  int32_t fmt, layout;
+  ScaleLayout sl;  // scales: NVFP4 [M, H/16], MXFP8 [M, H/32]
+  int32_t st32;    // q 32-byte aligned
+};
+
+// fp32 gates: the fast forms' error here is above the one measured over the
+// bf16 gates (the exponent's first product is no longer exact), so the
+// rounding test takes wider half-widths; exact-product gates (ReLU, the
+// identity) form the correctly rounded product directly.
+template <int ACT>
+struct GemmBracket {
+  static constexpr float kMx = kExactAct<ACT> ? 0.0f : 0x1p-15f;
+  static constexpr float kNv = kExactAct<ACT> ? 0x1p-21f : 0x1p-15f;
+  // gates at or below which the fast form is not used (exact path)
+  static constexpr float kLow = kExactAct<ACT> ? -__builtin_inff()
+                                : kErfAct<ACT> ? -13.0f
+                                : (ACT & 15) == 0 ? -64.0f : -7.0f;
+};
+
+template <int ACT>
+__device__ __forceinline__ float2 fast_pair(float2 g, float2 u) {
+  if constexpr (kExactAct<ACT>) return mul2(make_float2(xact<ACT>(g.x), xact<ACT>(g.y)), u);
+  else if constexpr (kErfAct<ACT>) return erf_h2(g, u);
+  else return fast_h2<ACT & 1>(g, u);
+}
+
+// Exactly rounded act(g) * u for fp32 operands.
+template <int ACT>
+__device__ __forceinline__ float exact_gu(float g, float u) {
+  if constexpr (kExactAct<ACT>) return __fmul_rn(xact<ACT>(g), u);
+  else return slow_act_mul_inl(ACT & 15, g, u);
+}
+
+template <int ACT, int FMT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_constant__ GemmP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* stages = smem;
+  float* scratch = reinterpret_cast<float*>(stages + kStages * kStageBytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(scratch) + kEpiThreads * kScratch);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t my_tiles = (p.tiles - blockIdx.x + G - 1) / G;
+  const int64_t nk = p.K / kBK;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&p.tm_x);
+    prefetch_tensormap(&p.tm_w);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->tfull[b], 1);
+      mbar_init(&ctl->tempty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(&ctl->done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&ctl->tmem, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t i = 0; i < my_tiles && ok; ++i) {
+        const int64_t t = blockIdx.x + i * G;
+        const int64_t mt = t % p.n_mt, nt = t / p.n_mt;
+        // W rows of the tile: interleaved, merged rows 256 nt .. + 255; split,
+        // gate rows 128 nt .. + 127 then up rows H + 128 nt ..
+        const int32_t w0 = LAYOUT == GLU_LAYOUT_INTERLEAVED ? int32_t(nt * kBN) : int32_t(nt * (kBN / 2));
+        const int32_t w1 = LAYOUT == GLU_LAYOUT_INTERLEAVED ? w0 + kBN / 2 : int32_t(p.H + nt * (kBN / 2));
+        for (int64_t kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kStages);
+          const uint32_t round = uint32_t(it / kStages);
+          if (!mbar_wait(&ctl->empty[s], (round & 1u) ^ 1u)) {
+            atomicOr(&g_err_gemm, kErrWaitEmpty);
+            ok = false;
+            break;
+          }
+          uint8_t* st = stages + s * kStageBytes;
+          mbar_arrive_expect_tx(&ctl->full[s], kStageBytes);
+          const int32_t k0 = int32_t(kb * kBK);
+          tma_load_2d(st, &p.tm_x, k0, int32_t(mt * kBM), &ctl->full[s]);
+          tma_load_2d(st + kABytes, &p.tm_w, k0, w0, &ctl->full[s]);
+          tma_load_2d(st + kABytes + kBBytes / 2, &p.tm_w, k0, w1, &ctl->full[s]);
+        }
+      }
+      // never leave with loads in flight: wait (bounded) for the last
+      // stages issued
+      for (int64_t j = it - kStages; j < it; ++j) {
+        if (j < 0) continue;
+        if (!mbar_wait(&ctl->full[j % kStages], uint32_t(j / kStages) & 1u)) atomicOr(&g_err_gemm, kErrDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t i = 0; i < my_tiles && ok; ++i) {
+        const int b = int(i & 1);
+        const uint32_t use = uint32_t(i >> 1);
+        if (!mbar_wait(&ctl->tempty[b], (use & 1u) ^ 1u)) {  // the epilogue has read this accumulator
+          atomicOr(&g_err_gemm, kErrWaitEmpty);
+          break;
+        }
+        tc::fence_after();
+        const uint32_t d = tmem + uint32_t(b * kBN);
+        for (int64_t kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kStages);
+          if (!mbar_wait(&ctl->full[s], uint32_t(it / kStages) & 1u)) {
+            atomicOr(&g_err_gemm, kErrWaitFull);
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          const uint32_t a_addr = smem_u32(stages + s * kStageBytes);
+          const uint64_t ad = tc::sw128_kmajor_desc(a_addr), bd = tc::sw128_kmajor_desc(a_addr + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // 16 K elements = 32 bytes = 2 units of the start address
+            tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdesc, uint32_t(kb | k));
+          tc::commit(&ctl->empty[s]);  // the stage is free once these MMAs are done
+        }
+        if (!ok) break;
+        tc::commit(&ctl->tfull[b]);  // the accumulator is complete
+      }
+      // every MMA issued has completed before the kernel winds down
+      tc::commit(&ctl->done);
+      if (!mbar_wait(&ctl->done, 0)) atomicOr(&g_err_gemm, kErrDrain);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;           // TMEM lanes 32 quarter .. + 31
+    const int et = (warp - 2) * 32 + lane;  // epilogue thread index
+    float* sg = scratch + et * 64;          // this thread's (gate, up) of a step, 16-byte chunks swizzled
+    auto sidx = [&](int k) { return 4 * ((k >> 2) ^ (et & 7)) + (k & 3); };  // k-th value (chunk k >> 2)
+    const float d_tab = FMT == GLU_FMT_NVFP4_E2M1 ? GemmBracket<ACT>::kNv : GemmBracket<ACT>::kMx;
+    for (int64_t i = 0; i < my_tiles; ++i) {
+      const int64_t t = blockIdx.x + i * G;
+      const int64_t mt = t % p.n_mt, nt = t / p.n_mt;
+      const int b = int(i & 1);
+      // lane 0 waits for the accumulator; the warp follows its verdict (the
+      // TMEM loads below are whole-warp instructions)
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&ctl->tfull[b], uint32_t(i >> 1) & 1u);
+        if (!ok) atomicOr(&g_err_gemm, kErrWaitFull);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+      tc::fence_after();
+      const int64_t row = mt * kBM + quarter * 32 + lane;
+      const bool row_ok = row < p.M;
+      const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
+      uint32_t scw0 = 0, scw1 = 0;  // the tile's scale bytes of this row (NVFP4: 8, MXFP8: 4)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        // 32 outputs: hidden columns 128 nt + 32 c .. + 31
+        uint32_t ra[32], rb[32];
+        if (LAYOUT == GLU_LAYOUT_INTERLEAVED) {
+          tc::ld32(tbase + uint32_t(64 * c), ra);       // pairs 0..15
+          tc::ld32(tbase + uint32_t(64 * c + 32), rb);  // pairs 16..31
+        } else {
+          tc::ld32(tbase + uint32_t(32 * c), ra);             // gates
+          tc::ld32(tbase + uint32_t(kBN / 2 + 32 * c), rb);   // ups
+        }
+        tc::wait_ld();
+        // (gate, up) of output e: scratch values 2e, 2e + 1
+        float v[32];
+        bool low = false;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 g2, u2;
+          if (LAYOUT == GLU_LAYOUT_INTERLEAVED) {
+            const uint32_t(&r)[32] = e < 16 ? ra : rb;
+            const int o = (e & 15) * 2;
+            g2 = make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 2]));
+            u2 = make_float2(__uint_as_float(r[o + 1]), __uint_as_float(r[o + 3]));
+          } else {
+            g2 = make_float2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+            u2 = make_float2(__uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
+          }
+          *reinterpret_cast<float4*>(sg + sidx(2 * e)) = make_float4(g2.x, u2.x, g2.y, u2.y);
+          low |= g2.x <= GemmBracket<ACT>::kLow || g2.y <= GemmBracket<ACT>::kLow;
+          const float2 h = fast_pair<ACT>(g2, u2);
+          v[e] = h.x;
+          v[e + 1] = h.y;
+        }
+        auto exact = [&](int e) { return exact_gu<ACT>(sg[sidx(2 * e)], sg[sidx(2 * e + 1)]); };
+        if (low) {  // rare: gates below the fast range
+#pragma unroll 1
+          for (int e = 0; e < 32; ++e)
+            if (sg[sidx(2 * e)] <= GemmBracket<ACT>::kLow) set_elem(v, e, exact(e));
+        }
+        if (FMT == GLU_FMT_NVFP4_E2M1) {
+          auto ex8 = [&](int e0, float (&x)[8]) {
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) x[j] = exact(e0 + j);
+          };
+          uint32_t w[4];
+          const uint32_t s0 = nv_block<0>(v, w[0], w[1], d_tab, exact, ex8);
+          const uint32_t s1 = nv_block<16>(v, w[2], w[3], d_tab, exact, ex8);
+          if (row_ok) st_stream(p.q + row * (p.H / 2) + nt * 64 + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
+          const uint32_t sp = s0 | (s1 << 8);
+          if (c < 2) scw0 |= sp << (16 * c);
+          else scw1 |= sp << (16 * (c - 2));
+        } else {
+          uint32_t q[8];
+          const uint32_t sc = mx_block(v, q, d_tab, exact);
+          if (row_ok) {
+            uint8_t* dst = p.q + row * p.H + nt * kBN / 2 + c * 32;
+            if (p.st32) {
+              st_stream32(dst, make_uint4(q[0], q[1], q[2], q[3]), make_uint4(q[4], q[5], q[6], q[7]));
+            } else {
+              st_stream(dst, make_uint4(q[0], q[1], q[2], q[3]));
+              st_stream(dst + 16, make_uint4(q[4], q[5], q[6], q[7]));
+            }
+          }
+          scw0 |= sc << (8 * c);
+        }
+      }
+      // the accumulator is read: hand it back to the MMA warp
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+      // scales: NVFP4, the tile's 8 columns (two 4-byte groups of the 128x4
+      // layout); MXFP8, its 4 columns (one word); rows past M are written as
+      // zero padding where the layout has them (the 128x4 tiles)
+      if (FMT == GLU_FMT_NVFP4_E2M1) {
+        const uint32_t z0 = row_ok ? scw0 : 0u, z1 = row_ok ? scw1 : 0u;
+        st_stream(p.s + p.sl.at(row, nt * 8), z0);
+        st_stream(p.s + p.sl.at(row, nt * 8 + 4), z1);
+      } else if (row_ok || p.sl.swz) {
+        st_stream(p.s + p.sl.at(row, nt * 4), row_ok ? scw0 : 0u);
+      }
+    }
+  }
+  // wind down: every role is done with TMEM, then warp 1 frees it
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int ACT, int FMT, int LAYOUT>
+cudaError_t launch_t(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d) {
+  auto kern = gemm_glu_kernel<ACT, FMT, LAYOUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  GemmP p;
+  memset(&p, 0, sizeof p);
+  e = make_tile_map(&p.tm_x, a.x, 2, a.K, a.M, a.ld_x * 2, kBK, kBM, 128);
+  if (e == cudaSuccess) e = make_tile_map(&p.tm_w, a.w, 2, a.K, 2 * a.H, a.ld_w * 2, kBK, kBN / 2, 128);
+  if (e != cudaSuccess) return e;
+  p.q = static_cast<uint8_t*>(a.q);
+  p.s = static_cast<uint8_t*>(a.s);
+  p.M = a.M;
+  p.H = a.H;
+  p.K = a.K;
+  p.n_mt = (a.M + kBM - 1) / kBM;
+  p.n_nt = a.H / (kBN / 2);
+  p.tiles = p.n_mt * p.n_nt;
+  p.fmt = a.fmt;
+  p.layout = a.layout;
+  p.sl = FMT == GLU_FMT_NVFP4_E2M1 ? scale_layout(a.H / 16, true)
+                                   : scale_layout(a.H / 32, a.fmt == GLU_FMT_MXFP8_E4M3_128X4);
+  p.st32 = (reinterpret_cast<uintptr_t>(a.q) & 31u) == 0;
+  const int grid = int(p.tiles < d.sms ? p.tiles : d.sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int ACT, int FMT>
+cudaError_t by_layout(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d) {
+  return a.layout == GLU_LAYOUT_INTERLEAVED ? launch_t<ACT, FMT, GLU_LAYOUT_INTERLEAVED>(a, s, d)
+                                            : launch_t<ACT, FMT, GLU_LAYOUT_SPLIT>(a, s, d);
+}
+
+template <int ACT>
+cudaError_t by_fmt(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d) {
+  return a.fmt == GLU_FMT_NVFP4_E2M1 ? by_layout<ACT, GLU_FMT_NVFP4_E2M1>(a, s, d)
+                                     : by_layout<ACT, GLU_FMT_MXFP8_E4M3>(a, s, d);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_glu(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d) {
+  switch (a.act) {
+    case GLU_ACT_SILU: return by_fmt<0>(a, s, d);
+    case GLU_ACT_GELU_TANH: return by_fmt<1>(a, s, d);
+    case GLU_ACT_RELU: return by_fmt<2>(a, s, d);
+    case GLU_ACT_IDENTITY: return by_fmt<3>(a, s, d);
+    default: return by_fmt<4>(a, s, d);
+  }
+}
+
+cudaError_t read_err_gemm(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_err_gemm, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_err_gemm, &z, sizeof(uint32_t));
+  }
+  return e;
+}
+
+}  // namespace gq

@@ -52,6 +52,9 @@ cudaError_t launch_fwd_mx_erf(const glu_quant_fwd_args& a, cudaStream_t s, const
 cudaError_t launch_fwd_nvfp4_erf(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
                                  const DevInfo& d);
 cudaError_t read_err_fwd_erf(uint32_t* v, bool clear);
+// The gate/up GEMM with the quantiser in its epilogue (gemm_glu.cu).
+cudaError_t launch_gemm_glu(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d);
+cudaError_t read_err_gemm(uint32_t* v, bool clear);
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);  // (includes the both-directions kernel's bits)
 cudaError_t read_err_bwd_cb(uint32_t* v, bool clear);
 

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define GLU_QUANT_ABI_VERSION 4
+#define GLU_QUANT_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define GLU_API __attribute__((visibility("default")))
@@ -218,6 +218,49 @@ GLU_API int glu_quant_fwd_nvfp4_gs(const glu_quant_fwd_args* args, const float* 
  * status. */
 GLU_API int glu_quant_bwd(const glu_quant_bwd_args* args, void* stream);
 
+/* ---- the gate/up GEMM with the quantiser in its epilogue (ABI 5) -------
+ * "feat(phyai-kernel): add Thor NVFP4 GeGLU kernel for pi0.5", Summary and
+ * Review map: one kernel for the merged gate/up projection, the gated
+ * activation and the quantised store, here with bf16 operands on GB300's
+ * tensor cores (tcgen05, fp32 accumulators in tensor memory):
+ *   C = X W^T, X [M, K], W [2H, K], both bf16 row-major (K contiguous) with
+ *   row strides ld_x, ld_w (elements);
+ *   gate_j, up_j = the columns of W rows 2j and 2j + 1 (INTERLEAVED: the
+ *   pages' pairwise-interleaved gate/up rows) or j and H + j (SPLIT);
+ *   h = act(gate) * up from the fp32 accumulators, quantised like the
+ *   forward: the codes and scales of the exactly rounded h of the fp32
+ *   accumulators.  Neither C nor h is stored.
+ * Outputs (caller-owned device memory):
+ *   GLU_FMT_NVFP4_E2M1:       q [M, H/2] packed E2M1 (element 2j in the low
+ *                             nibble), s the 128x4-layout E4M3 scales of
+ *                             [M, H/16], ceil(M/128)*128 * H/16 bytes,
+ *                             padding rows 0; global scale 1
+ *   GLU_FMT_MXFP8_E4M3:       q [M, H] E4M3, s [M, H/32] E8M0 row-major
+ *   GLU_FMT_MXFP8_E4M3_128X4: q as MXFP8, s [M, H/32] in the 128x4 layout
+ * Shapes: K % 64 == 0 and H % 128 == 0 (the kernel's 64-deep K slices and
+ * 128-wide output tiles); any M >= 1.  act: any of enum glu_act but the
+ * bf16-step flag.  Alignment: x, w, q, s 16-byte aligned; ld_x, ld_w
+ * multiples of 8, ld_x >= K, ld_w >= K.  Returns as glu_quant_fwd (the
+ * kernel holds all 512 tensor-memory columns of its SM while it runs). */
+typedef struct glu_quant_gemm_args {
+  int32_t act;      /* enum glu_act (no GLU_ACT_BF16_STEPS) */
+  int32_t fmt;      /* GLU_FMT_NVFP4_E2M1, GLU_FMT_MXFP8_E4M3 or _128X4 */
+  int32_t layout;   /* GLU_LAYOUT_INTERLEAVED or GLU_LAYOUT_SPLIT (of W's rows) */
+  int32_t reserved; /* 0 */
+  int64_t M, H, K;  /* X [M, K], W [2H, K], h [M, H] */
+  int64_t ld_x, ld_w;
+  const void* x;
+  const void* w;
+  void* q;
+  void* s;
+} glu_quant_gemm_args;
+
+GLU_API int glu_quant_gemm_fwd(const glu_quant_gemm_args* args, void* stream);
+
+/* Byte sizes of q and s for the GEMM entry point, after the same checks
+ * (pointers not looked at); touches no device. */
+GLU_API int glu_quant_gemm_sizes(const glu_quant_gemm_args* args, size_t sizes[2]);
+
 /* Byte sizes of the four outputs the arguments describe, in the order
  * q_row, s_row, q_col, s_col (for BF16/FP32, sizes[0] is the `out` size and
  * the rest are 0; disabled outputs are 0).  Checks the arguments like the
@@ -230,9 +273,10 @@ GLU_API int glu_quant_bwd_sizes(const glu_quant_bwd_args* args, size_t sizes[4])
 
 /* Device-side error bits recorded since the last clear, on the current
  * device (a bounded wait inside a kernel that gave up instead of spinning:
- * 1 = a consumer waited too long for a tile, 4 = copies still in flight at
- * exit; 0 = none).  *fwd_bits covers the forward MXFP8 kernels, *bwd_bits the
- * backward MXFP8 kernels.  Copies from device memory, so it waits for the
+ * 1 = a consumer waited too long for a tile, 2 = a producer waited too long
+ * for a free slot, 4 = copies or tensor-core operations still in flight at
+ * exit; 0 = none).  *fwd_bits covers the forward MXFP8 kernels and the
+ * GEMM entry point, *bwd_bits the backward MXFP8 kernels.  Copies from device memory, so it waits for the
  * kernels launched before it; call it outside stream capture.  `clear`
  * non-zero resets the bits afterwards.  Returns GLU_OK, GLU_EINVAL (NULL
  * pointer) or GLU_EDEVICE. */

@@ -57,6 +57,16 @@ class FwdArgs(ctypes.Structure):
                 ("h", ctypes.c_void_p)]
 
 
+class GemmArgs(ctypes.Structure):
+    _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("ld_x", ctypes.c_int64), ("ld_w", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("s", ctypes.c_void_p),
+                ("c", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+
+
 class BwdArgs(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32),
                 ("mode", ctypes.c_int32), ("layout", ctypes.c_int32),
@@ -102,6 +112,8 @@ def lib() -> ctypes.CDLL:
             l.orc_glu_fwd.restype = ctypes.c_int
             l.orc_glu_bwd.argtypes = [ctypes.POINTER(BwdArgs), ctypes.c_int]
             l.orc_glu_bwd.restype = ctypes.c_int
+            l.orc_gemm_glu_fwd.argtypes = [ctypes.POINTER(GemmArgs), ctypes.c_int]
+            l.orc_gemm_glu_fwd.restype = ctypes.c_int
             _lib = l
     return _lib
 
@@ -338,6 +350,44 @@ def glu_bwd(gate, up, dy, *, act: int, fmt: int, mode: int = ROW,
     rc = lib().orc_glu_bwd(ctypes.byref(a), nthreads or os.cpu_count() or 1)
     if rc != 0:
         raise ValueError("oracle rejected the backward arguments")
+    if want_h:
+        res["h"] = h
+    return res
+
+
+def gemm_glu_fwd(x, w, *, act: int, fmt: int, layout: int = INTERLEAVED, want_c: bool = False,
+                 want_h: bool = False, nthreads: int | None = None) -> dict:
+    """Run the oracle of the gate/up GEMM path: ``x`` bf16 bits [M, K], ``w``
+    bf16 bits [2H, K].  Returns q, s (NVFP4: packed codes and padded 128x4
+    scales; MXFP8 and MXFP8_128X4: codes and the scales in that layout) and,
+    when asked, the fp32 projection c [M, 2H] and h [M, H]."""
+    if fmt == MXFP8_128X4:
+        r = gemm_glu_fwd(x, w, act=act, fmt=MXFP8, layout=layout, want_c=want_c, want_h=want_h,
+                         nthreads=nthreads)
+        r["s"] = scales_128x4(r["s"])
+        return r
+    xb = np.ascontiguousarray(_bits(x))
+    wb = np.ascontiguousarray(_bits(w))
+    M, K = xb.shape
+    H = wb.shape[0] // 2
+    if wb.shape[1] != K or wb.shape[0] != 2 * H:
+        raise ValueError("w must be [2H, K]")
+    if fmt == NVFP4:
+        q = np.zeros((M, H // 2), np.uint8)
+        s = np.zeros((-(-M // 128) * 128) * (-(-(H // 16) // 4) * 4), np.uint8)
+    else:
+        q = np.zeros((M, H), np.uint8)
+        s = np.zeros((M, H // 32), np.uint8)
+    c = np.zeros((M, 2 * H), np.float32) if want_c else None
+    h = np.zeros((M, H), np.float32) if want_h else None
+    a = GemmArgs(act, fmt, layout, 0, M, H, K, K, K, _ptr(xb).value, _ptr(wb).value,
+                 _ptr(q).value, _ptr(s).value, None if c is None else _ptr(c).value,
+                 None if h is None else _ptr(h).value)
+    if lib().orc_gemm_glu_fwd(ctypes.byref(a), nthreads or os.cpu_count() or 1) != 0:
+        raise ValueError("oracle rejected the GEMM arguments")
+    res = {"q": q, "s": s}
+    if want_c:
+        res["c"] = c
     if want_h:
         res["h"] = h
     return res

@@ -595,6 +595,107 @@ int orc_glu_bwd(const orc_bwd_args* a, int nthreads) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* The gate/up GEMM path                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* "feat(phyai-kernel): add Thor NVFP4 GeGLU kernel for pi0.5", Summary and
+ * Supported contract: the merged gate/up projection C = X W^T (X [M, K], W
+ * [2H, K], gate/up weight rows pairwise interleaved), the GeGLU fold and the
+ * quantised store.  Each entry of C is the sum of the exact products of bf16
+ * values accumulated in double and rounded once to fp32 (exact whenever the
+ * double sum is, e.g. for operands with few significant bits).  gate_j, up_j
+ * are C[:, 2j], C[:, 2j + 1] (interleaved W rows) or C[:, j], C[:, H + j]
+ * (split).  h = act(gate) * up in double from the fp32 gate and up, rounded
+ * once to fp32, then quantised like the path's forward output (NVFP4 or
+ * MXFP8 rowwise). */
+typedef struct {
+  const orc_gemm_args* a;
+  sink_t sink;
+  int64_t nchunks;
+  int tid, nthreads, failed;
+} gemm_job_t;
+
+static void gemm_values(const orc_gemm_args* a, int64_t r0, int64_t nr, float* c, float* h) {
+  const int64_t H = a->H, K = a->K;
+  double* xr = (double*)malloc((size_t)K * sizeof(double));
+  for (int64_t r = 0; r < nr; ++r) {
+    for (int64_t k = 0; k < K; ++k) xr[k] = orc_bf16_to_f32(a->x[(r0 + r) * a->ld_x + k]);
+    for (int64_t n = 0; n < 2 * H; ++n) {
+      const uint16_t* wr = a->w + n * a->ld_w;
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += xr[k] * orc_bf16_to_f32(wr[k]);
+      c[r * 2 * H + n] = (float)acc;
+    }
+    for (int64_t j = 0; j < H; ++j) {
+      float g, u;
+      if (a->layout == ORC_INTERLEAVED) { g = c[r * 2 * H + 2 * j]; u = c[r * 2 * H + 2 * j + 1]; }
+      else { g = c[r * 2 * H + j]; u = c[r * 2 * H + H + j]; }
+      h[r * H + j] = (float)(orc_act(a->act, (double)g) * (double)u);
+    }
+  }
+  free(xr);
+}
+
+static void* gemm_worker(void* p) {
+  gemm_job_t* j = (gemm_job_t*)p;
+  const orc_gemm_args* a = j->a;
+  float* c = (float*)malloc((size_t)CHUNK_ROWS * (size_t)(2 * a->H) * sizeof(float));
+  float* h = (float*)malloc((size_t)CHUNK_ROWS * (size_t)a->H * sizeof(float));
+  if (!c || !h) { j->failed = 1; free(c); free(h); return NULL; }
+  for (int64_t ch = j->tid; ch < j->nchunks; ch += j->nthreads) {
+    int64_t r0 = ch * CHUNK_ROWS;
+    int64_t nr = (a->M - r0 < CHUNK_ROWS) ? a->M - r0 : CHUNK_ROWS;
+    gemm_values(a, r0, nr, c, h);
+    if (a->c) memcpy(a->c + r0 * 2 * a->H, c, (size_t)(nr * 2 * a->H) * sizeof(float));
+    if (a->h) memcpy(a->h + r0 * a->H, h, (size_t)(nr * a->H) * sizeof(float));
+    emit_chunk(&j->sink, h, r0, nr);
+  }
+  free(c);
+  free(h);
+  return NULL;
+}
+
+int orc_gemm_glu_fwd(const orc_gemm_args* a, int nthreads) {
+  if (a->act < ORC_SILU || a->act > ORC_GELU_ERF) return -1;
+  if (a->layout != ORC_SPLIT && a->layout != ORC_INTERLEAVED) return -1;
+  if (a->M <= 0 || a->H <= 0 || a->K <= 0 || a->ld_x < a->K || a->ld_w < a->K) return -1;
+  if (a->fmt == ORC_NVFP4) { if (a->H % 16) return -1; }
+  else if (a->fmt == ORC_MXFP8) { if (a->H % 32) return -1; }
+  else return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  gemm_job_t proto;
+  memset(&proto, 0, sizeof proto);
+  proto.a = a;
+  proto.sink.fmt = a->fmt;
+  proto.sink.mode = ORC_ROW;
+  proto.sink.M = a->M;
+  proto.sink.W = a->H;
+  if (a->fmt == ORC_NVFP4) { proto.sink.out = a->q; proto.sink.s_nvfp4 = a->s; }
+  else { proto.sink.q_row = a->q; proto.sink.s_row = a->s; }
+  proto.nchunks = (a->M + CHUNK_ROWS - 1) / CHUNK_ROWS;
+  pthread_t th[256];
+  gemm_job_t jobs[256];
+  int created[256];
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = proto;
+    jobs[t].tid = t;
+    jobs[t].nthreads = nthreads;
+    created[t] = 0;
+  }
+  for (int t = 1; t < nthreads; ++t)
+    created[t] = pthread_create(&th[t], NULL, gemm_worker, &jobs[t]) == 0;
+  gemm_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t) {
+    if (created[t]) pthread_join(th[t], NULL);
+    else gemm_worker(&jobs[t]);
+  }
+  for (int t = 0; t < nthreads; ++t)
+    if (jobs[t].failed) return -1;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Array helpers (for the tests; plain loops over the scalar functions)     */
 /* ------------------------------------------------------------------------ */
 

@@ -111,6 +111,19 @@ typedef struct {
 int orc_glu_fwd(const orc_fwd_args* a, int nthreads);
 int orc_glu_bwd(const orc_bwd_args* a, int nthreads);
 
+/* ---- the gate/up GEMM path ---------------------------------------------- */
+typedef struct {
+  int32_t act, fmt, layout, reserved;
+  int64_t M, H, K, ld_x, ld_w;
+  const uint16_t* x;    /* bf16 bits [M, K], row stride ld_x */
+  const uint16_t* w;    /* bf16 bits [2H, K], row stride ld_w */
+  uint8_t* q;           /* NVFP4: packed codes [M, H/2]; MXFP8: codes [M, H] */
+  uint8_t* s;           /* NVFP4: 128x4 scales (padded); MXFP8: [M, H/32] row-major */
+  float* c;             /* optional [M, 2H]: the fp32 projection C */
+  float* h;             /* optional [M, H]: the fp32 pre-quant activation */
+} orc_gemm_args;
+int orc_gemm_glu_fwd(const orc_gemm_args* a, int nthreads);
+
 /* ---- array helpers for the tests ---------------------------------------- */
 void orc_e4m3_encode_n(const float* v, uint8_t* c, int64_t n);
 void orc_e2m1_encode_n(const float* v, uint8_t* c, int64_t n);

@@ -25,14 +25,14 @@ def _declared():
 
 def test_every_declared_symbol_is_exported():
     names = _declared()
-    assert len(names) == 8, names
+    assert len(names) == 10, names
     lib = ctypes.CDLL(G.library_path())
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_status_strings():
-    assert G.glu_quant_abi_version() == 4
+    assert G.glu_quant_abi_version() == 5
     for st in (0, -1, -2, -3, -4, -5):
         assert G.glu_quant_status_str(st) != "unknown status"
     assert G.glu_quant_status_str(7) == "unknown status"
@@ -150,7 +150,8 @@ def test_binding_mirrors_the_header(tmp_path):
     import subprocess
     if shutil.which("gcc") is None:
         pytest.skip("no C compiler")
-    fields = {"glu_quant_fwd_args": G.GluQuantFwdArgs, "glu_quant_bwd_args": G.GluQuantBwdArgs}
+    fields = {"glu_quant_fwd_args": G.GluQuantFwdArgs, "glu_quant_bwd_args": G.GluQuantBwdArgs,
+              "glu_quant_gemm_args": G.GluQuantGemmArgs}
     consts = {"GLU_ACT_SILU": G.ACT_SILU, "GLU_ACT_GELU_TANH": G.ACT_GELU_TANH, "GLU_ACT_RELU": G.ACT_RELU,
               "GLU_ACT_IDENTITY": G.ACT_IDENTITY, "GLU_ACT_GELU_ERF": G.ACT_GELU_ERF, "GLU_ACT_BF16_STEPS": G.ACT_BF16_STEPS,
               "GLU_FMT_MXFP8_E4M3": G.FMT_MXFP8, "GLU_FMT_NVFP4_E2M1": G.FMT_NVFP4, "GLU_FMT_BF16": G.FMT_BF16,
@@ -194,3 +195,32 @@ def test_backward_activations(act, status):
     # the bf16 steps are a forward-only flag for every activation
     st, _ = G.glu_quant_bwd_sizes(bwd_args(act=act))
     assert st == status
+
+
+def gemm_args(**kw):
+    d = dict(act=1, fmt=1, layout=1, reserved=0, M=968, H=16384, K=2048, ld_x=2048, ld_w=2048,
+             x=256, w=256, q=256, s=256)
+    d.update(kw)
+    return G.GluQuantGemmArgs(*(d[n] for n, _ in G.GluQuantGemmArgs._fields_))
+
+
+def test_gemm_sizes():
+    # NVFP4: codes [M, H/2], 128x4 scales of [M, H/16] padded to 1024 rows
+    st, s = G.glu_quant_gemm_sizes(gemm_args())
+    assert st == 0 and s == (968 * 8192, 1024 * 1024)
+    st, s = G.glu_quant_gemm_sizes(gemm_args(fmt=0))
+    assert st == 0 and s == (968 * 16384, 968 * 512)
+    st, s = G.glu_quant_gemm_sizes(gemm_args(fmt=4))
+    assert st == 0 and s == (968 * 16384, 1024 * 512)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=2000, ld_x=2000, ld_w=2000), -2), (dict(H=96), -2), (dict(ld_x=1024), -2),
+    (dict(fmt=2), -1), (dict(fmt=3), -1), (dict(act=17), -1), (dict(act=5), -1), (dict(layout=2), -1),
+    (dict(reserved=1), -1), (dict(M=0), -1), (dict(ld_x=2052), -3), (dict(x=264), -3),
+    (dict(q=0), -1)])
+def test_gemm_rejections(kw, status):
+    a = gemm_args(**kw)
+    assert G.glu_quant_gemm_fwd(a, None) == status
+    if "x" not in kw and "q" not in kw:
+        assert G.glu_quant_gemm_sizes(a)[0] == status
