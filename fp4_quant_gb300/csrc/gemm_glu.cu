@@ -15,14 +15,15 @@
 // Work decomposition (GB300: 152 SMs, 227 KB shared memory and 512 TMEM
 // columns per SM): a persistent CTA per SM walks output tiles of 128 rows x
 // 128 hidden columns (256 columns of C: the gate and up halves), row tiles
-// first so that the CTAs working at once share W's column tile in L2.  Six
+// first so that the CTAs working at once share W's column tile in L2.  Ten
 // warps: warp 0 issues the TMA loads of X (128 x 64) and W (2 x 128 x 64)
 // K-slices into a four-stage ring (128-byte swizzle, the K-major layout the
 // MMA reads); warp 1 allocates TMEM and one of its lanes issues the
 // 128 x 256 x 16 tcgen05.mma instructions into one of two accumulators;
-// warps 2-5 (one TMEM lane quarter each, so one output row per thread) read
-// the other accumulator 64 columns at a time, form 32 values of h and
-// quantise them while the next tile accumulates.  Every wait is bounded; a
+// warps 2-9 (two per TMEM lane quarter, so one output row per thread, each
+// on half of the tile's columns) read the other accumulator 64 columns at a
+// time, form 32 values of h and quantise them while the next tile
+// accumulates (the rare exact path straight from those registers).  Every wait is bounded; a
 // wait that gives up records an error bit and the kernel winds down, TMEM
 // freed.
 //
@@ -45,11 +46,11 @@ constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 6 * 32;
-constexpr int kEpiThreads = 4 * 32;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each on half of a tile's columns
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN);
-constexpr int kScratch = 64 * 4;  // per epilogue thread: the 64 accumulator values of a step
 
 struct Ctl {
   uint64_t full[kStages], empty[kStages];
@@ -58,7 +59,7 @@ struct Ctl {
   uint32_t tmem;
 };
 
-constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiThreads * kScratch + int(sizeof(Ctl));
+constexpr int kSmem = 1024 + kStages * kStageBytes + int(sizeof(Ctl));
 static_assert(kSmem <= 232448, "shared memory per CTA exceeds 227 KB");
 
 __device__ uint32_t g_err_gemm;
@@ -96,9 +97,10 @@ __device__ __forceinline__ float2 fast_pair(float2 g, float2 u) {
   else return fast_h2<ACT & 1>(g, u);
 }
 
-// Exactly rounded act(g) * u for fp32 operands.
+// Exactly rounded act(g) * u for fp32 operands (fp64 evaluation; out of
+// line: the rare path calls it from an unrolled loop).
 template <int ACT>
-__device__ __forceinline__ float exact_gu(float g, float u) {
+__device__ __noinline__ float exact_gu(float g, float u) {
   if constexpr (kExactAct<ACT>) return __fmul_rn(xact<ACT>(g), u);
   else return slow_act_mul_inl(ACT & 15, g, u);
 }
@@ -108,8 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* stages = smem;
-  float* scratch = reinterpret_cast<float*>(stages + kStages * kStageBytes);
-  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<uint8_t*>(scratch) + kEpiThreads * kScratch);
+  Ctl* ctl = reinterpret_cast<Ctl*>(stages + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   const int64_t my_tiles = (p.tiles - blockIdx.x + G - 1) / G;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&ctl->tempty[b], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(&ctl->done, 1);
     fence_barrier_init();
@@ -212,9 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
   } else {
     // ---------------------------------------------------------- epilogue --
     const int quarter = warp & 3;           // TMEM lanes 32 quarter .. + 31
-    const int et = (warp - 2) * 32 + lane;  // epilogue thread index
-    float* sg = scratch + et * 64;          // this thread's (gate, up) of a step, 16-byte chunks swizzled
-    auto sidx = [&](int k) { return 4 * ((k >> 2) ^ (et & 7)) + (k & 3); };  // k-th value (chunk k >> 2)
+    const int half = (warp - 2) >> 2;       // steps 2 half, 2 half + 1 of the tile's four
     const float d_tab = FMT == GLU_FMT_NVFP4_E2M1 ? GemmBracket<ACT>::kNv : GemmBracket<ACT>::kMx;
     for (int64_t i = 0; i < my_tiles; ++i) {
       const int64_t t = blockIdx.x + i * G;
@@ -232,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
       const int64_t row = mt * kBM + quarter * 32 + lane;
       const bool row_ok = row < p.M;
       const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * kBN);
-      uint32_t scw0 = 0, scw1 = 0;  // the tile's scale bytes of this row (NVFP4: 8, MXFP8: 4)
+      uint32_t scw = 0;  // this half's scale bytes of the row (NVFP4: 4, MXFP8: 2)
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         // 32 outputs: hidden columns 128 nt + 32 c .. + 31
         uint32_t ra[32], rb[32];
         if (LAYOUT == GLU_LAYOUT_INTERLEAVED) {
@@ -245,48 +244,75 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
           tc::ld32(tbase + uint32_t(kBN / 2 + 32 * c), rb);   // ups
         }
         tc::wait_ld();
-        // (gate, up) of output e: scratch values 2e, 2e + 1
+        // gate and up of output e (compile-time indices into ra, rb)
+        auto gate_of = [&](int e) {
+          return __uint_as_float(LAYOUT == GLU_LAYOUT_INTERLEAVED ? (e < 16 ? ra[2 * e] : rb[2 * e - 32]) : ra[e]);
+        };
+        auto up_of = [&](int e) {
+          return __uint_as_float(LAYOUT == GLU_LAYOUT_INTERLEAVED ? (e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]) : rb[e]);
+        };
         float v[32];
-        bool low = false;
+        uint32_t low = 0;  // bit e: gate at or below the fast range
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float2 g2, u2;
-          if (LAYOUT == GLU_LAYOUT_INTERLEAVED) {
-            const uint32_t(&r)[32] = e < 16 ? ra : rb;
-            const int o = (e & 15) * 2;
-            g2 = make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 2]));
-            u2 = make_float2(__uint_as_float(r[o + 1]), __uint_as_float(r[o + 3]));
-          } else {
-            g2 = make_float2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
-            u2 = make_float2(__uint_as_float(rb[e]), __uint_as_float(rb[e + 1]));
-          }
-          *reinterpret_cast<float4*>(sg + sidx(2 * e)) = make_float4(g2.x, u2.x, g2.y, u2.y);
-          low |= g2.x <= GemmBracket<ACT>::kLow || g2.y <= GemmBracket<ACT>::kLow;
+          const float2 g2 = make_float2(gate_of(e), gate_of(e + 1)), u2 = make_float2(up_of(e), up_of(e + 1));
+          low |= (uint32_t(g2.x <= GemmBracket<ACT>::kLow) | (uint32_t(g2.y <= GemmBracket<ACT>::kLow) << 1)) << e;
           const float2 h = fast_pair<ACT>(g2, u2);
           v[e] = h.x;
           v[e + 1] = h.y;
         }
-        auto exact = [&](int e) { return exact_gu<ACT>(sg[sidx(2 * e)], sg[sidx(2 * e + 1)]); };
-        if (low) {  // rare: gates below the fast range
-#pragma unroll 1
-          for (int e = 0; e < 32; ++e)
-            if (sg[sidx(2 * e)] <= GemmBracket<ACT>::kLow) set_elem(v, e, exact(e));
+        // the fast decisions; a block with a gate below the fast range, an
+        // undecided scale, a NaN, an infinity or a tiny amax is redone from
+        // exact values throughout (whole), undecided codes one by one (em)
+        uint32_t w[4], q[8], sc[2], em[2], whole = 0;
+        float mul = 0.0f;
+        if (FMT == GLU_FMT_NVFP4_E2M1) {
+          sc[0] = nv_fast<0>(v, w[0], w[1], d_tab, em[0]);
+          sc[1] = nv_fast<16>(v, w[2], w[3], d_tab, em[1]);
+          whole = uint32_t(sc[0] == 0x100u || (low & 0xFFFFu) != 0u) |
+                  (uint32_t(sc[1] == 0x100u || (low >> 16) != 0u) << 1);
+        } else {
+          sc[0] = mx_fast(v, q, d_tab, mul, em[0]);
+          em[1] = 0;
+          whole = uint32_t(sc[0] == 0x100u || low != 0u);
+        }
+        const uint32_t emask = FMT == GLU_FMT_NVFP4_E2M1 ? (em[0] | (em[1] << 16)) : em[0];
+        if (__any_sync(0xFFFFFFFFu, (whole | emask) != 0u)) {
+          // rare: exact values where a decision needs them (fp64)
+          const uint32_t need = emask | (FMT == GLU_FMT_NVFP4_E2M1
+                                             ? ((whole & 1u) ? 0xFFFFu : 0u) | ((whole & 2u) ? 0xFFFF0000u : 0u)
+                                             : (whole ? 0xFFFFFFFFu : 0u));
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            x[e] = v[e];
+            if ((need >> e) & 1u) x[e] = exact_gu<ACT>(gate_of(e), up_of(e));
+          }
+          if (FMT == GLU_FMT_NVFP4_E2M1) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              if ((whole >> k) & 1u) {
+                sc[k] = k == 0 ? nv_exact<0>(x, w[0], w[1]) : nv_exact<16>(x, w[2], w[3]);
+              } else if (em[k] != 0u) {
+                const float s_ = e4m3_value(sc[k]), rs = __frcp_rn(s_);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if ((em[k] >> e) & 1u)
+                    patch_nibble(w[2 * k], w[2 * k + 1], e, e2m1x2(div_rn(x[16 * k + e], s_, rs), 0.0f));
+              }
+            }
+          } else if (whole) {
+            sc[0] = mx_exact(x, q);
+          } else if (em[0] != 0u) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if ((em[0] >> e) & 1u) patch_code(q, e, e4m3(x[e] * mul));
+          }
         }
         if (FMT == GLU_FMT_NVFP4_E2M1) {
-          auto ex8 = [&](int e0, float (&x)[8]) {
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) x[j] = exact(e0 + j);
-          };
-          uint32_t w[4];
-          const uint32_t s0 = nv_block<0>(v, w[0], w[1], d_tab, exact, ex8);
-          const uint32_t s1 = nv_block<16>(v, w[2], w[3], d_tab, exact, ex8);
           if (row_ok) st_stream(p.q + row * (p.H / 2) + nt * 64 + c * 16, make_uint4(w[0], w[1], w[2], w[3]));
-          const uint32_t sp = s0 | (s1 << 8);
-          if (c < 2) scw0 |= sp << (16 * c);
-          else scw1 |= sp << (16 * (c - 2));
+          scw |= (sc[0] | (sc[1] << 8)) << (16 * (c & 1));
         } else {
-          uint32_t q[8];
-          const uint32_t sc = mx_block(v, q, d_tab, exact);
           if (row_ok) {
             uint8_t* dst = p.q + row * p.H + nt * kBN / 2 + c * 32;
             if (p.st32) {
@@ -296,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
               st_stream(dst + 16, make_uint4(q[4], q[5], q[6], q[7]));
             }
           }
-          scw0 |= sc << (8 * c);
+          scw |= sc[0] << (8 * (c & 1));
         }
       }
       // the accumulator is read: hand it back to the MMA warp
@@ -307,11 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
       // layout); MXFP8, its 4 columns (one word); rows past M are written as
       // zero padding where the layout has them (the 128x4 tiles)
       if (FMT == GLU_FMT_NVFP4_E2M1) {
-        const uint32_t z0 = row_ok ? scw0 : 0u, z1 = row_ok ? scw1 : 0u;
-        st_stream(p.s + p.sl.at(row, nt * 8), z0);
-        st_stream(p.s + p.sl.at(row, nt * 8 + 4), z1);
+        st_stream(p.s + p.sl.at(row, nt * 8 + 4 * half), row_ok ? scw : 0u);
       } else if (row_ok || p.sl.swz) {
-        st_stream(p.s + p.sl.at(row, nt * 4), row_ok ? scw0 : 0u);
+        st_u16(p.s + p.sl.at(row, nt * 4 + 2 * half), row_ok ? scw : 0u);
       }
     }
   }

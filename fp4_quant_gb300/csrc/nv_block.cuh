@@ -165,4 +165,73 @@ __device__ __forceinline__ uint32_t nv_block(float (&v)[32], uint32_t& w0, uint3
   return sc;
 }
 
+// The fast part of nv_block alone, for kernels that keep the exact path out
+// of the hot code: returns the scale byte the rounding test decides (the
+// codes of elements B..B+15 in w0, w1) and sets `rs` to RN(1/scale), or
+// returns 0x100 when the scale is undecided (or the block holds a NaN, an
+// infinity or a tiny amax: every value must then be exact); `emask` gets
+// the elements (bit e, 0..15) whose codes the test cannot decide.
+template <int B>
+__device__ __forceinline__ uint32_t nv_fast(const float (&v)[32], uint32_t& w0, uint32_t& w1, const float d,
+                                            uint32_t& emask) {
+  emask = 0;
+  const float a = amax3(amax3(v[B], v[B + 1], v[B + 2]), amax3(v[B + 3], v[B + 4], v[B + 5]),
+                        amax3(v[B + 6], v[B + 7], v[B + 8]));
+  const float b = amax3(amax3(v[B + 9], v[B + 10], v[B + 11]), amax3(v[B + 12], v[B + 13], v[B + 14]),
+                        v[B + 15]);
+  const float amax = amax2(a, b);
+  const uint32_t ab = __float_as_uint(amax);
+  if (!(ab < kInfBits && (ab == 0u || ab >= kTinyBits))) return 0x100u;
+  const uint32_t sp = e4m3x2(__fmul_rn(amax, __fmul_rn(kRcp6, 1.0f - d)),
+                             __fmul_rn(amax, __fmul_rn(kRcp6, 1.0f + d)));
+  const uint32_t sc = sp & 0xFFu;
+  if (sc != (sp >> 8)) return 0x100u;
+  if (sc == 0u) {
+    w0 = sign_word<B>(v, 0);
+    w1 = sign_word<B>(v, 1);
+    return 0u;
+  }
+  const float rs = __frcp_rn(e4m3_value(sc));
+  const float mlo = __fmul_rn(rs, 1.0f - d), mhi = __fmul_rn(rs, 1.0f + d);
+  w0 = e2m1_word<B>(v, 0, mlo);
+  w1 = e2m1_word<B>(v, 1, mlo);
+  const uint32_t x0 = w0 ^ e2m1_word<B>(v, 0, mhi);
+  const uint32_t x1 = w1 ^ e2m1_word<B>(v, 1, mhi);
+  if ((x0 | x1) != 0u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      emask |= (uint32_t(((x0 >> (4 * i)) & 0xFu) != 0u) << i) | (uint32_t(((x1 >> (4 * i)) & 0xFu) != 0u) << (8 + i));
+  }
+  return sc;
+}
+
+// Scale byte and codes (w0, w1) of a block of 16 exact values v[B..B+15]
+// (the rules of nv_block's exact branch).
+template <int B>
+__device__ __forceinline__ uint32_t nv_exact(const float (&v)[32], uint32_t& w0, uint32_t& w1) {
+  const float a = amax3(amax3(v[B], v[B + 1], v[B + 2]), amax3(v[B + 3], v[B + 4], v[B + 5]),
+                        amax3(v[B + 6], v[B + 7], v[B + 8]));
+  const float b = amax3(amax3(v[B + 9], v[B + 10], v[B + 11]), amax3(v[B + 12], v[B + 13], v[B + 14]),
+                        v[B + 15]);
+  const float amax = amax2(a, b);
+  if (!(__float_as_uint(amax) < kInfBits)) {
+    w0 = w1 = 0u;
+    return 0x7Fu;
+  }
+  const uint32_t sc = e4m3(div_rn(amax, 6.0f, kRcp6));
+  if (sc == 0u) {
+    w0 = sign_word<B>(v, 0);
+    w1 = sign_word<B>(v, 1);
+    return 0u;
+  }
+  const float s = e4m3_value(sc), rs = __frcp_rn(s);
+  uint32_t c[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; i += 2)
+    c[i >> 3] |= e2m1x2(div_rn(v[B + i], s, rs), div_rn(v[B + i + 1], s, rs)) << (4 * (i & 7));
+  w0 = c[0];
+  w1 = c[1];
+  return sc;
+}
+
 }  // namespace gq
