@@ -406,7 +406,7 @@ cudaError_t by_layout(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo
 
 }  // namespace
 
-cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
+cudaError_t launch_bwd_both(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
   switch (a.act) {
     case GLU_ACT_SILU: return by_layout<0>(a, s, d);
     case GLU_ACT_GELU_TANH: return by_layout<1>(a, s, d);
@@ -416,7 +416,7 @@ cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
   }
 }
 
-cudaError_t read_err_bwd_cb(uint32_t* v, bool clear) {
+cudaError_t read_err_bwd_both(uint32_t* v, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(v, g_err_bwd_both, sizeof(uint32_t));
   if (e == cudaSuccess && clear) {
     const uint32_t z = 0;

@@ -1,5 +1,5 @@
-// Pieces shared by the backward MXFP8 kernels (bwd_mx.cu: rowwise;
-// bwd_cb.cu: colwise and both): the tile geometry, the kernel parameters,
+// Pieces shared by the backward MXFP8 kernels (bwd_mx.cu: rowwise and
+// colwise; bwd_both.cu: both directions): the tile geometry, the kernel parameters,
 // the stage view, and the exact path of one element.
 #pragma once
 

@@ -3,7 +3,7 @@
 // ("Add swiglu + MXFP8 fused CuTe DSL kernel", API: the backward takes
 // grad_h and gated_input and returns concatenated [dGate | dUp]; Numerics and
 // tests for the rowwise/colwise/both modes).  This file holds the kernel of
-// one direction (rowwise or colwise) and the dispatch; bwd_cb.cu holds the
+// one direction (rowwise or colwise) and the dispatch; bwd_both.cu holds the
 // kernel of both directions.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
@@ -510,7 +510,7 @@ cudaError_t by_mode(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& 
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d) {
   cudaError_t e;
   if (a.mode == GLU_MODE_BOTH) {
-    e = launch_bwd_cb(a, s, d);
+    e = launch_bwd_both(a, s, d);
   } else {
     switch (a.act) {
       case GLU_ACT_SILU: e = by_mode<0>(a, s, d); break;
@@ -532,10 +532,10 @@ cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const Dev
 }
 
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear) {
-  uint32_t cb = 0;
-  cudaError_t e = read_err_bwd_cb(&cb, clear);
+  uint32_t both = 0;
+  cudaError_t e = read_err_bwd_both(&both, clear);
   if (e == cudaSuccess) e = cudaMemcpyFromSymbol(v, g_err_bwd_dir, sizeof(uint32_t));
-  if (e == cudaSuccess) *v |= cb;
+  if (e == cudaSuccess) *v |= both;
   if (e == cudaSuccess && clear) {
     const uint32_t z = 0;
     e = cudaMemcpyToSymbol(g_err_bwd_dir, &z, sizeof(uint32_t));

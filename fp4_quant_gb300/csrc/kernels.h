@@ -16,7 +16,7 @@ struct DevInfo {
 
 cudaError_t launch_fwd_mx(const glu_quant_fwd_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t launch_bwd_mx(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);
-cudaError_t launch_bwd_cb(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);  // both directions
+cudaError_t launch_bwd_both(const glu_quant_bwd_args& a, cudaStream_t s, const DevInfo& d);  // both directions
 // amax: device pointer to the tensor amax for the global scale, or NULL
 cudaError_t launch_fwd_nvfp4(const glu_quant_fwd_args& a, const float* amax, cudaStream_t s,
                              const DevInfo& d);
@@ -56,6 +56,6 @@ cudaError_t read_err_fwd_erf(uint32_t* v, bool clear);
 cudaError_t launch_gemm_glu(const glu_quant_gemm_args& a, cudaStream_t s, const DevInfo& d);
 cudaError_t read_err_gemm(uint32_t* v, bool clear);
 cudaError_t read_err_bwd_mx(uint32_t* v, bool clear);  // (includes the both-directions kernel's bits)
-cudaError_t read_err_bwd_cb(uint32_t* v, bool clear);
+cudaError_t read_err_bwd_both(uint32_t* v, bool clear);
 
 }  // namespace gq

@@ -1,12 +1,15 @@
-"""Multi-rank host logic of the bench on CPU (gloo, world size 2).
+"""Multi-rank host logic on CPU (gloo, world size 2).
 
 The path shards by rows with no exchange step: each rank processes its own
-batch and the only cross-rank traffic is the barrier and the max-over-ranks
-of the timed region.  This checks that aggregation with real process groups.
+rows and the only cross-rank traffic is the barrier and the max-over-ranks
+of the timed region.  These tests check that aggregation with real process
+groups, and that row slices quantised on separate ranks (by the oracle)
+join to the full batch's output.
 """
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -49,6 +52,71 @@ def test_two_rank_weak_scaling_aggregation():
     for rank, worst, v in res:
         assert worst == 20.0                  # every rank sees the slowest time
         assert v == pytest.approx(2 * 1e9 * 4 / 20e-3 / 1e9)
+
+
+def _bf16_bits(rng, shape, spikes=0.0):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if spikes:
+        m = rng.random(shape) < spikes
+        x[m] = np.where(rng.random(int(m.sum())) < 0.5, -60.0, 60.0)
+    b = x.view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)  # round to nearest even
+
+
+def _slice_worker(rank, world, port, q):
+    """Each rank runs the oracle on its own 32-row-aligned slice of one
+    seeded batch (no exchange on the data path) and sends its outputs to
+    rank 0, which joins them."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle as O
+        rng = np.random.default_rng(77)
+        M, N = 160, 96  # five 32-row blocks: ranks get 96 and 64 rows
+        g, u, d = (_bf16_bits(rng, (M, N), 0.01) for _ in range(3))
+        per = -(-(M // 32) // world) * 32
+        r0, r1 = min(M, rank * per), min(M, (rank + 1) * per)
+        mine = {
+            "fwd": O.glu_fwd(g[r0:r1], u[r0:r1], act=O.SILU, fmt=O.MXFP8, mode=O.BOTH, nthreads=1),
+            "bwd": O.glu_bwd(g[r0:r1], u[r0:r1], d[r0:r1], act=O.GELU_TANH, fmt=O.MXFP8, mode=O.BOTH,
+                             nthreads=1),
+        }
+        parts = [None] * world if rank == 0 else None
+        dist.gather_object((r0, r1, mine), parts, dst=0)
+        if rank == 0:
+            q.put(parts)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_row_slices_join_to_the_full_batch():
+    """Two gloo ranks each quantise their 32-row-aligned slice (forward and
+    backward, both directions); joined (rowwise outputs by rows, colwise
+    outputs [W, M] by columns) they equal the oracle's full-batch output
+    byte for byte: the path shards by rows with no exchange step."""
+    import oracle as O
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_slice_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    parts = q.get(timeout=300)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    rng = np.random.default_rng(77)
+    M, N = 160, 96
+    g, u, d = (_bf16_bits(rng, (M, N), 0.01) for _ in range(3))
+    full = {
+        "fwd": O.glu_fwd(g, u, act=O.SILU, fmt=O.MXFP8, mode=O.BOTH, nthreads=1),
+        "bwd": O.glu_bwd(g, u, d, act=O.GELU_TANH, fmt=O.MXFP8, mode=O.BOTH, nthreads=1),
+    }
+    assert [p[:2] for p in parts] == [(0, 96), (96, 160)]
+    for k in ("fwd", "bwd"):
+        for key, axis in (("q_row", 0), ("s_row", 0), ("q_col", 1), ("s_col", 1)):
+            joined = np.concatenate([p[2][k][key] for p in parts], axis=axis)
+            assert np.array_equal(joined, full[k][key]), (k, key)
 
 
 def test_single_rank_reduce_is_identity():

@@ -476,6 +476,12 @@ def test_fp32_mode_is_rounded_exact_value():
         assert ob == O.round_bf16(O.round_bf16(float(a)) * float(y))
 
 
+def _around(m):
+    """m and the floats one ulp below and above it."""
+    m = np.float32(m)
+    return np.array([m, np.nextafter(m, np.float32(0)), np.nextafter(m, np.float32(np.inf))], np.float32)
+
+
 def test_boundary_distance():
     # 1.0625 is the midpoint between E4M3 1.0 and 1.125: distance 0; one
     # float above is 1 ulp away.
@@ -483,6 +489,39 @@ def test_boundary_distance():
     assert list(O.boundary_ulps(O.MXFP8, v)) == [0, 1, 1 << 19]
     assert O.boundary_ulps(O.NVFP4, np.array([0.25], np.float32))[0] == 0
     assert O.boundary_ulps(O.BF16, np.array([1.0 + 2.0 ** -8], np.float32))[0] == 0
+
+
+@pytest.mark.parametrize("fmt,mid", [
+    (O.MXFP8, 2.0 ** -10),        # E4M3: 0 | smallest subnormal 2^-9
+    (O.MXFP8, 3 * 2.0 ** -10),    # subnormals 2^-9 | 2^-8
+    (O.MXFP8, 7.5 * 2.0 ** -9),   # largest subnormal 7 * 2^-9 | smallest normal 2^-6
+    (O.MXFP8, 1.9375),            # binade edge 1.875 | 2
+    (O.MXFP8, 432.0),             # 416 | 448 (the largest finite)
+    (O.MXFP8, -3 * 2.0 ** -10),   # sign does not matter
+    (O.NVFP4, 5.0),               # E2M1 4 | 6
+    (O.NVFP4, 0.75),              # 0.5 | 1
+], ids=["e4m3_zero_sub", "e4m3_sub", "e4m3_sub_normal", "e4m3_binade", "e4m3_top", "e4m3_neg", "e2m1_4_6",
+        "e2m1_half_one"])
+def test_boundary_distance_at_midpoints(fmt, mid):
+    """Each rounding midpoint is at distance 0 and its two fp32 neighbours
+    at distance 1 (also where the midpoint is a power of two, so that the
+    neighbour below is half an ulp of the one above away)."""
+    assert list(O.boundary_ulps(fmt, _around(mid))) == [0, 1, 1]
+
+
+def test_boundary_distance_far_from_midpoints():
+    # worked by hand, counting fp32 values between the value and its nearest
+    # midpoint: E4M3 2^-9 (code 1) is 2^-10 below the midpoint 3 * 2^-10,
+    # 2^22 floats of spacing 2^-32 (and 2^23 above the midpoint 2^-10: the
+    # whole binade [2^-10, 2^-9))
+    v = np.array([2.0 ** -9, 6.0, 100.0], np.float32)
+    assert list(O.boundary_ulps(O.MXFP8, v[:1])) == [1 << 22]
+    # E2M1 6: nearest midpoint 5, (6 - 5) / 2^-21 (the spacing in [4, 8));
+    # 100 (saturates to 6; no midpoint above 5): [5, 8) at 2^-21, then the
+    # whole binades [8, 16), [16, 32), [32, 64) at 2^23 floats each, then
+    # [64, 100) at 2^-17
+    spans = 3 * 2 ** 21 + 3 * 2 ** 23 + 36 * 2 ** 17
+    assert list(O.boundary_ulps(O.NVFP4, v[1:])) == [1 << 21, spans]
 
 
 def test_oracle_rejects_unsupported_arguments():
