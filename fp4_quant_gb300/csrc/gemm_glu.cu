@@ -27,10 +27,15 @@
 // wait that gives up records an error bit and the kernel winds down, TMEM
 // freed.
 //
-// Numerics: h from the fast activation forms on the fp32 accumulators,
-// every code and scale decided by the rounding test with a half-width above
-// their error for fp32 gates, the undecided ones from h evaluated in fp64 (so
-// the result is that of the exactly rounded h of the fp32 accumulators).
+// Numerics: h from the fast activation forms on the fp32 accumulators (the
+// exponent carried in two words), every code and scale decided by the
+// rounding test with a half-width above their error for fp32 gates, the
+// undecided ones from h evaluated in fp64, so the result is that of the
+// exactly rounded h of the fp32 accumulators.  fp64 is slow on this GPU and
+// a warp held up in it holds up the accumulator it reads, so the exact path
+// is kept small: a block whose scale alone is undecided evaluates only the
+// elements that may hold its amax, then decides its codes against that
+// scale by the rounding test.
 #include <cstring>
 
 #include "kernels.h"
@@ -76,14 +81,15 @@ struct GemmP {
   int32_t st32;    // q 32-byte aligned
 };
 
-// fp32 gates: the fast forms' error here is above the one measured over the
-// bf16 gates (the exponent's first product is no longer exact), so the
-// rounding test takes wider half-widths; exact-product gates (ReLU, the
-// identity) form the correctly rounded product directly.
+// fp32 gates take the fast forms with the exponent in two words
+// (fast_h2_f32; GELU (erf) through normcdff): measured over about 4 M fp32
+// gates of the fast range their error stays a few units of 2^-24, and the
+// rounding test takes 2^-20 for codes and scales; exact-product gates
+// (ReLU, the identity) form the correctly rounded product directly.
 template <int ACT>
 struct GemmBracket {
-  static constexpr float kMx = kExactAct<ACT> ? 0.0f : 0x1p-15f;
-  static constexpr float kNv = kExactAct<ACT> ? 0x1p-21f : 0x1p-15f;
+  static constexpr float kMx = kExactAct<ACT> ? 0.0f : 0x1p-20f;
+  static constexpr float kNv = kExactAct<ACT> ? 0x1p-21f : 0x1p-20f;
   // gates at or below which the fast form is not used (exact path)
   static constexpr float kLow = kExactAct<ACT> ? -__builtin_inff()
                                 : kErfAct<ACT> ? -13.0f
@@ -94,7 +100,7 @@ template <int ACT>
 __device__ __forceinline__ float2 fast_pair(float2 g, float2 u) {
   if constexpr (kExactAct<ACT>) return mul2(make_float2(xact<ACT>(g.x), xact<ACT>(g.y)), u);
   else if constexpr (kErfAct<ACT>) return erf_h2(g, u);
-  else return fast_h2<ACT & 1>(g, u);
+  else return fast_h2_f32<ACT & 1>(g, u);
 }
 
 // Exactly rounded act(g) * u for fp32 operands (fp64 evaluation; out of
@@ -103,6 +109,37 @@ template <int ACT>
 __device__ __noinline__ float exact_gu(float g, float u) {
   if constexpr (kExactAct<ACT>) return __fmul_rn(xact<ACT>(g), u);
   else return slow_act_mul_inl(ACT & 15, g, u);
+}
+
+// Flags (bit e of the block) of the codes that the rounding test leaves
+// undecided for the NVFP4 block x[B .. B + 15] against the scale 1 / rs,
+// with the codes of the low bracket end in w0, w1.
+template <int B>
+__device__ __forceinline__ uint32_t nv_flags(const float (&x)[32], float rs, float d, uint32_t& w0, uint32_t& w1) {
+  const float mlo = __fmul_rn(rs, 1.0f - d), mhi = __fmul_rn(rs, 1.0f + d);
+  w0 = e2m1_word<B>(x, 0, mlo);
+  w1 = e2m1_word<B>(x, 1, mlo);
+  const uint32_t x0 = w0 ^ e2m1_word<B>(x, 0, mhi), x1 = w1 ^ e2m1_word<B>(x, 1, mhi);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    m |= (uint32_t(((x0 >> (4 * i)) & 0xFu) != 0u) << i) | (uint32_t(((x1 >> (4 * i)) & 0xFu) != 0u) << (8 + i));
+  return m;
+}
+
+// The same for the MXFP8 block x[0 .. 31] against the multiplier 2^-e.
+__device__ __forceinline__ uint32_t mx_flags(const float (&x)[32], float mul, float d, uint32_t (&q)[8]) {
+  const float mlo = __fmul_rn(mul, 1.0f - d), mhi = __fmul_rn(mul, 1.0f + d);
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    q[j] = e4m3x4(__fmul_rn(x[4 * j], mlo), __fmul_rn(x[4 * j + 1], mlo), __fmul_rn(x[4 * j + 2], mlo),
+                  __fmul_rn(x[4 * j + 3], mlo));
+    const uint32_t qh = e4m3x4(__fmul_rn(x[4 * j], mhi), __fmul_rn(x[4 * j + 1], mhi), __fmul_rn(x[4 * j + 2], mhi),
+                               __fmul_rn(x[4 * j + 3], mhi));
+    m |= byte_mask(q[j] ^ qh) << (4 * j);
+  }
+  return m;
 }
 
 template <int ACT, int FMT, int LAYOUT>
@@ -278,35 +315,102 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
         }
         const uint32_t emask = FMT == GLU_FMT_NVFP4_E2M1 ? (em[0] | (em[1] << 16)) : em[0];
         if (__any_sync(0xFFFFFFFFu, (whole | emask) != 0u)) {
-          // rare: exact values where a decision needs them (fp64)
-          const uint32_t need = emask | (FMT == GLU_FMT_NVFP4_E2M1
-                                             ? ((whole & 1u) ? 0xFFFFu : 0u) | ((whole & 2u) ? 0xFFFF0000u : 0u)
-                                             : (whole ? 0xFFFFFFFFu : 0u));
+          // rare: exact values (fp64) where a decision needs them, in at most
+          // two rounds over the 32 elements (static indices throughout: the
+          // accumulator registers stay registers).  Round 1: the gates below
+          // the fast range, the undecided codes of decided blocks and, in a
+          // block whose fast decision failed, the elements that may hold its
+          // amax (within the bracket of the fast amax); their exact amax is
+          // then the block's, which fixes its scale, and the codes follow by
+          // the rounding test against it.  Round 2: the codes that test
+          // leaves open, and every element of a block with a NaN, an infinity
+          // or a tiny amax (or whose amax sits at a gate below the fast range).
+          constexpr int kBlk = FMT == GLU_FMT_NVFP4_E2M1 ? 16 : 32;
+          constexpr int kNb = 32 / kBlk;
+          uint32_t r1 = low | emask, full = 0;
+#pragma unroll
+          for (int k = 0; k < kNb; ++k) {
+            if (!((whole >> k) & 1u)) continue;
+            const uint32_t bm = kBlk == 32 ? 0xFFFFFFFFu : (0xFFFFu << (16 * k));
+            float am_nl = 0.0f, am_l = 0.0f;
+#pragma unroll
+            for (int e = 0; e < kBlk; ++e) {
+              const int i = kBlk * k + e;
+              if ((low >> i) & 1u) am_l = amax_acc(am_l, v[i]);
+              else am_nl = amax_acc(am_nl, v[i]);
+            }
+            const uint32_t ab = __float_as_uint(am_nl);
+            const float thr = __fmul_rn(am_nl, 1.0f - 3.0f * d_tab);
+            if (!(ab < kInfBits) || (ab != 0u && ab < kTinyBits) || !(am_l < thr)) {
+              full |= bm;
+              continue;
+            }
+#pragma unroll
+            for (int e = 0; e < kBlk; ++e) r1 |= uint32_t(fabsf(v[kBlk * k + e]) >= thr) << (kBlk * k + e);
+          }
+          r1 &= ~full;
           float x[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = v[e];
-            if ((need >> e) & 1u) x[e] = exact_gu<ACT>(gate_of(e), up_of(e));
-          }
-          if (FMT == GLU_FMT_NVFP4_E2M1) {
+          for (int e = 0; e < 32; ++e) x[e] = ((r1 >> e) & 1u) ? exact_gu<ACT>(gate_of(e), up_of(e)) : v[e];
+          uint32_t r2 = full, fl[2] = {0u, 0u};
+          float rs_[2] = {0.0f, 0.0f};
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              if ((whole >> k) & 1u) {
-                sc[k] = k == 0 ? nv_exact<0>(x, w[0], w[1]) : nv_exact<16>(x, w[2], w[3]);
-              } else if (em[k] != 0u) {
-                const float s_ = e4m3_value(sc[k]), rs = __frcp_rn(s_);
+          for (int k = 0; k < kNb; ++k) {
+            const uint32_t bm = kBlk == 32 ? 0xFFFFFFFFu : (0xFFFFu << (16 * k));
+            if (full & bm) continue;
+            if ((whole >> k) & 1u) {
+              // the block's amax is exact now: its scale, then its codes
+              float am = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                  if ((em[k] >> e) & 1u)
-                    patch_nibble(w[2 * k], w[2 * k + 1], e, e2m1x2(div_rn(x[16 * k + e], s_, rs), 0.0f));
+              for (int e = 0; e < kBlk; ++e) am = amax_acc(am, x[kBlk * k + e]);
+              if (FMT == GLU_FMT_NVFP4_E2M1) {
+                sc[k] = e4m3(div_rn(am, 6.0f, kRcp6));
+                if (sc[k] == 0u) {
+                  w[2 * k] = k == 0 ? sign_word<0>(x, 0) : sign_word<16>(x, 0);
+                  w[2 * k + 1] = k == 0 ? sign_word<0>(x, 1) : sign_word<16>(x, 1);
+                  continue;
+                }
+                rs_[k] = __frcp_rn(e4m3_value(sc[k]));
+                fl[k] = k == 0 ? nv_flags<0>(x, rs_[k], d_tab, w[0], w[1]) : nv_flags<16>(x, rs_[k], d_tab, w[2], w[3]);
+              } else {
+                sc[0] = e8m0_of(am);
+                mul = e8m0_inv_scale(sc[0]);
+                fl[0] = mx_flags(x, mul, d_tab, q);
               }
+              r2 |= (fl[k] << (kBlk * k)) & ~r1;
+            } else if (FMT == GLU_FMT_NVFP4_E2M1) {
+              fl[k] = em[k];
+              rs_[k] = __frcp_rn(e4m3_value(sc[k]));
+            } else {
+              fl[0] = em[0];
             }
-          } else if (whole) {
-            sc[0] = mx_exact(x, q);
-          } else if (em[0] != 0u) {
+          }
+          if (r2 != 0u) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if ((em[0] >> e) & 1u) patch_code(q, e, e4m3(x[e] * mul));
+              if ((r2 >> e) & 1u) x[e] = exact_gu<ACT>(gate_of(e), up_of(e));
+          }
+          // codes: whole blocks from exact values, flagged codes patched
+#pragma unroll
+          for (int k = 0; k < kNb; ++k) {
+            const uint32_t bm = kBlk == 32 ? 0xFFFFFFFFu : (0xFFFFu << (16 * k));
+            if (full & bm) {
+              if (FMT == GLU_FMT_NVFP4_E2M1) sc[k] = k == 0 ? nv_exact<0>(x, w[0], w[1]) : nv_exact<16>(x, w[2], w[3]);
+              else sc[0] = mx_exact(x, q);
+              continue;
+            }
+            if (fl[k] == 0u) continue;
+            if (FMT == GLU_FMT_NVFP4_E2M1) {
+              const float s_ = e4m3_value(sc[k]);
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if ((fl[k] >> e) & 1u)
+                  patch_nibble(w[2 * k], w[2 * k + 1], e, e2m1x2(div_rn(x[16 * k + e], s_, rs_[k]), 0.0f));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if ((fl[0] >> e) & 1u) patch_code(q, e, e4m3(__fmul_rn(x[e], mul)));
+            }
           }
         }
         if (FMT == GLU_FMT_NVFP4_E2M1) {

@@ -417,6 +417,52 @@ __device__ __forceinline__ float2 fast_h2(float2 g, float2 u) {
   return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
+// act(g) * u for a pair of fp32 gates (a GEMM's accumulators rather than
+// bf16 inputs).  With a full 24-bit gate the exponent's products are no
+// longer exact, so the exponent t (E = 2^t) is carried in two words: th,
+// the rounded value, and tl, its error (the products' rounding errors
+// recovered by fma, the sums' by the two-sum, plus the constants' own
+// tails); then E = 2^th (1 + tl ln 2).
+//   SiLU: t = -g log2(e);
+//   GELU: t = g (B + A g^2), B = -2 sqrt(2/pi) log2(e), A = 0.044715 B.
+constexpr float kNL2eHi = -0x1.715476p+0f, kNL2eLo = -0x1.4ae0c0p-26f;
+constexpr float kGeluBHi = -0x1.26aec2p+1f, kGeluBLo = -0x1.bce75ap-27f;
+constexpr float kGeluAHi = -0x1.a5a7d0p-4f, kGeluALo = 0x1.151aaep-29f;
+constexpr float kLn2Hi = 0x1.62e430p-1f;
+
+// a - b, packed (one fma: exact negation, one rounding)
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return fma2(b, splat2(-1.0f), a); }
+// a b - c with one rounding (for c = RN(a b): the exact error of that product)
+__device__ __forceinline__ float2 fms2(float2 a, float2 b, float2 c) { return fma2(a, b, make_float2(-c.x, -c.y)); }
+
+template <int ACT>
+__device__ __forceinline__ void exp_arg2_f32(float2 g, float2& th, float2& tl) {
+  if (ACT == 0) {
+    th = mul2(g, splat2(kNL2eHi));
+    tl = fma2(g, splat2(kNL2eLo), fms2(g, splat2(kNL2eHi), th));
+  } else {
+    const float2 q = mul2(g, g), qe = fms2(g, g, q);                            // g^2 = q + qe
+    const float2 p = mul2(splat2(kGeluAHi), q), pe = fms2(splat2(kGeluAHi), q, p);  // A_hi q = p + pe
+    const float2 B = splat2(kGeluBHi);
+    const float2 s = add2(B, p);                                                 // B + A g^2, head
+    const float2 bb = sub2(s, B);
+    const float2 se = add2(sub2(B, sub2(s, bb)), sub2(p, bb));                   // two-sum error
+    const float2 r = add2(add2(se, pe), fma2(splat2(kGeluAHi), qe, fma2(splat2(kGeluALo), q, splat2(kGeluBLo))));
+    th = mul2(g, s);
+    tl = fma2(g, r, fms2(g, s, th));
+  }
+}
+
+template <int ACT>
+__device__ __forceinline__ float2 fast_h2_f32(float2 g, float2 u) {
+  float2 th, tl;
+  exp_arg2_f32<ACT>(g, th, tl);
+  const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+  const float2 E = fma2(e0, mul2(tl, splat2(kLn2Hi)), e0);
+  const float2 d = add2(E, splat2(1.0f));
+  return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
 // GELU (erf) forward for a pair: (g u) Phi(g), Phi from normcdff (at most 5
 // ulp by CUDA's documentation); measured over every bf16 gate of (-13, 64),
 // g Phi(g) is within 4.8 units of 2^-24 of the exact value.

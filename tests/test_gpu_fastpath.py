@@ -40,7 +40,8 @@ def probe(tmp_path_factory):
                     os.path.join(ROOT, "tests", "fastpath_probe.cu"), "-o", out], check=True)
     lib = ctypes.CDLL(out)
     lib.gq_probe_fast.argtypes = [ctypes.c_int, ctypes.c_void_p]
-    res = {}
+    lib.gq_probe_gemm.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    res = {"lib": lib}
     for act in (0, 1, 4):
         h = np.zeros(4 * 65536, np.float32)
         assert lib.gq_probe_fast(act, h.ctypes.data) == 0
@@ -111,3 +112,39 @@ def test_backward_forms(probe, act):
     assert room[worst] >= 0.0
     assert u_gate + SLACK <= WIDEST_STEP[act] * 2.0 ** 24
     assert u_far + SLACK <= 64.0
+
+
+# The gate/up GEMM's epilogue takes fp32 gates (the accumulators): its
+# forms' half-width (GemmBracket in gemm_glu.cu), units of 2^-24, and the
+# fast range (gates at or below the lower end take the exact path).
+GEMM_BRACKET = {0: 16.0, 1: 16.0, 4: 16.0}
+GEMM_RANGE = {0: (-64.0, 64.0), 1: (-7.0, 64.0), 4: (-13.0, 64.0)}
+
+
+def _f32_gates(lo, hi):
+    """fp32 gates: N(0, s) for a few spreads, uniform over the range, and
+    every fp32 of a few narrow windows (the tails, around 0 and +-1)."""
+    rng = np.random.default_rng(2024)
+    parts = [rng.standard_normal(1 << 20) * s for s in (0.5, 1.5, 4.0)]
+    parts.append(rng.uniform(lo, hi, 1 << 21))
+    for c in (lo + 0.5, -1.0, -2.0 ** -10, 2.0 ** -10, 1.0, 8.0):
+        b = np.float32(c).view(np.uint32)
+        parts.append((np.arange(-(1 << 16), 1 << 16, dtype=np.int64) + int(b)).astype(np.uint32).view(np.float32))
+    g = np.concatenate([np.asarray(p, np.float32) for p in parts])
+    return g[(g > lo) & (g < hi) & (np.abs(g) >= 2.0 ** -126)]
+
+
+@pytest.mark.parametrize("act", [0, 1, 4], ids=["silu", "gelu", "gelu_erf"])
+def test_gemm_epilogue_form(probe, act):
+    """The GEMM epilogue's act(g) for fp32 gates (exponent in two words):
+    worst error plus the roundings after it (the product with up, which
+    for fp32 operands is one more rounding) within its half-width."""
+    lo, hi = GEMM_RANGE[act]
+    g = np.ascontiguousarray(_f32_gates(lo, hi))
+    out = np.zeros_like(g)
+    assert probe["lib"].gq_probe_gemm(act, g.ctypes.data, out.ctypes.data, g.size) == 0
+    ex = O.act(act, g.astype(np.float64))
+    sel = ex != 0
+    u = _max_ulps(out, ex, sel)
+    print(f"GEMM epilogue form max error {u:.2f} units over {g.size} gates")
+    assert u + SLACK + 1.0 <= GEMM_BRACKET[act]
