@@ -51,23 +51,23 @@ constexpr int kModeNv = 4;
 __host__ __device__ constexpr bool row_walk(int mode) { return mode == GLU_MODE_ROW || mode == kModeNv; }
 constexpr int kWC = 32;                       // columns per warp sub-tile
 // Warps per group (one 32-column sub-tile each) and groups per CTA: two
-// groups of eight for rowwise and colwise (16 warps, up to 128 registers);
-// three groups of four for both (12 warps, up to 168 registers: the both
-// path spilled at 128).
+// groups of eight for rowwise and colwise, four groups of four for both
+// (16 warps, up to 128 registers; the both path keeps a few bytes of
+// spills there and measured 1 % faster than with twelve warps at 168).
 __host__ __device__ constexpr int group_warps_for(int mode) { return mode == GLU_MODE_BOTH ? 4 : 8; }
 __host__ __device__ constexpr int tc_for(int mode) { return kWC * group_warps_for(mode); }  // tile columns
-// Two groups of eight consumer warps: with two ring slots per group and the
-// hot table this fills about 190 KB of shared memory, and 544 threads leave
-// up to 120 registers per thread (three groups spilled and measured slower).
-__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 3 : 2; }
+// With two ring slots per group, the hot table and the code boxes this fills
+// up to 226 KB of shared memory; the both path takes a smaller hot slice
+// (eight binades) to make room for its fourth group.
+__host__ __device__ constexpr int groups_for(int mode) { return mode == GLU_MODE_BOTH ? 4 : 2; }
 __host__ __device__ constexpr int threads_for(int mode) { return groups_for(mode) * group_warps_for(mode) * 32; }
 // gate + up, or the pairs: 32 KB (256 columns) or 16 KB (128 columns)
 __host__ __device__ constexpr int stage_bytes_for(int mode) { return kTR * tc_for(mode) * 4; }
 // The exact path reads the hot slice of the activation table (2^-10 <= |g|
-// < 16) from shared memory; reading it from global memory through the
-// read-only cache measured 5-8% slower.
-__host__ __device__ constexpr uint32_t hot_lo_for(int) { return kHotExpLo; }
-__host__ __device__ constexpr uint32_t hot_bin_for(int) { return kHotBinades; }
+// < 16; both: 2^-6 <= |g| < 4) from shared memory; reading it from global
+// memory through the read-only cache measured 5-8% slower.
+__host__ __device__ constexpr uint32_t hot_lo_for(int mode) { return mode == GLU_MODE_BOTH ? 121u : kHotExpLo; }
+__host__ __device__ constexpr uint32_t hot_bin_for(int mode) { return mode == GLU_MODE_BOTH ? 8u : kHotBinades; }
 __host__ __device__ constexpr int hot_bytes_for(int mode) { return int(hot_bin_for(mode)) * 256 * 8; }
 // Each consumer group has a private ring of kSlots stages: a stage is always
 // consumed, in order, by the one group that waits on it, so an mbarrier
@@ -93,7 +93,7 @@ __host__ __device__ constexpr int qbytes_for(int mode) {
                          : (mode & GLU_MODE_ROW ? kQBytes : 0) + (mode & GLU_MODE_COL ? kQcBytes : 0);
 }
 
-using Ctl = RingCtl<3 * kSlots, 3>;
+using Ctl = RingCtl<4 * kSlots, 4>;
 constexpr int kCtlBytes = int(sizeof(Ctl));
 
 __host__ __device__ constexpr int smem_for(int mode) {
