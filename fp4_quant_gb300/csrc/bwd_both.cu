@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_both_kernel(const __grid_cons
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float2 dg2, du2, n2;
-        bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, n2);
+        bwd_fast2w<ACT>(gw[i], uw[i], dw[i], dg2, du2, n2);
         gmax = vmax_u16x2(gmax, gw[i]);
         if constexpr (!Bracket<ACT>::kExact) {
           // the sign bit of |N| - kNearN (set where |N| < kNearN), shifted

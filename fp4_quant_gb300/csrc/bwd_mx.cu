@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1) bwd_dir_kernel(const __g
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float2 dg2, du2, n2;
-          bwd_fast2<ACT>(bf16x2_f2(gw[i]), bf16x2_f2(uw[i]), bf16x2_f2(dw[i]), dg2, du2, n2);
+          bwd_fast2w<ACT>(gw[i], uw[i], dw[i], dg2, du2, n2);
           gmax = vmax_u16x2(gmax, gw[i]);
           nrow = absmin3(nrow, n2.x, n2.y);
           dg[2 * i] = dg2.x; dg[2 * i + 1] = dg2.y;

@@ -547,18 +547,22 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float2 g2, u2;
+          float2 g2, u2, gu;
           if (LAYOUT == GLU_LAYOUT_SPLIT) {
             g2 = bf16x2_f2(xw[j]);
             u2 = bf16x2_f2(xw[8 + j]);
+            gu = bmul2(xw[j], xw[8 + j]);
             gmax = vmax_u16x2(gmax, xw[j]);
           } else {
             const uint32_t p0 = xw[2 * j], p1 = xw[2 * j + 1];
             g2 = make_float2(bf16_lo(p0), bf16_lo(p1));
             u2 = make_float2(bf16_hi(p0), bf16_hi(p1));
+            gu = bmul2_pairs(p0, p1);
             gmax = vmax_u16x2(gmax, (p0 & 0xFFFFu) | (p1 << 16));
           }
-          const float2 h2 = fast_vals<ACT>(g2, u2, bad, 16 * half + 2 * j);
+          float2 h2;
+          if constexpr (!kExactAct<ACT> && !kErfAct<ACT> && !(ACT & 16)) h2 = mul2(gu, fast_s2<ACT & 1>(g2));
+          else h2 = fast_vals<ACT>(g2, u2, bad, 16 * half + 2 * j);
           h[16 * half + 2 * j] = h2.x;
           h[16 * half + 2 * j + 1] = h2.y;
         }

@@ -463,6 +463,45 @@ __device__ __forceinline__ float2 fast_h2_f32(float2 g, float2 u) {
   return mul2(mul2(g, u), make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
+// Exact products of bf16 operands straight from their raw words (a product
+// of two bf16 values has at most 16 significant bits, so fp32 holds it
+// exactly): the low halves and the high halves of a and b, or the two
+// halves of each of p0 and p1.  Adding -0 keeps the sign of a zero product.
+__device__ __forceinline__ float2 bmul2(uint32_t a, uint32_t b) {
+  float lo, hi;
+  asm("{.reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+      " fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n fma.rn.f32.bf16 %1, ah, bh, 0f80000000;}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(a), "r"(b));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ float2 bmul2_pairs(uint32_t p0, uint32_t p1) {
+  float x, y;
+  asm("{.reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+      " fma.rn.f32.bf16 %0, al, ah, 0f80000000;\n fma.rn.f32.bf16 %1, bl, bh, 0f80000000;}"
+      : "=f"(x), "=f"(y)
+      : "r"(p0), "r"(p1));
+  return make_float2(x, y);
+}
+
+// The factor S(g) of fast_h2 alone (h = (g u) S).
+template <int ACT>
+__device__ __forceinline__ float2 fast_s2(float2 g) {
+  float2 E;
+  if (ACT == 0) {
+    const float2 th = mul2(g, splat2(-0x1.7154p+0f));
+    const float2 tl = mul2(g, splat2(-4.888495368504664e-06f));
+    const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+    E = fma2(e0, tl, e0);
+  } else {
+    const float2 w = fma2(splat2(-0.10294324159622192f), mul2(g, g), splat2(-2.302208185195922851562f));
+    const float2 t = mul2(g, w);
+    E = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+  }
+  const float2 d = add2(E, splat2(1.0f));
+  return make_float2(rcp_approx(d.x), rcp_approx(d.y));
+}
+
 // GELU (erf) forward for a pair: (g u) Phi(g), Phi from normcdff (at most 5
 // ulp by CUDA's documentation); measured over every bf16 gate of (-13, 64),
 // g Phi(g) is within 4.8 units of 2^-24 of the exact value.
@@ -573,6 +612,39 @@ __device__ __forceinline__ void bwd_fast2(float2 g, float2 u, float2 d, float2& 
   const float2 ap = mul2(mul2(n, S), S);
   du = mul2(mul2(d, g), S);
   dg = mul2(mul2(d, u), ap);
+}
+
+// bwd_fast2 on raw bf16 words: the same values, with dY g and dY up formed
+// as exact mixed-precision products instead of unpacking up and dY.
+template <int ACT>
+__device__ __forceinline__ void bwd_fast2w(uint32_t gw, uint32_t uw, uint32_t dw, float2& dg, float2& du, float2& n) {
+  if constexpr (kExactAct<ACT> || kErfAct<ACT>) {
+    bwd_fast2<ACT>(bf16x2_f2(gw), bf16x2_f2(uw), bf16x2_f2(dw), dg, du, n);
+    return;
+  }
+  const float2 g = bf16x2_f2(gw);
+  float2 E, t1;
+  if (ACT == 0) {
+    const float2 th = mul2(g, splat2(-0x1.7154p+0f));
+    const float2 tl = mul2(g, splat2(-4.888495368504664e-06f));
+    const float2 e0 = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+    E = fma2(e0, tl, e0);
+    t1 = add2(g, splat2(1.0f));
+  } else {
+    const float2 q = mul2(g, g);
+    const float2 g3 = mul2(q, g);
+    const float2 w = fma2(splat2(-0.10294324159622192f), g3, mul2(g, splat2(-2.3139550575201895e-05f)));
+    const float2 t = add2(mul2(g, splat2(-0x1.26aep+1f)), w);
+    E = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    const float2 y2 = fma2(splat2(0.21406444881780073f), q, splat2(1.5957691216057308f));
+    t1 = fma2(g, y2, splat2(1.0f));
+  }
+  const float2 den = add2(E, splat2(1.0f));
+  const float2 S = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+  n = fma2(E, t1, splat2(1.0f));
+  const float2 ap = mul2(mul2(n, S), S);
+  du = mul2(bmul2(dw, gw), S);
+  dg = mul2(bmul2(dw, uw), ap);
 }
 
 // Relative half-width d of the rounding test: above the fast path's worst
