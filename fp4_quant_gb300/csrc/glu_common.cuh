@@ -799,15 +799,25 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
 }
 
 // E8M0 byte for amax, or 0x100 when the fast amax cannot decide it: the
-// bracket amax*(1 -/+ d) straddles a 448 * 2^k boundary, the block holds a
-// NaN/Inf (or an overflowed product), or the block is tiny (its elements'
-// subnormal precision would matter after scaling by up to 2^127).
-__device__ __forceinline__ uint32_t e8m0_checked(float amax, float d) {
+// bracket amax*(1 -/+ d) may straddle a 448 * 2^k boundary, the block holds
+// a NaN/Inf (or an overflowed product), or the block is tiny (its elements'
+// subnormal precision would matter after scaling by up to 2^127).  The byte
+// of x changes only where x crosses 448 * 2^k = 1.75 * 2^(k+8), i.e. where
+// the mantissa field passes 0x600000 (the byte formula is continuous across
+// binade edges), and amax (1 -/+ d) reaches that point only if amax's
+// mantissa lies within d * 2^24 of it (amax < 2^(E+1)): the test is that
+// window, K = d * 2^24 plus slack.
+__device__ __forceinline__ uint32_t e8m0_window(float amax, uint32_t K) {
   const uint32_t ab = __float_as_uint(amax);
-  if (!(ab < kInfBits) || (ab != 0u && ab < kTinyBits)) return 0x100u;
-  const uint32_t lo = e8m0_from_amax_bits(__float_as_uint(__fmul_rn(amax, 1.0f - d)));
-  const uint32_t hi = e8m0_from_amax_bits(__float_as_uint(__fmul_rn(amax, 1.0f + d)));
-  return lo == hi ? lo : 0x100u;
+  const uint32_t m = ab & 0x7FFFFFu;
+  const bool bad = ab >= kInfBits || ab - 1u < kTinyBits - 1u || m - (0x600000u - K) <= 2u * K;
+  const int biased = int(ab >> 23) - 8 + int(m > 0x600000u);
+  return bad ? 0x100u : uint32_t(max(biased, 0));
+}
+template <int D_LOG2>  // d = 2^D_LOG2
+constexpr uint32_t kScaleWindow = (1u << (24 + D_LOG2)) + 2u;
+__device__ __forceinline__ uint32_t e8m0_checked(float amax, float d) {
+  return e8m0_window(amax, uint32_t(d * 0x1p24f) + 2u);
 }
 
 // E4M3 codes of four values scaled by the block multiplier, decided from
