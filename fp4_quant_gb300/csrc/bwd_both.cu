@@ -16,18 +16,17 @@
 //     of both scale matrices (a row's 32 rowwise scales of 1024 columns, a
 //     column's 32 colwise scales of 1024 rows) while those are still in L2;
 //   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31:
-//     lane l copies row l of its gate, up and dY into registers and the
-//     stage is released at once (the warp that releases it last loads the
+//     lane l reads row l of its gate, up and dY from the stage eight
+//     columns at a time and writes the row's 32 dGate and 32 dUp values to
+//     the warp's 8 KB value buffer (per output 32 rows of 128 bytes, 16-byte
+//     chunks swizzled by row, so that a lane writing its row and a warp
+//     reading one column across its lanes are both free of bank conflicts);
+//     then the stage is released (the warp that releases it last loads the
 //     group's next tile into it);
-//   * the lane forms its row's 32 dGate and 32 dUp values, quantises the two
-//     rowwise blocks straight from its registers and stores each block's 32
-//     codes as one 32-byte sector; the values also go to the warp's 8 KB
-//     value buffer (per output 32 rows of 128 bytes, 16-byte chunks
-//     swizzled by row, so that a lane writing its row and a warp reading one
-//     column across its lanes are both free of bank conflicts);
-//   * lane l then reads column l of the buffer for each output, quantises
-//     the colwise block and stores its 32 codes (rows row0..row0+31 of the
-//     [2N, M] matrix) as one 32-byte sector;
+//   * four quantiser jobs from the buffer: lane l reads row l of each output
+//     (the rowwise blocks) and column l of each (the colwise blocks, rows
+//     row0..row0+31 of the [2N, M] matrix), and stores each block's 32 codes
+//     as one 32-byte sector;
 //   * codes and scales leave by plain stores: every code store is a whole
 //     sector; a lane's colwise scales of a unit's four row tiles are one
 //     word; rowwise scales are bytes, whose sectors the band walk completes
