@@ -12,7 +12,7 @@
 namespace gq {
 namespace {
 
-constexpr int kThreads = 768;
+constexpr int kThreads = 512;
 
 struct PlainP {
   const uint8_t* gate;
@@ -75,6 +75,124 @@ __device__ __forceinline__ void gu_at(const PlainP& p, int layout, int64_t r, in
   g = __uint_as_float(g16 << 16);
 }
 
+// One unit (VEC elements of row r from column c0) from its raw operand
+// words (VEC == 8: x, y the gate/up or pair words, d the dY words), written
+// to the output.
+template <int ACT, int BWD, int LAYOUT, typename OutT, int VEC>
+__device__ __forceinline__ void plain_unit(const PlainP& p, const uint8_t* smem, int64_t r, int64_t c0,
+                                           const uint4& wa, const uint4& wb, const uint4& wd) {
+  OutT* out = static_cast<OutT*>(p.out);
+  const int64_t W = BWD ? 2 * p.N : p.N;
+  float a[VEC], b[VEC];  // forward: a = h; backward: a = dGate, b = dUp
+  bool cold = false;
+  if (VEC == 8) {
+    const uint32_t x[4] = {wa.x, wa.y, wa.z, wa.w}, y[4] = {wb.x, wb.y, wb.z, wb.w};
+    const uint32_t d[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      uint32_t g16;
+      float u;
+      if (LAYOUT == GLU_LAYOUT_SPLIT) {
+        g16 = (k & 1) ? (x[k >> 1] >> 16) : (x[k >> 1] & 0xFFFFu);
+        u = (k & 1) ? bf16_hi(y[k >> 1]) : bf16_lo(y[k >> 1]);
+      } else {
+        const uint32_t w = (k < 4) ? x[k] : y[k - 4];
+        g16 = w & 0xFFFFu;
+        u = bf16_hi(w);
+      }
+      const uint32_t idx = tab_index(g16);
+      if (!kTabAct<ACT>) {  // exact products (GELU erf: fp64), rounded once (the bf16 steps: to bf16)
+        const float g = __uint_as_float(g16 << 16);
+        if (BWD) {
+          const float dv = (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
+          if constexpr (kErfAct<ACT>) {
+            b[k] = slow_act_mul(4, g, dv);
+            a[k] = slow_grad_mul(4, g, dv, u);
+          } else {
+            b[k] = __fmul_rn(dv, xact<ACT>(g));
+            a[k] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+          }
+        } else {
+          a[k] = exact_h<ACT>(nullptr, g, u);
+        }
+      } else if (BWD) {
+        const float dv = (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
+        const float4 e = reinterpret_cast<const float4*>(smem)[idx];
+        b[k] = tab_mul(make_float2(e.x, e.y), dv);
+        a[k] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
+        cold |= is_cold(a[k]) | is_cold(b[k]);
+      } else if (ACT & 16) {  // bf16 steps: RN_bf16(RN_bf16(act(g)) * u)
+        const float2 e = reinterpret_cast<const float2*>(smem)[idx];
+        a[k] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(e, __uint_as_float(g16 << 16)), u));
+      } else {
+        a[k] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
+        cold |= is_cold(a[k]);
+      }
+    }
+  } else {
+    float g, u;
+    uint32_t g16;
+    gu_at(p, LAYOUT, r, c0, g, g16, u);
+    const uint32_t idx = tab_index(g16);
+    if (!kTabAct<ACT>) {
+      if (BWD) {
+        const float dv =
+            __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0]) << 16);
+        if constexpr (kErfAct<ACT>) {
+          b[0] = slow_act_mul(4, g, dv);
+          a[0] = slow_grad_mul(4, g, dv, u);
+        } else {
+          b[0] = __fmul_rn(dv, xact<ACT>(g));
+          a[0] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
+        }
+      } else {
+        a[0] = exact_h<ACT>(nullptr, g, u);
+      }
+    } else if (BWD) {
+      const float dv =
+          __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0]) << 16);
+      const float4 e = reinterpret_cast<const float4*>(smem)[idx];
+      b[0] = tab_mul(make_float2(e.x, e.y), dv);
+      a[0] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
+      cold = is_cold(a[0]) | is_cold(b[0]);
+    } else if (ACT & 16) {
+      a[0] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(reinterpret_cast<const float2*>(smem)[idx], g), u));
+    } else {
+      a[0] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
+      cold = is_cold(a[0]);
+    }
+  }
+  if (kTabAct<ACT> && cold) {
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      float g, u;
+      uint32_t g16;
+      gu_at(p, LAYOUT, r, c0 + k, g, g16, u);
+      if (BWD) {
+        const float dv = __uint_as_float(
+            uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0 + k]) << 16);
+        if (is_cold(a[k])) a[k] = slow_grad_mul(ACT & 1, g, dv, u);
+        if (is_cold(b[k])) b[k] = slow_act_mul(ACT & 1, g, dv);
+      } else if (is_cold(a[k])) {
+        a[k] = slow_act_mul(ACT & 1, g, u);
+      }
+    }
+  }
+  if (VEC == 8) {
+    store8<OutT>(out + r * W + c0, reinterpret_cast<const float(&)[8]>(a));
+    if (BWD) store8<OutT>(out + r * W + p.N + c0, reinterpret_cast<const float(&)[8]>(b));
+  } else {
+    store1<OutT>(out + r * W + c0, a[0]);
+    if (BWD) store1<OutT>(out + r * W + p.N + c0, b[0]);
+  }
+}
+
+// Units per thread and sweep step: the loads of all of them are issued
+// before the first is computed, so that enough bytes are in flight to cover
+// the memory latency (one unit at a time left the kernel at about 70 % of
+// the HBM bandwidth).
+constexpr int kUnitsInFlight = 4;
+
 template <int ACT, int BWD, int LAYOUT, typename OutT, int VEC>
 __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -86,124 +204,31 @@ __global__ void __launch_bounds__(kThreads, 1) plain_kernel(const PlainP p) {
     for (int i = threadIdx.x; i < int(kTabEntries) * kEntry / 16; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
-  OutT* out = static_cast<OutT*>(p.out);
-  const int64_t W = BWD ? 2 * p.N : p.N;
-
-  for (int64_t unit = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; unit < p.units;
-       unit += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = unit / p.units_per_row;
-    const int64_t c0 = (unit - r * p.units_per_row) * VEC;
-    float a[VEC], b[VEC];  // forward: a = h; backward: a = dGate, b = dUp
-    bool cold = false;
-    if (VEC == 8) {
-      uint4 wa, wb, wd = make_uint4(0, 0, 0, 0);
-      if (LAYOUT == GLU_LAYOUT_SPLIT) {
-        wa = ld_stream(p.gate + (r * p.ld + c0) * 2);
-        wb = ld_stream(p.up + (r * p.ld + c0) * 2);
-      } else {
-        wa = ld_stream(p.gate + (r * p.ld + 2 * c0) * 2);
-        wb = ld_stream(p.gate + (r * p.ld + 2 * c0) * 2 + 16);
-      }
-      if (BWD) wd = ld_stream(p.dy + (r * p.ld_dy + c0) * 2);
-      const uint32_t x[4] = {wa.x, wa.y, wa.z, wa.w}, y[4] = {wb.x, wb.y, wb.z, wb.w};
-      const uint32_t d[4] = {wd.x, wd.y, wd.z, wd.w};
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  constexpr int U = VEC == 8 ? kUnitsInFlight : 1;
+  for (int64_t base = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; base < p.units; base += stride * U) {
+    uint4 wa[U], wb[U], wd[U];
+    int64_t rr[U], cc[U];
 #pragma unroll
-      for (int k = 0; k < VEC; ++k) {
-        uint32_t g16;
-        float u;
+    for (int i = 0; i < U; ++i) {
+      const int64_t unit = base + i * stride;
+      rr[i] = unit / p.units_per_row;
+      cc[i] = (unit - rr[i] * p.units_per_row) * VEC;
+      wa[i] = wb[i] = wd[i] = make_uint4(0, 0, 0, 0);
+      if (VEC == 8 && unit < p.units) {
         if (LAYOUT == GLU_LAYOUT_SPLIT) {
-          g16 = (k & 1) ? (x[k >> 1] >> 16) : (x[k >> 1] & 0xFFFFu);
-          u = (k & 1) ? bf16_hi(y[k >> 1]) : bf16_lo(y[k >> 1]);
+          wa[i] = ld_stream(p.gate + (rr[i] * p.ld + cc[i]) * 2);
+          wb[i] = ld_stream(p.up + (rr[i] * p.ld + cc[i]) * 2);
         } else {
-          const uint32_t w = (k < 4) ? x[k] : y[k - 4];
-          g16 = w & 0xFFFFu;
-          u = bf16_hi(w);
+          wa[i] = ld_stream(p.gate + (rr[i] * p.ld + 2 * cc[i]) * 2);
+          wb[i] = ld_stream(p.gate + (rr[i] * p.ld + 2 * cc[i]) * 2 + 16);
         }
-        const uint32_t idx = tab_index(g16);
-        if (!kTabAct<ACT>) {  // exact products (GELU erf: fp64), rounded once (the bf16 steps: to bf16)
-          const float g = __uint_as_float(g16 << 16);
-          if (BWD) {
-            const float dv = (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
-            if constexpr (kErfAct<ACT>) {
-              b[k] = slow_act_mul(4, g, dv);
-              a[k] = slow_grad_mul(4, g, dv, u);
-            } else {
-              b[k] = __fmul_rn(dv, xact<ACT>(g));
-              a[k] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
-            }
-          } else {
-            a[k] = exact_h<ACT>(nullptr, g, u);
-          }
-        } else if (BWD) {
-          const float dv = (k & 1) ? bf16_hi(d[k >> 1]) : bf16_lo(d[k >> 1]);
-          const float4 e = reinterpret_cast<const float4*>(smem)[idx];
-          b[k] = tab_mul(make_float2(e.x, e.y), dv);
-          a[k] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
-          cold |= is_cold(a[k]) | is_cold(b[k]);
-        } else if (ACT & 16) {  // bf16 steps: RN_bf16(RN_bf16(act(g)) * u)
-          const float2 e = reinterpret_cast<const float2*>(smem)[idx];
-          a[k] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(e, __uint_as_float(g16 << 16)), u));
-        } else {
-          a[k] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
-          cold |= is_cold(a[k]);
-        }
-      }
-    } else {
-      float g, u;
-      uint32_t g16;
-      gu_at(p, LAYOUT, r, c0, g, g16, u);
-      const uint32_t idx = tab_index(g16);
-      if (!kTabAct<ACT>) {
-        if (BWD) {
-          const float dv =
-              __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0]) << 16);
-          if constexpr (kErfAct<ACT>) {
-            b[0] = slow_act_mul(4, g, dv);
-            a[0] = slow_grad_mul(4, g, dv, u);
-          } else {
-            b[0] = __fmul_rn(dv, xact<ACT>(g));
-            a[0] = __fmul_rn(dv, __fmul_rn(u, xact_grad<ACT>(g)));
-          }
-        } else {
-          a[0] = exact_h<ACT>(nullptr, g, u);
-        }
-      } else if (BWD) {
-        const float dv =
-            __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0]) << 16);
-        const float4 e = reinterpret_cast<const float4*>(smem)[idx];
-        b[0] = tab_mul(make_float2(e.x, e.y), dv);
-        a[0] = tab_mul(make_float2(e.z, e.w), __fmul_rn(dv, u));
-        cold = is_cold(a[0]) | is_cold(b[0]);
-      } else if (ACT & 16) {
-        a[0] = bf16_rn(__fmul_rn(act_bf16_of_entry<ACT & 1>(reinterpret_cast<const float2*>(smem)[idx], g), u));
-      } else {
-        a[0] = tab_mul(reinterpret_cast<const float2*>(smem)[idx], u);
-        cold = is_cold(a[0]);
+        if (BWD) wd[i] = ld_stream(p.dy + (rr[i] * p.ld_dy + cc[i]) * 2);
       }
     }
-    if (kTabAct<ACT> && cold) {
 #pragma unroll
-      for (int k = 0; k < VEC; ++k) {
-        float g, u;
-        uint32_t g16;
-        gu_at(p, LAYOUT, r, c0 + k, g, g16, u);
-        if (BWD) {
-          const float dv = __uint_as_float(
-              uint32_t(reinterpret_cast<const uint16_t*>(p.dy)[r * p.ld_dy + c0 + k]) << 16);
-          if (is_cold(a[k])) a[k] = slow_grad_mul(ACT & 1, g, dv, u);
-          if (is_cold(b[k])) b[k] = slow_act_mul(ACT & 1, g, dv);
-        } else if (is_cold(a[k])) {
-          a[k] = slow_act_mul(ACT & 1, g, u);
-        }
-      }
-    }
-    if (VEC == 8) {
-      store8<OutT>(out + r * W + c0, reinterpret_cast<const float(&)[8]>(a));
-      if (BWD) store8<OutT>(out + r * W + p.N + c0, reinterpret_cast<const float(&)[8]>(b));
-    } else {
-      store1<OutT>(out + r * W + c0, a[0]);
-      if (BWD) store1<OutT>(out + r * W + p.N + c0, b[0]);
-    }
+    for (int i = 0; i < U; ++i)
+      if (base + i * stride < p.units) plain_unit<ACT, BWD, LAYOUT, OutT, VEC>(p, smem, rr[i], cc[i], wa[i], wb[i], wd[i]);
   }
 }
 
