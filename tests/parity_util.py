@@ -20,9 +20,18 @@ import oracle as O
 WINDOW_ULPS = 2
 
 
+# Counts over every comparison of the session (codes and scales compared,
+# codes differing by one step inside the 2-ulp window), reported at the end
+# of a pytest run (tests/conftest.py).
+TOTALS = {"elements": 0, "scales": 0, "window_mismatch": 0}
+
+
 class Stats(dict):
     def add(self, k, v):
         self[k] = self.get(k, 0) + int(v)
+        tail = k.rsplit(".", 1)[-1]
+        if tail in TOTALS:
+            TOTALS[tail] += int(v)
 
 
 def _adjacent_e4m3(a, b):
