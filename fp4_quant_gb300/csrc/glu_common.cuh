@@ -819,6 +819,21 @@ constexpr uint32_t kScaleWindow = (1u << (24 + D_LOG2)) + 2u;
 __device__ __forceinline__ uint32_t e8m0_checked(float amax, float d) {
   return e8m0_window(amax, uint32_t(d * 0x1p24f) + 2u);
 }
+// e8m0_checked, with the multiplier 2^-e of the candidate byte formed
+// straight from amax's exponent field (in parallel with the test, so that a
+// caller can start on the codes before the test's outcome is known; the
+// multiplier is meaningless when the result is 0x100).
+__device__ __forceinline__ uint32_t e8m0_spec(float amax, float d, float& mul) {
+  const uint32_t ab = __float_as_uint(amax);
+  const uint32_t m = ab & 0x7FFFFFu;
+  const uint32_t K = uint32_t(d * 0x1p24f) + 2u;
+  const bool bad = ab >= kInfBits || ab - 1u < kTinyBits - 1u || m - (0x600000u - K) <= 2u * K;
+  // the byte (ab >> 23) - 8 + (m > 0x600000), 0 for a zero block; 2^-e has
+  // exponent field 254 - byte
+  const int byte = max(int(ab >> 23) - 8 + int(m > 0x600000u), 0);
+  mul = __uint_as_float(uint32_t(254 - byte) << 23);
+  return bad ? 0x100u : uint32_t(byte);
+}
 
 // E4M3 codes of four values scaled by the block multiplier, decided from
 // the bracket: mlo = 2^-e (1 - d), mhi = 2^-e (1 + d) (exact products of a

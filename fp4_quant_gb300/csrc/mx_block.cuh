@@ -73,21 +73,22 @@ __device__ __forceinline__ void exact_fill(float (&v)[32], Exact8&& exact8) {
 template <class Exact, class Fill>
 __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], const float d,
                                              Exact&& exact, Fill&& fill) {
-  uint32_t sc = e8m0_checked(amax32(v), d);
-  if (sc != 0x100u) {
-    const float mul = e8m0_inv_scale(sc);
-    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-    // codes from the low bracket end; any byte where the high end differs
-    // leaves a bit in `diff`
-    uint32_t diff = 0;
+  float mul;
+  uint32_t sc = e8m0_spec(amax32(v), d, mul);
+  // codes from the low bracket end, formed while the scale test runs beside
+  // them (an undecided scale discards them); any byte where the high end
+  // differs leaves a bit in `diff`
+  const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+  uint32_t diff = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
-      const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
-      const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
-      q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
-      diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
-    }
+  for (int j = 0; j < 8; ++j) {
+    const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
+    const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
+    const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
+    q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
+    diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  }
+  if (sc != 0x100u) {
     if (diff != 0u) {
       // rare: the straddling elements get codes from their exact values
       uint32_t emask = 0;
@@ -128,9 +129,9 @@ __device__ __forceinline__ uint32_t mx_block(float (&v)[32], uint32_t (&q)[8], c
 __device__ __forceinline__ uint32_t mx_fast(const float (&v)[32], uint32_t (&q)[8], const float d, float& mul,
                                             uint32_t& emask) {
   emask = 0;
-  const uint32_t sc = e8m0_checked(amax32(v), d);
-  if (sc == 0x100u) return sc;
-  mul = e8m0_inv_scale(sc);
+  // the codes are formed while the scale test runs beside them (an
+  // undecided scale discards them)
+  const uint32_t sc = e8m0_spec(amax32(v), d, mul);
   const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
   uint32_t diff = 0;
 #pragma unroll
@@ -141,6 +142,7 @@ __device__ __forceinline__ uint32_t mx_fast(const float (&v)[32], uint32_t (&q)[
     q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
     diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
   }
+  if (sc == 0x100u) return sc;
   if (diff != 0u) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
