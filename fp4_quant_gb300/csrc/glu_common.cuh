@@ -665,8 +665,9 @@ template <int ACT> struct Bracket {
   // the widest dgate_bracket / dgate_bracket_erf step
   static constexpr float kDGate = kExact ? 0.0f : kErfAct<ACT> ? 0x1p-11f : 0x1p-14f;
   static constexpr float kDGateFar = kExact ? 0.0f : 0x1p-18f;  // |N| >= 1/8
-  // NVFP4: the activation's width plus the roundings of 1/6, 1/s and the
-  // bracket products (4 units of 2^-24 at most)
+  // NVFP4: the activation's width plus the roundings of 1/6 and of the
+  // bracket products and the approximate reciprocal of the scale (rcp.approx,
+  // one ulp): 6 units of 2^-24 at most
   static constexpr float kNv = kExact ? 0x1p-21f : 2.0f * kAct;
 };
 
@@ -765,6 +766,16 @@ __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
 
 // fp32 -> E4M3 byte (round to nearest even, saturating).
 __device__ __forceinline__ uint32_t e4m3(float a) { return e4m3x2(a, 0.0f) & 0xFFu; }
+
+// E4M3 byte (finite) -> fp32, exactly, by the hardware conversions (E4M3
+// -> f16 -> f32; every E4M3 value is an f16 value).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(c & 0xFFu)));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(uint16_t(h2 & 0xFFFFu)));
+  return f;
+}
 
 // E4M3 byte (finite) -> fp32, exactly.
 __device__ __forceinline__ float e4m3_value(uint32_t c) {

@@ -114,15 +114,19 @@ __device__ __forceinline__ uint32_t nv_block(float (&v)[32], uint32_t& w0, uint3
           w1 = sign_word<B>(v, 1);
           return 0u;
         }
-        const float rs = __frcp_rn(e4m3_value(sc));
-        const float mlo = __fmul_rn(rs, 1.0f - d), mhi = __fmul_rn(rs, 1.0f + d);
+        // the bracket takes 1/s from rcp.approx (within one ulp; d covers
+        // it): the hardware decode and one MUFU instead of the IEEE
+        // reciprocal on the scale-to-codes chain
+        const float ra = rcp_approx(e4m3_to_f32(sc));
+        const float mlo = __fmul_rn(ra, 1.0f - d), mhi = __fmul_rn(ra, 1.0f + d);
         w0 = e2m1_word<B>(v, 0, mlo);
         w1 = e2m1_word<B>(v, 1, mlo);
         const uint32_t x0 = w0 ^ e2m1_word<B>(v, 0, mhi);
         const uint32_t x1 = w1 ^ e2m1_word<B>(v, 1, mhi);
         if ((x0 | x1) != 0u) {
           // rare: codes of the straddling elements from their exact values
-          const float s = e4m3_value(sc);
+          // (correctly rounded quotients: rs = RN(1/s))
+          const float s = e4m3_value(sc), rs = __frcp_rn(s);
           uint32_t emask = 0;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -167,8 +171,8 @@ __device__ __forceinline__ uint32_t nv_block(float (&v)[32], uint32_t& w0, uint3
 
 // The fast part of nv_block alone, for kernels that keep the exact path out
 // of the hot code: returns the scale byte the rounding test decides (the
-// codes of elements B..B+15 in w0, w1) and sets `rs` to RN(1/scale), or
-// returns 0x100 when the scale is undecided (or the block holds a NaN, an
+// codes of elements B..B+15 in w0, w1), or returns 0x100 when the scale is
+// undecided (or the block holds a NaN, an
 // infinity or a tiny amax: every value must then be exact); `emask` gets
 // the elements (bit e, 0..15) whose codes the test cannot decide.
 template <int B>
@@ -191,8 +195,8 @@ __device__ __forceinline__ uint32_t nv_fast(const float (&v)[32], uint32_t& w0, 
     w1 = sign_word<B>(v, 1);
     return 0u;
   }
-  const float rs = __frcp_rn(e4m3_value(sc));
-  const float mlo = __fmul_rn(rs, 1.0f - d), mhi = __fmul_rn(rs, 1.0f + d);
+  const float ra = rcp_approx(e4m3_to_f32(sc));  // within one ulp of 1/s (d covers it)
+  const float mlo = __fmul_rn(ra, 1.0f - d), mhi = __fmul_rn(ra, 1.0f + d);
   w0 = e2m1_word<B>(v, 0, mlo);
   w1 = e2m1_word<B>(v, 1, mlo);
   const uint32_t x0 = w0 ^ e2m1_word<B>(v, 0, mhi);
