@@ -270,20 +270,22 @@ __device__ __forceinline__ void patch_code4(uint32_t (&q)[4], int e, uint32_t c)
 template <class Exact, class Fill>
 __device__ __forceinline__ uint32_t mx_half(float (&v)[16], uint32_t (&q)[4], const float d, Exact&& exact,
                                             Fill&& fill) {
-  uint32_t sc = e8m0_checked(pair_amax(amax16(v)), d);
+  float mul;
+  uint32_t sc = e8m0_spec(pair_amax(amax16(v)), d, mul);
   const bool undecided = sc == 0x100u;
-  if (!undecided) {
-    const float mul = e8m0_inv_scale(sc);
-    const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-    uint32_t diff = 0;
+  // the codes are formed while the scale test runs beside them (an
+  // undecided scale discards them)
+  const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
+  uint32_t diff = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
-      const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
-      const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
-      q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
-      diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
-    }
+  for (int j = 0; j < 4; ++j) {
+    const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
+    const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
+    const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
+    q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
+    diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  }
+  if (!undecided) {
     if (diff != 0u) {
       // rare: the straddling elements get codes from their exact values
       uint32_t emask = 0;
