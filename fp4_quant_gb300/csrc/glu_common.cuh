@@ -817,23 +817,10 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
 // the mantissa field passes 0x600000 (the byte formula is continuous across
 // binade edges), and amax (1 -/+ d) reaches that point only if amax's
 // mantissa lies within d * 2^24 of it (amax < 2^(E+1)): the test is that
-// window, K = d * 2^24 plus slack.
-__device__ __forceinline__ uint32_t e8m0_window(float amax, uint32_t K) {
-  const uint32_t ab = __float_as_uint(amax);
-  const uint32_t m = ab & 0x7FFFFFu;
-  const bool bad = ab >= kInfBits || ab - 1u < kTinyBits - 1u || m - (0x600000u - K) <= 2u * K;
-  const int biased = int(ab >> 23) - 8 + int(m > 0x600000u);
-  return bad ? 0x100u : uint32_t(max(biased, 0));
-}
-template <int D_LOG2>  // d = 2^D_LOG2
-constexpr uint32_t kScaleWindow = (1u << (24 + D_LOG2)) + 2u;
-__device__ __forceinline__ uint32_t e8m0_checked(float amax, float d) {
-  return e8m0_window(amax, uint32_t(d * 0x1p24f) + 2u);
-}
-// e8m0_checked, with the multiplier 2^-e of the candidate byte formed
-// straight from amax's exponent field (in parallel with the test, so that a
-// caller can start on the codes before the test's outcome is known; the
-// multiplier is meaningless when the result is 0x100).
+// window, K = d * 2^24 plus slack.  `mul` gets the multiplier 2^-e of the
+// candidate byte, formed straight from amax's exponent field beside the
+// test, so that a caller can start on the codes before the test's outcome
+// is known (it is meaningless when the result is 0x100).
 __device__ __forceinline__ uint32_t e8m0_spec(float amax, float d, float& mul) {
   const uint32_t ab = __float_as_uint(amax);
   const uint32_t m = ab & 0x7FFFFFu;

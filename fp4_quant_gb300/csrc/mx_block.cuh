@@ -154,65 +154,6 @@ __device__ __forceinline__ uint32_t mx_fast(const float (&v)[32], uint32_t (&q)[
   return sc;
 }
 
-// The pieces of mx_fast for a half-width d = 2^D_LOG2 (a power of two; d =
-// 0 for D_LOG2 <= -40), with the scale decided by its mantissa window
-// (e8m0_window), kept apart so that a caller can interleave several blocks:
-//   mx_scale_w: the scale byte, or 0x100 (undecided, or a NaN/Inf/tiny
-//     block: every value must then be exact);
-//   mx_codes_w: the low-end codes of the block for the multiplier mul =
-//     2^-e; returns nonzero when some code differs at the high end;
-//   mx_emask_w: the elements whose codes the test leaves undecided (bit e).
-template <int D_LOG2>
-constexpr float kHalfWidth = D_LOG2 <= -40 ? 0.0f : float(1.0 / double(1ull << (D_LOG2 <= -40 ? 0 : -D_LOG2)));
-
-template <int D_LOG2>
-__device__ __forceinline__ uint32_t mx_scale_w(const float (&v)[32]) {
-  return e8m0_window(amax32(v), kScaleWindow<D_LOG2 <= -40 ? -24 : D_LOG2>);
-}
-
-template <int D_LOG2>
-__device__ __forceinline__ uint32_t mx_codes_w(const float (&v)[32], float mul, uint32_t (&q)[8]) {
-  constexpr float d = kHalfWidth<D_LOG2>;
-  const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-  uint32_t diff = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float2 a = make_float2(v[4 * j], v[4 * j + 1]), b = make_float2(v[4 * j + 2], v[4 * j + 3]);
-    const float2 al = mul2(a, splat2(mlo)), bl = mul2(b, splat2(mlo));
-    q[j] = e4m3x4(al.x, al.y, bl.x, bl.y);
-    if (d != 0.0f) {
-      const float2 ah = mul2(a, splat2(mhi)), bh = mul2(b, splat2(mhi));
-      diff |= q[j] ^ e4m3x4(ah.x, ah.y, bh.x, bh.y);
-    }
-  }
-  return diff;
-}
-
-template <int D_LOG2>
-__device__ __forceinline__ uint32_t mx_emask_w(const float (&v)[32], float mul) {
-  constexpr float d = kHalfWidth<D_LOG2>;
-  const float mlo = mul * (1.0f - d), mhi = mul * (1.0f + d);
-  uint32_t emask = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t ql = e4m3x4(v[4 * j] * mlo, v[4 * j + 1] * mlo, v[4 * j + 2] * mlo, v[4 * j + 3] * mlo);
-    const uint32_t qh = e4m3x4(v[4 * j] * mhi, v[4 * j + 1] * mhi, v[4 * j + 2] * mhi, v[4 * j + 3] * mhi);
-    emask |= byte_mask(ql ^ qh) << (4 * j);
-  }
-  return emask;
-}
-
-// mx_fast from those pieces.
-template <int D_LOG2>
-__device__ __forceinline__ uint32_t mx_fast_w(const float (&v)[32], uint32_t (&q)[8], float& mul, uint32_t& emask) {
-  emask = 0;
-  const uint32_t sc = mx_scale_w<D_LOG2>(v);
-  if (sc == 0x100u) return sc;
-  mul = e8m0_inv_scale(sc);
-  if (mx_codes_w<D_LOG2>(v, mul, q) != 0u) emask = mx_emask_w<D_LOG2>(v, mul);
-  return sc;
-}
-
 // Scale byte and codes of a block of exact values (NaN/Inf -> 0xFF and
 // codes 0x7F).
 __device__ __forceinline__ uint32_t mx_exact(const float (&v)[32], uint32_t (&q)[8]) {

@@ -103,26 +103,28 @@ __device__ __forceinline__ uint32_t nv_block(float (&v)[32], uint32_t& w0, uint3
                           v[B + 15]);
     const float amax = amax2(a, b);
     const uint32_t ab = __float_as_uint(amax);
+    // both bracket ends in one conversion: low byte from amax (1 - d) / 6
+    const uint32_t sp = e4m3x2(__fmul_rn(amax, __fmul_rn(kRcp6, 1.0f - d)),
+                               __fmul_rn(amax, __fmul_rn(kRcp6, 1.0f + d)));
+    const uint32_t sc = sp & 0xFFu;
+    // the codes of the low end's scale are formed while the scale is tested
+    // (kept only if it is decided and nonzero); the bracket takes 1/s from
+    // rcp.approx (within one ulp; d covers it): the hardware decode and one
+    // MUFU instead of the IEEE reciprocal on the scale-to-codes chain
+    const float ra = rcp_approx(e4m3_to_f32(sc));
+    const float mlo = __fmul_rn(ra, 1.0f - d), mhi = __fmul_rn(ra, 1.0f + d);
+    const uint32_t c0 = e2m1_word<B>(v, 0, mlo), c1 = e2m1_word<B>(v, 1, mlo);
+    const uint32_t x0 = c0 ^ e2m1_word<B>(v, 0, mhi);
+    const uint32_t x1 = c1 ^ e2m1_word<B>(v, 1, mhi);
     if (ab < kInfBits && (ab == 0u || ab >= kTinyBits)) {
-      // both bracket ends in one conversion: low byte from amax (1 - d) / 6
-      const uint32_t sp = e4m3x2(__fmul_rn(amax, __fmul_rn(kRcp6, 1.0f - d)),
-                                 __fmul_rn(amax, __fmul_rn(kRcp6, 1.0f + d)));
-      const uint32_t sc = sp & 0xFFu;
       if (sc == (sp >> 8)) {
         if (sc == 0u) {
           w0 = sign_word<B>(v, 0);
           w1 = sign_word<B>(v, 1);
           return 0u;
         }
-        // the bracket takes 1/s from rcp.approx (within one ulp; d covers
-        // it): the hardware decode and one MUFU instead of the IEEE
-        // reciprocal on the scale-to-codes chain
-        const float ra = rcp_approx(e4m3_to_f32(sc));
-        const float mlo = __fmul_rn(ra, 1.0f - d), mhi = __fmul_rn(ra, 1.0f + d);
-        w0 = e2m1_word<B>(v, 0, mlo);
-        w1 = e2m1_word<B>(v, 1, mlo);
-        const uint32_t x0 = w0 ^ e2m1_word<B>(v, 0, mhi);
-        const uint32_t x1 = w1 ^ e2m1_word<B>(v, 1, mhi);
+        w0 = c0;
+        w1 = c1;
         if ((x0 | x1) != 0u) {
           // rare: codes of the straddling elements from their exact values
           // (correctly rounded quotients: rs = RN(1/s))
