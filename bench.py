@@ -40,6 +40,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -112,21 +113,53 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "of fallback (6.8 TB/s)"}
 
 
-def csrc_hash() -> str:
-    h = hashlib.sha256()
+# Translation unit that holds each call's kernel.
+KERNEL_TU = {"fwd": "fwd_mx.cu", "bwd_row": "bwd_mx.cu", "bwd_col": "bwd_mx.cu",
+             "bwd_both": "bwd_both.cu"}
+# Host files every launch goes through (entry points, tensor maps, the
+# generator of the activation tables).
+KERNEL_HOST = ("api.cu", "tmap.cu", "kernels.h", "gen_act_tables.c")
+
+
+def kernel_src_hash(tu: str) -> str:
+    """Hash of the sources one kernel is built from: its translation unit,
+    the library headers it includes (transitively) and the host files of
+    every launch."""
     d = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
+    seen, todo = set(KERNEL_HOST), [tu]
+    while todo:
+        n = todo.pop()
+        if n in seen:
+            continue
+        seen.add(n)
+        with open(os.path.join(d, n)) as f:
+            for line in f:
+                m = re.match(r'\s*#include\s+"([^"/]+)"', line)
+                if m:
+                    todo.append(m.group(1))
+    h = hashlib.sha256()
+    for n in sorted(seen):
         with open(os.path.join(d, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key: str):
+def profiled_traffic(direction: str, mode: str, M: int, N: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the sources the kernel is built from now (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
+    key = f"{direction}_mx_{mode}_{M}x{N}"
+    tu = KERNEL_TU.get(direction if direction == "fwd" else f"{direction}_{mode}")
+    if tu is None:
+        return None
+    cur = kernel_src_hash(tu)
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == key and parts[2] == cur:
+            return float(parts[1])
+    return None
     cur = csrc_hash()
     for line in open(p):
         parts = line.split()
@@ -372,7 +405,7 @@ def gpu_arm(args, rank, world, dist):
     dom = max(calls, key=lambda c: statistics.mean(per_call_ms[c]))
     dom_name = f"{dom[0]}_{MODE_NAME[dom[1]]}"
     dom_gbps = modes[dom_name]["gbps"]
-    traffic = profiled_traffic(f"{dom[0]}_mx_{MODE_NAME[dom[1]]}_{M}x{N}")
+    traffic = profiled_traffic(dom[0], MODE_NAME[dom[1]], M, N)
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,

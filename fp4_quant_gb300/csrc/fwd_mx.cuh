@@ -49,6 +49,12 @@ constexpr int kTR = 32;                       // tile rows
 // Internal mode of the NVFP4 format: walked and computed like rowwise MXFP8.
 constexpr int kModeNv = 4;
 __host__ __device__ constexpr bool row_walk(int mode) { return mode == GLU_MODE_ROW || mode == kModeNv; }
+// Order of the units (kSuper row tiles by one column tile) of the colwise
+// and both walks.  Colwise: row super-tile minor.  Both: column tile minor,
+// so the units that run at the same time cover whole rows and the rowwise
+// scale bytes they share in a 32-byte sector are written close in time
+// (measured 3 % faster than the colwise order, same outputs).
+__host__ __device__ constexpr bool cols_minor(int mode) { return mode == GLU_MODE_BOTH; }
 constexpr int kWC = 32;                       // columns per warp sub-tile
 // Warps per group (one 32-column sub-tile each) and groups per CTA: two
 // groups of eight for rowwise and colwise, four groups of four for both
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
       mbar_init(&ctl->full[st], 1);
       ctl->freed[st] = 0;
     }
-    const int64_t n_minor = row_walk(MODE) ? p.n_ct : p.n_rs;
+    const int64_t n_minor = (row_walk(MODE) || cols_minor(MODE)) ? p.n_ct : p.n_rs;
     for (int g = 0; g < kGroups; ++g) {
       const TileWalk tw(blockIdx.x + g * G, kGroups * G, n_minor);
       ctl->major[g] = tw.major;
@@ -376,8 +382,16 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
     if (lane == 0) {
       const int64_t major = ctl->major[g], minor = ctl->minor[g];
       const int j = int(kk % kPer);
-      rt = row_walk(MODE) ? major : kSuper * minor + j;
-      ct = row_walk(MODE) ? minor : major;
+      if (row_walk(MODE)) {
+        rt = major;
+        ct = minor;
+      } else if (cols_minor(MODE)) {
+        rt = kSuper * major + j;
+        ct = minor;
+      } else {
+        rt = kSuper * minor + j;
+        ct = major;
+      }
       ctl->rt[st] = rt;
       ctl->ct[st] = ct;
       if (j == kPer - 1) {

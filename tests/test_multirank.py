@@ -146,3 +146,14 @@ def test_algorithmic_bytes_per_format():
     assert bench.algo_bytes("fwd", 1, 784, 16384, "nvfp4") == 51380224 + 7225344
     assert bench.algo_bytes("bwd", 1, 8192, 14336, "nvfp4") == 6 * 8192 * 14336 + 8192 * 14336 * 9 // 8
     assert bench.algo_bytes("fwd", 1, 8192, 11008, "bf16") == 6 * 8192 * 11008
+
+
+def test_kernel_source_hash_follows_each_kernel_own_sources():
+    # every call maps to a translation unit whose includes resolve; the
+    # forward and the two backward kernels are keyed separately
+    hs = {tu: bench.kernel_src_hash(tu) for tu in set(bench.KERNEL_TU.values())}
+    assert len(set(hs.values())) == len(hs)
+    assert all(len(h) == 16 for h in hs.values())
+    for d, m in (("fwd", "row"), ("bwd", "both")):
+        t = bench.profiled_traffic(d, m, 131072, 8192)
+        assert t is None or t > bench.algo_bytes(d, 1 if m == "row" else 3, 131072, 8192) * 0.9
