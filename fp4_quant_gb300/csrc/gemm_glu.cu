@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
       const int64_t t = blockIdx.x + i * G;
       const int64_t mt = t % p.n_mt, nt = t / p.n_mt;
       const int b = int(i & 1);
-      // lane 0 waits for the accumulator; the warp follows its verdict (the
+      // lane 0 waits for the accumulator; the warp follows its answer (the
       // TMEM loads below are whole-warp instructions)
       bool ok = true;
       if (lane == 0) {
@@ -316,13 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_glu_kernel(const __grid_cons
         const uint32_t emask = FMT == GLU_FMT_NVFP4_E2M1 ? (em[0] | (em[1] << 16)) : em[0];
         if (__any_sync(0xFFFFFFFFu, (whole | emask) != 0u)) {
           // rare: exact values (fp64) where a decision needs them, in at most
-          // two rounds over the 32 elements (static indices throughout: the
-          // accumulator registers stay registers).  Round 1: the gates below
+          // two passes over the 32 elements (static indices throughout: the
+          // accumulator registers stay registers).  Pass 1: the gates below
           // the fast range, the undecided codes of decided blocks and, in a
           // block whose fast decision failed, the elements that may hold its
           // amax (within the bracket of the fast amax); their exact amax is
           // then the block's, which fixes its scale, and the codes follow by
-          // the rounding test against it.  Round 2: the codes that test
+          // the rounding test against it.  Pass 2: the codes that test
           // leaves open, and every element of a block with a NaN, an infinity
           // or a tiny amax (or whose amax sits at a gate below the fast range).
           constexpr int kBlk = FMT == GLU_FMT_NVFP4_E2M1 ? 16 : 32;
