@@ -235,8 +235,11 @@ uint8_t orc_nvfp4_scale(float amax) {
  * layout of that name: the padded scale matrix is cut into 128-row x
  * 4-column tiles stored row-tile-major, 512 bytes each; inside a tile,
  * row r and column c land at (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.
- * Parity: the layout itself is unpinned against the pages (named only);
- * tests pin that it is a bijection on the padded domain. */
+ * Parity: the pages only name the layout.  Tests pin it on the CPU as a
+ * bijection on the padded domain, and on the GPU against a consumer: a
+ * block-scaled GEMM of cuBLAS fed scale buffers in this layout reproduces
+ * the product of the operands dequantised with the plain row-major
+ * scales. */
 int64_t orc_swizzle_offset(int64_t r, int64_t c, int64_t scale_cols_padded) {
   int64_t tile = (r / 128) * (scale_cols_padded / 4) + c / 4;
   return tile * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4);
@@ -304,8 +307,10 @@ int64_t orc_boundary_ulps(int fmt, float v) {
  * q[i * qs].  A block holding a NaN or an infinity gets the E8M0 NaN scale
  * and the E4M3 NaN code everywhere (the pages name the NaN/Inf regime
  * without fixing its bytes; this is the plainest reading: the block's scale
- * is undefined, so every element is NaN).  Otherwise each value is scaled by
- * 2^-e in fp32 (exact: a power of two) and encoded. */
+ * is undefined, so every element is NaN).  Parity unpinned for these bytes;
+ * tests pin only what the format definitions fix, that such a block decodes
+ * to NaN in every element and no other block does.  Otherwise each value
+ * is scaled by 2^-e in fp32 (exact: a power of two) and encoded. */
 static void mx_block(const float* x, int64_t xs, uint8_t* q, int64_t qs, uint8_t* scale) {
   int nonfinite = 0;
   float amax = 0.0f;
@@ -330,7 +335,9 @@ static void mx_block(const float* x, int64_t xs, uint8_t* q, int64_t qs, uint8_t
  * division).  When the scale rounds to zero (amax < 6 * 2^-10) every code is
  * a zero carrying the sign of its value (the plainest reading: x / 0 would
  * give +-inf and saturate, which a scale of zero cannot mean).  A block with
- * a NaN or an infinity gets the E4M3 NaN scale 0x7F and zero codes. */
+ * a NaN or an infinity gets the E4M3 NaN scale 0x7F and zero codes (parity
+ * unpinned for these bytes, as for MXFP8: tests pin that the block decodes
+ * to NaN). */
 static uint8_t nvfp4_block(const float* x, uint8_t* c) {
   int nonfinite = 0;
   float amax = 0.0f;

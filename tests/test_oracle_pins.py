@@ -880,3 +880,77 @@ def test_gelu_erf_special_values_and_differences():
     assert np.allclose(O.act_grad(O.GELU_ERF, xs), fd, rtol=0, atol=1e-8)
     # close to the tanh approximation it was built to approximate (|diff| < 5e-4)
     assert np.max(np.abs(O.act(O.GELU_ERF, xs) - O.act(O.GELU_TANH, xs))) < 5e-4
+
+
+# ---- non-finite blocks ------------------------------------------------------
+# The pages name the NaN/Inf regime without fixing its bytes, so the bytes
+# the oracle writes are a reading.  What the format definitions do fix (OCP
+# MX v1.0: the E8M0 byte 0xFF and the E4M3 bytes 0x7F/0xFF are NaN; E2M1 has
+# no NaN) is checked here with ml_dtypes' decoders: a block whose fp32 values
+# hold a NaN or an infinity decodes to NaN in every element, and every other
+# block decodes to finite values.
+
+def _nonfinite_inputs(M, N, seed):
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal((M, N)).astype(np.float32)
+    u = rng.standard_normal((M, N)).astype(np.float32)
+    d = rng.standard_normal((M, N)).astype(np.float32)
+    for t in (g, u, d):
+        for _ in range(6):  # scattered, so rows, columns and blocks differ
+            t[rng.integers(M), rng.integers(N)] = rng.choice([np.nan, np.inf, -np.inf])
+    return _bf16_bits(g), _bf16_bits(u), _bf16_bits(d)
+
+
+def _blocks_nonfinite(h, along_rows, k):
+    """[blocks] mask: does each k-element block of h hold a NaN or an Inf."""
+    bad = ~np.isfinite(h)
+    if not along_rows:
+        bad = bad.T
+    R, C = bad.shape
+    return bad.reshape(R, C // k, k).any(axis=2)
+
+
+def _check_decoded(deq_blocks, bad):
+    assert bad.any() and (~bad).any()
+    assert np.isnan(deq_blocks[bad]).all()
+    assert np.isfinite(deq_blocks[~bad]).all()
+
+
+@pytest.mark.parametrize("kind", [O.SILU, O.GELU_TANH, O.RELU, O.IDENTITY, O.GELU_ERF])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_nonfinite_blocks_decode_to_nan_mxfp8(kind, direction):
+    M, N = 64, 256
+    g, u, d = _nonfinite_inputs(M, N, 40 + kind)
+    if direction == "fwd":
+        r = O.glu_fwd(g, u, act=kind, fmt=O.MXFP8, mode=O.BOTH, want_h=True)
+    else:
+        r = O.glu_bwd(g, u, d, act=kind, fmt=O.MXFP8, mode=O.BOTH, want_h=True)
+    h = r["h"]
+    e4m3 = lambda q: q.view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    e8m0 = lambda s: s.view(ml_dtypes.float8_e8m0fnu).astype(np.float64)
+    for along_rows, q, s in ((True, r["q_row"], r["s_row"]), (False, r["q_col"], r["s_col"])):
+        R, C = q.shape
+        deq = e4m3(q).reshape(R, C // 32, 32) * e8m0(s)[:, :, None]
+        _check_decoded(deq, _blocks_nonfinite(h, along_rows, 32))
+
+
+@pytest.mark.parametrize("kind", [O.SILU, O.GELU_TANH, O.RELU, O.IDENTITY, O.GELU_ERF])
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_nonfinite_blocks_decode_to_nan_nvfp4(kind, direction):
+    M, N = 160, 128  # two 128-row tiles of the scale layout, the second ragged
+    g, u, d = _nonfinite_inputs(M, N, 50 + kind)
+    if direction == "fwd":
+        r = O.glu_fwd(g, u, act=kind, fmt=O.NVFP4, want_h=True)
+    else:
+        r = O.glu_bwd(g, u, d, act=kind, fmt=O.NVFP4, want_h=True)
+    h = r["h"]
+    W = h.shape[1]
+    codes = np.empty((M, W), np.uint8)
+    codes[:, 0::2] = r["out"] & 0xF
+    codes[:, 1::2] = r["out"] >> 4
+    e2m1 = codes.view(ml_dtypes.float4_e2m1fn).astype(np.float64)
+    cp = -(-(W // 16) // 4) * 4
+    sb = np.array([[r["s_nvfp4"][O.swizzle_offset(i, j, cp)] for j in range(W // 16)] for i in range(M)],
+                  np.uint8)
+    deq = e2m1.reshape(M, W // 16, 16) * sb.view(ml_dtypes.float8_e4m3fn).astype(np.float64)[:, :, None]
+    _check_decoded(deq, _blocks_nonfinite(h, True, 16))
