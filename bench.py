@@ -88,6 +88,18 @@ def algo_bytes(direction: str, mode: int, M: int, N: int, fmt: str = "mxfp8") ->
     return read + write
 
 
+def padded_bytes(direction: str, mode: int, M: int, N: int, fmt: str = "mxfp8") -> int:
+    """Bytes of one call with NVFP4's scale matrix counted at its padded
+    128x4 size (rows to a multiple of 128, scale columns to a multiple of
+    4, the padding written as zeros); the same as algo_bytes otherwise."""
+    if fmt != "nvfp4":
+        return algo_bytes(direction, mode, M, N, fmt)
+    W = N if direction == "fwd" else 2 * N
+    scales = M * W // 16
+    padded = -(-M // 128) * 128 * (-(-(W // 16) // 4) * 4)
+    return algo_bytes(direction, mode, M, N, fmt) - scales + padded
+
+
 def reduce_max(x: float, dist, device) -> float:
     """Max of a per-rank scalar over all ranks (identity without a group)."""
     if dist is None:
@@ -558,6 +570,9 @@ def configs_block(args, G, dev, peaks, parity=True):
                  "us_graph": round(med, 3), "us_graph_min": round(mn, 3), "bytes": nbytes,
                  "gbps": round(gbps, 1), "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
                  "l2_resident": nbytes < L2_BYTES}
+            if fmt == "nvfp4":
+                pb = padded_bytes(dr, mode, M, N, fmt)
+                r.update({"bytes_padded": pb, "gbps_padded": round(pb / (med * 1e-6) / 1e9, 1)})
             if nbytes < L2_BYTES:
                 r.update(cold_l2(G, dev, sp, dr, mode, f, act, layout, nbytes, peaks))
             torch.cuda.synchronize(dev)
@@ -790,6 +805,9 @@ def sweep(path: str):
              "us_min": round(mn, 3), "bytes": nbytes, "gbps": round(gbps, 1),
              "frac_hbm": round(gbps / peaks["hbm_gbs"], 4),
              "l2_resident": nbytes < L2_BYTES}
+        if fmt == "nvfp4":
+            pb = padded_bytes(direction, mode, M, N, fmt)
+            r.update({"bytes_padded": pb, "gbps_padded": round(pb / (med * 1e-6) / 1e9, 1)})
         recs.append(r)
         print(json.dumps(r), file=sys.stderr, flush=True)
 

@@ -157,3 +157,13 @@ def test_kernel_source_hash_follows_each_kernel_own_sources():
     for d, m in (("fwd", "row"), ("bwd", "both")):
         t = bench.profiled_traffic(d, m, 131072, 8192)
         assert t is None or t > bench.algo_bytes(d, 1 if m == "row" else 3, 131072, 8192) * 0.9
+
+
+def test_padded_bytes_count_the_128x4_padding():
+    # C4 at 784 rows: 784 -> 896 padded rows of 1024 scale bytes
+    assert bench.padded_bytes("fwd", 1, 784, 16384, "nvfp4") == 51380224 + 784 * 8192 + 896 * 1024
+    # backward: [dGate | dUp] is 2N wide; 8192 rows need no row padding
+    assert bench.padded_bytes("bwd", 1, 8192, 14336, "nvfp4") == bench.algo_bytes("bwd", 1, 8192, 14336, "nvfp4")
+    # 40 rows, width 48: 3 scale columns padded to 4, 40 rows to 128
+    assert bench.padded_bytes("fwd", 1, 40, 48, "nvfp4") == 4 * 40 * 48 + 40 * 24 + 128 * 4
+    assert bench.padded_bytes("fwd", 3, 128, 128) == bench.algo_bytes("fwd", 3, 128, 128)
