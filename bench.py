@@ -172,12 +172,6 @@ def profiled_traffic(direction: str, mode: str, M: int, N: int):
         if len(parts) >= 3 and parts[0] == key and parts[2] == cur:
             return float(parts[1])
     return None
-    cur = csrc_hash()
-    for line in open(p):
-        parts = line.split()
-        if len(parts) >= 3 and parts[0] == kernel_key and parts[2] == cur:
-            return float(parts[1])
-    return None
 
 
 class Clocks:
