@@ -9,7 +9,7 @@
 //     gate/up tile is read from memory instead of a GEMM epilogue.
 //
 // Work decomposition (GB300: 152 SMs, up to 227 KB shared memory per CTA):
-//   * one persistent CTA per SM with two groups of eight warps (three groups
+//   * one persistent CTA per SM with two groups of eight warps (four groups
 //     of four for both directions).  Tiles are 32 rows x 256 columns (128
 //     for both); each group has a private two-slot ring of
 //     stages, filled by 2-D TMA loads (cp.async.bulk.tensor, completion
@@ -18,14 +18,17 @@
 //     128-byte swizzle, so that a lane can read its row, or a warp a column,
 //     of a box without shared-memory bank conflicts.  No warp is set aside to
 //     produce: the warp that frees a stage last issues the next load into it;
-//   * tiles go round-robin to the CTAs (column strips first for colwise and
-//     both, so that the CTAs working at once cover neighbouring 32-row groups
-//     of the same columns, rows first for rowwise) and rotate over the groups;
+//   * work units go round-robin to the CTAs and rotate over the groups: a
+//     tile for rowwise and NVFP4, walked along the rows; kSuper row tiles of
+//     one column strip for colwise, walked down the strips, so that the CTAs
+//     working at once cover neighbouring row groups of the same columns; the
+//     same units for both directions, walked along the rows, so that the
+//     rowwise scale bytes the units in flight share are written together;
 //   * warp w of a group owns the 32 x 32 sub-tile at columns 32w..32w+31.
 //     Rowwise: lane l takes row l, a 1x32 block (amax, scale and codes in
 //     registers); NVFP4 is rowwise with two 16-output blocks per lane.  Colwise: lane l reads column l straight from the stage.
-//     Both: the row values also go through a private swizzled transpose
-//     buffer from which lane l reads column l.  Code boxes (32 x 32 bytes)
+//     Both: the row values are written back over the warp's own part of the
+//     stage (swizzled) and lane l then reads column l from it.  Code boxes (32 x 32 bytes)
 //     leave through TMA stores; no barrier spans more than a warp;
 //   * the activation is the fast fp32 form; codes the rounding test cannot
 //     decide are recomputed one element at a time from the exact value, and a
