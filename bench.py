@@ -133,10 +133,36 @@ KERNEL_TU = {"fwd": "fwd_mx.cu", "bwd_row": "bwd_mx.cu", "bwd_col": "bwd_mx.cu",
 KERNEL_HOST = ("api.cu", "tmap.cu", "kernels.h", "gen_act_tables.c")
 
 
+def c_code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed,
+    so that an edit of comments or layout leaves the hash of the code alone
+    (string and character literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(" ".join(line.split()) for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_src_hash(tu: str) -> str:
-    """Hash of the sources one kernel is built from: its translation unit,
-    the library headers it includes (transitively) and the host files of
-    every launch."""
+    """Hash of the code one kernel is built from: its translation unit, the
+    library headers it includes (transitively) and the host files of every
+    launch, comments left out."""
     d = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
     seen, todo = set(KERNEL_HOST), [tu]
     while todo:
@@ -151,8 +177,8 @@ def kernel_src_hash(tu: str) -> str:
                     todo.append(m.group(1))
     h = hashlib.sha256()
     for n in sorted(seen):
-        with open(os.path.join(d, n), "rb") as f:
-            h.update(n.encode() + f.read())
+        with open(os.path.join(d, n)) as f:
+            h.update(n.encode() + c_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

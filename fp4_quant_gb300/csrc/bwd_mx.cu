@@ -20,7 +20,9 @@
 //     quantises its two 1x32 blocks.  Colwise: two passes of 16 columns;
 //     lanes 2i and 2i + 1 share column 16 pass + i (rows 0..15 and 16..31,
 //     read straight from the swizzled stage), each forming and encoding 16
-//     values per output, one shuffle joining the halves' amax.  The rare
+//     values per output, one shuffle joining the halves' amax.  NVFP4
+//     (internal mode 4) is rowwise with two 16-element blocks per output
+//     per lane, its E4M3 scales stored at their 128x4 offsets.  The rare
 //     exact path reads its operands from the stage (held until the codes
 //     are decided);
 //   * rowwise walks the tiles of a row band first, colwise down the column

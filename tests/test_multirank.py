@@ -167,3 +167,11 @@ def test_padded_bytes_count_the_128x4_padding():
     # 40 rows, width 48: 3 scale columns padded to 4, 40 rows to 128
     assert bench.padded_bytes("fwd", 1, 40, 48, "nvfp4") == 4 * 40 * 48 + 40 * 24 + 128 * 4
     assert bench.padded_bytes("fwd", 3, 128, 128) == bench.algo_bytes("fwd", 3, 128, 128)
+
+
+def test_code_hash_ignores_comments_only():
+    a = 'int f(int x) {  // doubles\n  return 2 * x; /* twice */\n}\nconst char* s = "/* kept */";\n'
+    b = '/* header */\nint f(int x) {\n  return 2 * x;\n}\n\nconst char* s = "/* kept */";  // note\n'
+    assert bench.c_code_only(a) == bench.c_code_only(b)
+    assert bench.c_code_only(a) != bench.c_code_only(a.replace("2 * x", "3 * x"))
+    assert bench.c_code_only(a) != bench.c_code_only(a.replace("/* kept */", "kept"))
