@@ -128,9 +128,11 @@ def measured_peaks() -> dict:
 # Translation unit that holds each call's kernel.
 KERNEL_TU = {"fwd": "fwd_mx.cu", "bwd_row": "bwd_mx.cu", "bwd_col": "bwd_mx.cu",
              "bwd_both": "bwd_both.cu"}
-# Host files every launch goes through (entry points, tensor maps, the
-# generator of the activation tables).
-KERNEL_HOST = ("api.cu", "tmap.cu", "kernels.h", "gen_act_tables.c")
+# Files besides its translation unit that shape every launch: the tensor
+# maps, the launch declarations and the generator of the activation tables.
+# The entry points' argument checks (api.cu) are left out: they decide which
+# calls run, not how a launch reads or writes memory.
+KERNEL_HOST = ("tmap.cu", "kernels.h", "gen_act_tables.c")
 
 
 def c_code_only(text: str) -> str:
@@ -160,9 +162,9 @@ def c_code_only(text: str) -> str:
 
 
 def kernel_src_hash(tu: str) -> str:
-    """Hash of the code one kernel is built from: its translation unit, the
-    library headers it includes (transitively) and the host files of every
-    launch, comments left out."""
+    """Hash of the code one kernel is built from: its translation unit
+    (kernel and launcher), the library headers it includes (transitively)
+    and KERNEL_HOST, comments left out."""
     d = os.path.join(ROOT, "fp4_quant_gb300", "csrc")
     seen, todo = set(KERNEL_HOST), [tu]
     while todo:

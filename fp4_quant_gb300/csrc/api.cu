@@ -53,6 +53,10 @@ int check_common(int32_t act, int32_t fmt, int32_t mode, int32_t layout, int64_t
   if (fmt == GLU_FMT_NVFP4_E2M1 && N % 16 != 0) return GLU_ESHAPE;
   const int64_t row_elems = (layout == GLU_LAYOUT_SPLIT) ? N : 2 * N;
   if (N > (INT64_MAX / 8) || ld_in < row_elems) return GLU_ESHAPE;
+  // TMA coordinates are 32-bit: rows, and columns of the [M, 2N] and [2N, M]
+  // outputs (the quantised formats; BF16/FP32 use plain 64-bit addressing)
+  if (fmt != GLU_FMT_BF16 && fmt != GLU_FMT_FP32 && (M > INT32_MAX || 2 * N > INT32_MAX))
+    return GLU_ESHAPE;
   int64_t t;
   if (!mul_ok(M, ld_in, &t) || !mul_ok(t, 4, &t)) return GLU_ESHAPE;
   if (!mul_ok(M, 2 * N, &t) || !mul_ok(t, 4, &t)) return GLU_ESHAPE;

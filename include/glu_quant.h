@@ -75,7 +75,8 @@ extern "C" {
                             pointer for a disabled output               */
 #define GLU_ESHAPE (-2)  /* N % 32 != 0 (MXFP8), M % 32 != 0 (COL),
                             N % 16 != 0 (NVFP4), ld smaller than the row,
-                            size overflow                                 */
+                            M or 2N above INT32_MAX (MXFP8, NVFP4: 32-bit
+                            TMA coordinates), size overflow              */
 #define GLU_EALIGN (-3)  /* a pointer not 16-byte aligned, or an ld not a
                             multiple of 8 elements                        */
 #define GLU_EDEVICE (-4) /* no CUDA device, or the current device is not

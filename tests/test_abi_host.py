@@ -84,6 +84,8 @@ def _no_gpu():
     (dict(ld_in=128), G.GLU_ESHAPE),                       # ld < N
     (dict(layout=1, up=None, ld_in=256), G.GLU_ESHAPE),    # interleaved ld < 2N
     (dict(M=1 << 62), G.GLU_ESHAPE),                       # size overflow
+    (dict(M=1 << 31), G.GLU_ESHAPE),                       # 32-bit TMA row coordinates
+    (dict(N=1 << 30, ld_in=1 << 30), G.GLU_ESHAPE),        # 2N columns of [dGate | dUp] / [2N, M]
     (dict(ld_in=260), G.GLU_EALIGN),                       # ld % 8
     (dict(gate=P + 2), G.GLU_EALIGN),
     (dict(s_row=P + 8), G.GLU_EALIGN),
@@ -224,3 +226,16 @@ def test_gemm_rejections(kw, status):
     assert G.glu_quant_gemm_fwd(a, None) == status
     if "x" not in kw and "q" not in kw:
         assert G.glu_quant_gemm_sizes(a)[0] == status
+
+
+def test_coordinate_limit_applies_to_the_quantised_formats_only():
+    # BF16 / FP32 address memory with 64-bit offsets: 2^31 rows are accepted
+    st, s = G.glu_quant_fwd_sizes(fwd_args(fmt=2, q_row=None, s_row=None, out=P, M=1 << 31, N=32, ld_in=32))
+    assert st == G.GLU_OK and s[0] == (1 << 31) * 32 * 2
+    # the largest quantised shapes inside the limit are accepted
+    st, _ = G.glu_quant_fwd_sizes(fwd_args(M=(1 << 31) - 32, N=32, ld_in=32))
+    assert st == G.GLU_OK
+    st, _ = G.glu_quant_bwd_sizes(bwd_args(M=32, N=(1 << 30) - 32, ld_in=(1 << 30) - 32, ld_dy=(1 << 30) - 32))
+    assert st == G.GLU_OK
+    st, _ = G.glu_quant_bwd_sizes(bwd_args(M=32, N=1 << 30, ld_in=1 << 30, ld_dy=1 << 30))
+    assert st == G.GLU_ESHAPE
