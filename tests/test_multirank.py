@@ -175,3 +175,19 @@ def test_code_hash_ignores_comments_only():
     assert bench.c_code_only(a) == bench.c_code_only(b)
     assert bench.c_code_only(a) != bench.c_code_only(a.replace("2 * x", "3 * x"))
     assert bench.c_code_only(a) != bench.c_code_only(a.replace("/* kept */", "kept"))
+
+
+def test_clock_summary_reads_the_sampled_csv(tmp_path):
+    # rows as nvidia-smi --format=csv,noheader,nounits writes them; the idle
+    # sample (power <= 200 W) is left out of the median and the reasons
+    c = bench.Clocks(0, enabled=False)
+    c.path = str(tmp_path / "clocks.csv")
+    c.proc = object()  # a sampler that ran
+    with open(c.path, "w") as f:
+        f.write("0, 1200, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+        f.write("0, 2070, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active\n")
+        f.write("0, 2055, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+        f.write("0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+        f.write("garbage line\n")
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
